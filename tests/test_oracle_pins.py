@@ -1,0 +1,500 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against something it cannot agree with by
+construction: hand-derived fixtures, exact rational arithmetic, closed forms,
+numpy/IEEE conversions, exact integer matmuls, or the rounding bounds of the
+quantizers.  A plausible mistake (a dropped term, a wrong sign, a swapped
+nibble, a wrong tie-break) fails at least one of them.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from gemv_quantize_q8_gb300 import synth
+from tests.blockpack import pack_q4_k, pack_q6_k, pack_q8_0, parse_fixture
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------- f16
+
+
+def test_half_to_float_matches_ieee_all_codes():
+    h = np.arange(65536, dtype=np.uint16)
+    ref = h.view(np.float16).astype(np.float32)
+    got = np.array([oracle.half_to_float(int(v)) for v in h], dtype=np.float32)
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_float_to_half_round_to_nearest_even():
+    g = np.random.default_rng(3)
+    finite = np.arange(65536, dtype=np.uint16).view(np.float16)
+    finite = finite[np.isfinite(finite)].astype(np.float64)
+    finite = np.unique(finite)
+    mids = (finite[:-1] + finite[1:]) / 2                     # exact midpoints (f64)
+    mids = mids[np.abs(mids) < 3e38]
+    mids32 = mids.astype(np.float32)
+    mids32 = mids32[mids32.astype(np.float64) == mids]        # keep those exact in fp32
+    rnd = (g.standard_normal(20000) * 10.0 ** g.integers(-9, 6, 20000)).astype(np.float32)
+    big = np.array([65504, 65519, 65520, 65536, 1e9, -65520, 6e-8, 3e-8, 2.9802322e-08, 1e-10], dtype=np.float32)
+    xs = np.concatenate([rnd, mids32, big])
+    ref = xs.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.float_to_half(float(v)) for v in xs], dtype=np.uint16)
+    assert (got == ref).all()
+
+
+# --------------------------------------------------------------------------- layouts
+
+
+@pytest.mark.parametrize("fname,dtype,nbytes", [("q4_k_blocks.txt", oracle.Q4_K, 144),
+                                                ("q6_k_blocks.txt", oracle.Q6_K, 210)])
+def test_hand_derived_blocks(fname, dtype, nbytes):
+    cases = list(parse_fixture(os.path.join(GOLDEN, fname), nbytes))
+    assert cases
+    for name, blk, exp in cases:
+        x = oracle.dequant(dtype, blk)
+        want = np.zeros(256)
+        for i, v in exp.items():
+            want[i] = v
+        assert np.array_equal(x, want), name
+
+
+def test_q4_k_every_element_position():
+    """A single nonzero code at element i must dequantise at i and nowhere else."""
+    for i in range(256):
+        codes = [0] * 256
+        codes[i] = 1 + (i % 15)
+        sc = [j + 1 for j in range(8)]
+        blk = pack_q4_k(1.0, 0.0, sc, [0] * 8, codes)
+        x = oracle.dequant(oracle.Q4_K, blk)
+        want = np.zeros(256)
+        want[i] = sc[i // 32] * codes[i]
+        assert np.array_equal(x, want), i
+
+
+def test_q4_k_scale_min_fields():
+    g = np.random.default_rng(5)
+    for _ in range(50):
+        sc = g.integers(0, 64, 8)
+        mn = g.integers(0, 64, 8)
+        codes = g.integers(0, 16, 256)
+        d, dmin = 0.5, 0.25
+        blk = pack_q4_k(d, dmin, sc, mn, codes)
+        x = oracle.dequant(oracle.Q4_K, blk)
+        want = np.array([d * sc[i // 32] * codes[i] - dmin * mn[i // 32] for i in range(256)])
+        assert np.array_equal(x, want)
+
+
+def test_q6_k_every_element_position():
+    for i in range(256):
+        codes = [32] * 256                 # 32 is the zero of the offset code
+        codes[i] = 32 + 1 + (i % 31)
+        sc = [(-1) ** j * (j + 1) for j in range(16)]
+        blk = pack_q6_k(1.0, sc, codes)
+        x = oracle.dequant(oracle.Q6_K, blk)
+        want = np.zeros(256)
+        want[i] = sc[i // 16] * (codes[i] - 32)
+        assert np.array_equal(x, want), i
+
+
+def test_q6_k_all_codes_roundtrip():
+    g = np.random.default_rng(6)
+    codes = g.permutation(np.tile(np.arange(64), 4))
+    sc = g.integers(-128, 128, 16)
+    blk = pack_q6_k(2.0, sc, codes)
+    x = oracle.dequant(oracle.Q6_K, blk)
+    want = np.array([2.0 * sc[i // 16] * (codes[i] - 32) for i in range(256)])
+    assert np.array_equal(x, want)
+
+
+# --------------------------------------------------------------------------- Q8_K quantizer
+
+
+def _q8k_fields(blk):
+    d = np.frombuffer(blk[0:4].tobytes(), dtype=np.float32)[0]
+    q = blk[4:260].view(np.int8).astype(np.int64)
+    bs = np.frombuffer(blk[260:292].tobytes(), dtype=np.int16).astype(np.int64)
+    return d, q, bs
+
+
+def test_q8_k_spike():
+    x = np.zeros((1, 256), dtype=np.float32)
+    x[0, 37] = 3.5
+    d, q, bs = _q8k_fields(oracle.quantize_q8_k(x)[0])
+    want = np.zeros(256, dtype=np.int64)
+    want[37] = -127                               # the max element maps to -127 (iscale = -127/mx)
+    assert np.array_equal(q, want)
+    assert d < 0 and abs(d * -127 - 3.5) <= 4 * np.spacing(np.float32(3.5))
+    assert bs[2] == -127 and np.count_nonzero(bs) == 1
+
+
+def test_q8_k_negative_spike_and_sign_of_d():
+    x = np.zeros((1, 256), dtype=np.float32)
+    x[0, 200] = -2.0
+    d, q, _ = _q8k_fields(oracle.quantize_q8_k(x)[0])
+    assert q[200] == -127 and d == np.float32(1.0) / np.float32(63.5)
+
+
+def test_q8_k_first_occurrence_tie():
+    x = np.zeros((1, 256), dtype=np.float32)
+    x[0, 5], x[0, 9] = -1.5, 1.5
+    d, q, _ = _q8k_fields(oracle.quantize_q8_k(x)[0])
+    assert q[5] == -127 and q[9] == 127 and d > 0
+
+
+def test_q8_k_zero_block():
+    out = oracle.quantize_q8_k(np.zeros((2, 512), dtype=np.float32))
+    assert not out.any()
+
+
+def test_q8_k_ramp_exact_rational():
+    """x_i = i - 128: mx = -128, iscale = 127/128 exactly; codes are the
+    round-half-even of the exact rationals k*127/128 (k = -128..127)."""
+    k = np.arange(256) - 128
+    x = k.astype(np.float32)[None, :]
+    d, q, bs = _q8k_fields(oracle.quantize_q8_k(x)[0])
+    want = []
+    for kk in k:
+        v = Fraction(int(kk) * 127, 128)
+        fl = math.floor(v)
+        r = v - fl
+        want.append(fl + (1 if (r > Fraction(1, 2) or (r == Fraction(1, 2) and fl % 2 == 1)) else 0))
+    assert np.array_equal(q, np.array(want))
+    assert q[128 + 64] == 64 and q[128 - 64] == -64    # the two exact half-way ties went to even
+    assert np.array_equal(bs, np.array(want).reshape(16, 16).sum(1))
+    assert d == np.float32(1.0) / np.float32(np.float32(127.0) / np.float32(128.0))
+
+
+def test_q8_k_rounding_bound_and_bsums():
+    g = np.random.default_rng(7)
+    x = synth.activations(16, 1024, g, outliers=True)
+    out = oracle.quantize_q8_k(x).reshape(16, 4, 292)
+    for m in range(16):
+        for b in range(4):
+            d, q, bs = _q8k_fields(out[m, b])
+            xb = x[m, 256 * b:256 * b + 256].astype(np.float64)
+            assert np.all(np.abs(q) <= 127)
+            err = np.abs(xb - float(d) * q)
+            assert err.max() <= abs(float(d)) * 0.5 * (1 + 1e-5)
+            assert np.array_equal(bs, q.reshape(16, 16).sum(1))
+            i = int(np.argmax(np.abs(xb)))             # first occurrence of the max
+            assert q[i] == -127
+
+
+def test_q8_k_nan_is_ignored_in_amax_and_coded_zero():
+    x = np.linspace(-1, 1, 256, dtype=np.float32)[None, :].copy()
+    x[0, 10] = np.nan
+    d, q, _ = _q8k_fields(oracle.quantize_q8_k(x)[0])
+    assert q[10] == 0 and np.isfinite(d) and q[0] == -127
+
+
+# --------------------------------------------------------------------------- Q8_1 quantizer
+
+
+def test_q8_1_bounds_zero_block_and_sum():
+    g = np.random.default_rng(8)
+    x = synth.activations(8, 256, g, outliers=True)
+    x[3, 32:64] = 0.0
+    out = oracle.quantize_q8_1(x).reshape(8, 8, 36)
+    for m in range(8):
+        for b in range(8):
+            blk = out[m, b]
+            xb = x[m, 32 * b:32 * b + 32]
+            d16 = blk[0:2].view(np.float16)[0]
+            s16 = blk[2:4].view(np.float16)[0]
+            q = blk[4:36].view(np.int8).astype(np.int64)
+            amax = np.float32(np.abs(xb).max())
+            dfull = np.float32(amax / np.float32(127.0))
+            assert d16 == np.float16(dfull)
+            if amax == 0:
+                assert not q.any() and float(s16) == 0.0
+                continue
+            err = np.abs(xb.astype(np.float64) - float(dfull) * q)
+            assert err.max() <= float(dfull) * 0.5 * (1 + 1e-5)
+            exact = math.fsum(float(v) for v in xb)
+            bound = 5 * 2.0 ** -24 * float(np.abs(xb).sum()) + abs(exact) * 2.0 ** -11 + 2.0 ** -24
+            assert abs(float(s16) - exact) <= bound + abs(float(s16)) * 2.0 ** -11
+
+
+def test_q8_1_roundf_half_away():
+    # amax = 127 -> d = 1 exactly; x = 2.5 -> roundf gives 3 (half away from zero), -0.5 -> -1
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, 0], x[0, 1], x[0, 2] = 127.0, 2.5, -0.5
+    blk = oracle.quantize_q8_1(x)[0]
+    q = blk[4:36].view(np.int8)
+    assert q[0] == 127 and q[1] == 3 and q[2] == -1
+
+
+# --------------------------------------------------------------------------- block dots
+
+
+def _integer_acts(M, K, g):
+    """Integer activations in [-127, 127] whose first max per 256 block is -127
+    (so Q8_K has iscale = 1, q = x, d = 1) -- also amax = 127 per 32 (Q8_1 d = 1)."""
+    x = g.integers(-126, 127, size=(M, K)).astype(np.float32)
+    x[:, ::32] = -127.0
+    return x
+
+
+def test_q8_0_unit_scales_is_integer_matmul():
+    g = np.random.default_rng(9)
+    M, N, K = 3, 5, 128
+    w = g.integers(-127, 128, size=(N, K))
+    wb = np.concatenate([np.concatenate([pack_q8_0(1.0, w[n, 32 * b:32 * b + 32]) for b in range(K // 32)])
+                         for n in range(N)])
+    x = _integer_acts(M, K, g)
+    xq = oracle.quantize_q8_1(x)
+    assert np.array_equal(xq.reshape(M, -1, 36)[:, :, 4:].view(np.int8).reshape(M, K), x.astype(np.int8))
+    y = oracle.gemm(oracle.Q8_0, wb, xq, M, N, K)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ w.T)
+
+
+def test_q4_k_unit_scales_is_integer_matmul():
+    g = np.random.default_rng(10)
+    M, N, K = 3, 4, 512
+    codes = g.integers(0, 16, size=(N, K))
+    wb = np.concatenate([np.concatenate([pack_q4_k(1.0, 0.0, [1] * 8, [0] * 8, codes[n, 256 * b:256 * b + 256])
+                                         for b in range(K // 256)]) for n in range(N)])
+    x = _integer_acts(M, K, g)
+    xq = oracle.quantize_q8_k(x)
+    y = oracle.gemm(oracle.Q4_K, wb, xq, M, N, K)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ codes.T)
+
+
+def test_q4_k_min_term_sign_and_bsums():
+    """d = 0, dmin = 1, m_j = 1: y = -sum(q), which exercises bsums and the minus sign."""
+    g = np.random.default_rng(11)
+    M, N, K = 2, 3, 256
+    wb = np.concatenate([pack_q4_k(0.0, 1.0, [5] * 8, [1] * 8, g.integers(0, 16, 256)) for _ in range(N)])
+    x = _integer_acts(M, K, g)
+    y = oracle.gemm(oracle.Q4_K, wb, oracle.quantize_q8_k(x), M, N, K)
+    want = -x.astype(np.int64).sum(1)
+    assert np.array_equal(y.astype(np.int64), np.repeat(want[:, None], N, 1))
+
+
+def test_q6_k_unit_scales_is_integer_matmul():
+    g = np.random.default_rng(12)
+    M, N, K = 3, 4, 512
+    codes = g.integers(0, 64, size=(N, K))
+    wb = np.concatenate([np.concatenate([pack_q6_k(1.0, [1] * 16, codes[n, 256 * b:256 * b + 256])
+                                         for b in range(K // 256)]) for n in range(N)])
+    x = _integer_acts(M, K, g)
+    y = oracle.gemm(oracle.Q6_K, wb, oracle.quantize_q8_k(x), M, N, K)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ (codes - 32).T)
+
+
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+def test_partials_identity_against_f64_dequant(dtype):
+    """sum_i deq_w(i) * deq_a(i) in f64 equals the scaled-integer identity built
+    from the oracle's int32 partials, to 1e-12 relative."""
+    g = np.random.default_rng(13 + dtype)
+    M, N, K = 2, 3, 512
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    xq = oracle.quantize_q8_1(x) if dtype == oracle.Q8_0 else oracle.quantize_q8_k(x)
+    P = oracle.partials(dtype, w, xq, M, N, K)
+    ad = oracle.ACT_DTYPE[dtype]
+    wd = oracle.dequant(dtype, w).reshape(N, K)
+    xd = oracle.dequant(ad, xq).reshape(M, K)
+    for m in range(M):
+        for n in range(N):
+            ref = float(np.dot(wd[n], xd[m]))
+            tot = 0.0
+            if dtype == oracle.Q8_0:
+                for b in range(K // 32):
+                    dw = float(w[n, 34 * b:34 * b + 2].view(np.float16)[0])
+                    da = float(xq[m, 36 * b:36 * b + 2].view(np.float16)[0])
+                    tot += dw * da * P[m, n, b]
+            else:
+                bb = 144 if dtype == oracle.Q4_K else 210
+                for b in range(K // 256):
+                    blk = w[n, bb * b:bb * b + bb]
+                    xb = xq[m, 292 * b:292 * b + 292]
+                    da = float(np.frombuffer(xb[0:4].tobytes(), np.float32)[0])
+                    bs = np.frombuffer(xb[260:292].tobytes(), np.int16).astype(np.int64)
+                    if dtype == oracle.Q4_K:
+                        s = blk[4:16].astype(np.int64)
+                        sc = [s[j] & 63 if j < 4 else (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4) for j in range(8)]
+                        mn = [s[j + 4] & 63 if j < 4 else (s[j + 4] >> 4) | ((s[j] >> 6) << 4) for j in range(8)]
+                        dw = float(blk[0:2].view(np.float16)[0])
+                        dmin = float(blk[2:4].view(np.float16)[0])
+                        sumi = sum(sc[j] * int(P[m, n, 8 * b + j]) for j in range(8))
+                        summ = sum(mn[j] * int(bs[2 * j] + bs[2 * j + 1]) for j in range(8))
+                        tot += da * (dw * sumi - dmin * summ)
+                    else:
+                        sc = blk[192:208].view(np.int8).astype(np.int64)
+                        dw = float(blk[208:210].view(np.float16)[0])
+                        tot += da * dw * sum(int(sc[j]) * int(P[m, n, 16 * b + j]) for j in range(16))
+            assert abs(tot - ref) <= 1e-12 * max(1.0, abs(ref)), (m, n, tot, ref)
+
+
+def _brute_force_f64(dtype, w, x_blocks, M, N, K):
+    """Independent pure-Python f64 evaluation from the canonical bytes."""
+    def unpack_w(row):
+        vals = []
+        if dtype == oracle.Q8_0:
+            for b in range(K // 32):
+                blk = row[34 * b:34 * b + 34]
+                d = float(blk[0:2].view(np.float16)[0])
+                vals += [d * int(v) for v in blk[2:34].view(np.int8)]
+            return vals
+        bb = 144 if dtype == oracle.Q4_K else 210
+        for b in range(K // 256):
+            blk = row[bb * b:bb * b + bb]
+            if dtype == oracle.Q4_K:
+                d = float(blk[0:2].view(np.float16)[0]); dm = float(blk[2:4].view(np.float16)[0])
+                s = [int(v) for v in blk[4:16]]
+                for i in range(256):
+                    j, c, r = i // 32, i // 64, i % 64
+                    sc = s[j] & 63 if j < 4 else (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4)
+                    mn = s[j + 4] & 63 if j < 4 else (s[j + 4] >> 4) | ((s[j] >> 6) << 4)
+                    byte = int(blk[16 + 32 * c + r % 32])
+                    code = byte & 15 if r < 32 else byte >> 4
+                    vals.append(d * sc * code - dm * mn)
+            else:
+                d = float(blk[208:210].view(np.float16)[0])
+                for i in range(256):
+                    h, r = i // 128, i % 128
+                    qtr, l = r // 32, r % 32
+                    lo = int(blk[64 * h + l + (32 if qtr & 1 else 0)])
+                    lo = lo >> 4 if qtr & 2 else lo & 15
+                    hi = (int(blk[128 + 32 * h + l]) >> (2 * qtr)) & 3
+                    vals.append(d * int(blk[192:208].view(np.int8)[i // 16]) * ((lo | hi << 4) - 32))
+        return vals
+
+    def unpack_x(row):
+        vals = []
+        if dtype == oracle.Q8_0:
+            for b in range(K // 32):
+                blk = row[36 * b:36 * b + 36]
+                d = float(blk[0:2].view(np.float16)[0])
+                vals += [d * int(v) for v in blk[4:36].view(np.int8)]
+        else:
+            for b in range(K // 256):
+                blk = row[292 * b:292 * b + 292]
+                d = float(np.frombuffer(blk[0:4].tobytes(), np.float32)[0])
+                vals += [d * int(v) for v in blk[4:260].view(np.int8)]
+        return vals
+
+    W = [unpack_w(w[n]) for n in range(N)]
+    X = [unpack_x(x_blocks[m]) for m in range(M)]
+    return np.array([[math.fsum(a * b for a, b in zip(X[m], W[n])) for n in range(N)] for m in range(M)])
+
+
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+def test_brute_force_tiny(dtype):
+    g = np.random.default_rng(20 + dtype)
+    M, N, K = 3, 4, 512
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g)
+    xq = oracle.quantize_q8_1(x) if dtype == oracle.Q8_0 else oracle.quantize_q8_k(x)
+    y = oracle.gemm(dtype, w, xq, M, N, K).astype(np.float64)
+    ref = _brute_force_f64(dtype, w, xq, M, N, K)
+    scale = np.abs(ref).max()
+    assert np.abs(y - ref).max() <= 1e-5 * scale
+
+
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+def test_f64_band_and_zero_input(dtype):
+    g = np.random.default_rng(30 + dtype)
+    M, N, K = 8, 64, 1024
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    qf = oracle.quantize_q8_1 if dtype == oracle.Q8_0 else oracle.quantize_q8_k
+    xq = qf(x)
+    y = oracle.gemm(dtype, w, xq, M, N, K).astype(np.float64)
+    wd = oracle.dequant(dtype, w).reshape(N, K)
+    xd = oracle.dequant(oracle.ACT_DTYPE[dtype], xq).reshape(M, K)
+    y64 = xd @ wd.T
+    rel = np.linalg.norm(y - y64) / np.linalg.norm(y64)
+    assert rel <= 5e-4          # the pages' f64 dequant band
+    assert rel <= 1e-6          # what exact integer dots + fp32 scaling actually give
+    yz = oracle.gemm(dtype, w, qf(np.zeros((M, K), np.float32)), M, N, K)
+    assert np.all(yz == 0.0)
+
+
+# --------------------------------------------------------------------------- grouped + weighted sum
+
+
+def test_grouped_reduces_to_dense_and_per_row_arm():
+    g = np.random.default_rng(40)
+    E, M, N, K = 3, 5, 16, 512
+    w = synth.weights(oracle.Q4_K, E * N, K, g)
+    x = synth.activations(M, K, g)
+    xq = oracle.quantize_q8_k(x)
+    ids = np.zeros((M, 1), np.int32)
+    y, bad = oracle.gemm_grouped(oracle.Q4_K, w, E, xq, 1, ids, M, 1, N, K)
+    dense = oracle.gemm(oracle.Q4_K, w[:N], xq, M, N, K)
+    assert bad == 0 and np.array_equal(y[:, 0, :], dense)
+    # per-row arm: slot (t, k) reads activation row t*top_k + k
+    top_k = 2
+    ids = np.array([[t % E, (t + 1) % E] for t in range(M)], np.int32)
+    xr = synth.activations(M * top_k, K, g)
+    xrq = oracle.quantize_q8_k(xr)
+    y2, _ = oracle.gemm_grouped(oracle.Q4_K, w, E, xrq, top_k, ids, M, top_k, N, K)
+    for t in range(M):
+        for k in range(top_k):
+            e = ids[t, k]
+            ref = oracle.gemm(oracle.Q4_K, w[e * N:(e + 1) * N], xrq[t * top_k + k:t * top_k + k + 1], 1, N, K)
+            assert np.array_equal(y2[t, k], ref[0])
+
+
+def test_grouped_invalid_ids_counted_and_untouched():
+    g = np.random.default_rng(41)
+    E, M, N, K = 2, 3, 8, 256
+    w = synth.weights(oracle.Q6_K, E * N, K, g)
+    xq = oracle.quantize_q8_k(synth.activations(M, K, g))
+    ids = np.array([[0, 5], [-1, 1], [1, 0]], np.int32)
+    y, bad = oracle.gemm_grouped(oracle.Q6_K, w, E, xq, 1, ids, M, 2, N, K)
+    assert bad == 2
+    assert np.isnan(y[0, 1]).all() and np.isnan(y[1, 0]).all() and np.isfinite(y[2]).all()
+
+
+def test_weighted_sum_one_hot_and_f64_bound():
+    g = np.random.default_rng(42)
+    M, top_k, N = 4, 8, 64
+    ys = g.standard_normal((M, top_k, N)).astype(np.float32)
+    onehot = np.zeros((M, top_k), np.float32)
+    onehot[np.arange(M), np.arange(M) % top_k] = 1.0
+    out = oracle.moe_weighted_sum(ys, onehot)
+    assert np.array_equal(out, ys[np.arange(M), np.arange(M) % top_k])
+    _, w = synth.routing(M, 16, top_k, g)
+    out = oracle.moe_weighted_sum(ys, w).astype(np.float64)
+    ref = np.einsum("tk,tkn->tn", w.astype(np.float64), ys.astype(np.float64))
+    bound = 2 * top_k * 2.0 ** -24 * np.einsum("tk,tkn->tn", np.abs(w), np.abs(ys)).astype(np.float64)
+    assert np.all(np.abs(out - ref) <= bound)
+
+
+def test_swiglu_against_f64():
+    g = np.random.default_rng(43)
+    gg = (g.standard_normal((4, 256)) * 4).astype(np.float32)
+    uu = g.standard_normal((4, 256)).astype(np.float32)
+    h = oracle.swiglu(gg, uu).astype(np.float64)
+    g64, u64 = gg.astype(np.float64), uu.astype(np.float64)
+    ref = g64 / (1 + np.exp(-g64)) * u64
+    assert np.all(np.abs(h - ref) <= 8 * 2.0 ** -24 * np.abs(ref) + 1e-30)
+
+
+def test_routing_generator_shapes():
+    g = np.random.default_rng(44)
+    ids, w = synth.routing(64, 256, 8, g)
+    assert ids.shape == (64, 8) and all(len(set(r)) == 8 for r in ids)
+    assert np.allclose(w.sum(1), 1.0, atol=1e-6) and (ids >= 0).all() and (ids < 256).all()
+
+
+def test_q8_k_half_way_ties_go_to_even():
+    """mx = -127 gives iscale = 1 exactly, so x = n + 1/2 is an exact tie:
+    the nearest-integer reading is round-half-to-even (2.5 -> 2, 3.5 -> 4)."""
+    x = np.zeros((1, 256), dtype=np.float32)
+    x[0, 0] = -127.0
+    halves = np.arange(-60, 60) + 0.5
+    x[0, 1:1 + halves.size] = halves
+    d, q, _ = _q8k_fields(oracle.quantize_q8_k(x)[0])
+    assert d == 1.0
+    want = [math.floor(v) + (math.floor(v) % 2) for v in halves]   # the even neighbour of each tie
+    assert list(q[1:1 + halves.size]) == want
