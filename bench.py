@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the keep-quant int8 matmul path on GB300.
+
+Default workload ("prefill"): the six Q4_K/Q6_K weight shapes [4096x4096],
+[14336x4096], [4096x14336] at M = 128, 512 and 2048 tokens (18 GEMMs per
+step).  One step = for every (M, dtype, shape): quantise X[M, K] (fp32, N(0,1)
+with 1% x10 outliers) to Q8_K, then the GEMM Y = X . W^T.  `value` is the
+whole-step int8-equivalent throughput, sum(2*M*N*K) / step time, in TOPS.
+
+The same JSON line carries the decode GEMV (M = 1, fused activation quant) on
+Q4_K [9728x2560], Q4_K [2560x9728] and Q6_K [2560x9728]: 1000 back-to-back
+calls per shape, captured in a CUDA graph, each call reading a different copy
+of the weight (copies totalling >= 3x the L2 size), reported as weight GB/s.
+
+Multi-GPU: the path does not shard (each GPU runs independent replicas of the
+workload, no collective on the data path); `--gpus N` under torchrun runs N
+replicas, value = total work / max time over ranks (weak scaling).
+
+`--impl reference` times the CPU oracle (plain C, all host cores) on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "Q4_K/Q6_K GEMM int8 TOPS at prefill; GEMV weight GB/s vs HBM peak"
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks sampler
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+def prefill_cases():
+    from gemv_quantize_q8_gb300 import synth
+    cases = []
+    for M in synth.PREFILL_M:
+        for dtype in (synth.Q4_K, synth.Q6_K):
+            for (N, K) in synth.PREFILL_SHAPES:
+                cases.append((M, dtype, N, K))
+    return cases
+
+
+def build_prefill_inputs(device, only=None):
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    from gemv_quantize_q8_gb300 import synth
+    g = synth.rng(0)
+    weights = {}
+    for dtype in (synth.Q4_K, synth.Q6_K):
+        for (N, K) in synth.PREFILL_SHAPES:
+            if only and (dtype, N, K) not in {(c[1], c[2], c[3]) for c in only}:
+                continue
+            wc = torch.from_numpy(synth.weights(dtype, N, K, g).reshape(-1)).to(device)
+            wn = torch.empty(kq.native_bytes(dtype, N, K), dtype=torch.uint8, device=device)
+            kq.kq_repack_weights(dtype, wc, wn, N, K)
+            weights[(dtype, N, K)] = wn
+            del wc
+    Kmax = max(K for (_, K) in synth.PREFILL_SHAPES)
+    Mmax = max(synth.PREFILL_M)
+    x_host = synth.activations(Mmax, Kmax, g, outliers=True)
+    return weights, x_host
+
+
+def run_prefill(args, device, rank, world):
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    cases = prefill_cases()
+    if args.only:
+        dt = {"q4_k": 1, "q6_k": 2}[args.only.split(":")[0]]
+        nk, m = args.only.split(":")[1], int(args.only.split(":")[2])
+        N, K = (int(v) for v in nk.split("x"))
+        cases = [(m, dt, N, K)]
+    weights, x_host = build_prefill_inputs(device, only=cases if args.only else None)
+    Mmax, Kmax = x_host.shape
+    x_dev = torch.from_numpy(x_host).to(device)
+    x_pin = torch.from_numpy(x_host).pin_memory()
+    max_y = max(M * N for (M, _, N, _) in cases)
+    y = torch.empty(max_y, dtype=torch.float32, device=device)
+    y_pin = torch.empty(max_y, dtype=torch.float32).pin_memory()
+    xq = torch.empty(max(kq.q8k_bytes(M, K) for (M, _, _, K) in cases), dtype=torch.uint8, device=device)
+    ws_need = max(kq.gemm_workspace_bytes(dt, M, N, K) for (M, dt, N, K) in cases)
+    ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    ops = sum(2.0 * M * N * K for (M, _, N, K) in cases)
+
+    def step(events=None):
+        for i, (M, dt, N, K) in enumerate(cases):
+            kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)           # X[:M, :K] (row stride Kmax)
+            if events is not None:
+                events[i][0].record(stream)
+            kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, y, N, ws, ws_need)
+            if events is not None:
+                events[i][1].record(stream)
+
+    def step_e2e():
+        for (M, dt, N, K) in cases:
+            xd = x_dev[:M, :K]
+            xd.copy_(x_pin[:M, :K], non_blocking=True)           # host -> device, pinned
+            kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)
+            kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, y, N, ws, ws_need)
+            y_pin[:M * N].copy_(y[:M * N], non_blocking=True)     # device -> host, pinned
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches0 = kq.launch_count()
+    clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
+    if rank == 0:
+        clocks.start()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cases]
+          for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    launches = kq.launch_count() - launches0
+    ms = t0.elapsed_time(t1) / args.steps
+    gemm_ms = sum(a.elapsed_time(b) for row in ev for (a, b) in row) / args.steps
+    # per-case kernel times (ms) for the report
+    per_case = {}
+    for i, (M, dt, N, K) in enumerate(cases):
+        t = statistics.median(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
+        per_case[f"{'q4_k' if dt == 1 else 'q6_k'}_{N}x{K}_m{M}"] = round(2.0 * M * N * K / (t * 1e-3) / 1e12, 2)
+
+    # end to end through the C ABI with host buffers
+    for _ in range(max(1, args.warmup // 2)):
+        step_e2e()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = sum(M * K * 4 for (M, _, _, K) in cases)
+    d2h = sum(M * N * 4 for (M, _, N, _) in cases)
+    return dict(ops=ops, ms=ms, gemm_ms=gemm_ms, per_case=per_case, clocks=clk, launches=launches,
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, cases=cases)
+
+
+def run_decode(args, device, calls=1000):
+    """1000 back-to-back fused-quant GEMV calls per shape from a CUDA graph; weight copies rotate."""
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    from gemv_quantize_q8_gb300 import synth
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    g = synth.rng(0)
+    out = {}
+    total_bytes = 0.0
+    total_ms = 0.0
+    for cfg in synth.DECODE:
+        dtype, N, K = cfg["dtype"], cfg["N"], cfg["K"]
+        wc = torch.from_numpy(synth.weights(dtype, N, K, g).reshape(-1)).to(device)
+        nb = kq.native_bytes(dtype, N, K)
+        copies = max(3, -(-3 * l2 // nb))
+        ws = torch.empty((copies, nb), dtype=torch.uint8, device=device)
+        for c in range(copies):
+            kq.kq_repack_weights(dtype, wc, ws[c], N, K)
+        x = torch.from_numpy(synth.activations(1, K, g)).to(device)
+        y = torch.empty(N, dtype=torch.float32, device=device)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(3):
+                kq.kq_gemv(dtype, ws[i % copies], x, None, N, K, y)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(calls):
+                kq.kq_gemv(dtype, ws[i % copies], x, None, N, K, y)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            reps.append(a.elapsed_time(b))
+        ms = statistics.median(reps)
+        wbytes = N * (K // 256) * (144 if dtype == synth.Q4_K else 210)
+        algo = wbytes + K * 4 + N * 4
+        us = ms * 1e3 / calls
+        out[cfg["name"]] = {"us_per_call": round(us, 3), "gbs": round(algo / (us * 1e-6) / 1e9, 1),
+                            "weight_copies": copies}
+        total_bytes += algo * calls
+        total_ms += ms
+        del ws, graph
+        torch.cuda.empty_cache()
+    return out, total_bytes / (total_ms * 1e-3) / 1e9
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The CPU oracle as it stands, all host threads, on a bounded sample of the prefill workload:
+    the first `m` token rows of every (dtype, shape) GEMM (quantisation included)."""
+    import oracle
+    from gemv_quantize_q8_gb300 import synth
+    oracle.build()
+    threads = oracle.max_threads()
+    g = synth.rng(0)
+    ws = {(dt, N, K): synth.weights(dt, N, K, g) for dt in (synth.Q4_K, synth.Q6_K) for (N, K) in synth.PREFILL_SHAPES}
+    x = synth.activations(64, max(K for _, K in synth.PREFILL_SHAPES), g, outliers=True)
+    m, ops, el = 1, 0.0, 0.0
+    while True:
+        t = time.perf_counter()
+        ops_i = 0.0
+        for (dt, N, K), w in ws.items():
+            xq = oracle.quantize_q8_k(x[:m, :K])
+            oracle.gemm(dt, w, xq, m, N, K, threads=threads)
+            ops_i += 2.0 * m * N * K
+        dt_ = time.perf_counter() - t
+        ops, el = ops_i, dt_
+        if dt_ * 2.2 > budget_s or m >= 64:
+            break
+        m *= 2
+    return {"value": ops / el / 1e12, "unit": "TOPS", "cores": threads, "kind": "oracle",
+            "sample": f"first {m} token rows of each of the 6 Q4_K/Q6_K prefill GEMMs, quantize included "
+                      f"({ops:.3g} int8 ops in {el:.2f} s)"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(budget_s=4.0)
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(budget_s=4.0))
+    v = statistics.median(b["value"] for b in vals)
+    last = vals[-1]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": "prefill_q4_k_q6_k_6shapes_m128_512_2048", "sample": last["sample"]},
+            "cpu_baseline": {"value": v, "unit": "TOPS", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": v, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
+    ap.add_argument("--only", default=None, help="profile one GEMM, e.g. q4_k:4096x4096:512")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    device = torch.device(f"cuda:{local}")
+    from gemv_quantize_q8_gb300 import build as kqbuild
+    if rank == 0:
+        kqbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    res = run_prefill(args, device, rank, world)
+    ms = res["ms"]
+    e2e_ms = res["e2e_ms"]
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    decode = None
+    if not args.no_decode and not args.only:
+        decode, decode_gbs = run_decode(args, device)
+    if rank == 0:
+        pk, src = peaks()
+        value = world * res["ops"] / (ms * 1e-3) / 1e12
+        gemm_tops = res["ops"] / (res["gemm_ms"] * 1e-3) / 1e12
+        tensor_peak = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": "prefill_q4_k_q6_k_6shapes_m128_512_2048" if not args.only else args.only,
+                       "gemms_per_step": len(res["cases"]), "activation": "fp32 N(0,1), 1% x10 outliers, Q8_K",
+                       "l2": "step working set > 0.5 GB vs 129 MB L2; a weight recurs only after 5 other GEMMs",
+                       "parallelism": f"replicas x{world}"},
+            "e2e": {"value": round(world * res["ops"] / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TOPS",
+                    "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+            "gpu_launches": res["launches"],
+            "roofline": {"bound": "tensor", "achieved": round(gemm_tops, 2), "peak": tensor_peak,
+                         "unit": "TFLOP/s", "frac": round(gemm_tops / tensor_peak, 4), "traffic": None,
+                         "kernel": "kq_gemm (all 18 prefill GEMMs)",
+                         "peak_source": f"{src} bf16_tflops_sustained (f16 tensor rate = bf16 rate)"},
+            "per_gemm_tops": res["per_case"],
+            "clocks": res["clocks"],
+        }
+        if decode is not None:
+            hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
+            line["decode_gemv"] = {"gbs": round(decode_gbs, 1), "frac_of_hbm": round(decode_gbs / hbm, 4),
+                                   "hbm_peak_gbs": hbm, "peak_source": src, "shapes": decode}
+        if not args.no_cpu and not args.only:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,282 @@
+// kq_gemm.cu -- C ABI of the matmul entry points: dense GEMM dispatch, debug partials, routed-expert
+// GEMM (routing compaction + per-expert tiles), device flag, weighted expert sum.
+//
+// Routed experts follow strix-llama.cpp PR #18 ("Optimize ROCM Prefill and Decode"): the
+// (token, slot) pairs are compacted per expert and each expert gets tiles sized by ITS row count,
+// not by the total number of pairs (the routed-compact commit's lesson: a tile chosen from the total
+// left 50-87% of every tile as padding).  The compaction is a stable per-expert scan, so the row
+// order -- and the result -- is deterministic.
+#include "kq_internal.cuh"
+#include "kq_mmq_exact.cuh"
+#include "kq_tc.cuh"
+
+namespace kq {
+
+constexpr int kTileM = 64;
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct GroupedWs {
+    size_t off_flag, off_tile_count, off_count, off_offset, off_tiles, off_lists, total;
+    int64_t max_tiles;
+};
+
+static GroupedWs grouped_ws(int64_t M, int64_t top_k, int64_t E) {
+    GroupedWs w{};
+    const int64_t pairs = M * top_k;
+    w.max_tiles = (pairs + kTileM - 1) / kTileM + E;
+    size_t o = 0;
+    w.off_flag = o; o += align256(sizeof(long long));
+    w.off_tile_count = o; o += align256(sizeof(int));
+    w.off_count = o; o += align256(sizeof(int) * E);
+    w.off_offset = o; o += align256(sizeof(int) * E);
+    w.off_tiles = o; o += align256(sizeof(int) * 2 * w.max_tiles);
+    w.off_lists = o; o += align256(sizeof(int) * pairs);
+    w.total = o;
+    return w;
+}
+
+// One block per expert: number of pairs routed to it.  Block 0 also counts invalid ids.
+__global__ void route_count_kernel(const int32_t *__restrict__ ids, int64_t pairs, int E, int *__restrict__ count,
+                                   long long *__restrict__ flag) {
+    __shared__ int red[256];
+    __shared__ int bad_red[256];
+    const int e = blockIdx.x;
+    int c = 0, bad = 0;
+    for (int64_t p = threadIdx.x; p < pairs; p += blockDim.x) {
+        const int id = ids[p];
+        c += id == e;
+        bad += (id < 0 || id >= E);
+    }
+    red[threadIdx.x] = c;
+    bad_red[threadIdx.x] = bad;
+    __syncthreads();
+    for (int s = 128; s > 0; s >>= 1) {
+        if (threadIdx.x < s) {
+            red[threadIdx.x] += red[threadIdx.x + s];
+            bad_red[threadIdx.x] += bad_red[threadIdx.x + s];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        count[e] = red[0];
+        if (e == 0) *flag = bad_red[0];
+    }
+}
+
+// Single block: exclusive scan of the counts and the tile table (expert, first row) per expert.
+__global__ void route_scan_kernel(const int *__restrict__ count, int E, int *__restrict__ offset,
+                                  int *__restrict__ tiles, int *__restrict__ tile_count) {
+    if (threadIdx.x != 0) return;
+    int off = 0, nt = 0;
+    for (int e = 0; e < E; ++e) {
+        offset[e] = off;
+        const int c = count[e];
+        for (int s = 0; s < c; s += kTileM) {
+            tiles[2 * nt] = e;
+            tiles[2 * nt + 1] = s;
+            ++nt;
+        }
+        off += c;
+    }
+    *tile_count = nt;
+}
+
+// One block per expert: stable compaction of its pairs, in ascending pair order.
+__global__ void route_fill_kernel(const int32_t *__restrict__ ids, int64_t pairs, const int *__restrict__ offset,
+                                  int *__restrict__ lists) {
+    __shared__ int scan[256];
+    const int e = blockIdx.x;
+    int base = offset[e];
+    for (int64_t p0 = 0; p0 < pairs; p0 += blockDim.x) {
+        const int64_t p = p0 + threadIdx.x;
+        const int f = (p < pairs && ids[p] == e) ? 1 : 0;
+        scan[threadIdx.x] = f;
+        __syncthreads();
+        for (int s = 1; s < 256; s <<= 1) {  // inclusive Hillis-Steele scan
+            int v = threadIdx.x >= s ? scan[threadIdx.x - s] : 0;
+            __syncthreads();
+            scan[threadIdx.x] += v;
+            __syncthreads();
+        }
+        if (f) lists[base + scan[threadIdx.x] - 1] = (int)p;
+        const int tot = scan[255];
+        __syncthreads();
+        base += tot;
+    }
+}
+
+// out[t][n] = w[t][0]*y[t][0][n] + ... in slot order, products rounded before each add.
+template <bool VEC>
+__global__ void weighted_sum_kernel(const float *__restrict__ ys, const float *__restrict__ w, int64_t M, int top_k,
+                                    int64_t N, float *__restrict__ out) {
+    const int64_t per_row = VEC ? N / 4 : N;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M * per_row) return;
+    const int64_t t = i / per_row, j = i % per_row;
+    const float *wt = w + t * top_k;
+    if (VEC) {
+        const float4 *y4 = reinterpret_cast<const float4 *>(ys + t * top_k * N) + j;
+        float4 v = y4[0];
+        const float w0 = wt[0];
+        float4 acc = make_float4(__fmul_rn(w0, v.x), __fmul_rn(w0, v.y), __fmul_rn(w0, v.z), __fmul_rn(w0, v.w));
+        for (int k = 1; k < top_k; ++k) {
+            v = y4[k * (N / 4)];
+            const float wk = wt[k];
+            acc.x = __fadd_rn(acc.x, __fmul_rn(wk, v.x));
+            acc.y = __fadd_rn(acc.y, __fmul_rn(wk, v.y));
+            acc.z = __fadd_rn(acc.z, __fmul_rn(wk, v.z));
+            acc.w = __fadd_rn(acc.w, __fmul_rn(wk, v.w));
+        }
+        reinterpret_cast<float4 *>(out + t * N)[j] = acc;
+    } else {
+        const float *yr = ys + t * top_k * N + j;
+        float acc = __fmul_rn(wt[0], yr[0]);
+        for (int k = 1; k < top_k; ++k) acc = __fadd_rn(acc, __fmul_rn(wt[k], yr[k * N]));
+        out[t * N + j] = acc;
+    }
+}
+
+static kq_status check_matmul_args(const char *name, kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N,
+                                   int64_t K) {
+    if (wt != KQ_Q4_K && wt != KQ_Q6_K && wt != KQ_Q8_0)
+        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "%s: weight dtype %s is not Q4_K, Q6_K or Q8_0", name, dtype_name(wt));
+    if (!w || !xq) return fail(KQ_ERR_INVALID_ARG, "%s: null pointer", name);
+    if (M <= 0 || N <= 0 || K <= 0 || K % 256)
+        return fail(KQ_ERR_INVALID_ARG, "%s: need M, N > 0 and K a positive multiple of 256 (M=%lld N=%lld K=%lld)",
+                    name, (long long)M, (long long)N, (long long)K);
+    if (!aligned(w, 16)) return fail(KQ_ERR_ALIGNMENT, "%s: w must be 16-byte aligned", name);
+    if (!aligned(xq, 4)) return fail(KQ_ERR_ALIGNMENT, "%s: xq must be 4-byte aligned", name);
+    return KQ_OK;
+}
+
+}  // namespace kq
+
+using namespace kq;
+
+extern "C" {
+
+size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K, int64_t n_experts, int64_t top_k) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    if (n_experts > 0) return grouped_ws(M, top_k > 0 ? top_k : 1, n_experts).total;
+    return tc_workspace_bytes(wt, M, N, K);
+}
+
+kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                  void *workspace, size_t ws_bytes, kq_stream_t stream) {
+    kq_status s = check_matmul_args("kq_gemm", wt, w, xq, M, N, K);
+    if (s != KQ_OK) return s;
+    if (!y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: null y");
+    if (ldy < N) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: ldy %lld < N %lld", (long long)ldy, (long long)N);
+    if (!aligned(y, 4)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm: y must be 4-byte aligned");
+    const size_t need = kq_gemm_workspace_bytes(wt, M, N, K, 0, 0);
+    if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(KQ_ERR_WORKSPACE, "kq_gemm: workspace of %zu bytes needed, %zu given", need, workspace ? ws_bytes : 0);
+    if (workspace && !aligned(workspace, 256)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm: workspace must be 256-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (tc_eligible(wt, M, N, K))
+        return tc_gemm(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
+                       static_cast<uint8_t *>(workspace), st);
+    MmqExactArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy;
+    const int64_t gy = (M + kTileM - 1) / kTileM;
+    if (gy > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: M=%lld too large", (long long)M);
+    return launch_mmq_exact(wt, 0, false, a, (unsigned)gy, st);
+}
+
+kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,
+                            int32_t *partials, kq_stream_t stream) {
+    kq_status s = check_matmul_args("kq_debug_partials", wt, w, xq, M, N, K);
+    if (s != KQ_OK) return s;
+    if (!partials) return fail(KQ_ERR_INVALID_ARG, "kq_debug_partials: null partials");
+    MmqExactArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.M = M; a.N = N; a.K = K; a.partials = partials;
+    const int64_t gy = (M + kTileM - 1) / kTileM;
+    if (gy > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_debug_partials: M=%lld too large", (long long)M);
+    return launch_mmq_exact(wt, 1, false, a, (unsigned)gy, (cudaStream_t)stream);
+}
+
+kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const void *xq, int64_t xq_rows_per_token,
+                          const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y, void *workspace,
+                          size_t ws_bytes, kq_stream_t stream) {
+    kq_status s = check_matmul_args("kq_gemm_grouped", wt, w, xq, M, N, K);
+    if (s != KQ_OK) return s;
+    if (!ids || !y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: null ids or y");
+    if (n_experts <= 0 || top_k <= 0 || n_experts > 65535)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: need 0 < n_experts <= 65535 and top_k > 0");
+    if (xq_rows_per_token != 1 && xq_rows_per_token != top_k)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: xq_rows_per_token must be 1 or top_k");
+    if (N % 16) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: N=%lld must be a multiple of 16", (long long)N);
+    if (M * top_k > (int64_t)1 << 30) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: too many (token, slot) pairs");
+    if (!aligned(ids, 4) || !aligned(y, 4)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm_grouped: ids/y must be 4-byte aligned");
+    const GroupedWs L = grouped_ws(M, top_k, n_experts);
+    if (!workspace || ws_bytes < L.total)
+        return fail(KQ_ERR_WORKSPACE, "kq_gemm_grouped: workspace of %zu bytes needed, %zu given", L.total,
+                    workspace ? ws_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm_grouped: workspace must be 256-byte aligned");
+    if (L.max_tiles > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: too many tiles");
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    long long *flag = reinterpret_cast<long long *>(ws + L.off_flag);
+    int *tile_count = reinterpret_cast<int *>(ws + L.off_tile_count);
+    int *count = reinterpret_cast<int *>(ws + L.off_count);
+    int *offset = reinterpret_cast<int *>(ws + L.off_offset);
+    int *tiles = reinterpret_cast<int *>(ws + L.off_tiles);
+    int *lists = reinterpret_cast<int *>(ws + L.off_lists);
+    const int64_t pairs = M * top_k;
+    route_count_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, (int)n_experts, count, flag);
+    route_scan_kernel<<<1, 32, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count);
+    route_fill_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, offset, lists);
+    s = check_launch("kq_gemm_grouped routing");
+    if (s != KQ_OK) return s;
+    count_launch(R_ROUTE, 3);
+    MmqExactArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = N;
+    a.tile_count = tile_count; a.tiles = tiles; a.expert_count = count; a.expert_offset = offset; a.lists = lists;
+    a.rows_per_token = (int)xq_rows_per_token;
+    a.top_k = (int)top_k;
+    return launch_mmq_exact(wt, 0, true, a, (unsigned)L.max_tiles, st);
+}
+
+kq_status kq_read_device_flag(void *workspace, int64_t *n_bad, kq_stream_t stream) {
+    if (!workspace) return fail(KQ_ERR_INVALID_ARG, "kq_read_device_flag: null workspace");
+    long long v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_read_device_flag: %s", cudaGetErrorString(e));
+    if (n_bad) *n_bad = v;
+    if (v != 0) {
+        long long zero = 0;
+        e = cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, (cudaStream_t)stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+        if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_read_device_flag: %s", cudaGetErrorString(e));
+        return fail(KQ_ERR_DEVICE_FLAG, "kq_read_device_flag: %lld (token, slot) pairs had an expert id out of range", v);
+    }
+    return KQ_OK;
+}
+
+kq_status kq_moe_weighted_sum(const float *y_slots, const float *w, int64_t M, int64_t top_k, int64_t N, float *out,
+                              kq_stream_t stream) {
+    if (!y_slots || !w || !out) return fail(KQ_ERR_INVALID_ARG, "kq_moe_weighted_sum: null pointer");
+    if (M <= 0 || top_k <= 0 || N <= 0 || top_k > 1024)
+        return fail(KQ_ERR_INVALID_ARG, "kq_moe_weighted_sum: need M, N > 0 and 0 < top_k <= 1024");
+    if (!aligned(y_slots, 4) || !aligned(w, 4) || !aligned(out, 4))
+        return fail(KQ_ERR_ALIGNMENT, "kq_moe_weighted_sum: pointers must be 4-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool vec = N % 4 == 0 && aligned(y_slots, 16) && aligned(out, 16);
+    const int64_t items = vec ? M * (N / 4) : M * N;
+    const int64_t grid = (items + 255) / 256;
+    if (vec) weighted_sum_kernel<true><<<(unsigned)grid, 256, 0, st>>>(y_slots, w, M, (int)top_k, N, out);
+    else weighted_sum_kernel<false><<<(unsigned)grid, 256, 0, st>>>(y_slots, w, M, (int)top_k, N, out);
+    kq_status s = check_launch("kq_moe_weighted_sum");
+    if (s == KQ_OK) count_launch(R_WSUM);
+    return s;
+}
+
+}  // extern "C"

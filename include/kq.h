@@ -1,0 +1,202 @@
+/*
+ * kq.h -- C ABI of the keep-quant int8 matmul library for GB300 (sm_103a).
+ *
+ * Block-quantised weights (Q4_K, Q6_K, Q8_0) stay packed in device memory;
+ * activations are quantised on the fly to Q8_K (256-element blocks) or Q8_1
+ * (32-element blocks) and multiplied with integer dot products, scaled into
+ * fp32.  Sources of the operations (prose descriptions on three pages):
+ *   [vllm-2890]  vllm.cpp PR #2890 "fuse silu-mul with Q8_K quant epilogue
+ *                (VT_SILU_QUANT_FUSED)" -- Q8_K quantizer, keep-quant provider,
+ *                MMVQ decode GEMV, fused SiLU-mul + quant.
+ *   [vllm-3035]  vllm.cpp PR #3035 "scope a cooperative activation share for
+ *                the WMMA kernels" -- prefill GEMM with one activation tile
+ *                staged once per block and shared by all warps.
+ *   [llama-18]   strix-llama.cpp PR #18 "Optimize ROCM Prefill and Decode" --
+ *                Q8_1 quantizer, fused-quant MMVQ, routed-expert MMQ
+ *                (MUL_MAT_ID), weighted expert sum.
+ *
+ * Conventions (every entry point):
+ *   - All pointers named w, x, xq, y, g, u, ids, workspace... are DEVICE
+ *     pointers unless stated; the caller owns every buffer.  The library
+ *     allocates nothing and keeps no state between calls.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream) and is
+ *     asynchronous: no entry point synchronises, except kq_read_device_flag.
+ *   - Return value: KQ_OK, or an error status without launching anything;
+ *     kq_last_error() then holds a one-line, thread-local description that
+ *     names the offending argument or dtype.  A CUDA launch failure returns
+ *     KQ_ERR_CUDA.  Unsupported dtypes are rejected, never routed elsewhere.
+ *   - Results are deterministic: no atomics in any reduction.
+ *   - Sizes are elements unless named *_bytes.  K must be a multiple of 256
+ *     for every path (all K-quant super-blocks, and Q8_0 rows are grouped in
+ *     256-element chunks in the native layout).
+ *
+ * Canonical (GGUF-style) block layouts, little-endian:
+ *   Q4_K (144 B / 256): f16 d, f16 dmin, 12 bytes of packed 6-bit sub-block
+ *        scales and mins (8 each), 128 bytes of 4-bit codes; element 64c+l is
+ *        the low nibble and 64c+32+l the high nibble of code byte 32c+l.
+ *        x = d*sc_j*c - dmin*m_j, j = sub-block of 32.
+ *   Q6_K (210 B / 256): ql[128], qh[64], int8 scales[16], f16 d;
+ *        x = d*sc_j*(c - 32), j = sub-block of 16.
+ *   Q8_0 (34 B / 32):   f16 d, int8 w[32]; x = d*w.
+ *   Q8_K (292 B / 256): f32 d, int8 q[256], int16 bsums[16] (sums of 16 q).
+ *   Q8_1 (36 B / 32):   f16 d, f16 s (block sum of the input), int8 q[32].
+ *
+ * Native weight layout (what the matmul entry points consume; produced by
+ * kq_repack_weights): rows are taken in groups of 16 (the last group is
+ * padded with zero rows) and each group is stored as consecutive chunks of
+ * 256 elements along K.  A chunk holds the 16 rows' fields as planes:
+ *   Q4_K chunk (2304 B): codes [16][128], then headers [16][16] (d, dmin,
+ *        12 scale/min bytes -- the first 16 bytes of the canonical block).
+ *   Q6_K chunk (3360 B): codes [16][192] (ql then qh), scales [16][16],
+ *        d [16] (f16).
+ *   Q8_0 chunk (4352 B): codes [16][256], d [16][8] (f16).
+ * Every chunk starts on a 16-byte boundary when the buffer does.
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KQ_API __attribute__((visibility("default")))
+#else
+#define KQ_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *kq_stream_t; /* same handle as cudaStream_t */
+
+typedef enum { KQ_Q4_K = 1, KQ_Q6_K = 2, KQ_Q8_0 = 3, KQ_Q8_K = 4, KQ_Q8_1 = 5 } kq_dtype;
+
+typedef enum {
+    KQ_OK = 0,
+    KQ_ERR_INVALID_ARG = 1,       /* null pointer, negative/zero size, K not a multiple of 256, bad ld */
+    KQ_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not handled by this entry point (named in kq_last_error) */
+    KQ_ERR_ALIGNMENT = 3,         /* a pointer or leading dimension breaks the stated alignment */
+    KQ_ERR_WORKSPACE = 4,         /* workspace missing or smaller than *_workspace_bytes */
+    KQ_ERR_CUDA = 5,              /* a CUDA call failed (message in kq_last_error) */
+    KQ_ERR_DEVICE_FLAG = 6        /* a kernel recorded an invalid input (e.g. an expert id out of range) */
+} kq_status;
+
+/* Static description of a status.  Never NULL. */
+KQ_API const char *kq_status_string(kq_status s);
+
+/* Thread-local detail of the last failing call on this host thread ("" if none). */
+KQ_API const char *kq_last_error(void);
+
+/* Library ABI version (major*100 + minor). */
+KQ_API int kq_version(void);
+
+/* Elements per canonical block (256 or 32) and bytes per canonical block; 0 for an unknown dtype. */
+KQ_API int64_t kq_block_elems(kq_dtype dtype);
+KQ_API int64_t kq_block_bytes(kq_dtype dtype);
+
+/* Bytes of one canonical row of K elements (K/block_elems * block_bytes); 0 if K is not a block multiple. */
+KQ_API int64_t kq_row_bytes(kq_dtype dtype, int64_t K);
+
+/* Bytes of the native layout for an [N, K] weight (N padded to a multiple of 16). 0 if unsupported. */
+KQ_API int64_t kq_native_bytes(kq_dtype dtype, int64_t N, int64_t K);
+
+/* Repack canonical weight rows [N][K] (w_canon, N*kq_row_bytes bytes) into the native layout
+ * (w_native, kq_native_bytes bytes, 16-byte aligned).  This is the stage-once step of the keep-quant
+ * provider ([vllm-2890], keep-quant provider commit: weights are staged once and dispatched many
+ * times).  For routed experts, repack [E*N][K] at once: with N a multiple of 16 each expert's rows
+ * stay in their own row groups.  Padding rows are written as zeros.  Dtypes: Q4_K, Q6_K, Q8_0. */
+KQ_API kq_status kq_repack_weights(kq_dtype dtype, const void *w_canon, void *w_native, int64_t N, int64_t K,
+                            kq_stream_t stream);
+
+/* Q8_K quantizer ([vllm-2890], warp-cooperative quantizer commit and the NaN/amax-seeding fix).
+ * x: fp32 [M][ldx] (row m starts at x + m*ldx; ldx >= K); xq: M*(K/256) Q8_K blocks, row-major.
+ * Per 256-element block: amax = largest |x| (strict >, so the first occurrence wins; NaN never
+ * wins), mx = that element's signed value, iscale = -127/mx, q = clamp(nearest-even(iscale*x),
+ * -127, 127) with NaN -> 0, d = 1/iscale, bsums[j] = sum of q[16j..16j+15].  A block with amax = 0
+ * (all zeros, or only NaN/zeros) is the zero block.  x and xq need 4-byte alignment. */
+KQ_API kq_status kq_quantize_q8k(const float *x, int64_t M, int64_t K, int64_t ldx, void *xq, kq_stream_t stream);
+
+/* Q8_1 quantizer ([llama-18], fused-quant MMVQ commit).  Per 32 elements: amax = max|x| (NaN
+ * ignored), d = amax/127 (IEEE division), q = roundf(x/d) (0 if amax = 0 or the quotient is not
+ * finite), s = sum of the 32 inputs in xor-butterfly order (strides 16, 8, 4, 2, 1); d and s are
+ * stored as f16 (round to nearest even).  Layout as kq_quantize_q8k with 36-byte blocks. */
+KQ_API kq_status kq_quantize_q8_1(const float *x, int64_t M, int64_t K, int64_t ldx, void *xq, kq_stream_t stream);
+
+/* Fused SwiGLU + Q8_1 ([vllm-2890] fused SiLU-mul quant epilogue; [llama-18] "SwiGLU
+ * quantization"): h = (g / (1 + expf(-g))) * u in fp32 (no bf16 round trip), then Q8_1 of h as
+ * kq_quantize_q8_1.  g and u: fp32 [M][ld] (they may be two column ranges of one buffer).
+ * h_out: optional fp32 [M][K] copy of h (NULL to skip). */
+KQ_API kq_status kq_swiglu_quantize_q8_1(const float *g, const float *u, int64_t M, int64_t K, int64_t ld, void *xq,
+                                  float *h_out, kq_stream_t stream);
+
+/* Fused SwiGLU + Q8_K: as kq_swiglu_quantize_q8_1 but the quantizer is kq_quantize_q8k's
+ * (used between the routed gate/up and down projections). */
+KQ_API kq_status kq_swiglu_quantize_q8k(const float *g, const float *u, int64_t M, int64_t K, int64_t ld, void *xq,
+                                 float *h_out, kq_stream_t stream);
+
+/* Decode GEMV, one activation column (MMVQ; [vllm-2890] MMVQ arm, [llama-18] fused-quant MMVQ).
+ * w: native [N][K] of dtype wt (Q4_K or Q6_K: activation Q8_K; Q8_0: activation Q8_1).
+ * Exactly one of x (fp32 [K]: quantised inside the kernel, no separate launch) and xq (pre-quantised
+ * activation row, K/256 Q8_K or K/32 Q8_1 blocks) must be non-NULL.  y: fp32 [N].
+ * y[n] = sum over blocks of the scaled integer block dots (the kq_gemm formula); the reduction
+ * order is fixed, so results are deterministic.  Pointers: w 16-byte aligned, x/xq/y 4-byte. */
+KQ_API kq_status kq_gemv(kq_dtype wt, const void *w, const float *x, const void *xq, int64_t N, int64_t K, float *y,
+                  kq_stream_t stream);
+
+/* Workspace bytes needed by kq_gemm (n_experts = 0, top_k = 0) or by kq_gemm_grouped for the
+ * same arguments.  0 means no workspace is needed. */
+KQ_API size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K, int64_t n_experts, int64_t top_k);
+
+/* Prefill GEMM (MMQ; [vllm-3035]: one activation tile staged in shared memory per block and shared
+ * by every warp).  Y[m][n] = sum_sb blockdot(W row n, X row m):
+ *   Q4_K x Q8_K: per super-block d_a*(d_w*sum_j sc_j*P_j - dmin*sum_j m_j*(bs_2j + bs_2j+1)),
+ *                P_j = sum of c*q over sub-block j (32 elements)
+ *   Q6_K x Q8_K: per super-block d_a*d_w*sum_j sc_j*P_j, P_j = sum of (c-32)*q over 16 elements
+ *   Q8_0 x Q8_1: per 32-block d_w*d_a*P_b
+ * w: native [N][K]; xq: M activation rows (Q8_K or Q8_1 per wt); y: fp32 rows of stride ldy >= N.
+ * workspace: device buffer of at least kq_gemm_workspace_bytes(wt, M, N, K, 0, 0) bytes (may be
+ * NULL when that is 0), 256-byte aligned. */
+KQ_API kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
+                  int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream);
+
+/* Routed-expert GEMM (MUL_MAT_ID; [llama-18] routed-compact MMQ and per-expert tile width).
+ * w: n_experts native weights, repacked together as one [n_experts*N][K] matrix (N % 16 == 0).
+ * ids: int32 [M][top_k] expert of each (token, slot).  xq: activation rows; xq_rows_per_token = 1
+ * ("broadcast": slot (t,k) reads row t) or top_k ("per-row": slot (t,k) reads row t*top_k+k).
+ * y: fp32 [M][top_k][N]; y[t][k] = W_{ids[t][k]} . X_row.  Rows are gathered per expert in
+ * (token, slot) order, so the result is deterministic.  An id outside [0, n_experts) is skipped
+ * (its y row is not written) and recorded in the workspace's device flag: kq_read_device_flag
+ * then returns KQ_ERR_DEVICE_FLAG.  workspace: kq_gemm_workspace_bytes(wt, M, N, K, n_experts,
+ * top_k) bytes, 256-byte aligned. */
+KQ_API kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const void *xq, int64_t xq_rows_per_token,
+                          const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y,
+                          void *workspace, size_t ws_bytes, kq_stream_t stream);
+
+/* Read (and clear) the device flag of a grouped workspace.  Synchronises `stream`.
+ * Returns KQ_OK, KQ_ERR_DEVICE_FLAG (an invalid expert id was seen; count in *n_bad if non-NULL),
+ * or KQ_ERR_CUDA. */
+KQ_API kq_status kq_read_device_flag(void *workspace, int64_t *n_bad, kq_stream_t stream);
+
+/* Weighted expert sum ([llama-18] weighted_expert_sum commit): out[t][n] = w[t][0]*y[t][0][n] +
+ * w[t][1]*y[t][1][n] + ... in slot order, each product rounded before its add (no fused
+ * multiply-add).  y_slots: fp32 [M][top_k][N]; w: fp32 [M][top_k]; out: fp32 [M][N]. */
+KQ_API kq_status kq_moe_weighted_sum(const float *y_slots, const float *w, int64_t M, int64_t top_k, int64_t N, float *out,
+                              kq_stream_t stream);
+
+/* Routing witness (host-side dispatch counters): number of kernel launches made by this library
+ * since load, in total (route = NULL) or for one route: "quantize", "repack", "gemv", "mmq_exact",
+ * "mmq_tc", "route", "weighted_sum".  Unknown route names return -1.  Thread-safe. */
+KQ_API int64_t kq_launch_count(const char *route);
+
+/* Debug: the integer sub-block dots of kq_gemm, partials[m][n][j] (int32):
+ * Q4_K: K/32 per (m,n), P_j = sum c*q; Q6_K: K/16, P_j = sum (c-32)*q; Q8_0: K/32, P_b = sum w*q.
+ * Computed by the same integer machinery as kq_gemm's exact path; bit-exact by contract. */
+KQ_API kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,
+                            int32_t *partials, kq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KQ_H */

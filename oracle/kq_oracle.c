@@ -60,12 +60,14 @@ ORC_API float orc_half_to_float(uint16_t h) {
     return sign ? -mag : mag;
 }
 
-/* Round-to-nearest-even conversion, overflow to infinity, NaN kept NaN. */
+/* Round-to-nearest-even conversion, overflow to infinity.  Any NaN becomes the
+ * one quiet NaN 0x7e00 (IEEE arithmetic does not fix the sign or payload of a
+ * NaN result, so no sign is carried). */
 ORC_API uint16_t orc_float_to_half(float f) {
     uint32_t bits;
     memcpy(&bits, &f, 4);
     uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
-    if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+    if (isnan(f)) return (uint16_t)0x7e00u;
     double a = fabs((double)f);               /* exact copy of |f| */
     if (a == 0.0) return sign;
     /* find the binary16 exponent: value = m * 2^(e-10), 1024 <= m < 2048 */

@@ -1,0 +1,68 @@
+"""The C-ABI library loads and exports every symbol include/kq.h declares (no GPU calls)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+import gemv_quantize_q8_gb300 as kq
+from gemv_quantize_q8_gb300 import build as kqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kq.h")).read()
+    return sorted(set(re.findall(r"^KQ_API [^(]*?\b(kq_\w+)\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    return kqbuild.build()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for fn in ["kq_quantize_q8k", "kq_quantize_q8_1", "kq_gemv", "kq_gemm", "kq_gemm_grouped",
+               "kq_repack_weights", "kq_debug_partials", "kq_moe_weighted_sum", "kq_swiglu_quantize_q8_1"]:
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(built):
+    out = subprocess.run(["nm", "-D", "--defined-only", built], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r" T (kq_\w+)$", out, flags=re.M))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+
+
+def test_binding_covers_every_symbol_and_loads(built):
+    L = kq.lib()
+    for name in _declared():
+        assert hasattr(L, name)
+        assert name in kq._SIGS, f"binding has no signature for {name}"
+    assert kq.version() >= 100
+    # pure host queries (no device work)
+    assert kq.block_bytes(kq.Q4_K) == 144 and kq.block_bytes(kq.Q6_K) == 210 and kq.block_bytes(kq.Q8_0) == 34
+    assert kq.row_bytes(kq.Q4_K, 2560) == 10 * 144
+    assert kq.native_bytes(kq.Q4_K, 9728, 2560) == 9728 * 10 * 144
+    assert kq.native_bytes(kq.Q6_K, 17, 256) == 2 * 3360          # rows padded to a multiple of 16
+    assert kq.native_bytes(kq.Q8_0, 16, 1024) == 4 * 4352
+    assert kq.native_bytes(kq.Q8_0, 16, 100) == 0
+
+
+def test_host_validation_errors_without_gpu(built):
+    """Argument errors are returned before any CUDA call, naming the problem."""
+    L = kq.lib()
+    st = L.kq_gemm(7, 16, 16, 8, 256, 1024, 16, 256, None, 0, None)
+    assert st == 2 and b"not Q4_K" in L.kq_last_error()
+    st = L.kq_gemv(kq.Q4_K, 16, 16, 16, 256, 1000, 16, None)
+    assert st == 1
+    st = L.kq_quantize_q8k(None, 1, 256, 256, 16, None)
+    assert st == 1
+    st = L.kq_gemm(kq.Q4_K, 8, 16, 8, 256, 1024, 16, 256, None, 0, None)   # w not 16-byte aligned
+    assert st == 3
+    st = L.kq_gemm_grouped(kq.Q4_K, 16, 4, 16, 3, 16, 8, 2, 256, 1024, 16, 256, 1 << 20, None)
+    assert st == 1 and b"xq_rows_per_token" in L.kq_last_error()
+    st = L.kq_gemm_grouped(kq.Q4_K, 16, 4, 16, 1, 16, 8, 2, 256, 1024, 16, 256, 16, None)
+    assert st == 4
+    assert L.kq_status_string(6) == b"device reported invalid input"

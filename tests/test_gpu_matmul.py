@@ -1,0 +1,311 @@
+"""GPU parity of the decode GEMV, the prefill GEMM, the debug partials, the
+routed-expert GEMM and the weighted expert sum against the CPU oracle.
+
+Bars: integer partials bit-exact; fp32 outputs within NMSE <= 1e-6 (the
+pages' gate).  The exact-integer kernels (GEMV, dp4a MMQ) also reproduce the
+oracle's sequential fp32 order, so for them the test asserts bit-equality.
+Outputs are poisoned with NaN before each call so an unwritten element fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemv_quantize_q8_gb300 as kq
+import oracle
+from gemv_quantize_q8_gb300 import synth
+from tests.gpu_util import DEV, act_quant, dev, gemm, host, nmse, repack
+
+pytestmark = pytest.mark.gpu
+
+DTS = [kq.Q4_K, kq.Q6_K, kq.Q8_0]
+
+
+def _oracle_act(dtype, x):
+    return oracle.quantize_q8_1(x) if dtype == kq.Q8_0 else oracle.quantize_q8_k(x)
+
+
+# ----------------------------------------------------------------------------- GEMV
+
+
+@pytest.mark.parametrize("dtype", DTS)
+@pytest.mark.parametrize("N,K", [(40, 512), (256, 1024), (100, 4096), (16, 256)])
+@pytest.mark.parametrize("fused", [True, False])
+def test_gemv_small(dtype, N, K, fused):
+    g = synth.rng(200 + N + K + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(1, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xd = dev(x)
+    y = torch.full((N,), float("nan"), device=DEV)
+    if fused:
+        kq.kq_gemv(dtype, wn, xd, None, N, K, y)
+    else:
+        kq.kq_gemv(dtype, wn, None, act_quant(dtype, xd, 1, K), N, K, y)
+    ref = oracle.gemm(dtype, w, _oracle_act(dtype, x), 1, N, K)[0]
+    got = host(y)
+    assert np.array_equal(got, ref), (nmse(got, ref), np.abs(got - ref).max())
+
+
+@pytest.mark.parametrize("cfg", synth.DECODE, ids=lambda c: c["name"])
+def test_gemv_decode_full_size(cfg):
+    dtype, N, K = cfg["dtype"], cfg["N"], cfg["K"]
+    g = synth.rng(0)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(1, K, g)
+    wn = repack(dtype, w, N, K)
+    y = torch.full((N,), float("nan"), device=DEV)
+    kq.kq_gemv(dtype, wn, dev(x), None, N, K, y)
+    ref = oracle.gemm(dtype, w, _oracle_act(dtype, x), 1, N, K)[0]
+    got = host(y)
+    assert np.isfinite(got).all()
+    assert np.array_equal(got, ref), nmse(got, ref)
+
+
+# ----------------------------------------------------------------------------- GEMM + partials
+
+
+@pytest.mark.parametrize("dtype", DTS)
+@pytest.mark.parametrize("M,N,K", [(8, 256, 1024), (70, 80, 512), (1, 48, 256), (130, 200, 768)])
+def test_gemm_small_and_partials(dtype, M, N, K):
+    g = synth.rng(300 + M + N + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    xq_ref = _oracle_act(dtype, x)
+    assert np.array_equal(host(xq).reshape(M, -1), xq_ref)
+    y = host(gemm(dtype, wn, xq, M, N, K))
+    ref = oracle.gemm(dtype, w, xq_ref, M, N, K)
+    assert np.isfinite(y).all()
+    assert nmse(y, ref) <= 1e-6
+    sub = oracle.SUBBLOCK[dtype]
+    P = torch.full((M, N, K // sub), -7, dtype=torch.int32, device=DEV)
+    kq.kq_debug_partials(dtype, wn, xq, M, N, K, P)
+    assert np.array_equal(host(P), oracle.partials(dtype, w, xq_ref, M, N, K))
+
+
+def test_tiny_config_bit_exact():
+    """The tiny Q4_K workload (W [256, 1024], X [8, 1024], seed 0) end to end."""
+    c = synth.TINY
+    g = synth.rng(0)
+    w = synth.weights(c["dtype"], c["N"], c["K"], g)
+    x = synth.activations(c["M"], c["K"], g)
+    wn = repack(c["dtype"], w, c["N"], c["K"])
+    xq = act_quant(c["dtype"], dev(x), c["M"], c["K"])
+    y = host(gemm(c["dtype"], wn, xq, c["M"], c["N"], c["K"]))
+    ref = oracle.gemm(c["dtype"], w, oracle.quantize_q8_k(x), c["M"], c["N"], c["K"])
+    assert nmse(y, ref) <= 1e-6
+    P = torch.zeros((c["M"], c["N"], c["K"] // 32), dtype=torch.int32, device=DEV)
+    kq.kq_debug_partials(c["dtype"], wn, xq, c["M"], c["N"], c["K"], P)
+    assert np.array_equal(host(P), oracle.partials(c["dtype"], w, oracle.quantize_q8_k(x), c["M"], c["N"], c["K"]))
+
+
+def test_gemm_zero_activations_exact_zero():
+    g = synth.rng(5)
+    M, N, K = 64, 64, 512
+    for dtype in DTS:
+        w = synth.weights(dtype, N, K, g)
+        wn = repack(dtype, w, N, K)
+        xq = act_quant(dtype, torch.zeros((M, K), device=DEV), M, K)
+        assert (host(gemm(dtype, wn, xq, M, N, K)) == 0).all()
+
+
+def test_gemm_adversarial_max_magnitudes():
+    """All codes and scales at their extremes: integer sums reach their largest values."""
+    M, N, K = 64, 64, 512
+    for dtype in (kq.Q4_K, kq.Q6_K):
+        bb = 144 if dtype == kq.Q4_K else 210
+        w = np.full((N, K // 256 * bb), 0xFF, dtype=np.uint8)
+        for b in range(K // 256):     # keep d finite: f16 1.0 (Q4_K: d and dmin, Q6_K: d)
+            if dtype == kq.Q4_K:
+                w[:, b * bb:b * bb + 4] = np.frombuffer(np.array([1.0, 1.0], np.float16).tobytes(), np.uint8)
+            else:
+                w[:, b * bb + 208:b * bb + 210] = np.frombuffer(np.array([1.0], np.float16).tobytes(), np.uint8)
+                w[:, b * bb + 192:b * bb + 208] = 0x80       # int8 scale -128
+        x = np.full((M, K), 1.0, np.float32)
+        x[1::2] = -1.0
+        wn = repack(dtype, w, N, K)
+        xq = act_quant(dtype, dev(x), M, K)
+        y = host(gemm(dtype, wn, xq, M, N, K))
+        ref = oracle.gemm(dtype, w, oracle.quantize_q8_k(x), M, N, K)
+        assert nmse(y, ref) <= 1e-12
+
+
+@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K])
+@pytest.mark.parametrize("shape", synth.PREFILL_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
+def test_gemm_prefill_full_size_sampled(dtype, shape):
+    N, K = shape
+    M = 2048
+    g = synth.rng(0)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    y = host(gemm(dtype, wn, xq, M, N, K))
+    assert np.isfinite(y).all()
+    xq_h = host(xq).reshape(M, -1)
+    mi = g.integers(0, M, 3000)
+    ni = g.integers(0, N, 3000)
+    mi[:4] = [0, M - 1, 0, M - 1]
+    ni[:4] = [0, N - 1, N - 1, 0]
+    ref = oracle.gemm_sampled(dtype, w, xq_h, K, mi, ni)
+    assert nmse(y[mi, ni], ref) <= 1e-6
+
+
+def test_q8_0_swiglu_full_size_sampled():
+    c = synth.SWIGLU_Q8_0
+    M, N, K = c["M"], c["N"], c["K"]
+    g = synth.rng(0)
+    w = synth.weights(kq.Q8_0, N, K, g)
+    gu = synth.activations(M, 2 * K, g)
+    wn = repack(kq.Q8_0, w, N, K)
+    d = dev(gu)
+    xq = torch.empty(kq.q8_1_bytes(M, K), dtype=torch.uint8, device=DEV)
+    kq.kq_swiglu_quantize_q8_1(d, d[:, K:], M, K, 2 * K, xq)
+    y = host(gemm(kq.Q8_0, wn, xq, M, N, K))
+    assert np.isfinite(y).all()
+    mi, ni = g.integers(0, M, 2000), g.integers(0, N, 2000)
+    # oracle on the oracle's own activation (its own SwiGLU + Q8_1)
+    rows = np.unique(mi)
+    h_ref = oracle.swiglu(gu[rows, :K], gu[rows, K:])
+    xq_ref = np.zeros((M, K // 32 * 36), np.uint8)
+    xq_ref[rows] = oracle.quantize_q8_1(h_ref)
+    ref = oracle.gemm_sampled(kq.Q8_0, w, xq_ref, K, mi, ni)
+    assert nmse(y[mi, ni], ref) <= 1e-6
+
+
+# ----------------------------------------------------------------------------- routed experts
+
+
+def _grouped(dtype, wn, E, xq, rpt, ids, M, top_k, N, K):
+    y = torch.full((M, top_k, N), float("nan"), device=DEV)
+    wsb = kq.gemm_workspace_bytes(dtype, M, N, K, E, top_k)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    kq.kq_gemm_grouped(dtype, wn, E, xq, rpt, dev(ids), M, top_k, N, K, y, ws, wsb)
+    return y, ws
+
+
+@pytest.mark.parametrize("dtype", DTS)
+@pytest.mark.parametrize("rpt", ["broadcast", "per_row"])
+def test_grouped_small(dtype, rpt):
+    g = synth.rng(400 + dtype)
+    E, M, top_k, N, K = 8, 50, 3, 48, 512
+    w = synth.weights(dtype, E * N, K, g)
+    ids, _ = synth.routing(M, E, top_k, g)
+    rows = M if rpt == "broadcast" else M * top_k
+    x = synth.activations(rows, K, g)
+    wn = repack(dtype, w, E * N, K)
+    xq = act_quant(dtype, dev(x), rows, K)
+    y, ws = _grouped(dtype, wn, E, xq, 1 if rpt == "broadcast" else top_k, ids, M, top_k, N, K)
+    assert kq.kq_read_device_flag(ws) == 0
+    ref, bad = oracle.gemm_grouped(dtype, w, E, _oracle_act(dtype, x), 1 if rpt == "broadcast" else top_k, ids, M,
+                                   top_k, N, K)
+    assert bad == 0
+    assert np.array_equal(host(y), ref)
+
+
+def test_grouped_invalid_ids_flag_and_untouched_rows():
+    g = synth.rng(410)
+    E, M, top_k, N, K = 4, 20, 2, 32, 256
+    w = synth.weights(kq.Q4_K, E * N, K, g)
+    ids, _ = synth.routing(M, E, top_k, g)
+    ids[3, 1] = 9
+    ids[7, 0] = -2
+    x = synth.activations(M, K, g)
+    wn = repack(kq.Q4_K, w, E * N, K)
+    xq = act_quant(kq.Q4_K, dev(x), M, K)
+    y, ws = _grouped(kq.Q4_K, wn, E, xq, 1, ids, M, top_k, N, K)
+    assert kq.kq_read_device_flag(ws) == 2
+    assert kq.kq_read_device_flag(ws) == 0           # read clears
+    yh = host(y)
+    assert np.isnan(yh[3, 1]).all() and np.isnan(yh[7, 0]).all()
+    ref, bad = oracle.gemm_grouped(kq.Q4_K, w, E, oracle.quantize_q8_k(x), 1, ids, M, top_k, N, K)
+    assert bad == 2
+    ok = np.isfinite(ref)
+    assert np.array_equal(yh[ok], ref[ok])
+
+
+def test_grouped_top1_single_expert_equals_dense():
+    g = synth.rng(411)
+    E, M, N, K = 3, 70, 64, 512
+    w = synth.weights(kq.Q6_K, E * N, K, g)
+    x = synth.activations(M, K, g)
+    wn = repack(kq.Q6_K, w, E * N, K)
+    xq = act_quant(kq.Q6_K, dev(x), M, K)
+    y, _ = _grouped(kq.Q6_K, wn, E, xq, 1, np.zeros((M, 1), np.int32), M, 1, N, K)
+    dense = gemm(kq.Q6_K, repack(kq.Q6_K, w[:N], N, K), xq, M, N, K)
+    assert np.array_equal(host(y)[:, 0], host(dense))
+
+
+def test_weighted_sum_bit_exact():
+    g = synth.rng(420)
+    M, top_k, N = 33, 8, 2048
+    ys = g.standard_normal((M, top_k, N)).astype(np.float32)
+    _, w = synth.routing(M, 64, top_k, g)
+    out = torch.full((M, N), float("nan"), device=DEV)
+    kq.kq_moe_weighted_sum(dev(ys), dev(w), M, top_k, N, out)
+    assert np.array_equal(host(out), oracle.moe_weighted_sum(ys, w))
+    out2 = torch.full((M, 30), float("nan"), device=DEV)     # scalar path (N % 4 != 0)
+    ys2 = np.ascontiguousarray(ys[:, :, :30])
+    kq.kq_moe_weighted_sum(dev(ys2), dev(w), M, top_k, 30, out2)
+    assert np.array_equal(host(out2), oracle.moe_weighted_sum(ys2, w))
+
+
+def _moe_pipeline(x, w_gu, w_dn, ids, wts, E, top_k, H, F):
+    """The routed MoE block through the C ABI: quantize -> gate/up -> SwiGLU+Q8_K -> down -> weighted sum."""
+    M = x.shape[0]
+    xq = act_quant(kq.Q4_K, x, M, H)
+    y_gu, _ = _grouped(kq.Q4_K, w_gu, E, xq, 1, ids, M, top_k, 2 * F, H)
+    hq = torch.empty(kq.q8k_bytes(M * top_k, F), dtype=torch.uint8, device=DEV)
+    h = torch.empty((M * top_k, F), device=DEV)
+    flat = y_gu.reshape(M * top_k, 2 * F)
+    kq.kq_swiglu_quantize_q8k(flat, flat[:, F:], M * top_k, F, 2 * F, hq, h)
+    y_dn, _ = _grouped(kq.Q6_K, w_dn, E, hq, top_k, ids, M, top_k, H, F)
+    out = torch.full((M, H), float("nan"), device=DEV)
+    kq.kq_moe_weighted_sum(y_dn, dev(wts), M, top_k, H, out)
+    return y_gu, h, hq, y_dn, out
+
+
+def test_moe_block_small_end_to_end():
+    g = synth.rng(430)
+    E, top_k, M, H, F = 16, 4, 96, 512, 256
+    w_gu = synth.weights(kq.Q4_K, E * 2 * F, H, g)
+    w_dn = synth.weights(kq.Q6_K, E * H, F, g)
+    x = synth.activations(M, H, g)
+    ids, wts = synth.routing(M, E, top_k, g)
+    y_gu, h, hq, y_dn, out = _moe_pipeline(dev(x), repack(kq.Q4_K, w_gu, E * 2 * F, H),
+                                           repack(kq.Q6_K, w_dn, E * H, F), ids, wts, E, top_k, H, F)
+    ref_gu, _ = oracle.gemm_grouped(kq.Q4_K, w_gu, E, oracle.quantize_q8_k(x), 1, ids, M, top_k, 2 * F, H)
+    assert np.array_equal(host(y_gu), ref_gu)
+    # downstream of exp(): the oracle continues from the GPU's h (ulp-level exp differences
+    # are bounded separately), then every later stage must match bit for bit
+    hq_ref = oracle.quantize_q8_k(host(h))
+    assert np.array_equal(host(hq).reshape(M * top_k, -1), hq_ref)
+    ref_dn, _ = oracle.gemm_grouped(kq.Q6_K, w_dn, E, hq_ref, top_k, ids, M, top_k, H, F)
+    assert np.array_equal(host(y_dn), ref_dn)
+    assert np.array_equal(host(out), oracle.moe_weighted_sum(ref_dn, wts))
+    # and the whole block against the oracle's own SwiGLU
+    h_ref = oracle.swiglu(ref_gu.reshape(-1, 2 * F)[:, :F], ref_gu.reshape(-1, 2 * F)[:, F:])
+    dn2, _ = oracle.gemm_grouped(kq.Q6_K, w_dn, E, oracle.quantize_q8_k(h_ref), top_k, ids, M, top_k, H, F)
+    assert nmse(host(out), oracle.moe_weighted_sum(dn2, wts)) <= 1e-6
+
+
+def test_moe_block_full_size_sampled():
+    c = synth.MOE
+    E, top_k, M, H, F = c["n_experts"], c["top_k"], c["M"], c["hidden"], c["ffn"]
+    g = synth.rng(0)
+    w_gu = synth.weights(kq.Q4_K, E * 2 * F, H, g)
+    w_dn = synth.weights(kq.Q6_K, E * H, F, g)
+    x = synth.activations(M, H, g)
+    ids, wts = synth.routing(M, E, top_k, g)
+    y_gu, h, hq, y_dn, out = _moe_pipeline(dev(x), repack(kq.Q4_K, w_gu, E * 2 * F, H),
+                                           repack(kq.Q6_K, w_dn, E * H, F), ids, wts, E, top_k, H, F)
+    toks = g.choice(M, 12, replace=False)
+    xq_ref = oracle.quantize_q8_k(x[toks])
+    ref_gu, _ = oracle.gemm_grouped(kq.Q4_K, w_gu, E, xq_ref, 1, ids[toks], len(toks), top_k, 2 * F, H)
+    assert np.array_equal(host(y_gu)[toks], ref_gu)
+    hh = host(h).reshape(M, top_k, F)[toks].reshape(-1, F)
+    hq_ref = oracle.quantize_q8_k(hh)
+    ref_dn, _ = oracle.gemm_grouped(kq.Q6_K, w_dn, E, hq_ref, top_k, ids[toks], len(toks), top_k, H, F)
+    assert np.array_equal(host(y_dn)[toks], ref_dn)
+    assert np.array_equal(host(out)[toks], oracle.moe_weighted_sum(ref_dn, wts[toks]))

@@ -1,0 +1,123 @@
+"""GPU parity of the activation quantizers against the CPU oracle (bit-exact).
+
+Where fp32 decides an integer code, both sides take the decision in fp32 with
+the same IEEE operations (division, multiply, nearest-even or roundf), so
+codes, scales and bsums must match byte for byte.  The fused SwiGLU variants
+differ only in exp(): the GPU's expf and the host's may differ by an ulp, so
+the test bounds h and checks the quantizer bit-exactly on the GPU's own h.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemv_quantize_q8_gb300 as kq
+import oracle
+from gemv_quantize_q8_gb300 import synth
+from tests.gpu_util import DEV, dev, host, q8_1, q8k
+
+pytestmark = pytest.mark.gpu
+
+
+def _special_rows(K):
+    rows = []
+    z = np.zeros(K, np.float32); rows.append(z)
+    s = np.zeros(K, np.float32); s[37] = 3.5; s[300 % K] = -1e-3; rows.append(s)
+    t = np.zeros(K, np.float32); t[5], t[9] = -1.5, 1.5; rows.append(t)
+    r = (np.arange(K) % 256 - 128).astype(np.float32); rows.append(r)
+    h = np.zeros(K, np.float32); h[0] = -127.0; h[1:121] = np.arange(-60, 60) + 0.5; rows.append(h)
+    n = np.linspace(-1, 1, K, dtype=np.float32); n[10] = np.nan; rows.append(n)
+    i = np.linspace(-1, 1, K, dtype=np.float32); i[3] = np.inf; rows.append(i)
+    tiny = np.full(K, 1e-40, np.float32); tiny[1] = -3e-39; rows.append(tiny)
+    big = np.full(K, 3e38, np.float32); big[2] = -3.4e38; rows.append(big)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("M,K,outliers", [(8, 1024, False), (3, 2560, True), (1, 9728, False), (64, 4096, True)])
+def test_q8k_bit_exact(M, K, outliers):
+    g = synth.rng(100 + M)
+    x = synth.activations(M, K, g, outliers=outliers)
+    got = host(q8k(dev(x), M, K)).reshape(M, -1)
+    assert np.array_equal(got, oracle.quantize_q8_k(x))
+
+
+def test_q8k_special_values_bit_exact():
+    x = _special_rows(512)
+    M = x.shape[0]
+    got = host(q8k(dev(x), M, 512)).reshape(M, -1)
+    assert np.array_equal(got, oracle.quantize_q8_k(x))
+
+
+def test_q8k_strided_rows():
+    g = synth.rng(101)
+    full = synth.activations(5, 1280, g)
+    got = host(q8k(dev(full), 5, 1024, ld=1280)).reshape(5, -1)
+    assert np.array_equal(got, oracle.quantize_q8_k(full[:, :1024]))
+
+
+def test_q8k_full_prefill_size():
+    g = synth.rng(102)
+    x = synth.activations(2048, 4096, g, outliers=True)
+    got = host(q8k(dev(x), 2048, 4096)).reshape(2048, -1)
+    assert np.array_equal(got, oracle.quantize_q8_k(x))
+
+
+@pytest.mark.parametrize("M,K", [(8, 1024), (3, 2560), (7, 96), (2048, 512)])
+def test_q8_1_bit_exact(M, K):
+    g = synth.rng(110 + M)
+    x = synth.activations(M, K, g, outliers=True)
+    got = host(q8_1(dev(x), M, K)).reshape(M, -1)
+    assert np.array_equal(got, oracle.quantize_q8_1(x))
+
+
+def test_q8_1_special_values():
+    x = _special_rows(512)
+    M = x.shape[0]
+    got = host(q8_1(dev(x), M, 512)).reshape(M, -1)
+    ref = oracle.quantize_q8_1(x)
+    assert np.array_equal(got, ref)
+
+
+def _swiglu_gpu(fn, g, u, M, K, ld, nbytes):
+    xq = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device=DEV)
+    h = torch.full((M, K), float("nan"), dtype=torch.float32, device=DEV)
+    fn(g, u, M, K, ld, xq, h)
+    return host(xq).reshape(M, -1), host(h)
+
+
+@pytest.mark.parametrize("q81", [True, False])
+def test_swiglu_quant(q81):
+    gen = synth.rng(120)
+    M, K = 64, 1024
+    gu = (synth.activations(M, 2 * K, gen) * 3).astype(np.float32)     # g = cols [0, K), u = [K, 2K)
+    d = dev(gu)
+    fn = kq.kq_swiglu_quantize_q8_1 if q81 else kq.kq_swiglu_quantize_q8k
+    nbytes = kq.q8_1_bytes(M, K) if q81 else kq.q8k_bytes(M, K)
+    xq, h = _swiglu_gpu(fn, d, d[:, K:], M, K, 2 * K, nbytes)
+    h_ref = oracle.swiglu(gu[:, :K], gu[:, K:])
+    ulp = np.abs(h.view(np.int32).astype(np.int64) - h_ref.view(np.int32).astype(np.int64))
+    assert ulp.max() <= 2, ulp.max()                      # expf differs by at most an ulp or two
+    qf = oracle.quantize_q8_1 if q81 else oracle.quantize_q8_k
+    assert np.array_equal(xq, qf(h))                      # quantizer bit-exact on the GPU's own h
+    diff = (xq != qf(h_ref)).mean()
+    assert diff < 1e-3                                    # codes flip only at rounding boundaries
+
+
+def test_swiglu_q8_1_full_size_sampled_rows():
+    gen = synth.rng(121)
+    M, K = 2048, 9728
+    gu = synth.activations(M, 2 * K, gen)
+    d = dev(gu)
+    xq, h = _swiglu_gpu(kq.kq_swiglu_quantize_q8_1, d, d[:, K:], M, K, 2 * K, kq.q8_1_bytes(M, K))
+    rows = gen.choice(M, 16, replace=False)
+    assert np.array_equal(xq[rows], oracle.quantize_q8_1(h[rows]))
+    h_ref = oracle.swiglu(gu[rows, :K], gu[rows, K:])
+    ulp = np.abs(h[rows].view(np.int32).astype(np.int64) - h_ref.view(np.int32).astype(np.int64))
+    assert ulp.max() <= 2
+
+
+def test_quantizer_rejects_bad_args():
+    x = torch.zeros(300, device=DEV)
+    out = torch.zeros(1024, dtype=torch.uint8, device=DEV)
+    with pytest.raises(kq.KqError) as e:
+        kq.kq_quantize_q8k(x, 1, 300, 300, out)
+    assert e.value.status == 1
