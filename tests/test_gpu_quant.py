@@ -3,8 +3,10 @@
 Where fp32 decides an integer code, both sides take the decision in fp32 with
 the same IEEE operations (division, multiply, nearest-even or roundf), so
 codes, scales and bsums must match byte for byte.  The fused SwiGLU variants
-differ only in exp(): the GPU's expf and the host's may differ by an ulp, so
-the test bounds h and checks the quantizer bit-exactly on the GPU's own h.
+differ only in exp(): CUDA's expf is within 2 ulp and the host's within 1 ulp
+of exp, and 1 + e, the division and the product each add at most half an ulp,
+so h on the two sides differs by at most 6 ulp; the test bounds h by that and
+checks the quantizer bit-exactly on the GPU's own h.
 """
 import numpy as np
 import pytest
@@ -94,10 +96,10 @@ def test_swiglu_quant(q81):
     nbytes = kq.q8_1_bytes(M, K) if q81 else kq.q8k_bytes(M, K)
     xq, h = _swiglu_gpu(fn, d, d[:, K:], M, K, 2 * K, nbytes)
     h_ref = oracle.swiglu(gu[:, :K], gu[:, K:])
-    ulp = np.abs(h.view(np.int32).astype(np.int64) - h_ref.view(np.int32).astype(np.int64))
-    assert ulp.max() <= 2, ulp.max()                      # expf differs by at most an ulp or two
     qf = oracle.quantize_q8_1 if q81 else oracle.quantize_q8_k
     assert np.array_equal(xq, qf(h))                      # quantizer bit-exact on the GPU's own h
+    ulp = np.abs(h.view(np.int32).astype(np.int64) - h_ref.view(np.int32).astype(np.int64))
+    assert ulp.max() <= 6, ulp.max()                      # exp() implementations differ by a few ulp
     diff = (xq != qf(h_ref)).mean()
     assert diff < 1e-3                                    # codes flip only at rounding boundaries
 
@@ -112,7 +114,7 @@ def test_swiglu_q8_1_full_size_sampled_rows():
     assert np.array_equal(xq[rows], oracle.quantize_q8_1(h[rows]))
     h_ref = oracle.swiglu(gu[rows, :K], gu[rows, K:])
     ulp = np.abs(h[rows].view(np.int32).astype(np.int64) - h_ref.view(np.int32).astype(np.int64))
-    assert ulp.max() <= 2
+    assert ulp.max() <= 6
 
 
 def test_quantizer_rejects_bad_args():
