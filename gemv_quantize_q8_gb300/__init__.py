@@ -61,6 +61,7 @@ _SIGS = {
     "kq_moe_weighted_sum": ([_P, _P, _I64, _I64, _I64, _P, _P], _I32),
     "kq_debug_partials": ([_I32, _P, _P, _I64, _I64, _I64, _P, _P], _I32),
     "kq_launch_count": ([ctypes.c_char_p], _I64),
+    "kq_gemm_grouped_noalloc": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P], _I32),
 }
 
 
@@ -172,6 +173,12 @@ def kq_gemm_grouped(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K
                     stream=None):
     _check(lib().kq_gemm_grouped(wt, _ptr(w), n_experts, _ptr(xq), xq_rows_per_token, _ptr(ids), M, top_k, N, K,
                                  _ptr(y), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def kq_gemm_grouped_noalloc(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K, y, stream=None):
+    """kq_gemm_grouped for callers that cannot allocate: routing scratch is a fixed array inside the library."""
+    _check(lib().kq_gemm_grouped_noalloc(wt, _ptr(w), n_experts, _ptr(xq), xq_rows_per_token, _ptr(ids), M, top_k,
+                                         N, K, _ptr(y), _stream(stream)))
 
 
 def kq_read_device_flag(workspace, stream=None) -> int:

@@ -6,6 +6,8 @@
 // not by the total number of pairs (the routed-compact commit's lesson: a tile chosen from the total
 // left 50-87% of every tile as padding).  The compaction is a stable per-expert scan, so the row
 // order -- and the result -- is deterministic.
+#include <mutex>
+
 #include "kq_internal.cuh"
 #include "kq_mmq_exact.cuh"
 #include "kq_tc.cuh"
@@ -280,3 +282,91 @@ kq_status kq_moe_weighted_sum(const float *y_slots, const float *w, int64_t M, i
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Routed-expert GEMM without a caller workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the MoE layer: code that
+// runs under a memory pool it does not own, plug-ins whose host framework hands them only the
+// input and output buffers, or code that must not call cudaMalloc after start-up.  For them the
+// routing scratch (expert counts, offsets, tile table and per-expert row lists) lives in one
+// fixed array in this library's device memory instead of a workspace.
+namespace kq {
+
+constexpr size_t kStaticScratchBytes = (size_t)1 << 20;  // 1 MiB: up to ~250k (token, slot) pairs
+static __device__ __align__(256) uint8_t g_grouped_scratch[kStaticScratchBytes];
+
+static std::mutex g_scratch_mu;
+static void *g_scratch_addr[256];  // device address of g_grouped_scratch, per device ordinal
+
+// Device address of the static scratch on the current device; looked up once per device.
+static kq_status static_scratch(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm_grouped_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 256) return fail(KQ_ERR_CUDA, "kq_gemm_grouped_noalloc: device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_grouped_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(KQ_ERR_CUDA, "kq_gemm_grouped_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return KQ_OK;
+}
+
+}  // namespace kq
+
+extern "C" kq_status kq_gemm_grouped_noalloc(kq_dtype wt, const void *w, int64_t n_experts, const void *xq,
+                                             int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k,
+                                             int64_t N, int64_t K, float *y, kq_stream_t stream) {
+    kq_status s = check_matmul_args("kq_gemm_grouped_noalloc", wt, w, xq, M, N, K);
+    if (s != KQ_OK) return s;
+    if (!ids || !y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_noalloc: null ids or y");
+    if (n_experts <= 0 || top_k <= 0 || n_experts > 65535)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_noalloc: need 0 < n_experts <= 65535 and top_k > 0");
+    if (xq_rows_per_token != 1 && xq_rows_per_token != top_k)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_noalloc: xq_rows_per_token must be 1 or top_k");
+    if (N % 16) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_noalloc: N=%lld must be a multiple of 16", (long long)N);
+    if (M > ((int64_t)1 << 30) / top_k)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_noalloc: too many (token, slot) pairs");
+    if (!aligned(ids, 4) || !aligned(y, 4))
+        return fail(KQ_ERR_ALIGNMENT, "kq_gemm_grouped_noalloc: ids/y must be 4-byte aligned");
+    const GroupedWs L = grouped_ws(M, top_k, n_experts);
+    if (L.total > kStaticScratchBytes)
+        return fail(KQ_ERR_INVALID_ARG,
+                    "kq_gemm_grouped_noalloc: M*top_k=%lld pairs with %lld experts need %zu bytes of routing scratch, "
+                    "more than the fixed %zu; use kq_gemm_grouped with a workspace",
+                    (long long)(M * top_k), (long long)n_experts, L.total, kStaticScratchBytes);
+    if (L.max_tiles > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_noalloc: too many tiles");
+    void *scratch = nullptr;
+    s = static_scratch(&scratch);
+    if (s != KQ_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *ws = static_cast<uint8_t *>(scratch);
+    long long *flag = reinterpret_cast<long long *>(ws + L.off_flag);
+    int *tile_count = reinterpret_cast<int *>(ws + L.off_tile_count);
+    int *count = reinterpret_cast<int *>(ws + L.off_count);
+    int *offset = reinterpret_cast<int *>(ws + L.off_offset);
+    int *tiles = reinterpret_cast<int *>(ws + L.off_tiles);
+    int *lists = reinterpret_cast<int *>(ws + L.off_lists);
+    const int64_t pairs = M * top_k;
+    // Every scratch field is fully rewritten below before it is read, so nothing left by an earlier
+    // call needs clearing.
+    route_count_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, (int)n_experts, count, flag);
+    route_scan_kernel<<<1, 32, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count);
+    route_fill_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, offset, lists);
+    s = check_launch("kq_gemm_grouped_noalloc routing");
+    if (s != KQ_OK) return s;
+    count_launch(R_ROUTE, 3);
+    MmqExactArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = N;
+    a.tile_count = tile_count; a.tiles = tiles; a.expert_count = count; a.expert_offset = offset; a.lists = lists;
+    a.rows_per_token = (int)xq_rows_per_token;
+    a.top_k = (int)top_k;
+    return launch_mmq_exact(wt, 0, true, a, (unsigned)L.max_tiles, st);
+}

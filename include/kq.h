@@ -174,6 +174,23 @@ KQ_API kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, 
                           const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y,
                           void *workspace, size_t ws_bytes, kq_stream_t stream);
 
+/* kq_gemm_grouped without a workspace, for callers that cannot allocate device memory when they
+ * run this layer (for example a plug-in that is handed only its input and output buffers, or code
+ * that must not call cudaMalloc after start-up).  The pages have no counterpart to this entry
+ * point; it exists only for such callers.
+ * Arguments, layouts, results and determinism are those of kq_gemm_grouped.  The routing scratch
+ * lives in one fixed 1 MiB array in this library's device memory (every GPU that loads the library
+ * holds it until the process exits), which allows about 250k (token, slot) pairs; larger
+ * M*top_k (or n_experts) is rejected with KQ_ERR_INVALID_ARG before anything is launched.
+ * The first call on a device looks the array's address up (cudaGetSymbolAddress, once per
+ * device, with that device current); make that first call before any stream capture.  The call
+ * allocates nothing.  All calls share the one array, so calls that overlap on the GPU (other
+ * streams, other host threads) race: serialise them.  Ids outside [0, n_experts) are skipped (their
+ * y rows are not written) but, unlike kq_gemm_grouped, their number is not reported. */
+KQ_API kq_status kq_gemm_grouped_noalloc(kq_dtype wt, const void *w, int64_t n_experts, const void *xq,
+                                         int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k,
+                                         int64_t N, int64_t K, float *y, kq_stream_t stream);
+
 /* Read (and clear) the device flag of a grouped workspace.  Synchronises `stream`.
  * Returns KQ_OK, KQ_ERR_DEVICE_FLAG (an invalid expert id was seen; count in *n_bad if non-NULL),
  * or KQ_ERR_CUDA. */
