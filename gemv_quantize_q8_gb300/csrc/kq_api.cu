@@ -46,42 +46,59 @@ const char *dtype_name(kq_dtype d) {
     }
 }
 
-// One thread block per (row group, K-chunk): copies the 16 rows' canonical blocks of that chunk
-// into the chunk's planes.  Rows past N are written as zeros.
+// One thread block per (row group, K-chunk).  Each thread owns one (row, 64-element kblock) slice of
+// the chunk and writes that slice's planes; rows past N are written as zeros.
 __global__ void repack_kernel(int dtype, const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int64_t N,
                               int64_t K) {
     const int64_t g = blockIdx.y, c = blockIdx.x;
     const int64_t nchunk = K / kChunkK;
     uint8_t *out = dst + chunk_offset(dtype, g, c, nchunk);
     const int tid = threadIdx.x;
+    if (tid >= kRowGroup * 4) return;
+    const int r = tid >> 2, kb = tid & 3;
+    const int64_t n = g * kRowGroup + r;
+    const bool valid = n < N;
     if (dtype == KQ_Q4_K) {
-        const int64_t rowb = nchunk * 144;
-        for (int i = tid; i < kQ4KChunk; i += blockDim.x) {
-            int r, off;
-            bool code = i < kRowGroup * kQ4KCodeBytes;
-            if (code) { r = i / kQ4KCodeBytes; off = 16 + i % kQ4KCodeBytes; }
-            else { int j = i - kRowGroup * kQ4KCodeBytes; r = j / kQ4KHdrBytes; off = j % kQ4KHdrBytes; }
-            int64_t n = g * kRowGroup + r;
-            out[i] = n < N ? src[n * rowb + c * 144 + off] : 0;
-        }
+        const uint8_t *blk = src + n * (nchunk * 144) + c * 144;
+        uint8_t *codes = out + kb * 512 + r * 32;
+        for (int l = 0; l < 32; ++l) codes[l] = valid ? blk[16 + 32 * kb + l] : 0;
+        if (kb == 0)
+            for (int i = 0; i < 16; ++i) out[2048 + r * 16 + i] = valid ? blk[i] : 0;
     } else if (dtype == KQ_Q6_K) {
-        const int64_t rowb = nchunk * 210;
-        for (int i = tid; i < kQ6KChunk; i += blockDim.x) {
-            int r, off;
-            if (i < kRowGroup * 192) { r = i / 192; off = i % 192; }
-            else if (i < kRowGroup * 208) { int j = i - kRowGroup * 192; r = j / 16; off = 192 + j % 16; }
-            else { int j = i - kRowGroup * 208; r = j / 2; off = 208 + j % 2; }
-            int64_t n = g * kRowGroup + r;
-            out[i] = n < N ? src[n * rowb + c * 210 + off] : 0;
+        const uint8_t *blk = src + n * (nchunk * 210) + c * 210;
+        uint8_t code[64];
+        for (int e = 0; e < 64; ++e) {
+            const int el = 64 * kb + e;            // element within the super-block
+            uint8_t v = 0;
+            if (valid) {
+                const uint8_t *ql = blk + 64 * (el / 128);
+                const uint8_t *qh = blk + 128 + 32 * (el / 128);
+                const int rr = el % 128, quarter = rr / 32, l = rr % 32;
+                int lo = (quarter & 1) ? ql[l + 32] : ql[l];
+                lo = (quarter & 2) ? (lo >> 4) : (lo & 15);
+                const int hi = (qh[l] >> (2 * quarter)) & 3;
+                v = (uint8_t)(lo | (hi << 4));
+            }
+            code[e] = v;
         }
-    } else {  // Q8_0: 8 canonical blocks of 34 bytes per chunk
+        uint8_t *nib = out + kb * 512 + r * 32;
+        for (int l = 0; l < 32; ++l) nib[l] = (code[l] & 15) | ((code[l + 32] & 15) << 4);
+        uint8_t *hb = out + 2048 + kb * 256 + r * 16;
+        for (int j = 0; j < 16; ++j)
+            hb[j] = (code[j] >> 4) | ((code[j + 16] >> 4) << 2) | ((code[j + 32] >> 4) << 4) | ((code[j + 48] >> 4) << 6);
+        if (kb == 0) {
+            for (int i = 0; i < 16; ++i) out[3072 + r * 16 + i] = valid ? blk[192 + i] : 0;
+            out[3328 + r * 2] = valid ? blk[208] : 0;
+            out[3328 + r * 2 + 1] = valid ? blk[209] : 0;
+        }
+    } else {  // Q8_0: 8 canonical 34-byte blocks per chunk, two per kblock
         const int64_t rowb = (K / 32) * 34;
-        for (int i = tid; i < kQ80Chunk; i += blockDim.x) {
-            int r, b, off;
-            if (i < kRowGroup * 256) { r = i / 256; b = (i % 256) / 32; off = 2 + i % 32; }
-            else { int j = i - kRowGroup * 256; r = j / 16; b = (j % 16) / 2; off = j % 2; }
-            int64_t n = g * kRowGroup + r;
-            out[i] = n < N ? src[n * rowb + (c * 8 + b) * 34 + off] : 0;
+        uint8_t *codes = out + kb * 1024 + r * 64;
+        for (int h = 0; h < 2; ++h) {
+            const uint8_t *blk = src + n * rowb + (c * 8 + 2 * kb + h) * 34;
+            for (int i = 0; i < 32; ++i) codes[32 * h + i] = valid ? blk[2 + i] : 0;
+            out[4096 + r * 16 + 2 * (2 * kb + h)] = valid ? blk[0] : 0;
+            out[4096 + r * 16 + 2 * (2 * kb + h) + 1] = valid ? blk[1] : 0;
         }
     }
 }
@@ -171,7 +188,7 @@ kq_status kq_repack_weights(kq_dtype dtype, const void *w_canon, void *w_native,
         grid.y = (unsigned)gn;
         const uint8_t *src = static_cast<const uint8_t *>(w_canon) + g0 * kRowGroup * kq_row_bytes(dtype, K);
         uint8_t *dst = static_cast<uint8_t *>(w_native) + chunk_offset(dtype, g0, 0, K / kChunkK);
-        repack_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(dtype, src, dst, N - g0 * kRowGroup, K);
+        repack_kernel<<<grid, 64, 0, (cudaStream_t)stream>>>(dtype, src, dst, N - g0 * kRowGroup, K);
         kq_status s = check_launch("kq_repack_weights");
         if (s != KQ_OK) return s;
         count_launch(R_REPACK);

@@ -37,34 +37,32 @@ struct GemvTraits<KQ_Q6_K> { static constexpr int terms = 1; static constexpr bo
 template <>
 struct GemvTraits<KQ_Q8_0> { static constexpr int terms = 8; static constexpr bool q81 = true; };
 
-// Registers holding one lane's slice of one chunk.
+// Registers holding one lane's slice of one chunk.  Lane t of a row owns kblock c = t/2 and the
+// 16-byte half seg = t%2 of that kblock's codes: elements 64c+16seg+i (low nibbles) and
+// 64c+32+16seg+i (high nibbles), i < 16.  (Q8_0: lane t owns 32-element block t.)
 struct LaneRegs {
-    uint4 a;   // Q4_K: 16 code bytes; Q6_K: ql lo (x,y) + ql hi (z,w); Q8_0: codes 0..15
-    uint4 b;   // Q4_K: header (d, dmin, scales); Q6_K: qh (x,y) + scales bytes (z,w); Q8_0: codes 16..31
-    uint32_t c;  // Q6_K: f16 d; Q8_0: f16 d
+    uint4 a;     // Q4_K/Q6_K: 16 code bytes (low 4 bits); Q8_0: codes 0..15
+    uint4 b;     // Q4_K: header (d, dmin, scales); Q6_K: 16 high-bit bytes; Q8_0: codes 16..31
+    uint32_t c;  // Q6_K: scale bytes of sub-blocks 4c..4c+3; Q8_0: f16 d
+    uint32_t d;  // Q6_K: f16 d
 };
 
 template <int DT>
 __device__ __forceinline__ void gemv_load(const uint8_t *__restrict__ chunk, int r, int t, LaneRegs &R) {
+    const int c = t >> 1, seg = t & 1;
     if (DT == KQ_Q4_K) {
-        R.a = __ldg(reinterpret_cast<const uint4 *>(chunk + r * 128 + 16 * t));
-        R.b = __ldg(reinterpret_cast<const uint4 *>(chunk + 16 * 128 + r * 16));
+        R.a = __ldg(reinterpret_cast<const uint4 *>(chunk + c * 512 + r * 32 + seg * 16));
+        R.b = __ldg(reinterpret_cast<const uint4 *>(chunk + 2048 + r * 16));
     } else if (DT == KQ_Q6_K) {
-        const int h = t >> 2, l0 = 8 * (t & 3);
-        const uint8_t *codes = chunk + r * 192;
-        uint2 lo = __ldg(reinterpret_cast<const uint2 *>(codes + 64 * h + l0));
-        uint2 hi = __ldg(reinterpret_cast<const uint2 *>(codes + 64 * h + 32 + l0));
-        uint2 qh = __ldg(reinterpret_cast<const uint2 *>(codes + 128 + 32 * h + l0));
-        // scales of the lane's half (sub-blocks 8h .. 8h+7)
-        uint4 sc = __ldg(reinterpret_cast<const uint4 *>(chunk + 16 * 192 + r * 16));
-        R.a = make_uint4(lo.x, lo.y, hi.x, hi.y);
-        R.b = make_uint4(qh.x, qh.y, h ? sc.z : sc.x, h ? sc.w : sc.y);
-        R.c = __ldg(reinterpret_cast<const uint16_t *>(chunk + 16 * 208 + r * 2));
+        R.a = __ldg(reinterpret_cast<const uint4 *>(chunk + c * 512 + r * 32 + seg * 16));
+        R.b = __ldg(reinterpret_cast<const uint4 *>(chunk + 2048 + c * 256 + r * 16));
+        R.c = __ldg(reinterpret_cast<const uint32_t *>(chunk + 3072 + r * 16 + 4 * c));
+        R.d = __ldg(reinterpret_cast<const uint16_t *>(chunk + 3328 + r * 2));
     } else {
-        const uint8_t *codes = chunk + r * 256 + 32 * t;
+        const uint8_t *codes = chunk + c * 1024 + r * 64 + 32 * seg;
         R.a = __ldg(reinterpret_cast<const uint4 *>(codes));
         R.b = __ldg(reinterpret_cast<const uint4 *>(codes + 16));
-        R.c = __ldg(reinterpret_cast<const uint16_t *>(chunk + 16 * 256 + r * 16 + 2 * t));
+        R.c = __ldg(reinterpret_cast<const uint16_t *>(chunk + 4096 + r * 16 + 2 * t));
     }
 }
 
@@ -76,73 +74,61 @@ template <int DT>
 __device__ __forceinline__ void gemv_compute(const LaneRegs &R, int t, const int8_t *__restrict__ q,
                                              const float *__restrict__ da, const int16_t *__restrict__ bs,
                                              float *term_out) {
-    if (DT == KQ_Q4_K) {
-        const int c = t >> 1, l0 = 16 * (t & 1);
-        const int4 qlo = *reinterpret_cast<const int4 *>(q + 64 * c + l0);
-        const int4 qhi = *reinterpret_cast<const int4 *>(q + 64 * c + 32 + l0);
+    const int c = t >> 1, seg = t & 1;
+    if (DT == KQ_Q4_K || DT == KQ_Q6_K) {
+        const int4 qlo = *reinterpret_cast<const int4 *>(q + 64 * c + 16 * seg);
+        const int4 qhi = *reinterpret_cast<const int4 *>(q + 64 * c + 32 + 16 * seg);
         const uint32_t w[4] = {R.a.x, R.a.y, R.a.z, R.a.w};
+        const uint32_t hb[4] = {R.b.x, R.b.y, R.b.z, R.b.w};
         const int ql[4] = {qlo.x, qlo.y, qlo.z, qlo.w}, qh[4] = {qhi.x, qhi.y, qhi.z, qhi.w};
         int plo = 0, phi = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            plo = dp4a((int)(w[i] & 0x0f0f0f0fu), ql[i], plo);
-            phi = dp4a((int)((w[i] >> 4) & 0x0f0f0f0fu), qh[i], phi);
-        }
-        uint8_t s12[12];
-        const uint32_t hw[3] = {R.b.y, R.b.z, R.b.w};
-#pragma unroll
-        for (int i = 0; i < 12; ++i) s12[i] = (hw[i / 4] >> (8 * (i % 4))) & 0xff;
-        int sc0, m0, sc1, m1;
-        q4k_scale_min(s12, 2 * c, sc0, m0);
-        q4k_scale_min(s12, 2 * c + 1, sc1, m1);
-        int sumi = sc0 * plo + sc1 * phi;
-        // bsums of the lane's two 16-element groups; the other half of each sub-block's bsum is
-        // added by the partner lane (t ^ 1), so the row-wide sum over lanes is exact.
-        int summ = m0 * bs[4 * c + (t & 1)] + m1 * bs[4 * c + 2 + (t & 1)];
-#pragma unroll
-        for (int s = 4; s >= 1; s >>= 1) {
-            sumi += __shfl_xor_sync(0xffffffffu, sumi, s);
-            summ += __shfl_xor_sync(0xffffffffu, summ, s);
-        }
-        if (t == 0) {
-            const float dw = half_bits_to_float((uint16_t)(R.b.x & 0xffff));
-            const float dmin = half_bits_to_float((uint16_t)(R.b.x >> 16));
-            const float a = da[0];
-            float t1 = __fmul_rn(a, dw);
-            float t2 = __fmul_rn(t1, (float)sumi);
-            float t3 = __fmul_rn(a, dmin);
-            float t4 = __fmul_rn(t3, (float)summ);
-            term_out[0] = __fsub_rn(t2, t4);
-        }
-    } else if (DT == KQ_Q6_K) {
-        const int h = t >> 2, l0 = 8 * (t & 3);
-        const uint32_t lo[2] = {R.a.x, R.a.y}, hi[2] = {R.a.z, R.a.w}, qh[2] = {R.b.x, R.b.y};
-        const uint32_t scw[2] = {R.b.z, R.b.w};  // scales 8h .. 8h+7
-        int sumi = 0;
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-            const int pos = 128 * h + 32 * qq + l0;  // first element of this run of 8
-            const int2 qa = *reinterpret_cast<const int2 *>(q + pos);
-            const int qa2[2] = {qa.x, qa.y};
-            int p = 0;
-#pragma unroll
-            for (int wi = 0; wi < 2; ++wi) {
-                uint32_t base = (qq & 1) ? hi[wi] : lo[wi];
-                uint32_t nib = (qq & 2) ? ((base >> 4) & 0x0f0f0f0fu) : (base & 0x0f0f0f0fu);
-                uint32_t hb = ((qh[wi] >> (2 * qq)) & 0x03030303u) << 4;
-                uint32_t code = __vsub4(nib | hb, 0x20202020u);
-                p = dp4a((int)code, qa2[wi], p);
+            uint32_t lo = w[i] & 0x0f0f0f0fu, hi = (w[i] >> 4) & 0x0f0f0f0fu;
+            if (DT == KQ_Q6_K) {
+                lo = __vsub4(lo | (((hb[i] >> (2 * seg)) & 0x03030303u) << 4), 0x20202020u);
+                hi = __vsub4(hi | (((hb[i] >> (4 + 2 * seg)) & 0x03030303u) << 4), 0x20202020u);
             }
-            const int jl = 2 * qq + (l0 >> 4);  // sub-block index within the half: 0..7
-            const int sc = sext8(scw[jl >> 2], jl & 3);
-            sumi += sc * p;
+            plo = dp4a((int)lo, ql[i], plo);
+            phi = dp4a((int)hi, qh[i], phi);
         }
+        if (DT == KQ_Q4_K) {
+            uint8_t s12[12];
+            const uint32_t hw[3] = {R.b.y, R.b.z, R.b.w};
 #pragma unroll
-        for (int s = 4; s >= 1; s >>= 1) sumi += __shfl_xor_sync(0xffffffffu, sumi, s);
-        if (t == 0) {
-            const float dw = half_bits_to_float((uint16_t)R.c);
-            const float t1 = __fmul_rn(da[0], dw);
-            term_out[0] = __fmul_rn(t1, (float)sumi);
+            for (int i = 0; i < 12; ++i) s12[i] = (hw[i / 4] >> (8 * (i % 4))) & 0xff;
+            int sc0, m0, sc1, m1;
+            q4k_scale_min(s12, 2 * c, sc0, m0);
+            q4k_scale_min(s12, 2 * c + 1, sc1, m1);
+            int sumi = sc0 * plo + sc1 * phi;
+            // bsums of the lane's two 16-element groups; the partner lane (t ^ 1) adds the other
+            // half of each sub-block, so the row-wide integer sum over lanes is exact.
+            int summ = m0 * bs[4 * c + seg] + m1 * bs[4 * c + 2 + seg];
+#pragma unroll
+            for (int s = 4; s >= 1; s >>= 1) {
+                sumi += __shfl_xor_sync(0xffffffffu, sumi, s);
+                summ += __shfl_xor_sync(0xffffffffu, summ, s);
+            }
+            if (t == 0) {
+                const float dw = half_bits_to_float((uint16_t)(R.b.x & 0xffff));
+                const float dmin = half_bits_to_float((uint16_t)(R.b.x >> 16));
+                const float a = da[0];
+                float t1 = __fmul_rn(a, dw);
+                float t2 = __fmul_rn(t1, (float)sumi);
+                float t3 = __fmul_rn(a, dmin);
+                float t4 = __fmul_rn(t3, (float)summ);
+                term_out[0] = __fsub_rn(t2, t4);
+            }
+        } else {
+            // sub-blocks of 16: low run = 4c+seg, high run = 4c+2+seg (scale bytes seg and 2+seg of R.c)
+            int sumi = sext8(R.c, seg) * plo + sext8(R.c, 2 + seg) * phi;
+#pragma unroll
+            for (int s = 4; s >= 1; s >>= 1) sumi += __shfl_xor_sync(0xffffffffu, sumi, s);
+            if (t == 0) {
+                const float dw = half_bits_to_float((uint16_t)R.d);
+                const float t1 = __fmul_rn(da[0], dw);
+                term_out[0] = __fmul_rn(t1, (float)sumi);
+            }
         }
     } else {
         const int4 q0 = *reinterpret_cast<const int4 *>(q + 32 * t);

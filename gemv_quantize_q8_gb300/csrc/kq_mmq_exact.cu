@@ -49,71 +49,65 @@ __device__ __forceinline__ void stage_weights(ExactSmem &s, const uint8_t *__res
             for (int j = 0; j < 8; ++j) { s.wmn[row][j] = 0; s.wd[row][j] = 0.0f; }
         }
     }
-    if (DT == KQ_Q4_K) {
+    if (DT == KQ_Q4_K || DT == KQ_Q6_K) {
+        // unit = (row, kblock kb, 16-byte half seg): low nibbles -> elements 64kb+16seg+i,
+        // high nibbles -> 64kb+32+16seg+i; Q6_K adds two high bits per element and the -32 offset.
         for (int u = tid; u < rows_valid * 8; u += 256) {
-            const int row = u >> 3, seg = u & 7;
+            const int row = u >> 3, kb = (u >> 1) & 3, seg = u & 1;
             const uint8_t *ch = wtile + ((row >> 4) * nchunk + c) * (int64_t)cb;
-            uint4 v = __ldg(reinterpret_cast<const uint4 *>(ch + (row & 15) * 128 + seg * 16));
-            const int cc = seg >> 1, l0 = 16 * (seg & 1);
-            uint4 lo = make_uint4(v.x & 0x0f0f0f0fu, v.y & 0x0f0f0f0fu, v.z & 0x0f0f0f0fu, v.w & 0x0f0f0f0fu);
-            uint4 hi = make_uint4((v.x >> 4) & 0x0f0f0f0fu, (v.y >> 4) & 0x0f0f0f0fu, (v.z >> 4) & 0x0f0f0f0fu,
-                                  (v.w >> 4) & 0x0f0f0f0fu);
-            *reinterpret_cast<uint4 *>(&s.wq[row][64 * cc + l0]) = lo;
-            *reinterpret_cast<uint4 *>(&s.wq[row][64 * cc + 32 + l0]) = hi;
-        }
-        if (tid < rows_valid) {
-            const uint8_t *ch = wtile + ((tid >> 4) * nchunk + c) * (int64_t)cb;
-            const uint8_t *h = ch + 16 * 128 + (tid & 15) * 16;
-            s.wd[tid][0] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(h));
-            s.wd[tid][1] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(h + 2));
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(ch + kb * 512 + (row & 15) * 32 + seg * 16));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t lo[4], hi[4];
+            if (DT == KQ_Q6_K) {
+                const uint4 h = __ldg(reinterpret_cast<const uint4 *>(ch + 2048 + kb * 256 + (row & 15) * 16));
+                const uint32_t hb[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                int sc, mn;
-                q4k_scale_min(h + 4, j, sc, mn);
-                s.wsc[tid][j] = sc;
-                s.wmn[tid][j] = mn;
-            }
-        }
-    } else if (DT == KQ_Q6_K) {
-        for (int u = tid; u < rows_valid * 8; u += 256) {
-            const int row = u >> 3, hh = (u >> 2) & 1, l0 = 8 * (u & 3);
-            const uint8_t *ch = wtile + ((row >> 4) * nchunk + c) * (int64_t)cb;
-            const uint8_t *codes = ch + (row & 15) * 192;
-            uint2 lo = __ldg(reinterpret_cast<const uint2 *>(codes + 64 * hh + l0));
-            uint2 hi = __ldg(reinterpret_cast<const uint2 *>(codes + 64 * hh + 32 + l0));
-            uint2 qh = __ldg(reinterpret_cast<const uint2 *>(codes + 128 + 32 * hh + l0));
-            const uint32_t L[2] = {lo.x, lo.y}, H[2] = {hi.x, hi.y}, Q[2] = {qh.x, qh.y};
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                uint32_t out[2];
-#pragma unroll
-                for (int wi = 0; wi < 2; ++wi) {
-                    uint32_t base = (qq & 1) ? H[wi] : L[wi];
-                    uint32_t nib = (qq & 2) ? ((base >> 4) & 0x0f0f0f0fu) : (base & 0x0f0f0f0fu);
-                    uint32_t hb = ((Q[wi] >> (2 * qq)) & 0x03030303u) << 4;
-                    out[wi] = __vsub4(nib | hb, 0x20202020u);
+                for (int i = 0; i < 4; ++i) {
+                    lo[i] = __vsub4((w[i] & 0x0f0f0f0fu) | (((hb[i] >> (2 * seg)) & 0x03030303u) << 4), 0x20202020u);
+                    hi[i] = __vsub4(((w[i] >> 4) & 0x0f0f0f0fu) | (((hb[i] >> (4 + 2 * seg)) & 0x03030303u) << 4),
+                                    0x20202020u);
                 }
-                *reinterpret_cast<uint2 *>(&s.wq[row][128 * hh + 32 * qq + l0]) = make_uint2(out[0], out[1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    lo[i] = w[i] & 0x0f0f0f0fu;
+                    hi[i] = (w[i] >> 4) & 0x0f0f0f0fu;
+                }
             }
+            *reinterpret_cast<uint4 *>(&s.wq[row][64 * kb + 16 * seg]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(&s.wq[row][64 * kb + 32 + 16 * seg]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
         if (tid < rows_valid) {
             const uint8_t *ch = wtile + ((tid >> 4) * nchunk + c) * (int64_t)cb;
-            const int8_t *sc = reinterpret_cast<const int8_t *>(ch + 16 * 192 + (tid & 15) * 16);
+            if (DT == KQ_Q4_K) {
+                const uint8_t *h = ch + 2048 + (tid & 15) * 16;
+                s.wd[tid][0] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(h));
+                s.wd[tid][1] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(h + 2));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) s.wsc[tid][j] = sc[j];
-            s.wd[tid][0] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(ch + 16 * 208 + (tid & 15) * 2));
+                for (int j = 0; j < 8; ++j) {
+                    int sc, mn;
+                    q4k_scale_min(h + 4, j, sc, mn);
+                    s.wsc[tid][j] = sc;
+                    s.wmn[tid][j] = mn;
+                }
+            } else {
+                const int8_t *sc = reinterpret_cast<const int8_t *>(ch + 3072 + (tid & 15) * 16);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) s.wsc[tid][j] = sc[j];
+                s.wd[tid][0] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(ch + 3328 + (tid & 15) * 2));
+            }
         }
     } else {
         for (int u = tid; u < rows_valid * 16; u += 256) {
             const int row = u >> 4, seg = u & 15;
             const uint8_t *ch = wtile + ((row >> 4) * nchunk + c) * (int64_t)cb;
             *reinterpret_cast<uint4 *>(&s.wq[row][seg * 16]) =
-                __ldg(reinterpret_cast<const uint4 *>(ch + (row & 15) * 256 + seg * 16));
+                __ldg(reinterpret_cast<const uint4 *>(ch + (seg >> 2) * 1024 + (row & 15) * 64 + (seg & 3) * 16));
         }
         for (int u = tid; u < rows_valid * 8; u += 256) {
             const int row = u >> 3, b = u & 7;
             const uint8_t *ch = wtile + ((row >> 4) * nchunk + c) * (int64_t)cb;
-            s.wd[row][b] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(ch + 16 * 256 + (row & 15) * 16 + 2 * b));
+            s.wd[row][b] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(ch + 4096 + (row & 15) * 16 + 2 * b));
         }
     }
 }

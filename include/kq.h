@@ -44,12 +44,17 @@
  * Native weight layout (what the matmul entry points consume; produced by
  * kq_repack_weights): rows are taken in groups of 16 (the last group is
  * padded with zero rows) and each group is stored as consecutive chunks of
- * 256 elements along K.  A chunk holds the 16 rows' fields as planes:
- *   Q4_K chunk (2304 B): codes [16][128], then headers [16][16] (d, dmin,
- *        12 scale/min bytes -- the first 16 bytes of the canonical block).
- *   Q6_K chunk (3360 B): codes [16][192] (ql then qh), scales [16][16],
- *        d [16] (f16).
- *   Q8_0 chunk (4352 B): codes [16][256], d [16][8] (f16).
+ * 256 elements along K.  Inside a chunk, the codes of each 64-element
+ * "kblock" kb (0..3) are stored for the 16 rows together, so one kblock of a
+ * row group is one contiguous run:
+ *   Q4_K chunk (2304 B): codes [kb][16 rows][32 B] -- byte l holds element
+ *        64kb+l (low nibble) and 64kb+32+l (high nibble); then headers
+ *        [16][16 B] (d, dmin, 12 scale/min bytes: the canonical first 16).
+ *   Q6_K chunk (3360 B): low 4 code bits [kb][16][32 B] (nibble order as
+ *        Q4_K); high 2 code bits [kb][16][16 B] (byte j: elements 64kb+j,
+ *        +16+j, +32+j, +48+j in bits 0-1, 2-3, 4-5, 6-7); int8 scales
+ *        [16][16]; f16 d [16].
+ *   Q8_0 chunk (4352 B): codes [kb][16][64 B]; f16 d [16][8].
  * Every chunk starts on a 16-byte boundary when the buffer does.
  */
 #ifndef KQ_H

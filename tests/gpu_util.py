@@ -44,6 +44,8 @@ def gemm(dtype: int, w_native: torch.Tensor, xq: torch.Tensor, M: int, N: int, K
     wsb = kq.gemm_workspace_bytes(dtype, M, N, K)
     ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=DEV) if wsb else None
     kq.kq_gemm(dtype, w_native, xq, M, N, K, y, N, ws, wsb)
+    if wsb:
+        assert kq.kq_read_device_flag(ws) == 0, "tensor-core pipeline reported a timeout"
     return y
 
 

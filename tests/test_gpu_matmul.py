@@ -65,7 +65,8 @@ def test_gemv_decode_full_size(cfg):
 
 
 @pytest.mark.parametrize("dtype", DTS)
-@pytest.mark.parametrize("M,N,K", [(8, 256, 1024), (70, 80, 512), (1, 48, 256), (130, 200, 768)])
+@pytest.mark.parametrize("M,N,K", [(8, 256, 1024), (70, 80, 512), (1, 48, 256), (130, 200, 768), (128, 128, 256),
+                                   (300, 392, 1536)])
 def test_gemm_small_and_partials(dtype, M, N, K):
     g = synth.rng(300 + M + N + dtype)
     w = synth.weights(dtype, N, K, g)
@@ -110,9 +111,11 @@ def test_gemm_zero_activations_exact_zero():
         assert (host(gemm(dtype, wn, xq, M, N, K)) == 0).all()
 
 
-def test_gemm_adversarial_max_magnitudes():
-    """All codes and scales at their extremes: integer sums reach their largest values."""
-    M, N, K = 64, 64, 512
+@pytest.mark.parametrize("M", [64, 256])
+def test_gemm_adversarial_max_magnitudes(M):
+    """All codes and scales at their extremes: integer sums reach their largest values
+    (M = 64 takes the dp4a kernel, M = 256 the tensor-core kernel)."""
+    N, K = 256, 512
     for dtype in (kq.Q4_K, kq.Q6_K):
         bb = 144 if dtype == kq.Q4_K else 210
         w = np.full((N, K // 256 * bb), 0xFF, dtype=np.uint8)
@@ -124,11 +127,14 @@ def test_gemm_adversarial_max_magnitudes():
                 w[:, b * bb + 192:b * bb + 208] = 0x80       # int8 scale -128
         x = np.full((M, K), 1.0, np.float32)
         x[1::2] = -1.0
+        x[::3, ::5] = 0.25
         wn = repack(dtype, w, N, K)
         xq = act_quant(dtype, dev(x), M, K)
         y = host(gemm(dtype, wn, xq, M, N, K))
         ref = oracle.gemm(dtype, w, oracle.quantize_q8_k(x), M, N, K)
-        assert nmse(y, ref) <= 1e-12
+        # the dp4a path is exact; the tensor-core path accumulates in fp32, which rounds once
+        # partial sums pass 2^24 (these extreme blocks reach ~3e7), so allow a tiny residue
+        assert nmse(y, ref) <= 1e-10
 
 
 @pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K])
