@@ -132,6 +132,7 @@ def build_prefill_inputs(device, only=None):
             wc = torch.from_numpy(synth.weights(dtype, N, K, g).reshape(-1)).to(device)
             wn = torch.empty(kq.native_bytes(dtype, N, K), dtype=torch.uint8, device=device)
             kq.kq_repack_weights(dtype, wc, wn, N, K)
+            torch.cuda.synchronize()
             weights[(dtype, N, K)] = wn
             del wc
     Kmax = max(K for (_, K) in synth.PREFILL_SHAPES)
@@ -229,12 +230,13 @@ def run_prefill(args, device, rank, world):
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, cases=cases)
 
 
-def run_decode(args, device, calls=1000):
+def run_decode(args, device, calls=None):
     """1000 back-to-back fused-quant GEMV calls per shape from a CUDA graph; weight copies rotate."""
     import torch
 
     import gemv_quantize_q8_gb300 as kq
     from gemv_quantize_q8_gb300 import synth
+    calls = calls or args.gemv_calls
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     g = synth.rng(0)
     out = {}
@@ -248,6 +250,7 @@ def run_decode(args, device, calls=1000):
         ws = torch.empty((copies, nb), dtype=torch.uint8, device=device)
         for c in range(copies):
             kq.kq_repack_weights(dtype, wc, ws[c], N, K)
+        torch.cuda.synchronize()      # weights are staged once, before any GEMV streams them
         x = torch.from_numpy(synth.activations(1, K, g)).to(device)
         y = torch.empty(N, dtype=torch.float32, device=device)
         s = torch.cuda.Stream()
@@ -342,6 +345,8 @@ def main():
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
     ap.add_argument("--only", default=None, help="profile one GEMM, e.g. q4_k:4096x4096:512")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", action="store_true", help="time only the decode GEMV (for profiling)")
+    ap.add_argument("--gemv-calls", type=int, default=1000, help="back-to-back GEMV calls per decode shape")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
 
@@ -364,6 +369,11 @@ def main():
     if world > 1:
         torch.distributed.barrier()
 
+    if args.decode_only:
+        decode, decode_gbs = run_decode(args, device)
+        if rank == 0:
+            print(json.dumps({"decode_gemv_gbs": round(decode_gbs, 1), "shapes": decode}), flush=True)
+        return
     res = run_prefill(args, device, rank, world)
     ms = res["ms"]
     e2e_ms = res["e2e_ms"]

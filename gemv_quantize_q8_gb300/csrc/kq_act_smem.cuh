@@ -22,8 +22,14 @@ __device__ __forceinline__ void warp_quantize_q8k_smem(const float *__restrict__
                                                        int16_t *bs) {
     const int lane = threadIdx.x & 31;
     float v[8];
+    if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const float4 a = reinterpret_cast<const float4 *>(x)[2 * lane];
+        const float4 b = reinterpret_cast<const float4 *>(x)[2 * lane + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = x[lane * 8 + i];
+        for (int i = 0; i < 8; ++i) v[i] = x[lane * 8 + i];
+    }
     float amax = 0.0f, mx = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -60,8 +66,13 @@ __device__ __forceinline__ void warp_quantize_q8_1x4_smem(const float *__restric
     const int lane = threadIdx.x & 31;
     const int t = lane & 7;
     float v[4];
+    if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const float4 a = reinterpret_cast<const float4 *>(x)[lane];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = x[lane * 4 + i];
+        for (int i = 0; i < 4; ++i) v[i] = x[lane * 4 + i];
+    }
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int s = 4; s >= 1; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));

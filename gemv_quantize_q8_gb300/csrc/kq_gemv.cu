@@ -1,32 +1,40 @@
 // kq_gemv.cu -- decode GEMV (one activation column) over native block-quantised weights.
 //
-// Design (GB300): the weight stream is the whole cost, so every byte is read once with 16-byte
-// (or 8-byte) coalesced loads, and the next chunk's loads are issued before the current chunk is
-// consumed.  A thread block owns one 16-row group and a contiguous range of 256-element chunks;
-// rows with long K are split across the CTAs of a thread-block cluster, whose partial results are
-// combined through distributed shared memory (no workspace, no atomics).
+// Design (GB300): the weight stream is the whole cost.  A thread block owns 32 rows (two native row
+// groups) and a range of 256-element chunks; each warp owns one chunk and streams its codes into
+// shared memory with bulk copies (cp.async.bulk + mbarrier), so all of the block's bytes are in
+// flight at once, and waits for them asleep rather than spinning.  A lane owns one row of that
+// chunk (128-256 code bytes), which keeps the instruction count per weight byte low; 32 rows per
+// block also halve the activation work each block repeats.
+// Rows with long K are split across the CTAs of a thread-block cluster, whose partial results are
+// combined through distributed shared memory (no workspace, no atomics).  Launches allow
+// programmatic dependent launch: the next kernel in the stream is scheduled early and waits on the
+// hardware dependency before touching memory, which hides the launch gap between decode kernels.
 //
-// Each (row, chunk) term is formed exactly as the prefill GEMM forms it -- integer sub-block dots
-// (dp4a), integer scale/min sums reduced across the 8 lanes of a row with shuffles, then one fp32
-// expression per super-block -- and the terms of a row are added in ascending K order by a single
-// thread.  The result is therefore bit-identical to the sequential CPU accumulation order, the
+// Each (row, chunk) term is formed exactly as the CPU oracle forms it -- integer sub-block dots
+// (dp4a), integer scale/min sums, then one fp32 expression per super-block -- and the terms of a
+// row are added in ascending K order by a single thread.  The result is therefore bit-identical to the sequential CPU accumulation order, the
 // property the keep-quant provider of vllm.cpp PR #2890 gates on, and it does not depend on the
 // launch shape (strix-llama.cpp PR #18 keeps batch-one MMVQ on a fixed reduction order for the
 // same reason).
 //
 // With x != NULL the activation is quantised inside the kernel (fused-quant MMVQ of
-// strix-llama.cpp PR #18): each CTA quantises the part of x its K range needs into shared memory,
-// after its first weight loads are already in flight.
+// strix-llama.cpp PR #18): each warp quantises the 256 activation values of its own chunk into
+// shared memory while its weight copies are in flight.
 #include <cooperative_groups.h>
 
 #include "kq_act_smem.cuh"
 #include "kq_internal.cuh"
+#include "kq_sm100.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace kq {
 
-constexpr int kGemvThreads = 256;  // 2 chunk slots x 16 rows x 8 lanes
+using namespace sm100;
+
+constexpr int kGemvRows = 32;      // rows per thread block (two native row groups), one per lane
+constexpr int kGemvMaxWarps = 32;
 
 template <int DT>
 struct GemvTraits;
@@ -37,213 +45,253 @@ struct GemvTraits<KQ_Q6_K> { static constexpr int terms = 1; static constexpr bo
 template <>
 struct GemvTraits<KQ_Q8_0> { static constexpr int terms = 8; static constexpr bool q81 = true; };
 
-// Registers holding one lane's slice of one chunk.  Lane t of a row owns kblock c = t/2 and the
-// 16-byte half seg = t%2 of that kblock's codes: elements 64c+16seg+i (low nibbles) and
-// 64c+32+16seg+i (high nibbles), i < 16.  (Q8_0: lane t owns 32-element block t.)
-struct LaneRegs {
-    uint4 a;     // Q4_K/Q6_K: 16 code bytes (low 4 bits); Q8_0: codes 0..15
-    uint4 b;     // Q4_K: header (d, dmin, scales); Q6_K: 16 high-bit bytes; Q8_0: codes 16..31
-    uint32_t c;  // Q6_K: scale bytes of sub-blocks 4c..4c+3; Q8_0: f16 d
-    uint32_t d;  // Q6_K: f16 d
-};
-
-template <int DT>
-__device__ __forceinline__ void gemv_load(const uint8_t *__restrict__ chunk, int r, int t, LaneRegs &R) {
-    const int c = t >> 1, seg = t & 1;
-    if (DT == KQ_Q4_K) {
-        R.a = __ldg(reinterpret_cast<const uint4 *>(chunk + c * 512 + r * 32 + seg * 16));
-        R.b = __ldg(reinterpret_cast<const uint4 *>(chunk + 2048 + r * 16));
-    } else if (DT == KQ_Q6_K) {
-        R.a = __ldg(reinterpret_cast<const uint4 *>(chunk + c * 512 + r * 32 + seg * 16));
-        R.b = __ldg(reinterpret_cast<const uint4 *>(chunk + 2048 + c * 256 + r * 16));
-        R.c = __ldg(reinterpret_cast<const uint32_t *>(chunk + 3072 + r * 16 + 4 * c));
-        R.d = __ldg(reinterpret_cast<const uint16_t *>(chunk + 3328 + r * 2));
-    } else {
-        const uint8_t *codes = chunk + c * 1024 + r * 64 + 32 * seg;
-        R.a = __ldg(reinterpret_cast<const uint4 *>(codes));
-        R.b = __ldg(reinterpret_cast<const uint4 *>(codes + 16));
-        R.c = __ldg(reinterpret_cast<const uint16_t *>(chunk + 4096 + r * 16 + 2 * t));
-    }
-}
-
 __device__ __forceinline__ int sext8(uint32_t w, int i) { return (int)(int8_t)((w >> (8 * i)) & 0xff); }
 
-// Computes this lane's integer contributions for one chunk and, on lane 0 of the row, the exact
-// fp32 term(s) of the super-block.  q/da/bs point at the chunk's activation in shared memory.
+// Per-warp shared region: the chunk's codes for the block's two row groups, then its activation.
 template <int DT>
-__device__ __forceinline__ void gemv_compute(const LaneRegs &R, int t, const int8_t *__restrict__ q,
-                                             const float *__restrict__ da, const int16_t *__restrict__ bs,
-                                             float *term_out) {
-    const int c = t >> 1, seg = t & 1;
+struct GemvWarpSmem {
+    static constexpr int CB = chunk_bytes(DT);
+    static constexpr int Q_OFF = 2 * CB;          // int8 q[256]
+    static constexpr int D_OFF = Q_OFF + 256;     // f32 d: 1 (Q8_K) or 8 (Q8_1)
+    static constexpr int B_OFF = D_OFF + 32;      // int16 bsums[16]
+    static constexpr int BYTES = B_OFF + 32;      // multiple of 16
+};
+
+// One lane = one row: the exact fp32 term(s) of (row, chunk) from the integer sub-block dots.
+// Q4_K: term = (d_a*d_w)*sumi - (d_a*dmin)*summ; Q6_K: term = (d_a*d_w)*sumi;
+// Q8_0: 8 terms (d_w*d_a)*P_b, one per 32-element block.
+template <int DT>
+__device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk, int r,
+                                               const int8_t *__restrict__ q, const float *__restrict__ da,
+                                               const int16_t *__restrict__ bs, float *__restrict__ term) {
     if (DT == KQ_Q4_K || DT == KQ_Q6_K) {
-        const int4 qlo = *reinterpret_cast<const int4 *>(q + 64 * c + 16 * seg);
-        const int4 qhi = *reinterpret_cast<const int4 *>(q + 64 * c + 32 + 16 * seg);
-        const uint32_t w[4] = {R.a.x, R.a.y, R.a.z, R.a.w};
-        const uint32_t hb[4] = {R.b.x, R.b.y, R.b.z, R.b.w};
-        const int ql[4] = {qlo.x, qlo.y, qlo.z, qlo.w}, qh[4] = {qhi.x, qhi.y, qhi.z, qhi.w};
-        int plo = 0, phi = 0;
+        int P[16];  // Q4_K: 8 sub-blocks of 32; Q6_K: 16 sub-blocks of 16
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t lo = w[i] & 0x0f0f0f0fu, hi = (w[i] >> 4) & 0x0f0f0f0fu;
+        for (int kb = 0; kb < 4; ++kb) {
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(chunk + kb * 512 + r * 32);
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(chunk + kb * 512 + r * 32 + 16);
+            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t hb[4] = {0u, 0u, 0u, 0u};
             if (DT == KQ_Q6_K) {
-                lo = __vsub4(lo | (((hb[i] >> (2 * seg)) & 0x03030303u) << 4), 0x20202020u);
-                hi = __vsub4(hi | (((hb[i] >> (4 + 2 * seg)) & 0x03030303u) << 4), 0x20202020u);
+                const uint4 h = *reinterpret_cast<const uint4 *>(chunk + 2048 + kb * 256 + r * 16);
+                hb[0] = h.x; hb[1] = h.y; hb[2] = h.z; hb[3] = h.w;
             }
-            plo = dp4a((int)lo, ql[i], plo);
-            phi = dp4a((int)hi, qh[i], phi);
+            const int4 qa0 = *reinterpret_cast<const int4 *>(q + 64 * kb);
+            const int4 qa1 = *reinterpret_cast<const int4 *>(q + 64 * kb + 16);
+            const int4 qb0 = *reinterpret_cast<const int4 *>(q + 64 * kb + 32);
+            const int4 qb1 = *reinterpret_cast<const int4 *>(q + 64 * kb + 48);
+            const int ql[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+            const int qh[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+            int plo[2] = {0, 0}, phi[2] = {0, 0};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int seg = i >> 2;  // elements 64kb+16seg+.. (low nibbles) / 64kb+32+16seg+.. (high)
+                uint32_t lo = w[i] & 0x0f0f0f0fu, hi = (w[i] >> 4) & 0x0f0f0f0fu;
+                if (DT == KQ_Q6_K) {
+                    lo = __vsub4(lo | (((hb[i & 3] >> (2 * seg)) & 0x03030303u) << 4), 0x20202020u);
+                    hi = __vsub4(hi | (((hb[i & 3] >> (4 + 2 * seg)) & 0x03030303u) << 4), 0x20202020u);
+                }
+                plo[seg] = dp4a((int)lo, ql[i], plo[seg]);
+                phi[seg] = dp4a((int)hi, qh[i], phi[seg]);
+            }
+            if (DT == KQ_Q4_K) {
+                P[2 * kb] = plo[0] + plo[1];      // sub-block 2kb   (elements 64kb .. 64kb+31)
+                P[2 * kb + 1] = phi[0] + phi[1];  // sub-block 2kb+1 (elements 64kb+32 .. 64kb+63)
+            } else {
+                P[4 * kb] = plo[0];      // sub-block 4kb   (elements 64kb .. +15)
+                P[4 * kb + 1] = plo[1];  // sub-block 4kb+1 (64kb+16 .. +31)
+                P[4 * kb + 2] = phi[0];  // sub-block 4kb+2 (64kb+32 .. +47)
+                P[4 * kb + 3] = phi[1];  // sub-block 4kb+3 (64kb+48 .. +63)
+            }
         }
         if (DT == KQ_Q4_K) {
+            const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + 2048 + r * 16);
             uint8_t s12[12];
-            const uint32_t hw[3] = {R.b.y, R.b.z, R.b.w};
+            const uint32_t hw[3] = {hv.y, hv.z, hv.w};
 #pragma unroll
             for (int i = 0; i < 12; ++i) s12[i] = (hw[i / 4] >> (8 * (i % 4))) & 0xff;
-            int sc0, m0, sc1, m1;
-            q4k_scale_min(s12, 2 * c, sc0, m0);
-            q4k_scale_min(s12, 2 * c + 1, sc1, m1);
-            int sumi = sc0 * plo + sc1 * phi;
-            // bsums of the lane's two 16-element groups; the partner lane (t ^ 1) adds the other
-            // half of each sub-block, so the row-wide integer sum over lanes is exact.
-            int summ = m0 * bs[4 * c + seg] + m1 * bs[4 * c + 2 + seg];
+            const uint4 b0 = *reinterpret_cast<const uint4 *>(bs);
+            const uint4 b1 = *reinterpret_cast<const uint4 *>(bs + 8);
+            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            int sumi = 0, summ = 0;
 #pragma unroll
-            for (int s = 4; s >= 1; s >>= 1) {
-                sumi += __shfl_xor_sync(0xffffffffu, sumi, s);
-                summ += __shfl_xor_sync(0xffffffffu, summ, s);
+            for (int j = 0; j < 8; ++j) {
+                int sc, mn;
+                q4k_scale_min(s12, j, sc, mn);
+                sumi += sc * P[j];
+                // bsums 2j and 2j+1 are the two int16 halves of word j
+                summ += mn * ((int)(int16_t)(bw[j] & 0xffff) + (int)(int16_t)(bw[j] >> 16));
             }
-            if (t == 0) {
-                const float dw = half_bits_to_float((uint16_t)(R.b.x & 0xffff));
-                const float dmin = half_bits_to_float((uint16_t)(R.b.x >> 16));
-                const float a = da[0];
-                float t1 = __fmul_rn(a, dw);
-                float t2 = __fmul_rn(t1, (float)sumi);
-                float t3 = __fmul_rn(a, dmin);
-                float t4 = __fmul_rn(t3, (float)summ);
-                term_out[0] = __fsub_rn(t2, t4);
-            }
+            const float dw = half_bits_to_float((uint16_t)(hv.x & 0xffff));
+            const float dmin = half_bits_to_float((uint16_t)(hv.x >> 16));
+            const float a = da[0];
+            const float t1 = __fmul_rn(a, dw);
+            const float t2 = __fmul_rn(t1, (float)sumi);
+            const float t3 = __fmul_rn(a, dmin);
+            const float t4 = __fmul_rn(t3, (float)summ);
+            term[0] = __fsub_rn(t2, t4);
         } else {
-            // sub-blocks of 16: low run = 4c+seg, high run = 4c+2+seg (scale bytes seg and 2+seg of R.c)
-            int sumi = sext8(R.c, seg) * plo + sext8(R.c, 2 + seg) * phi;
+            const uint4 sv = *reinterpret_cast<const uint4 *>(chunk + 3072 + r * 16);
+            const uint32_t sw4[4] = {sv.x, sv.y, sv.z, sv.w};
+            int sumi = 0;
 #pragma unroll
-            for (int s = 4; s >= 1; s >>= 1) sumi += __shfl_xor_sync(0xffffffffu, sumi, s);
-            if (t == 0) {
-                const float dw = half_bits_to_float((uint16_t)R.d);
-                const float t1 = __fmul_rn(da[0], dw);
-                term_out[0] = __fmul_rn(t1, (float)sumi);
-            }
+            for (int j = 0; j < 16; ++j) sumi += sext8(sw4[j / 4], j % 4) * P[j];
+            const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + r * 2));
+            const float t1 = __fmul_rn(da[0], dw);
+            term[0] = __fmul_rn(t1, (float)sumi);
         }
     } else {
-        const int4 q0 = *reinterpret_cast<const int4 *>(q + 32 * t);
-        const int4 q1 = *reinterpret_cast<const int4 *>(q + 32 * t + 16);
-        int p = 0;
-        p = dp4a((int)R.a.x, q0.x, p); p = dp4a((int)R.a.y, q0.y, p);
-        p = dp4a((int)R.a.z, q0.z, p); p = dp4a((int)R.a.w, q0.w, p);
-        p = dp4a((int)R.b.x, q1.x, p); p = dp4a((int)R.b.y, q1.y, p);
-        p = dp4a((int)R.b.z, q1.z, p); p = dp4a((int)R.b.w, q1.w, p);
-        const float dw = half_bits_to_float((uint16_t)R.c);
-        const float t1 = __fmul_rn(dw, da[t]);
-        term_out[t] = __fmul_rn(t1, (float)p);
+        const uint4 dv = *reinterpret_cast<const uint4 *>(chunk + 4096 + r * 16);
+        const uint32_t dw4[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const uint8_t *codes = chunk + (b >> 1) * 1024 + r * 64 + 32 * (b & 1);
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(codes);
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(codes + 16);
+            const int4 q0 = *reinterpret_cast<const int4 *>(q + 32 * b);
+            const int4 q1 = *reinterpret_cast<const int4 *>(q + 32 * b + 16);
+            int p = 0;
+            p = dp4a((int)a0.x, q0.x, p); p = dp4a((int)a0.y, q0.y, p);
+            p = dp4a((int)a0.z, q0.z, p); p = dp4a((int)a0.w, q0.w, p);
+            p = dp4a((int)a1.x, q1.x, p); p = dp4a((int)a1.y, q1.y, p);
+            p = dp4a((int)a1.z, q1.z, p); p = dp4a((int)a1.w, q1.w, p);
+            const float dw = half_bits_to_float((uint16_t)((dw4[b >> 1] >> (16 * (b & 1))) & 0xffff));
+            const float t1 = __fmul_rn(dw, da[b]);
+            term[b] = __fmul_rn(t1, (float)p);
+        }
     }
 }
 
-// grid: (S, groups); cluster (S, 1, 1).  CTA rank k of a cluster covers chunks [k*cpr, ...).
+// grid: (S, ceil(N/32)); cluster (S, 1, 1) when S > 1; block: 32 * cpr threads.  Warp w of cluster
+// rank k owns chunk k*cpr + w for all 32 rows of the block (lane = row): it bulk-copies that chunk's
+// codes for the block's two row groups into its own shared region, quantises (or copies) the
+// chunk's activation there, and forms the 32 rows' terms.  No warp waits for another until the
+// final ordered reduction.
 template <int DT, bool FUSED>
-__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__restrict__ w,
-                                                            const float *__restrict__ x,
-                                                            const uint8_t *__restrict__ xq, int64_t N,
-                                                            int nchunk, int cpr, float *__restrict__ y) {
+__global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const uint8_t *__restrict__ w,
+                                                                         const float *__restrict__ x,
+                                                                         const uint8_t *__restrict__ xq,
+                                                                         int64_t N, int nchunk, int cpr,
+                                                                         float *__restrict__ y) {
     using Tr = GemvTraits<DT>;
-    extern __shared__ __align__(16) uint8_t smem[];
+    using WS = GemvWarpSmem<DT>;
+    constexpr int CB = chunk_bytes(DT);
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t bars[kGemvMaxWarps];
+    __shared__ uint64_t gather_bar;  // cluster rank 0: one arrival per other rank once its terms landed
+    __shared__ int abort_flag;
     const int S = gridDim.x;
     const int rank = blockIdx.x;
-    const int64_t g = blockIdx.y;
+    const int64_t rb = blockIdx.y;                   // 32-row block = row groups 2rb, 2rb+1
+    const int64_t groups_total = (N + 15) / 16;
+    const int64_t g0 = rb * 2;
+    const int ngroups = (int)min((int64_t)2, groups_total - g0);
     const int c_begin = rank * cpr;
-    const int c_end = min(nchunk, c_begin + cpr);
-    const int nloc = max(0, c_end - c_begin);
+    const int nloc = max(0, min(nchunk, c_begin + cpr) - c_begin);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tstride = cpr * Tr::terms;
+    // shared layout: per-warp buffers [cpr][WS] | terms [32][cpr*terms] | (S > 1) gather [S-1][32][cpr*terms]
+    float *terms = reinterpret_cast<float *>(smem + (size_t)cpr * WS::BYTES);
+    float *gather = terms + kGemvRows * tstride;
 
-    // shared layout: q [cpr*256] | da [cpr*terms_per_chunk_d] | bs [cpr*16] | terms [16][cpr*terms]
-    constexpr int kDaPerChunk = Tr::q81 ? 8 : 1;
-    int8_t *q_s = reinterpret_cast<int8_t *>(smem);
-    float *da_s = reinterpret_cast<float *>(smem + cpr * 256);
-    int16_t *bs_s = reinterpret_cast<int16_t *>(smem + cpr * 256 + cpr * kDaPerChunk * 4);
-    float *terms = reinterpret_cast<float *>(smem + cpr * 256 + cpr * kDaPerChunk * 4 + cpr * 32);
-
-    const int tid = threadIdx.x;
-    const int slot = tid >> 7, r = (tid >> 3) & 15, t = tid & 7;
-    const int cb = chunk_bytes(DT);
-    const uint8_t *wg = w + (g * nchunk) * (int64_t)cb;
-
-    // issue the first chunk's weight loads before touching the activation
-    LaneRegs cur;
-    int c = c_begin + slot;
-    if (c < c_end) gemv_load<DT>(wg + (int64_t)c * cb, r, t, cur);
-
-    // ---- activation prologue: quantise (FUSED) or copy the K range into shared memory
-    const int warp = tid >> 5, lane = tid & 31;
-    if (FUSED) {
-        if (!Tr::q81) {
-            for (int cc = warp; cc < nloc; cc += kGemvThreads / 32)
-                warp_quantize_q8k_smem(x + (int64_t)(c_begin + cc) * 256, q_s + cc * 256, da_s + cc, bs_s + cc * 16);
-        } else {
-            for (int part = warp; part < nloc * 2; part += kGemvThreads / 32)
-                warp_quantize_q8_1x4_smem(x + (int64_t)c_begin * 256 + part * 128, q_s + part * 128, da_s + part * 4);
-        }
-    } else {
-        if (!Tr::q81) {
-            for (int cc = warp; cc < nloc; cc += kGemvThreads / 32) {
-                const uint8_t *blk = xq + (int64_t)(c_begin + cc) * kQ8KBytes;
-                const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4);
-                reinterpret_cast<uint2 *>(q_s + cc * 256)[lane] = make_uint2(src[2 * lane], src[2 * lane + 1]);
-                if (lane < 16) bs_s[cc * 16 + lane] = reinterpret_cast<const int16_t *>(blk + 260)[lane];
-                if (lane == 0) da_s[cc] = *reinterpret_cast<const float *>(blk);
-            }
-        } else {
-            for (int b = tid; b < nloc * 8; b += kGemvThreads) {
-                const uint8_t *blk = xq + ((int64_t)c_begin * 8 + b) * kQ81Bytes;
-                const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4);
-                uint32_t *dst = reinterpret_cast<uint32_t *>(q_s + b * 32);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = src[i];
-                da_s[b] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-            }
-        }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < cpr; ++i) mbar_init(&bars[i], 1);
+        if (S > 1) mbar_init(&gather_bar, S - 1);
+        abort_flag = 0;
+        fence_mbar_init();
     }
     __syncthreads();
+    if (S > 1) cluster_arrive_relaxed();  // "my barriers are initialised"; waited for before any remote access
+    // Let the next kernel in the stream get scheduled; it waits on this grid before touching memory.
+    grid_launch_dependents();
 
-    // ---- main loop: two chunk slots in flight per row, next chunk prefetched into registers
-    const int tstride = cpr * Tr::terms;
-    for (; c < c_end; c += 2) {
-        LaneRegs nxt;
-        const int cn = c + 2;
-        if (cn < c_end) gemv_load<DT>(wg + (int64_t)cn * cb, r, t, nxt);
-        const int cl = c - c_begin;
-        gemv_compute<DT>(cur, t, q_s + cl * 256, da_s + cl * kDaPerChunk, bs_s + cl * 16,
-                         terms + r * tstride + cl * Tr::terms);
-        cur = nxt;
+    const bool active = warp < nloc;
+    const int c = c_begin + warp;
+    uint8_t *ws = smem + (size_t)warp * WS::BYTES;
+    // The weight is staged once and never written by the kernel that runs just before this one in
+    // the stream, so its copy starts before the dependency wait and overlaps that kernel's tail.
+    if (active && lane == 0) {
+        mbar_arrive_expect_tx(&bars[warp], ngroups * CB);
+        for (int gi = 0; gi < ngroups; ++gi)
+            bulk_load(ws + gi * CB, w + ((g0 + gi) * nchunk + c) * (int64_t)CB, CB, &bars[warp]);
+    }
+    // Everything below reads memory (the activation) that an earlier kernel may have written.
+    grid_dependency_wait();
+    if (active) {
+        int8_t *q_s = reinterpret_cast<int8_t *>(ws + WS::Q_OFF);
+        float *da_s = reinterpret_cast<float *>(ws + WS::D_OFF);
+        int16_t *bs_s = reinterpret_cast<int16_t *>(ws + WS::B_OFF);
+        if (FUSED) {
+            if (!Tr::q81) {
+                warp_quantize_q8k_smem(x + (int64_t)c * 256, q_s, da_s, bs_s);
+            } else {
+                warp_quantize_q8_1x4_smem(x + (int64_t)c * 256, q_s, da_s);
+                warp_quantize_q8_1x4_smem(x + (int64_t)c * 256 + 128, q_s + 128, da_s + 4);
+            }
+        } else if (!Tr::q81) {
+            const uint8_t *blk = xq + (int64_t)c * kQ8KBytes;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4);
+            reinterpret_cast<uint2 *>(q_s)[lane] = make_uint2(src[2 * lane], src[2 * lane + 1]);
+            if (lane < 16) bs_s[lane] = reinterpret_cast<const int16_t *>(blk + 260)[lane];
+            if (lane == 0) da_s[0] = *reinterpret_cast<const float *>(blk);
+        } else {
+            const int b = lane >> 2, part = lane & 3;  // 8 blocks x 4 lanes
+            const uint8_t *blk = xq + ((int64_t)c * 8 + b) * kQ81Bytes;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4 + 8 * part);  // 4-byte aligned
+            reinterpret_cast<uint2 *>(q_s + 32 * b)[part] = make_uint2(src[0], src[1]);
+            if (part == 0) da_s[b] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+        }
+        __syncwarp();
+        if (mbar_wait_sleep(&bars[warp], 0, &abort_flag)) {
+            const int gi = lane >> 4;
+            if (gi < ngroups)
+                gemv_row_chunk<DT>(ws + gi * CB, lane & 15, q_s, da_s, bs_s, terms + lane * tstride + warp * Tr::terms);
+        } else if (lane == 0) {
+            int no_abort = 0;  // drain this warp's copies (bounded) before the block may exit
+            mbar_wait(&bars[warp], 0, &no_abort, 100000000ull);
+        }
     }
 
     // ---- ordered reduction: one thread per row adds the row's terms in ascending K order
     if (S == 1) {
         __syncthreads();
-        if (tid < 16) {
-            const int64_t n = g * 16 + tid;
+        if (threadIdx.x < kGemvRows) {
+            const int64_t n = rb * kGemvRows + threadIdx.x;
             float acc = 0.0f;
-            for (int i = 0; i < nloc * Tr::terms; ++i) acc = __fadd_rn(acc, terms[tid * tstride + i]);
-            if (n < N) y[n] = acc;
+            for (int i = 0; i < nloc * Tr::terms; ++i) acc = __fadd_rn(acc, terms[threadIdx.x * tstride + i]);
+            if (n < N) y[n] = abort_flag ? __int_as_float(0x7fc00000) : acc;
         }
     } else {
+        // Every rank pushes its terms into rank 0's gather buffer and signals rank 0's barrier; only
+        // rank 0 waits, then adds each row's terms in ascending K order.
         cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (rank == 0 && tid < 16) {
-            const int64_t n = g * 16 + tid;
-            float acc = 0.0f;
-            for (int k = 0; k < S; ++k) {
-                const float *rt = cluster.map_shared_rank(terms, k);
-                const int kb = k * cpr, ke = min(nchunk, kb + cpr);
-                const int cnt = max(0, ke - kb) * Tr::terms;
-                for (int i = 0; i < cnt; ++i) acc = __fadd_rn(acc, rt[tid * tstride + i]);
+        cluster_wait();  // every CTA of the cluster has initialised its barriers
+        __syncthreads();
+        const int per = kGemvRows * tstride;
+        if (rank != 0) {
+            float *dst = cluster.map_shared_rank(gather, 0) + (size_t)(rank - 1) * per;
+            for (int i = threadIdx.x; i < per; i += blockDim.x) dst[i] = terms[i];
+            fence_acq_rel_cluster();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                if (abort_flag) *cluster.map_shared_rank(&abort_flag, 0) = 1;
+                fence_acq_rel_cluster();
+                mbar_arrive_remote(&gather_bar, 0);
             }
-            if (n < N) y[n] = acc;
+        } else {
+            const bool got = mbar_wait_sleep(&gather_bar, 0, &abort_flag);
+            if (threadIdx.x < kGemvRows) {
+                const int64_t n = rb * kGemvRows + threadIdx.x;
+                float acc = 0.0f;
+                for (int k = 0; k < S; ++k) {
+                    const int kb = k * cpr, ke = min(nchunk, kb + cpr);
+                    const int cnt = max(0, ke - kb) * Tr::terms;
+                    const float *src = (k == 0 ? terms : gather + (size_t)(k - 1) * per) + threadIdx.x * tstride;
+                    for (int i = 0; i < cnt; ++i) acc = __fadd_rn(acc, src[i]);
+                }
+                if (n < N) y[n] = (!got || abort_flag) ? __int_as_float(0x7fc00000) : acc;
+            }
         }
-        cluster.sync();
     }
 }
 
@@ -251,35 +299,44 @@ template <int DT, bool FUSED>
 static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq, int64_t N, int64_t K, float *y,
                              cudaStream_t st) {
     using Tr = GemvTraits<DT>;
+    using WS = GemvWarpSmem<DT>;
     const int nchunk = (int)(K / 256);
-    const int64_t groups = (N + 15) / 16;
-    // split K across a cluster when there are too few row groups to fill the GPU
+    const int64_t rblocks = (N + kGemvRows - 1) / kGemvRows;
+    // Smallest power-of-two cluster split (at most 8) with at most 32 chunks per block; then split
+    // further while there are fewer than two blocks per SM and each block keeps >= 5 chunks.
     int S = 1;
-    while (S < 8 && groups * S < 4 * 152 && nchunk >= 4 * S * 2) S *= 2;
+    while (S < 8 && (nchunk + S - 1) / S > kGemvMaxWarps) S *= 2;
+    if ((nchunk + S - 1) / S > kGemvMaxWarps)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemv: K=%lld too large (at most %d)", (long long)K,
+                    8 * kGemvMaxWarps * 256);
+    while (S < 8 && rblocks * S < 2 * 152 && (nchunk + 2 * S - 1) / (2 * S) >= 5) S *= 2;
     const int cpr = (nchunk + S - 1) / S;
-    constexpr int kDaPerChunk = Tr::q81 ? 8 : 1;
-    const size_t smem = (size_t)cpr * 256 + (size_t)cpr * kDaPerChunk * 4 + (size_t)cpr * 32 +
-                        (size_t)16 * cpr * Tr::terms * 4;
-    if (smem > 200 * 1024) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: K=%lld too large", (long long)K);
-    if (groups > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: N=%lld too large", (long long)N);
+    const size_t smem = (size_t)cpr * WS::BYTES + (size_t)S * kGemvRows * cpr * Tr::terms * 4;
+    if (smem > 220 * 1024) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: K=%lld too large", (long long)K);
+    if (rblocks > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: N=%lld too large", (long long)N);
     auto kern = gemv_kernel<DT, FUSED>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: %s", cudaGetErrorString(e));
-    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S, (unsigned)groups, 1);
-    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.gridDim = dim3(S, (unsigned)rblocks, 1);
+    cfg.blockDim = dim3(32 * cpr, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = S;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (S > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = S;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, w, x, xq, N, nchunk, cpr, y);
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, kern, w, x, xq, N, nchunk, cpr, y);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: launch failed: %s", cudaGetErrorString(e));
     count_launch(R_GEMV);
     return KQ_OK;

@@ -21,6 +21,7 @@
 // warps 8-11 weight converters, warp 12 TMA producer, warp 13 MMA issuer and TMEM owner.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records an error in the workspace's
 // device flag and leaves after draining its own copies and MMAs; it never spins forever.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,8 +43,7 @@ struct TcCfg<KQ_Q4_K> {
     static constexpr int NSA = 4, NSB = 4;
     static constexpr int B_STAGE = TILE_BYTES;   // one tile
     static constexpr int CB = kQ4KChunk;        // packed chunk bytes per row group
-    static constexpr int HB = 256, HOFF = 2048;  // header bytes per row group, offset in chunk
-    static constexpr int HSLOT = 8 * 256;
+    static constexpr int HSLOT = 128 * 8;        // per-row (d, -dmin) float pairs of one super-block
     static constexpr bool EXT = true;
 };
 template <>
@@ -51,8 +51,7 @@ struct TcCfg<KQ_Q6_K> {
     static constexpr int NSA = 4, NSB = 3;
     static constexpr int B_STAGE = 2 * TILE_BYTES;  // lo and hi tiles
     static constexpr int CB = kQ6KChunk;
-    static constexpr int HB = 32, HOFF = 3328;     // f16 d plane
-    static constexpr int HSLOT = 8 * 32;
+    static constexpr int HSLOT = 128 * 8;          // per-row (d, 0) float pairs of one super-block
     static constexpr bool EXT = false;
 };
 
@@ -80,8 +79,26 @@ struct TcParams {
     float *y;
     int64_t ldy;
     int M, N, K, M_pad;
-    unsigned long long *err;  // device flag (workspace header)
+    int nsplit, sb_per_split;  // split-K: cluster rank z covers super-blocks [z*sb_per_split, ...)
+    unsigned long long *err;   // device flag (workspace header)
 };
+
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+          "l"(*reinterpret_cast<uint64_t *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
+}
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
@@ -165,7 +182,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t *b_full = a_empty + C::NSA, *b_empty = b_full + C::NSB;
     uint64_t *p_full = b_empty + C::NSB, *p_empty = p_full + 2;
     uint64_t *e_full = p_empty + 2, *be_full = e_full + 2, *e_empty = be_full + 2;
-    uint64_t *h_full = e_empty + 2, *h_empty = h_full + 4;
+    uint64_t *h_full = e_empty + 2, *h_empty = h_full + 4;  // per-super-block row-scale ring (4 slots)
     uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
@@ -173,8 +190,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * TC_N, m0 = blockIdx.y * TC_M;
-    const int nsb = P.K / 256;
-    const int nchunk = nsb;
+    const int nchunk = P.K / 256;
+    const int sb0 = blockIdx.z * P.sb_per_split;
+    const int nsb = min(nchunk, sb0 + P.sb_per_split) - sb0;  // super-blocks of this CTA (t = sb - sb0)
     const int groups_total = (P.N + 15) / 16;
     const int g0 = n0 / 16;
     const int valid_groups = min(8, groups_total - g0);
@@ -188,7 +206,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&e_full[i], 1); mbar_init(&be_full[i], 128); mbar_init(&e_empty[i], 1);
             mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 8);
         }
-        for (int i = 0; i < 4; ++i) { mbar_init(&h_full[i], 1); mbar_init(&h_empty[i], 8); }
+        for (int i = 0; i < 4; ++i) { mbar_init(&h_full[i], 128); mbar_init(&h_empty[i], 8); }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -202,42 +220,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_holder;
+    float acc[64];       // epilogue: this thread's 64 outputs (token row, column half)
+    bool epi_ok = false;
 
     if (warp == 12) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int last_a[C::NSA], last_p[2], last_h[4], last_e[2];
+            int last_a[C::NSA], last_p[2], last_e[2];
             for (int i = 0; i < C::NSA; ++i) last_a[i] = -1;
             for (int i = 0; i < 2; ++i) { last_p[i] = -1; last_e[i] = -1; }
-            for (int i = 0; i < 4; ++i) last_h[i] = -1;
             bool ok = true;
             for (int sb = 0; sb < nsb && ok; ++sb) {
+                const int gsb = sb0 + sb;
                 const int p = sb & 1, pph = (sb >> 1) & 1;
                 if (!(ok = mbar_wait(&p_empty[p], pph ^ 1, abort_flag))) break;
                 mbar_arrive_expect_tx(&p_full[p], valid_groups * C::CB);
                 for (int gi = 0; gi < valid_groups; ++gi)
-                    bulk_load(sP + (p * 8 + gi) * C::CB, P.w + ((int64_t)(g0 + gi) * nchunk + sb) * C::CB, C::CB,
+                    bulk_load(sP + (p * 8 + gi) * C::CB, P.w + ((int64_t)(g0 + gi) * nchunk + gsb) * C::CB, C::CB,
                               &p_full[p]);
                 last_p[p] = pph;
-                const int h = sb & 3, hph = (sb >> 2) & 1;
-                if (!(ok = mbar_wait(&h_empty[h], hph ^ 1, abort_flag))) break;
-                mbar_arrive_expect_tx(&h_full[h], valid_groups * C::HB);
-                for (int gi = 0; gi < valid_groups; ++gi)
-                    bulk_load(sH + h * C::HSLOT + gi * C::HB,
-                              P.w + ((int64_t)(g0 + gi) * nchunk + sb) * C::CB + C::HOFF, C::HB, &h_full[h]);
-                last_h[h] = hph;
                 if (C::EXT) {
                     const int e = sb & 1, eph = (sb >> 1) & 1;
                     if (!(ok = mbar_wait(&e_empty[e], eph ^ 1, abort_flag))) break;
                     mbar_arrive_expect_tx(&e_full[e], 4096);
-                    tma_load_2d(sEA + e * 4096, &tmE, &e_full[e], sb * 16, m0);
+                    tma_load_2d(sEA + e * 4096, &tmE, &e_full[e], gsb * 16, m0);
                     last_e[e] = eph;
                 }
                 for (int kb = 0; kb < 4; ++kb) {
                     const int kk = sb * 4 + kb, s = kk % C::NSA, ph = (kk / C::NSA) & 1;
                     if (!(ok = mbar_wait(&a_empty[s], ph ^ 1, abort_flag))) break;
                     mbar_arrive_expect_tx(&a_full[s], TILE_BYTES);
-                    tma_load_2d(sA + s * TILE_BYTES, &tmA, &a_full[s], sb * 256 + kb * TC_KB, m0);
+                    tma_load_2d(sA + s * TILE_BYTES, &tmA, &a_full[s], gsb * 256 + kb * TC_KB, m0);
                     last_a[s] = ph;
                 }
             }
@@ -250,8 +263,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (last_p[i] >= 0) { no_abort = 0; mbar_wait(&p_full[i], last_p[i], &no_abort, 100000000ull); }
                     if (last_e[i] >= 0) { no_abort = 0; mbar_wait(&e_full[i], last_e[i], &no_abort, 100000000ull); }
                 }
-                for (int i = 0; i < 4; ++i)
-                    if (last_h[i] >= 0) { no_abort = 0; mbar_wait(&h_full[i], last_h[i], &no_abort, 100000000ull); }
             }
         }
     } else if (warp == 13) {
@@ -303,44 +314,71 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ weight converters
-        const int ct = tid - 256;
+        // Thread ct owns B-tile row ct for the whole super-block: its scales are decoded once, and
+        // eight consecutive threads write eight different rows, whose swizzled 16-byte chunks fall
+        // in eight different bank groups.
+        const int row = tid - 256;
+        const bool rvalid = row < rows_valid;
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int p = sb & 1;
             if (!(ok = mbar_wait(&p_full[p], (sb >> 1) & 1, abort_flag))) break;
-            const uint8_t *pk = sP + p * 8 * C::CB;
+            const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
+            int sc[16], mn[8];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sc[j] = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mn[j] = 0;
+            float2 dpair = make_float2(0.0f, 0.0f);  // (d, -dmin) of this row for the epilogue
+            if (rvalid) {
+                if (C::EXT) {
+                    const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + 2048 + (row & 15) * 16);
+                    dpair = make_float2(half_bits_to_float((uint16_t)(hv.x & 0xffff)),
+                                        -half_bits_to_float((uint16_t)(hv.x >> 16)));
+                    uint8_t s12[12];
+                    const uint32_t hw[3] = {hv.y, hv.z, hv.w};
+#pragma unroll
+                    for (int i = 0; i < 12; ++i) s12[i] = (hw[i / 4] >> (8 * (i % 4))) & 0xff;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) q4k_scale_min(s12, j, sc[j], mn[j]);
+                } else {
+                    const uint4 sv = *reinterpret_cast<const uint4 *>(chunk + 3072 + (row & 15) * 16);
+                    const uint32_t sw4[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sc[j] = (int)(int8_t)((sw4[j / 4] >> (8 * (j % 4))) & 0xff);
+                    dpair = make_float2(half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + (row & 15) * 2)),
+                                        0.0f);
+                }
+            }
+            {
+                const int h = sb & 3;
+                if (!(ok = mbar_wait(&h_empty[h], ((sb >> 2) & 1) ^ 1, abort_flag))) break;
+                reinterpret_cast<float2 *>(sH + h * C::HSLOT)[row] = dpair;
+                mbar_arrive(&h_full[h]);
+            }
+#pragma unroll
             for (int kb = 0; kb < 4; ++kb) {
                 const int kk = sb * 4 + kb, s = kk % C::NSB;
                 if (!(ok = mbar_wait(&b_empty[s], ((kk / C::NSB) & 1) ^ 1, abort_flag))) break;
-                uint8_t *bt = sB + s * C::B_STAGE;
+                uint8_t *brow = sB + s * C::B_STAGE + row * 128;
+                if (!rvalid) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int u = ct + 128 * i, row = u >> 1, seg = u & 1;
-                    uint8_t *brow = bt + row * 128;
-                    if (row >= rows_valid) {
-                        const uint4 z = make_uint4(0, 0, 0, 0);
-                        const int sw = row & 7;
-                        const int chs[4] = {2 * seg, 2 * seg + 1, 4 + 2 * seg, 5 + 2 * seg};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            *reinterpret_cast<uint4 *>(brow + ((chs[j] ^ sw) << 4)) = z;
-                            if (!C::EXT) *reinterpret_cast<uint4 *>(brow + TILE_BYTES + ((chs[j] ^ sw) << 4)) = z;
-                        }
-                        continue;
+                    for (int j = 0; j < 8; ++j) {
+                        *reinterpret_cast<uint4 *>(brow + j * 16) = z;
+                        if (!C::EXT) *reinterpret_cast<uint4 *>(brow + TILE_BYTES + j * 16) = z;
                     }
-                    const uint8_t *chunk = pk + (row >> 4) * C::CB;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(chunk + kb * 512 + (row & 15) * 32 + seg * 16);
+                } else {
+                    const uint8_t *codes = chunk + kb * 512 + (row & 15) * 32;
+                    const uint4 v0 = *reinterpret_cast<const uint4 *>(codes);
+                    const uint4 v1 = *reinterpret_cast<const uint4 *>(codes + 16);
                     if (C::EXT) {
-                        const uint8_t *s12 = chunk + 2048 + (row & 15) * 16 + 4;
-                        int sc0, m0v, sc1, m1v;
-                        q4k_scale_min(s12, 2 * kb, sc0, m0v);
-                        q4k_scale_min(s12, 2 * kb + 1, sc1, m1v);
-                        convert_q4k_unit(v, sc0, sc1, brow, row, seg);
+                        convert_q4k_unit(v0, sc[2 * kb], sc[2 * kb + 1], brow, row, 0);
+                        convert_q4k_unit(v1, sc[2 * kb], sc[2 * kb + 1], brow, row, 1);
                     } else {
                         const uint4 h = *reinterpret_cast<const uint4 *>(chunk + 2048 + kb * 256 + (row & 15) * 16);
-                        const int8_t *scs = reinterpret_cast<const int8_t *>(chunk + 3072 + (row & 15) * 16);
-                        convert_q6k_unit(v, h, scs[4 * kb + seg], scs[4 * kb + 2 + seg], brow, brow + TILE_BYTES, row,
-                                         seg);
+                        convert_q6k_unit(v0, h, sc[4 * kb], sc[4 * kb + 2], brow, brow + TILE_BYTES, row, 0);
+                        convert_q6k_unit(v1, h, sc[4 * kb + 1], sc[4 * kb + 3], brow, brow + TILE_BYTES, row, 1);
                     }
                 }
                 fence_proxy_async_smem();
@@ -351,20 +389,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // extension B row: the 8 sub-block mins, each repeated for its two bsum groups
                 const int e = sb & 1;
                 if (!(ok = mbar_wait(&e_empty[e], ((sb >> 1) & 1) ^ 1, abort_flag))) break;
-                const int row = ct;
                 uint32_t mm[8];
-                if (row < rows_valid) {
-                    const uint8_t *s12 = pk + (row >> 4) * C::CB + 2048 + (row & 15) * 16 + 4;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        int sc, mn;
-                        q4k_scale_min(s12, j, sc, mn);
-                        mm[j] = h2u(__float2half2_rn((float)mn));
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) mm[j] = 0u;
-                }
+                for (int j = 0; j < 8; ++j) mm[j] = h2u(__float2half2_rn((float)mn[j]));
                 uint8_t *erow = sEB + e * 4096 + row * 32;
                 const int sw = (row >> 2) & 1;  // 32-byte swizzle: 16-byte chunk index ^= address bit 7
                 *reinterpret_cast<uint4 *>(erow + ((0 ^ sw) << 4)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
@@ -378,20 +405,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ------------------------------------------------------------ epilogue: per-super-block promotion
         const int wq = warp & 3, half = warp >> 2;
         const int m = m0 + 32 * wq + lane;
-        float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
         const uint32_t lane_base = tbase + ((uint32_t)(32 * wq) << 16);
-        float da_next = P.da[m];
+        float da_next = P.da[(int64_t)sb0 * P.M_pad + m];
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int buf = sb & 1, h = sb & 3;
             const float da = da_next;
-            if (sb + 1 < nsb) da_next = P.da[(int64_t)(sb + 1) * P.M_pad + m];
+            if (sb + 1 < nsb) da_next = P.da[(int64_t)(sb0 + sb + 1) * P.M_pad + m];
             if (!(ok = mbar_wait(&acc_full[buf], (sb >> 1) & 1, abort_flag))) break;
             if (!(ok = mbar_wait(&h_full[h], (sb >> 2) & 1, abort_flag))) break;
             tc_fence_after();
-            const uint8_t *hdr = sH + h * C::HSLOT;
+            const float4 *dsc = reinterpret_cast<const float4 *>(sH + h * C::HSLOT) + half * 32;
+            const float2 da2 = make_float2(da, da);
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 const int col = half * 64 + ch * 16;
@@ -400,18 +427,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tmem_ld16(lane_base + 256 + buf * TC_N + col, s2);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int nl = col + i;
+                for (int i = 0; i < 16; i += 2) {
+                    const float4 sc2 = dsc[ch * 8 + i / 2];  // (d, -dmin) of columns col+i, col+i+1
+                    float2 &a = *reinterpret_cast<float2 *>(&acc[ch * 16 + i]);
                     if (C::EXT) {
-                        const __half2 dd = *reinterpret_cast<const __half2 *>(hdr + nl * 16);
-                        const float dw = __low2float(dd), dmin = __high2float(dd);
-                        const float u = s2[i] * dmin;
-                        const float v = fmaf(s1[i], dw, -u);
-                        acc[ch * 16 + i] = fmaf(v, da, acc[ch * 16 + i]);
+                        // acc += da * (d*S1 - dmin*S2)
+                        const float2 u = fmul2(make_float2(s2[i], s2[i + 1]), make_float2(sc2.y, sc2.w));
+                        const float2 v = ffma2(make_float2(s1[i], s1[i + 1]), make_float2(sc2.x, sc2.z), u);
+                        a = ffma2(v, da2, a);
                     } else {
-                        const float dw = __half2float(*reinterpret_cast<const __half *>(hdr + nl * 2));
-                        const float v = fmaf(16.0f, s2[i], s1[i]);
-                        acc[ch * 16 + i] = fmaf(da * dw, v, acc[ch * 16 + i]);
+                        // acc += (da*d) * (S_lo + 16*S_hi)
+                        const float2 v = ffma2(make_float2(16.0f, 16.0f), make_float2(s2[i], s2[i + 1]),
+                                               make_float2(s1[i], s1[i + 1]));
+                        const float2 t = fmul2(da2, make_float2(sc2.x, sc2.z));
+                        a = ffma2(t, v, a);
                     }
                 }
             }
@@ -422,7 +451,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive(&h_empty[h]);
             }
         }
-        if (ok && m < P.M) {
+        epi_ok = ok;
+        if (ok && P.nsplit == 1 && m < P.M) {
             float *yr = P.y + (int64_t)m * P.ldy + n0 + half * 64;
             const int nrem = P.N - (n0 + half * 64);
             if (nrem >= 64 && (reinterpret_cast<uintptr_t>(yr) & 15) == 0) {
@@ -439,6 +469,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 
     __syncthreads();
+    if (P.nsplit > 1) {
+        // Split-K across the CTAs of a cluster: every CTA parks its fp32 tile in its own (now idle)
+        // pipeline buffers, then each CTA sums a slice of rows over all CTAs of the cluster in rank
+        // order through distributed shared memory and writes it -- deterministic, no workspace.
+        constexpr int RS = TC_N + 4;  // padded row stride (floats): conflict-free row-per-lane writes
+        float *red = reinterpret_cast<float *>(sA);
+        if (warp < 8) {
+            const int ml = 32 * (warp & 3) + lane;
+            float *rr = red + ml * RS + (warp >> 2) * 64;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                reinterpret_cast<float4 *>(rr)[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        }
+        cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+        cluster.sync();
+        const int S = P.nsplit, rank = blockIdx.z;
+        const int rows_per = (TC_M + S - 1) / S;
+        const int r0 = rank * rows_per, r1 = min(TC_M, r0 + rows_per);
+        for (int idx = tid; idx < (r1 - r0) * TC_N; idx += TC_THREADS) {
+            const int ml = r0 + idx / TC_N, nl = idx % TC_N;
+            float v = 0.0f;
+            for (int k = 0; k < S; ++k) v += cluster.map_shared_rank(red, k)[ml * RS + nl];
+            const int mm = m0 + ml, nn = n0 + nl;
+            if (mm < P.M && nn < P.N) P.y[(int64_t)mm * P.ldy + nn] = v;
+        }
+        cluster.sync();
+    }
+    (void)epi_ok;
     if (tid == 0 && *abort_flag) atomicAdd(P.err, 1ull);
     if (warp == 13) {
         tc_fence_after();
@@ -507,6 +565,26 @@ bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     return true;
 }
 
+// Split-K factor: the number of CTAs per output tile (a cluster along z) that best fills whole
+// waves of the 152 SMs, with at least 4 super-blocks per CTA; 1 when the tiles alone fill the GPU.
+static int tc_splits(int64_t M, int64_t N, int64_t K) {
+    const int64_t tiles = ((M + TC_M - 1) / TC_M) * ((N + TC_N - 1) / TC_N);
+    const int nsb = (int)(K / 256);
+    const int num_sms = 152;
+    if (tiles >= 2 * num_sms) return 1;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int S = 1; S <= 8; ++S) {
+        const int per = (nsb + S - 1) / S;
+        if (S > 1 && per < 4) break;
+        if ((nsb + per - 1) / per != S) continue;  // S must be exactly realisable
+        const int64_t ctas = tiles * S;
+        const double eff = (double)ctas / (double)(((ctas + num_sms - 1) / num_sms) * num_sms);
+        if (eff > best_eff + 1e-9) { best_eff = eff; best = S; }
+    }
+    return best;
+}
+
 size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     if (!tc_eligible(wt, M, N, K)) return 0;
     return tc_ws(M, K).total;
@@ -559,13 +637,28 @@ static kq_status launch_tc(const uint8_t *w, int64_t M, int64_t N, int64_t K, fl
     p.y = y;
     p.ldy = ldy;
     p.M = (int)M; p.N = (int)N; p.K = (int)K; p.M_pad = L.M_pad;
+    const int S = tc_splits(M, N, K);
+    p.nsplit = S;
+    p.sb_per_split = (int)((nsb + S - 1) / S);
     p.err = reinterpret_cast<unsigned long long *>(ws + L.off_flag);
     auto kern = tc_gemm_kernel<DT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm: %s", cudaGetErrorString(e));
-    dim3 grid((unsigned)((N + TC_N - 1) / TC_N), (unsigned)(L.M_pad / TC_M), 1);
-    kern<<<grid, TC_THREADS, Lay::ALLOC, st>>>(tmA, tmE, p);
-    return check_launch("kq_gemm (tensor core)");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + TC_N - 1) / TC_N), (unsigned)(L.M_pad / TC_M), (unsigned)S);
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Lay::ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)S;
+    cfg.attrs = attr;
+    cfg.numAttrs = S > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmE, p);
+    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm (tensor core): launch failed: %s", cudaGetErrorString(e));
+    return KQ_OK;
 }
 
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,

@@ -142,6 +142,10 @@ KQ_API kq_status kq_swiglu_quantize_q8k(const float *g, const float *u, int64_t 
                                  float *h_out, kq_stream_t stream);
 
 /* Decode GEMV, one activation column (MMVQ; [vllm-2890] MMVQ arm, [llama-18] fused-quant MMVQ).
+ * Launched with programmatic dependent launch: the kernel may start, and start streaming w, while the
+ * kernel issued just before it on `stream` is still running; it waits for that kernel before it
+ * reads x/xq or writes y.  So w must already be in place when that earlier kernel runs: stage the
+ * weights once (kq_repack_weights, then any synchronisation) as the keep-quant provider does.
  * w: native [N][K] of dtype wt (Q4_K or Q6_K: activation Q8_K; Q8_0: activation Q8_1).
  * Exactly one of x (fp32 [K]: quantised inside the kernel, no separate launch) and xq (pre-quantised
  * activation row, K/256 Q8_K or K/32 Q8_1 blocks) must be non-NULL.  y: fp32 [N].

@@ -20,6 +20,7 @@ def repack(dtype: int, w_canon: np.ndarray, N: int, K: int) -> torch.Tensor:
     src = dev(w_canon.reshape(-1))
     dst = torch.empty(kq.native_bytes(dtype, N, K), dtype=torch.uint8, device=DEV)
     kq.kq_repack_weights(dtype, src, dst, N, K)
+    torch.cuda.synchronize()   # weights are staged once, before any matmul reads them
     return dst
 
 
