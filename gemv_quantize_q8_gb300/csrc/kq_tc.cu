@@ -19,6 +19,8 @@
 //
 // Roles (448 threads): warps 0-7 epilogue (TMEM lane quarter = warp % 4, column half = warp / 4),
 // warps 8-11 weight converters, warp 12 TMA producer, warp 13 MMA issuer and TMEM owner.
+// Waiting warps sleep on their mbarrier (try_wait with a suspend hint) instead of spinning, so
+// they do not steal issue slots or shared-memory bandwidth from the converter and epilogue warps.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records an error in the workspace's
 // device flag and leaves after draining its own copies and MMAs; it never spins forever.
 #include <cooperative_groups.h>
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int sb = 0; sb < nsb && ok; ++sb) {
                 const int gsb = sb0 + sb;
                 const int p = sb & 1, pph = (sb >> 1) & 1;
-                if (!(ok = mbar_wait(&p_empty[p], pph ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&p_empty[p], pph ^ 1, abort_flag))) break;
                 mbar_arrive_expect_tx(&p_full[p], valid_groups * C::CB);
                 for (int gi = 0; gi < valid_groups; ++gi)
                     bulk_load(sP + (p * 8 + gi) * C::CB, P.w + ((int64_t)(g0 + gi) * nchunk + gsb) * C::CB, C::CB,
@@ -241,14 +243,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 last_p[p] = pph;
                 if (C::EXT) {
                     const int e = sb & 1, eph = (sb >> 1) & 1;
-                    if (!(ok = mbar_wait(&e_empty[e], eph ^ 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&e_empty[e], eph ^ 1, abort_flag))) break;
                     mbar_arrive_expect_tx(&e_full[e], 4096);
                     tma_load_2d(sEA + e * 4096, &tmE, &e_full[e], gsb * 16, m0);
                     last_e[e] = eph;
                 }
                 for (int kb = 0; kb < 4; ++kb) {
                     const int kk = sb * 4 + kb, s = kk % C::NSA, ph = (kk / C::NSA) & 1;
-                    if (!(ok = mbar_wait(&a_empty[s], ph ^ 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&a_empty[s], ph ^ 1, abort_flag))) break;
                     mbar_arrive_expect_tx(&a_full[s], TILE_BYTES);
                     tma_load_2d(sA + s * TILE_BYTES, &tmA, &a_full[s], gsb * 256 + kb * TC_KB, m0);
                     last_a[s] = ph;
@@ -273,14 +275,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             for (int sb = 0; sb < nsb && ok; ++sb) {
                 const int buf = sb & 1;
-                if (!(ok = mbar_wait(&acc_empty[buf], ((sb >> 1) & 1) ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&acc_empty[buf], ((sb >> 1) & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
                 const uint32_t d1 = tbase + buf * TC_N, d2 = tbase + 256 + buf * TC_N;
                 for (int kb = 0; kb < 4 && ok; ++kb) {
                     const int kk = sb * 4 + kb;
                     const int sa = kk % C::NSA, sbb = kk % C::NSB;
-                    if (!(ok = mbar_wait(&a_full[sa], (kk / C::NSA) & 1, abort_flag))) break;
-                    if (!(ok = mbar_wait(&b_full[sbb], (kk / C::NSB) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&a_full[sa], (kk / C::NSA) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&b_full[sbb], (kk / C::NSB) & 1, abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k16 = 0; k16 < 4; ++k16) {
@@ -299,8 +301,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!ok) break;
                 if (C::EXT) {
                     const int e = sb & 1, eph = (sb >> 1) & 1;
-                    if (!(ok = mbar_wait(&e_full[e], eph, abort_flag))) break;
-                    if (!(ok = mbar_wait(&be_full[e], eph, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&e_full[e], eph, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&be_full[e], eph, abort_flag))) break;
                     tc_fence_after();
                     mma_f16(d2, smem_desc(sEA_u + e * 4096, 256, 6), smem_desc(sEB_u + e * 4096, 256, 6), idesc, 0);
                     mma_commit(&e_empty[e]);
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int p = sb & 1;
-            if (!(ok = mbar_wait(&p_full[p], (sb >> 1) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait_sleep(&p_full[p], (sb >> 1) & 1, abort_flag))) break;
             const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
             int sc[16], mn[8];
 #pragma unroll
@@ -352,14 +354,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             {
                 const int h = sb & 3;
-                if (!(ok = mbar_wait(&h_empty[h], ((sb >> 2) & 1) ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&h_empty[h], ((sb >> 2) & 1) ^ 1, abort_flag))) break;
                 reinterpret_cast<float2 *>(sH + h * C::HSLOT)[row] = dpair;
                 mbar_arrive(&h_full[h]);
             }
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb) {
                 const int kk = sb * 4 + kb, s = kk % C::NSB;
-                if (!(ok = mbar_wait(&b_empty[s], ((kk / C::NSB) & 1) ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&b_empty[s], ((kk / C::NSB) & 1) ^ 1, abort_flag))) break;
                 uint8_t *brow = sB + s * C::B_STAGE + row * 128;
                 if (!rvalid) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (C::EXT) {
                 // extension B row: the 8 sub-block mins, each repeated for its two bsum groups
                 const int e = sb & 1;
-                if (!(ok = mbar_wait(&e_empty[e], ((sb >> 1) & 1) ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&e_empty[e], ((sb >> 1) & 1) ^ 1, abort_flag))) break;
                 uint32_t mm[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mm[j] = h2u(__float2half2_rn((float)mn[j]));
@@ -414,8 +416,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int buf = sb & 1, h = sb & 3;
             const float da = da_next;
             if (sb + 1 < nsb) da_next = P.da[(int64_t)(sb0 + sb + 1) * P.M_pad + m];
-            if (!(ok = mbar_wait(&acc_full[buf], (sb >> 1) & 1, abort_flag))) break;
-            if (!(ok = mbar_wait(&h_full[h], (sb >> 2) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait_sleep(&acc_full[buf], (sb >> 1) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait_sleep(&h_full[h], (sb >> 2) & 1, abort_flag))) break;
             tc_fence_after();
             const float4 *dsc = reinterpret_cast<const float4 *>(sH + h * C::HSLOT) + half * 32;
             const float2 da2 = make_float2(da, da);
