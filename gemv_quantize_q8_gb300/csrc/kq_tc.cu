@@ -318,8 +318,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp >= TC_EPI_WARPS) {
         // ------------------------------------------------------------ weight converters
-        // Thread (group, row) converts kblocks {group, group+2} of its weight row into its TMEM lane;
-        // group 0 also publishes the row's super-block scales (and, for Q4_K, the mins operand).
+        // Thread (group, row) converts kblocks {group, group+2} of its weight row into its TMEM lane.
+        // The kblocks go first, since the MMA waits on them; afterwards group 0 publishes the row's
+        // super-block scales for the epilogue and, for Q4_K, group 1 publishes the mins operand of the
+        // extension MMA -- both are needed only once the super-block's main MMAs are done.
         const int cw = warp - TC_EPI_WARPS, grp = cw >> 2, q = cw & 3;
         const int row = 32 * q + lane;
         const bool rvalid = row < rows_valid;
@@ -330,80 +332,54 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!(ok = mbar_wait_sleep(&p_full[p], (t >> 1) & 1, abort_flag))) break;
             // rows past N were not loaded: their scales are forced to 0, so they convert to zeros
             const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
-            int sc[16], mn[8];
+            const int r16 = row & 15;
+            // every shared-memory read of the super-block is issued up front
+            uint4 cv[2][2], qh[2];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) sc[j] = 0;
+            for (int j = 0; j < 2; ++j) {
+                const uint8_t *codes = chunk + (grp + 2 * j) * 512 + r16 * 32;
+                cv[j][0] = *reinterpret_cast<const uint4 *>(codes);
+                cv[j][1] = *reinterpret_cast<const uint4 *>(codes + 16);
+                if (!C::EXT) qh[j] = *reinterpret_cast<const uint4 *>(chunk + 2048 + (grp + 2 * j) * 256 + r16 * 16);
+            }
+            // Q4_K: d, dmin and the 12 packed scale bytes; Q6_K: the 16 int8 sub-block scales
+            uint4 hv = *reinterpret_cast<const uint4 *>(chunk + (C::EXT ? 2048 : 3072) + r16 * 16);
+            if (!rvalid) hv = make_uint4(0, 0, 0, 0);
+            int ksc[2][4];  // sub-block scales of kblocks grp and grp+2
+            if (C::EXT) {
+                // 6-bit scales: sub-block j < 4 in byte j; j >= 4 from the low nibble of byte j+4 and
+                // the top two bits of byte j-4.  Group g needs sub-blocks 2g, 2g+1, 2g+4, 2g+5.
+                const uint32_t lo = grp ? (hv.y >> 16) : hv.y;   // bytes 2g, 2g+1
+                const uint32_t hi8 = grp ? (hv.w >> 16) : hv.w;  // bytes 8+2g, 9+2g
+                ksc[0][0] = lo & 63;
+                ksc[0][1] = (lo >> 8) & 63;
+                ksc[1][0] = (hi8 & 0x0f) | (((lo >> 6) & 3) << 4);
+                ksc[1][1] = ((hi8 >> 8) & 0x0f) | (((lo >> 14) & 3) << 4);
+                ksc[0][2] = ksc[0][3] = ksc[1][2] = ksc[1][3] = 0;
+            } else {
+                const uint32_t wa = grp ? hv.y : hv.x, wb = grp ? hv.w : hv.z;  // sub-blocks 4kb..4kb+3
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mn[j] = 0;
-            float2 dpair = make_float2(0.0f, 0.0f);  // (d, -dmin) of this row for the epilogue
-            if (rvalid) {
-                if (C::EXT) {
-                    const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + 2048 + (row & 15) * 16);
-                    dpair = make_float2(half_bits_to_float((uint16_t)(hv.x & 0xffff)),
-                                        -half_bits_to_float((uint16_t)(hv.x >> 16)));
-                    uint8_t s12[12];
-                    const uint32_t hw[3] = {hv.y, hv.z, hv.w};
-#pragma unroll
-                    for (int i = 0; i < 12; ++i) s12[i] = (hw[i / 4] >> (8 * (i % 4))) & 0xff;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) q4k_scale_min(s12, j, sc[j], mn[j]);
-                } else {
-                    const uint4 sv = *reinterpret_cast<const uint4 *>(chunk + 3072 + (row & 15) * 16);
-                    const uint32_t sw4[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) sc[j] = (int)(int8_t)((sw4[j / 4] >> (8 * (j % 4))) & 0xff);
-                    dpair = make_float2(
-                        half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + (row & 15) * 2)), 0.0f);
+                for (int k = 0; k < 4; ++k) {
+                    ksc[0][k] = (int)(int8_t)((wa >> (8 * k)) & 0xff);
+                    ksc[1][k] = (int)(int8_t)((wb >> (8 * k)) & 0xff);
                 }
             }
-            if (grp == 0) {
-                const int h = t & 3;
-                if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag))) break;
-                reinterpret_cast<float2 *>(sH + h * TC_ROWS * 8)[row] = dpair;
-                mbar_arrive(&h_full[h]);
-                if (C::EXT) {
-                    // extension A row: the 8 sub-block mins, each repeated for its two bsum groups
-                    const int e = t & 1;
-                    if (!(ok = mbar_wait_sleep(&e_empty[e], ((t >> 1) & 1) ^ 1, abort_flag))) break;
-                    uint32_t mm[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) mm[j] = h2u(__float2half2_rn((float)mn[j]));
-                    uint8_t *erow = sEA + e * 4096 + row * 32;
-                    const int sw = (row >> 2) & 1;  // 32-byte swizzle: 16-byte chunk index ^= address bit 7
-                    *reinterpret_cast<uint4 *>(erow + ((0 ^ sw) << 4)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
-                    *reinterpret_cast<uint4 *>(erow + ((1 ^ sw) << 4)) = make_uint4(mm[4], mm[5], mm[6], mm[7]);
-                    fence_proxy_async_smem();
-                    mbar_arrive(&ea_full[e]);
-                }
-            }
-            // scales of this group's two kblocks, picked with constant indices (grp is warp-uniform)
-            constexpr int SPK = C::EXT ? 2 : 4;  // sub-block scales per kblock
-            int ksc[2][4];
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    ksc[j][k] = k < SPK ? (grp ? sc[SPK * (2 * j + 1) + k % SPK] : sc[SPK * (2 * j) + k % SPK]) : 0;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int kb = grp + 2 * j;
                 if (!(ok = mbar_wait_sleep(&a_empty[kb], (t & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
                 const uint32_t ta = lane_base + C::TM_A + kb * C::A_COLS;
-                const uint8_t *codes = chunk + kb * 512 + (row & 15) * 32;
-                const uint4 v0 = *reinterpret_cast<const uint4 *>(codes);
-                const uint4 v1 = *reinterpret_cast<const uint4 *>(codes + 16);
                 if (C::EXT) {
                     uint32_t r[32];
-                    convert_q4k_kblock(v0, v1, ksc[j][0], ksc[j][1], r);
+                    convert_q4k_kblock(cv[j][0], cv[j][1], ksc[j][0], ksc[j][1], r);
                     tmem_st32(ta, r);
                 } else {
-                    const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + 2048 + kb * 256 + (row & 15) * 16);
-                    const uint32_t hb[4] = {hv.x, hv.y, hv.z, hv.w};
+                    const uint32_t hb[4] = {qh[j].x, qh[j].y, qh[j].z, qh[j].w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         // sub-block 4kb+k: low nibbles of bytes 0-15 / 16-31, then high nibbles
-                        const uint4 v = (k & 1) ? v1 : v0;
+                        const uint4 v = (k & 1) ? cv[j][1] : cv[j][0];
                         const int ns = (k >> 1) * 4;
                         const uint32_t nib[4] = {v.x >> ns, v.y >> ns, v.z >> ns, v.w >> ns};
                         uint32_t lo[8], hi[8];
@@ -417,6 +393,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive(&a_full[kb]);
             }
             if (!ok) break;
+            if (grp == 0) {
+                // the row's (d, -dmin) for the epilogue
+                const int h = t & 3;
+                if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag))) break;
+                float2 dpair = make_float2(0.0f, 0.0f);
+                if (C::EXT)
+                    dpair = make_float2(half_bits_to_float((uint16_t)(hv.x & 0xffff)),
+                                        -half_bits_to_float((uint16_t)(hv.x >> 16)));
+                else if (rvalid)
+                    dpair = make_float2(
+                        half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + r16 * 2)), 0.0f);
+                reinterpret_cast<float2 *>(sH + h * TC_ROWS * 8)[row] = dpair;
+                mbar_arrive(&h_full[h]);
+            } else if (C::EXT) {
+                // extension A row: the 8 sub-block mins, each repeated for its two bsum groups
+                const int e = t & 1;
+                if (!(ok = mbar_wait_sleep(&e_empty[e], ((t >> 1) & 1) ^ 1, abort_flag))) break;
+                uint8_t s12[12];
+                const uint32_t hw[3] = {hv.y, hv.z, hv.w};
+#pragma unroll
+                for (int i = 0; i < 12; ++i) s12[i] = (hw[i / 4] >> (8 * (i % 4))) & 0xff;
+                uint32_t mm[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    int s, m;
+                    q4k_scale_min(s12, j, s, m);
+                    mm[j] = h2u(__float2half2_rn((float)m));
+                }
+                uint8_t *erow = sEA + e * 4096 + row * 32;
+                const int sw = (row >> 2) & 1;  // 32-byte swizzle: 16-byte chunk index ^= address bit 7
+                *reinterpret_cast<uint4 *>(erow + ((0 ^ sw) << 4)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
+                *reinterpret_cast<uint4 *>(erow + ((1 ^ sw) << 4)) = make_uint4(mm[4], mm[5], mm[6], mm[7]);
+                fence_proxy_async_smem();
+                mbar_arrive(&ea_full[e]);
+            }
             mbar_arrive(&p_empty[p]);
         }
     } else {
