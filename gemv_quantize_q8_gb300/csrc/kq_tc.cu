@@ -19,10 +19,11 @@
 // The integer parts are therefore the oracle's integers; only the fp32 scaling uses fused
 // multiply-adds, which keeps the result within a few ulps of the sequential CPU order.
 //
-// Roles (832 threads, 26 warps): warps 0-15 epilogue (TMEM lane quarter = warp % 4, token quarter =
+// Roles (864 threads, 27 warps): warps 0-15 epilogue (TMEM lane quarter = warp % 4, token quarter =
 // warp / 4), warps 16-23 weight converters (lane quarter = warp % 4; warps 16-19 convert kblocks 0
-// and 2 of every super-block, warps 20-23 kblocks 1 and 3), warp 24 TMA producer, warp 25 MMA
-// issuer and TMEM owner.
+// and 2 of every super-block, warps 20-23 kblocks 1 and 3), warp 24 producer of the packed weights,
+// bsums and activation scales, warp 25 MMA issuer and TMEM owner, warp 26 producer of the
+// activation tiles (a stream of its own, so it runs ahead without waiting on the other rings).
 // Waiting warps sleep on their mbarrier (try_wait with a suspend hint) instead of spinning, so
 // they do not steal issue slots or shared-memory bandwidth from the converter and epilogue warps.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records an error in the workspace's
@@ -43,7 +44,8 @@ constexpr int TC_TOK = 128;   // tokens per CTA: MMA N, TMEM columns of one accu
 constexpr int TC_KB = 64;     // K elements per kblock (one activation tile, one TMEM A stage)
 constexpr int TC_EPI_WARPS = 16, TC_CONV_WARPS = 8;
 constexpr int TC_WARP_PROD = TC_EPI_WARPS + TC_CONV_WARPS, TC_WARP_MMA = TC_WARP_PROD + 1;
-constexpr int TC_THREADS = (TC_WARP_MMA + 1) * 32;
+constexpr int TC_WARP_ACT = TC_WARP_MMA + 1;
+constexpr int TC_THREADS = (TC_WARP_ACT + 1) * 32;
 constexpr int ACT_TILE = TC_TOK * TC_KB * 2;  // 16 KB: 128 tokens x 64 f16
 constexpr int NACT = 8;                       // activation ring: two super-blocks ahead
 constexpr int TMEM_COLS = 512;
@@ -208,10 +210,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_mbar_init();
     }
     if (warp == TC_WARP_MMA) tmem_alloc(tmem_holder, TMEM_COLS);
-    if (warp == TC_WARP_PROD && lane == 0) {
-        prefetch_tmap(&tmA);
-        if (C::EXT) prefetch_tmap(&tmE);
-    }
+    if (warp == TC_WARP_ACT && lane == 0) prefetch_tmap(&tmA);
+    if (C::EXT && warp == TC_WARP_PROD && lane == 0) prefetch_tmap(&tmE);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -219,10 +219,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     float acc[32];  // epilogue: this thread's 32 outputs (one weight row, a quarter of the tokens)
 
     if (warp == TC_WARP_PROD) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ weight-side producer
         if (lane == 0) {
-            int last_a[NACT], last_p[2], last_e[2], last_d[4];
-            for (int i = 0; i < NACT; ++i) last_a[i] = -1;
+            int last_p[2], last_e[2], last_d[4];
             for (int i = 0; i < 2; ++i) { last_p[i] = -1; last_e[i] = -1; }
             for (int i = 0; i < 4; ++i) last_d[i] = -1;
             bool ok = true;
@@ -249,25 +248,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     bulk_load(sDA + h * TC_TOK * 4, P.da + (int64_t)gsb * P.M_pad + m0, TC_TOK * 4, &da_full[h]);
                     last_d[h] = hph;
                 }
-                for (int kb = 0; kb < 4; ++kb) {
-                    const int kk = t * 4 + kb, s = kk % NACT, ph = (kk / NACT) & 1;
-                    if (!(ok = mbar_wait_sleep(&act_empty[s], ph ^ 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(&act_full[s], ACT_TILE);
-                    tma_load_2d(sAct + s * ACT_TILE, &tmA, &act_full[s], gsb * 256 + kb * TC_KB, m0);
-                    last_a[s] = ph;
-                }
             }
             if (!ok) {
                 // drain: wait (bounded) for every copy this thread issued to land before leaving
                 volatile int no_abort = 0;
-                for (int i = 0; i < NACT; ++i)
-                    if (last_a[i] >= 0) { no_abort = 0; mbar_wait(&act_full[i], last_a[i], &no_abort, 100000000ull); }
                 for (int i = 0; i < 2; ++i) {
                     if (last_p[i] >= 0) { no_abort = 0; mbar_wait(&p_full[i], last_p[i], &no_abort, 100000000ull); }
                     if (last_e[i] >= 0) { no_abort = 0; mbar_wait(&eb_full[i], last_e[i], &no_abort, 100000000ull); }
                 }
                 for (int i = 0; i < 4; ++i)
                     if (last_d[i] >= 0) { no_abort = 0; mbar_wait(&da_full[i], last_d[i], &no_abort, 100000000ull); }
+            }
+        }
+    } else if (warp == TC_WARP_ACT) {
+        // ------------------------------------------------------------ activation-tile producer
+        if (lane == 0) {
+            int last_a[NACT];
+            for (int i = 0; i < NACT; ++i) last_a[i] = -1;
+            bool ok = true;
+            for (int kk = 0; kk < nsb * 4 && ok; ++kk) {
+                const int s = kk % NACT, ph = (kk / NACT) & 1;
+                if (!(ok = mbar_wait_sleep(&act_empty[s], ph ^ 1, abort_flag))) break;
+                mbar_arrive_expect_tx(&act_full[s], ACT_TILE);
+                tma_load_2d(sAct + s * ACT_TILE, &tmA, &act_full[s], (sb0 + kk / 4) * 256 + (kk % 4) * TC_KB, m0);
+                last_a[s] = ph;
+            }
+            if (!ok) {
+                volatile int no_abort = 0;
+                for (int i = 0; i < NACT; ++i)
+                    if (last_a[i] >= 0) { no_abort = 0; mbar_wait(&act_full[i], last_a[i], &no_abort, 100000000ull); }
             }
         }
     } else if (warp == TC_WARP_MMA) {
