@@ -48,6 +48,7 @@ constexpr int TC_WARP_ACT = TC_WARP_MMA + 1;
 constexpr int TC_THREADS = (TC_WARP_ACT + 1) * 32;
 constexpr int ACT_TILE = TC_TOK * TC_KB * 2;  // 16 KB: 128 tokens x 64 f16
 constexpr int NACT = 8;                       // activation ring: two super-blocks ahead
+constexpr int NPAIR = NACT / 2;               // the ring is handed over in pairs of kblocks
 constexpr int TMEM_COLS = 512;
 
 template <int DT>
@@ -81,7 +82,7 @@ struct TcLayout {
     static constexpr int H_OFF = EB_OFF + (C::EXT ? 2 * 4096 : 0);
     static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * 8;
     static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4;
-    static constexpr int NBAR = 2 * NACT + 2 * 2 + 2 * 4 + 3 * 2 + 3 * 4 + 2 * 2 + 1;
+    static constexpr int NBAR = 2 * NPAIR + 2 * 2 + 2 * 2 + 3 * 4 + 2 * 2 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = MISC_OFF + 16;
     static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment of the base
@@ -173,10 +174,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t *sH = sm + L::H_OFF;    // per-row (d, -dmin) of a super-block, 4-slot ring
     uint8_t *sDA = sm + L::DA_OFF;  // per-token activation scales of a super-block, same ring
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
-    uint64_t *act_full = bars, *act_empty = act_full + NACT;
-    uint64_t *p_full = act_empty + NACT, *p_empty = p_full + 2;
-    uint64_t *a_full = p_empty + 2, *a_empty = a_full + 4;  // converted kblock stages in TMEM
-    uint64_t *ea_full = a_empty + 4, *eb_full = ea_full + 2, *e_empty = eb_full + 2;
+    // k_full/k_empty: one slot per pair of kblocks -- its two activation tiles (TMA) and its two
+    // converted kblocks (TMEM, from both converter groups) complete the same phase, and a single MMA
+    // commit frees both, so the MMA thread waits once per 128 K-elements.
+    uint64_t *k_full = bars, *k_empty = k_full + NPAIR;
+    uint64_t *p_full = k_empty + NPAIR, *p_empty = p_full + 2;
+    uint64_t *e_full = p_empty + 2, *e_empty = e_full + 2;  // Q4_K: bsums (TMA) + mins (converters)
     uint64_t *h_full = e_empty + 2, *da_full = h_full + 4, *h_empty = da_full + 4;
     uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
@@ -194,11 +197,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int rows_valid = valid_groups * 16;
 
     if (tid == 0) {
-        for (int i = 0; i < NACT; ++i) { mbar_init(&act_full[i], 1); mbar_init(&act_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 32 * TC_CONV_WARPS); }
-        for (int i = 0; i < 4; ++i) { mbar_init(&a_full[i], 32 * TC_CONV_WARPS / 2); mbar_init(&a_empty[i], 1); }
+        for (int i = 0; i < NPAIR; ++i) { mbar_init(&k_full[i], 32 * TC_CONV_WARPS + 1); mbar_init(&k_empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ea_full[i], 32 * TC_CONV_WARPS / 2); mbar_init(&eb_full[i], 1); mbar_init(&e_empty[i], 1);
+            mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 32 * TC_CONV_WARPS);
+            mbar_init(&e_full[i], 32 * TC_CONV_WARPS / 2 + 1); mbar_init(&e_empty[i], 1);
             mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS);
         }
         for (int i = 0; i < 4; ++i) {
@@ -237,8 +239,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (C::EXT) {
                     const int e = t & 1, eph = (t >> 1) & 1;
                     if (!(ok = mbar_wait_sleep(&e_empty[e], eph ^ 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(&eb_full[e], 4096);
-                    tma_load_2d(sEB + e * 4096, &tmE, &eb_full[e], gsb * 16, m0);
+                    mbar_arrive_expect_tx(&e_full[e], 4096);
+                    tma_load_2d(sEB + e * 4096, &tmE, &e_full[e], gsb * 16, m0);
                     last_e[e] = eph;
                 }
                 {
@@ -250,11 +252,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
             if (!ok) {
-                // drain: wait (bounded) for every copy this thread issued to land before leaving
+                // drain: wait (bounded) for every copy this thread issued to land before leaving.  A phase
+                // that also counts converter arrivals may never complete after an abort; the 100 ms bound
+                // still leaves the copy far more time than it needs to land.
                 volatile int no_abort = 0;
                 for (int i = 0; i < 2; ++i) {
                     if (last_p[i] >= 0) { no_abort = 0; mbar_wait(&p_full[i], last_p[i], &no_abort, 100000000ull); }
-                    if (last_e[i] >= 0) { no_abort = 0; mbar_wait(&eb_full[i], last_e[i], &no_abort, 100000000ull); }
+                    if (last_e[i] >= 0) { no_abort = 0; mbar_wait(&e_full[i], last_e[i], &no_abort, 100000000ull); }
                 }
                 for (int i = 0; i < 4; ++i)
                     if (last_d[i] >= 0) { no_abort = 0; mbar_wait(&da_full[i], last_d[i], &no_abort, 100000000ull); }
@@ -263,62 +267,70 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == TC_WARP_ACT) {
         // ------------------------------------------------------------ activation-tile producer
         if (lane == 0) {
-            int last_a[NACT];
-            for (int i = 0; i < NACT; ++i) last_a[i] = -1;
+            int last_k[NPAIR];
+            for (int i = 0; i < NPAIR; ++i) last_k[i] = -1;
             bool ok = true;
-            for (int kk = 0; kk < nsb * 4 && ok; ++kk) {
-                const int s = kk % NACT, ph = (kk / NACT) & 1;
-                if (!(ok = mbar_wait_sleep(&act_empty[s], ph ^ 1, abort_flag))) break;
-                mbar_arrive_expect_tx(&act_full[s], ACT_TILE);
-                tma_load_2d(sAct + s * ACT_TILE, &tmA, &act_full[s], (sb0 + kk / 4) * 256 + (kk % 4) * TC_KB, m0);
-                last_a[s] = ph;
+            for (int pp = 0; pp < nsb * 2 && ok; ++pp) {
+                const int s = pp % NPAIR, ph = (pp / NPAIR) & 1;
+                if (!(ok = mbar_wait_sleep(&k_empty[s], ph ^ 1, abort_flag))) break;
+                mbar_arrive_expect_tx(&k_full[s], 2 * ACT_TILE);
+                const int x = (sb0 + pp / 2) * 256 + (pp & 1) * 2 * TC_KB;
+                tma_load_2d(sAct + (2 * s) * ACT_TILE, &tmA, &k_full[s], x, m0);
+                tma_load_2d(sAct + (2 * s + 1) * ACT_TILE, &tmA, &k_full[s], x + TC_KB, m0);
+                last_k[s] = ph;
             }
             if (!ok) {
+                // bounded drain (see the weight-side producer)
                 volatile int no_abort = 0;
-                for (int i = 0; i < NACT; ++i)
-                    if (last_a[i] >= 0) { no_abort = 0; mbar_wait(&act_full[i], last_a[i], &no_abort, 100000000ull); }
+                for (int i = 0; i < NPAIR; ++i)
+                    if (last_k[i] >= 0) { no_abort = 0; mbar_wait(&k_full[i], last_k[i], &no_abort, 100000000ull); }
             }
         }
     } else if (warp == TC_WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
+        // Lean issue loop: the tensor pipe queues only an MMA or two, so every instruction between
+        // MMAs can leave it idle.  Descriptors are built once and stepped by adding to their address
+        // field; one wait and one commit cover a pair of kblocks.  Q4_K's min-term MMA of super-block
+        // t-1 is issued under the accumulator wait of super-block t (both need the epilogue to be
+        // done with t-2), and the accumulator of t-1 is handed to the epilogue right after it.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(TC_ROWS, TC_TOK);
-            const uint32_t sAct_u = smem_u32(sAct), sEA_u = smem_u32(sEA), sEB_u = smem_u32(sEB);
+            const uint64_t dAct = smem_desc(smem_u32(sAct), 1024, 2);
+            const uint64_t dEA = smem_desc(smem_u32(sEA), 256, 6), dEB = smem_desc(smem_u32(sEB), 256, 6);
             bool ok = true;
-            for (int t = 0; t < nsb && ok; ++t) {
+            for (int t = 0; t < nsb + (C::EXT ? 1 : 0) && ok; ++t) {
                 const int buf = t & 1;
                 if (!(ok = mbar_wait_sleep(&acc_empty[buf], ((t >> 1) & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
-                const uint32_t d1 = tbase + buf * TC_TOK;
-                for (int kb = 0; kb < 4 && ok; ++kb) {
-                    const int kk = t * 4 + kb, sa = kk % NACT;
-                    if (!(ok = mbar_wait_sleep(&act_full[sa], (kk / NACT) & 1, abort_flag))) break;
-                    if (!(ok = mbar_wait_sleep(&a_full[kb], t & 1, abort_flag))) break;
+                if (C::EXT && t > 0) {
+                    const int e = (t - 1) & 1;
+                    if (!(ok = mbar_wait_sleep(&e_full[e], ((t - 1) >> 1) & 1, abort_flag))) break;
                     tc_fence_after();
-                    const uint32_t a0 = tbase + C::TM_A + kb * C::A_COLS;
-#pragma unroll
-                    for (int k16 = 0; k16 < 4; ++k16) {
-                        const uint64_t bd = smem_desc(sAct_u + sa * ACT_TILE + k16 * 32, 1024, 2);
-                        mma_f16_ts(d1, a0 + k16 * 8, bd, idesc, (kb | k16) != 0);
-                        if (!C::EXT) mma_f16_ts(d1, a0 + 32 + k16 * 8, bd, idesc, 1);
-                    }
-                    mma_commit(&act_empty[sa]);
-                    mma_commit(&a_empty[kb]);
-                }
-                if (!ok) break;
-                if (C::EXT) {
-                    const int e = t & 1, eph = (t >> 1) & 1;
-                    if (!(ok = mbar_wait_sleep(&eb_full[e], eph, abort_flag))) break;
-                    if (!(ok = mbar_wait_sleep(&ea_full[e], eph, abort_flag))) break;
-                    // the min-term tile is single-buffered: the epilogue must be done with super-block t-1
-                    if (t > 0 && !(ok = mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag)))
-                        break;
-                    tc_fence_after();
-                    mma_f16(tbase + C::TM_S2, smem_desc(sEA_u + e * 4096, 256, 6), smem_desc(sEB_u + e * 4096, 256, 6),
+                    mma_f16(tbase + C::TM_S2, dEA + (uint64_t)(e * (4096 >> 4)), dEB + (uint64_t)(e * (4096 >> 4)),
                             idesc, 0);
                     mma_commit(&e_empty[e]);
+                    mma_commit(&acc_full[e]);
                 }
-                mma_commit(&acc_full[buf]);
+                if (t == nsb) break;
+                const uint32_t d1 = tbase + buf * TC_TOK;
+                for (int pr = 0; pr < 2 && ok; ++pr) {
+                    const int pp = 2 * t + pr, s = pp % NPAIR;
+                    if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
+                        const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
+#pragma unroll
+                        for (int k16 = 0; k16 < 4; ++k16) {
+                            mma_f16_ts(d1, a0 + k16 * 8, bd + (uint64_t)(k16 * 2), idesc, (pr | h | k16) != 0);
+                            if (!C::EXT) mma_f16_ts(d1, a0 + 32 + k16 * 8, bd + (uint64_t)(k16 * 2), idesc, 1);
+                        }
+                    }
+                    mma_commit(&k_empty[s]);
+                }
+                if (!ok) break;
+                if (!C::EXT) mma_commit(&acc_full[buf]);
             }
             // every MMA this thread issued has finished before TMEM is released
             mma_commit(mma_done);
@@ -375,8 +387,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
+                // kblock grp+2j belongs to pair j of the super-block; its TMEM stage is free once the
+                // MMA of the same pair one super-block earlier has completed
                 const int kb = grp + 2 * j;
-                if (!(ok = mbar_wait_sleep(&a_empty[kb], (t & 1) ^ 1, abort_flag))) break;
+                if (t > 0) {
+                    const int pq = 2 * (t - 1) + j;
+                    if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag))) break;
+                }
                 tc_fence_after();
                 const uint32_t ta = lane_base + C::TM_A + kb * C::A_COLS;
                 if (C::EXT) {
@@ -399,7 +416,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&a_full[kb]);
+                mbar_arrive(&k_full[(2 * t + j) % NPAIR]);
             }
             if (!ok) break;
             if (grp == 0) {
@@ -435,7 +452,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 *reinterpret_cast<uint4 *>(erow + ((0 ^ sw) << 4)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
                 *reinterpret_cast<uint4 *>(erow + ((1 ^ sw) << 4)) = make_uint4(mm[4], mm[5], mm[6], mm[7]);
                 fence_proxy_async_smem();
-                mbar_arrive(&ea_full[e]);
+                mbar_arrive(&e_full[e]);
             }
             mbar_arrive(&p_empty[p]);
         }
