@@ -19,11 +19,12 @@
 // The integer parts are therefore the oracle's integers; only the fp32 scaling uses fused
 // multiply-adds, which keeps the result within a few ulps of the sequential CPU order.
 //
-// Roles (864 threads, 27 warps): warps 0-15 epilogue (TMEM lane quarter = warp % 4, token quarter =
+// Roles (896 threads, 28 warps): warps 0-15 epilogue (TMEM lane quarter = warp % 4, token quarter =
 // warp / 4), warps 16-23 weight converters (lane quarter = warp % 4; warps 16-19 convert kblocks 0
 // and 2 of every super-block, warps 20-23 kblocks 1 and 3), warp 24 producer of the packed weights,
-// bsums and activation scales, warp 25 MMA issuer and TMEM owner, warp 26 producer of the
-// activation tiles (a stream of its own, so it runs ahead without waiting on the other rings).
+// bsums and activation scales, warp 26 producer of the activation tiles (a stream of its own, so it
+// runs ahead without waiting on the other rings), warps 25 and 27 MMA issuers for the even and odd
+// super-blocks (warp 25 also owns the TMEM allocation).
 // Waiting warps sleep on their mbarrier (try_wait with a suspend hint) instead of spinning, so
 // they do not steal issue slots or shared-memory bandwidth from the converter and epilogue warps.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records an error in the workspace's
@@ -44,8 +45,8 @@ constexpr int TC_TOK = 128;   // tokens per CTA: MMA N, TMEM columns of one accu
 constexpr int TC_KB = 64;     // K elements per kblock (one activation tile, one TMEM A stage)
 constexpr int TC_EPI_WARPS = 16, TC_CONV_WARPS = 8;
 constexpr int TC_WARP_PROD = TC_EPI_WARPS + TC_CONV_WARPS, TC_WARP_MMA = TC_WARP_PROD + 1;
-constexpr int TC_WARP_ACT = TC_WARP_MMA + 1;
-constexpr int TC_THREADS = (TC_WARP_ACT + 1) * 32;
+constexpr int TC_WARP_ACT = TC_WARP_MMA + 1, TC_WARP_MMA2 = TC_WARP_ACT + 1;
+constexpr int TC_THREADS = (TC_WARP_MMA2 + 1) * 32;
 constexpr int ACT_TILE = TC_TOK * TC_KB * 2;  // 16 KB: 128 tokens x 64 f16
 constexpr int NACT = 8;                       // activation ring: two super-blocks ahead
 constexpr int NPAIR = NACT / 2;               // the ring is handed over in pairs of kblocks
@@ -82,7 +83,7 @@ struct TcLayout {
     static constexpr int H_OFF = EB_OFF + (C::EXT ? 2 * 4096 : 0);
     static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * 8;
     static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4;
-    static constexpr int NBAR = 2 * NPAIR + 2 * 2 + 2 * 2 + 3 * 4 + 2 * 2 + 1;
+    static constexpr int NBAR = 2 * NPAIR + 2 * 2 + 2 * 2 + 3 * 4 + 2 * 2 + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = MISC_OFF + 16;
     static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment of the base
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t *e_full = p_empty + 2, *e_empty = e_full + 2;  // Q4_K: bsums (TMA) + mins (converters)
     uint64_t *h_full = e_empty + 2, *da_full = h_full + 4, *h_empty = da_full + 4;
     uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 2;
-    uint64_t *mma_done = acc_empty + 2;
+    uint64_t *mma_done = acc_empty + 2;  // one per MMA issuer
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 4);
 
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&h_full[i], 32 * TC_CONV_WARPS / 2); mbar_init(&da_full[i], 1);
             mbar_init(&h_empty[i], TC_EPI_WARPS);
         }
-        mbar_init(mma_done, 1);
+        mbar_init(&mma_done[0], 1);
+        mbar_init(&mma_done[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -286,33 +288,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (last_k[i] >= 0) { no_abort = 0; mbar_wait(&k_full[i], last_k[i], &no_abort, 100000000ull); }
             }
         }
-    } else if (warp == TC_WARP_MMA) {
-        // ------------------------------------------------------------ MMA issuer
-        // Lean issue loop: the tensor pipe queues only an MMA or two, so every instruction between
-        // MMAs can leave it idle.  Descriptors are built once and stepped by adding to their address
-        // field; one wait and one commit cover a pair of kblocks.  Q4_K's min-term MMA of super-block
-        // t-1 is issued under the accumulator wait of super-block t (both need the epilogue to be
-        // done with t-2), and the accumulator of t-1 is handed to the epilogue right after it.
+    } else if (warp == TC_WARP_MMA || warp == TC_WARP_MMA2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two issuers on different SM sub-partitions: TC_WARP_MMA takes the even super-blocks
+        // (accumulator buffer 0), TC_WARP_MMA2 the odd ones (buffer 1).  One thread sharing its
+        // sub-partition with busy warps cannot issue MMAs as fast as the tensor pipe retires them;
+        // two interleaved streams can.  Their MMAs touch disjoint pair slots, TMEM stages and
+        // accumulators, so no ordering between the issuers is needed beyond the barriers.
+        // Lean issue loop: descriptors are built once and stepped by adding to their address field,
+        // one wait and one commit cover a pair of kblocks.  Q4_K's min-term tile is single: the
+        // extension MMA of super-block t waits until the epilogue is done with t-1.
         if (lane == 0) {
+            const int w = warp == TC_WARP_MMA ? 0 : 1;
             constexpr uint32_t idesc = idesc_f16_f32(TC_ROWS, TC_TOK);
             const uint64_t dAct = smem_desc(smem_u32(sAct), 1024, 2);
             const uint64_t dEA = smem_desc(smem_u32(sEA), 256, 6), dEB = smem_desc(smem_u32(sEB), 256, 6);
+            const uint32_t d1 = tbase + w * TC_TOK;
             bool ok = true;
-            for (int t = 0; t < nsb + (C::EXT ? 1 : 0) && ok; ++t) {
-                const int buf = t & 1;
-                if (!(ok = mbar_wait_sleep(&acc_empty[buf], ((t >> 1) & 1) ^ 1, abort_flag))) break;
+            for (int t = w; t < nsb && ok; t += 2) {
+                if (!(ok = mbar_wait_sleep(&acc_empty[w], ((t >> 1) & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
-                if (C::EXT && t > 0) {
-                    const int e = (t - 1) & 1;
-                    if (!(ok = mbar_wait_sleep(&e_full[e], ((t - 1) >> 1) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    mma_f16(tbase + C::TM_S2, dEA + (uint64_t)(e * (4096 >> 4)), dEB + (uint64_t)(e * (4096 >> 4)),
-                            idesc, 0);
-                    mma_commit(&e_empty[e]);
-                    mma_commit(&acc_full[e]);
-                }
-                if (t == nsb) break;
-                const uint32_t d1 = tbase + buf * TC_TOK;
                 for (int pr = 0; pr < 2 && ok; ++pr) {
                     const int pp = 2 * t + pr, s = pp % NPAIR;
                     if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag))) break;
@@ -330,12 +325,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     mma_commit(&k_empty[s]);
                 }
                 if (!ok) break;
-                if (!C::EXT) mma_commit(&acc_full[buf]);
+                if (C::EXT) {
+                    const int e = t & 1;
+                    if (!(ok = mbar_wait_sleep(&e_full[e], (t >> 1) & 1, abort_flag))) break;
+                    if (t > 0 && !(ok = mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    mma_f16(tbase + C::TM_S2, dEA + (uint64_t)(e * (4096 >> 4)), dEB + (uint64_t)(e * (4096 >> 4)),
+                            idesc, 0);
+                    mma_commit(&e_empty[e]);
+                }
+                mma_commit(&acc_full[w]);
             }
             // every MMA this thread issued has finished before TMEM is released
-            mma_commit(mma_done);
+            mma_commit(&mma_done[w]);
             volatile int no_abort = 0;
-            mbar_wait(mma_done, 0, &no_abort, 100000000ull);
+            mbar_wait(&mma_done[w], 0, &no_abort, 100000000ull);
         }
     } else if (warp >= TC_EPI_WARPS) {
         // ------------------------------------------------------------ weight converters
