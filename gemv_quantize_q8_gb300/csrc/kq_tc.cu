@@ -611,22 +611,26 @@ bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     return true;
 }
 
-// Split-K factor: the number of CTAs per output tile (a cluster along z) that best fills whole
-// waves of the 152 SMs, with at least 4 super-blocks per CTA; 1 when the tiles alone fill the GPU.
-static int tc_splits(int64_t M, int64_t N, int64_t K) {
+// Split-K factor: the number of CTAs per output tile (a cluster along z).  Chosen with a small
+// cost model measured on GB300 -- every CTA pays a pipeline fill and drain (~2.5 us) and each
+// super-block costs ~1.3 us (Q4_K) or ~1.75 us (Q6_K); a split adds a cluster reduction (~1 us)
+// and clusters of S CTAs fill whole GPCs only in multiples of S -- over power-of-two splits that
+// leave at least two super-blocks per CTA.
+static int tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     const int64_t tiles = ((M + TC_TOK - 1) / TC_TOK) * ((N + TC_ROWS - 1) / TC_ROWS);
     const int nsb = (int)(K / 256);
-    const int num_sms = 152;
-    if (tiles >= 2 * num_sms) return 1;
+    const double t_sb = wt == KQ_Q4_K ? 1.3 : 1.75, t_fill = 2.5, t_red = 1.0;
+    const int num_sms = 152, gpcs = 8, sms_per_gpc = 19;
     int best = 1;
-    double best_eff = 0.0;
-    for (int S = 1; S <= 8; ++S) {
+    double best_t = 1e30;
+    for (int S = 1; S <= 8; S *= 2) {
         const int per = (nsb + S - 1) / S;
-        if (S > 1 && per < 4) break;
+        if (S > 1 && per < 2) break;
         if ((nsb + per - 1) / per != S) continue;  // S must be exactly realisable
-        const int64_t ctas = tiles * S;
-        const double eff = (double)ctas / (double)(((ctas + num_sms - 1) / num_sms) * num_sms);
-        if (eff > best_eff + 1e-9) { best_eff = eff; best = S; }
+        const int64_t usable = S == 1 ? num_sms : (int64_t)gpcs * (sms_per_gpc / S) * S;
+        const int64_t waves = (tiles * S + usable - 1) / usable;
+        const double t = (double)waves * (t_fill + per * t_sb + (S > 1 ? t_red : 0.0));
+        if (t < best_t - 1e-9) { best_t = t; best = S; }
     }
     return best;
 }
@@ -683,7 +687,7 @@ static kq_status launch_tc(const uint8_t *w, int64_t M, int64_t N, int64_t K, fl
     p.y = y;
     p.ldy = ldy;
     p.M = (int)M; p.N = (int)N; p.K = (int)K; p.M_pad = L.M_pad;
-    const int S = tc_splits(M, N, K);
+    const int S = tc_splits((kq_dtype)DT, M, N, K);
     p.nsplit = S;
     p.sb_per_split = (int)((nsb + S - 1) / S);
     p.err = reinterpret_cast<unsigned long long *>(ws + L.off_flag);
