@@ -268,6 +268,101 @@ def run_prefill(args, device, rank, world):
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, cases=cases)
 
 
+def _time_graph(fn, reps, warmup=2):
+    """Capture fn() once as a CUDA graph; median ms of `reps` timed replays (events on the stream)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        fn()
+    for _ in range(warmup):
+        gr.replay()
+    torch.cuda.synchronize()
+    ts = []
+    stream = torch.cuda.current_stream()
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        gr.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_aux(args, device):
+    """The two other hot-path pipelines, timed whole from CUDA graphs (not part of `value`):
+    Q8_0 GEMM behind the fused SwiGLU -> Q8_1 prologue, and the routed-expert MoE block."""
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    from gemv_quantize_q8_gb300 import synth
+    out = {}
+    # --- SwiGLU -> Q8_1 prologue + Q8_0 GEMM, M=2048 N=2560 K=9728
+    c = synth.SWIGLU_Q8_0
+    M, N, K = c["M"], c["N"], c["K"]
+    g = synth.rng(0)
+    wc = torch.from_numpy(synth.weights(synth.Q8_0, N, K, g).reshape(-1)).to(device)
+    wn = torch.empty(kq.native_bytes(synth.Q8_0, N, K), dtype=torch.uint8, device=device)
+    kq.kq_repack_weights(synth.Q8_0, wc, wn, N, K)
+    del wc
+    gu = torch.from_numpy(synth.activations(M, 2 * K, g)).to(device)
+    xq = torch.empty(kq.q8_1_bytes(M, K), dtype=torch.uint8, device=device)
+    y = torch.empty((M, N), device=device)
+    wsb = kq.gemm_workspace_bytes(synth.Q8_0, M, N, K)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
+    t_pro = _time_graph(lambda: kq.kq_swiglu_quantize_q8_1(gu, gu[:, K:], M, K, 2 * K, xq), 5)
+    t_gemm = _time_graph(lambda: kq.kq_gemm(synth.Q8_0, wn, xq, M, N, K, y, N, ws, wsb), 5)
+    pro_bytes = 2 * M * K * 4 + kq.q8_1_bytes(M, K)
+    out["q8_0_swiglu_gemm"] = {
+        "workload": c["name"], "prologue_us": round(t_pro * 1e3, 1),
+        "prologue_gbs": round(pro_bytes / (t_pro * 1e-3) / 1e9, 1), "gemm_us": round(t_gemm * 1e3, 1),
+        "gemm_tops": round(2.0 * M * N * K / (t_gemm * 1e-3) / 1e12, 2),
+        "total_us": round((t_pro + t_gemm) * 1e3, 1)}
+    del gu, xq, y, ws, wn
+    # --- MoE block: quantize -> grouped Q4_K gate/up -> SwiGLU + Q8_K -> grouped Q6_K down -> weighted sum
+    c = synth.MOE
+    E, top_k, M, H, F = c["n_experts"], c["top_k"], c["M"], c["hidden"], c["ffn"]
+    g = synth.rng(0)
+    w_gu = torch.empty(kq.native_bytes(synth.Q4_K, E * 2 * F, H), dtype=torch.uint8, device=device)
+    w_dn = torch.empty(kq.native_bytes(synth.Q6_K, E * H, F), dtype=torch.uint8, device=device)
+    wc = torch.from_numpy(synth.weights(synth.Q4_K, E * 2 * F, H, g).reshape(-1)).to(device)
+    kq.kq_repack_weights(synth.Q4_K, wc, w_gu, E * 2 * F, H)
+    del wc
+    wc = torch.from_numpy(synth.weights(synth.Q6_K, E * H, F, g).reshape(-1)).to(device)
+    kq.kq_repack_weights(synth.Q6_K, wc, w_dn, E * H, F)
+    del wc
+    x = torch.from_numpy(synth.activations(M, H, g)).to(device)
+    ids_h, wts_h = synth.routing(M, E, top_k, g)
+    ids, wts = torch.from_numpy(ids_h).to(device), torch.from_numpy(wts_h).to(device)
+    xq = torch.empty(kq.q8k_bytes(M, H), dtype=torch.uint8, device=device)
+    y_gu = torch.empty((M, top_k, 2 * F), device=device)
+    hq = torch.empty(kq.q8k_bytes(M * top_k, F), dtype=torch.uint8, device=device)
+    h = torch.empty((M * top_k, F), device=device)
+    y_dn = torch.empty((M, top_k, H), device=device)
+    o = torch.empty((M, H), device=device)
+    wsb = max(kq.gemm_workspace_bytes(synth.Q4_K, M, 2 * F, H, E, top_k),
+              kq.gemm_workspace_bytes(synth.Q6_K, M, H, F, E, top_k))
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
+
+    def moe():
+        kq.kq_quantize_q8k(x, M, H, H, xq)
+        kq.kq_gemm_grouped(synth.Q4_K, w_gu, E, xq, 1, ids, M, top_k, 2 * F, H, y_gu, ws, wsb)
+        flat = y_gu.view(M * top_k, 2 * F)
+        kq.kq_swiglu_quantize_q8k(flat, flat[:, F:], M * top_k, F, 2 * F, hq, h)
+        kq.kq_gemm_grouped(synth.Q6_K, w_dn, E, hq, top_k, ids, M, top_k, H, F, y_dn, ws, wsb)
+        kq.kq_moe_weighted_sum(y_dn, wts, M, top_k, H, o)
+
+    t = _time_graph(moe, 5)
+    ops = 2.0 * M * top_k * (2 * F * H + H * F)
+    out["moe_mul_mat_id"] = {"workload": c["name"], "block_us": round(t * 1e3, 1),
+                             "tops": round(ops / (t * 1e-3) / 1e12, 2),
+                             "weight_gbs": round((w_gu.numel() + w_dn.numel()) / (t * 1e-3) / 1e9, 1)}
+    assert kq.kq_read_device_flag(ws) == 0, "MoE routing reported bad expert ids"
+    return out
+
+
 def run_decode(args, device, calls=None):
     """1000 back-to-back fused-quant GEMV calls per shape from a CUDA graph; weight copies rotate."""
     import torch
@@ -383,6 +478,7 @@ def main():
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
     ap.add_argument("--only", default=None, help="profile one GEMM, e.g. q4_k:4096x4096:512")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-aux", action="store_true", help="skip the Q8_0+SwiGLU and MoE pipeline timings")
     ap.add_argument("--decode-only", action="store_true", help="time only the decode GEMV (for profiling)")
     ap.add_argument("--gemv-calls", type=int, default=1000, help="back-to-back GEMV calls per decode shape")
     ap.add_argument("--no-cpu", action="store_true")
@@ -422,6 +518,7 @@ def main():
     decode = None
     if not args.no_decode and not args.only:
         decode, decode_gbs = run_decode(args, device)
+    aux = run_aux(args, device) if rank == 0 and not args.only and not args.no_aux else None
     if rank == 0:
         pk, src = peaks()
         value = world * res["ops"] / (ms * 1e-3) / 1e12
@@ -451,6 +548,8 @@ def main():
             hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
             line["decode_gemv"] = {"gbs": round(decode_gbs, 1), "frac_of_hbm": round(decode_gbs / hbm, 4),
                                    "hbm_peak_gbs": hbm, "peak_source": src, "shapes": decode}
+        if aux is not None:
+            line.update(aux)
         if not args.no_cpu and not args.only:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)

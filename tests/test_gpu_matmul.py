@@ -28,7 +28,7 @@ def _oracle_act(dtype, x):
 
 
 @pytest.mark.parametrize("dtype", DTS)
-@pytest.mark.parametrize("N,K", [(40, 512), (256, 1024), (100, 4096), (16, 256)])
+@pytest.mark.parametrize("N,K", [(40, 512), (256, 1024), (100, 4096), (16, 256), (48, 16384)])
 @pytest.mark.parametrize("fused", [True, False])
 def test_gemv_small(dtype, N, K, fused):
     g = synth.rng(200 + N + K + dtype)
@@ -44,6 +44,51 @@ def test_gemv_small(dtype, N, K, fused):
     ref = oracle.gemm(dtype, w, _oracle_act(dtype, x), 1, N, K)[0]
     got = host(y)
     assert np.array_equal(got, ref), (nmse(got, ref), np.abs(got - ref).max())
+
+
+@pytest.mark.parametrize("dtype", DTS)
+def test_gemv_unaligned_activation(dtype):
+    # x only 4-byte aligned: the fused prologue takes its scalar-load path
+    N, K = 64, 2048
+    g = synth.rng(250 + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(1, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    buf = torch.zeros(K + 1, device=DEV)
+    buf[1:] = dev(x)[0]
+    y = torch.full((N,), float("nan"), device=DEV)
+    kq.kq_gemv(dtype, wn, buf[1:], None, N, K, y)
+    ref = oracle.gemm(dtype, w, _oracle_act(dtype, x), 1, N, K)[0]
+    assert np.array_equal(host(y), ref)
+
+
+def test_gemv_back_to_back_calls():
+    # consecutive calls overlap through programmatic dependent launch: each must still see the
+    # activation written before it and leave its own result, also when two calls share an output
+    cases = [(kq.Q4_K, 9728 // 8, 2560), (kq.Q6_K, 320, 9728), (kq.Q8_0, 256, 2560), (kq.Q4_K, 640, 9728)]
+    g = synth.rng(260)
+    wc, ws, xs, refs = [], [], [], []
+    for dt, N, K in cases:
+        w = synth.weights(dt, N, K, g)
+        x = synth.activations(1, K, g)
+        wc.append(w)
+        ws.append(repack(dt, w, N, K))
+        xs.append(dev(x))
+        refs.append(oracle.gemm(dt, w, _oracle_act(dt, x), 1, N, K)[0])
+    ys = [torch.full((N,), float("nan"), device=DEV) for (_, N, _) in cases]
+    shared = torch.full((cases[0][1],), float("nan"), device=DEV)
+    x2 = synth.activations(1, cases[0][2], g)
+    x2d = dev(x2)
+    for rep in range(3):
+        for i, (dt, N, K) in enumerate(cases):
+            kq.kq_gemv(dt, ws[i], xs[i], None, N, K, ys[i])
+        kq.kq_gemv(cases[0][0], ws[0], xs[0], None, cases[0][1], cases[0][2], shared)
+        kq.kq_gemv(cases[0][0], ws[0], x2d, None, cases[0][1], cases[0][2], shared)  # the later call wins
+    for i in range(len(cases)):
+        assert np.array_equal(host(ys[i]), refs[i]), i
+    dt, N, K = cases[0]
+    ref2 = oracle.gemm(dt, wc[0], _oracle_act(dt, x2), 1, N, K)[0]
+    assert np.array_equal(host(shared), ref2)
 
 
 @pytest.mark.parametrize("cfg", synth.DECODE, ids=lambda c: c["name"])
