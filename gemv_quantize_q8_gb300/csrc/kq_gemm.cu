@@ -23,6 +23,24 @@ struct GroupedWs {
     int64_t max_tiles;
 };
 
+// Regions the tensor-core grouped path appends to the routing workspace.
+struct GroupedTcWs {
+    size_t off_poff, off_tile_count, off_tiles, off_panels, total;
+    int64_t max_tiles;
+};
+
+static GroupedTcWs grouped_tc_ws(size_t base, int64_t pairs, int64_t E, int64_t K) {
+    GroupedTcWs w{};
+    w.max_tiles = (pairs + kTcTileRows - 1) / kTcTileRows + E;
+    size_t o = base;
+    w.off_poff = o; o += align256(sizeof(int) * E);
+    w.off_tile_count = o; o += align256(sizeof(int));
+    w.off_tiles = o; o += align256(sizeof(int) * 2 * w.max_tiles);
+    w.off_panels = o; o += tc_grouped_panels(pairs, E, K).bytes;
+    w.total = o;
+    return w;
+}
+
 static GroupedWs grouped_ws(int64_t M, int64_t top_k, int64_t E) {
     GroupedWs w{};
     const int64_t pairs = M * top_k;
@@ -80,6 +98,25 @@ __global__ void route_scan_kernel(const int *__restrict__ count, int E, int *__r
             ++nt;
         }
         off += c;
+    }
+    *tile_count = nt;
+}
+
+// Tensor-core tile table (single thread): expert rows padded to a multiple of 4 in the activation
+// panels (poff), and one (expert, tile) entry per 128 routed rows of each expert.
+__global__ void route_tc_tiles_kernel(const int *__restrict__ count, int E, int *__restrict__ poff,
+                                      int *__restrict__ tiles, int *__restrict__ tile_count) {
+    if (threadIdx.x != 0) return;
+    int off = 0, nt = 0;
+    for (int e = 0; e < E; ++e) {
+        poff[e] = off;
+        const int c = count[e];
+        for (int j = 0; j * kTcTileRows < c; ++j) {
+            tiles[2 * nt] = e;
+            tiles[2 * nt + 1] = j;
+            ++nt;
+        }
+        off += (c + 3) & ~3;
     }
     *tile_count = nt;
 }
@@ -160,7 +197,11 @@ extern "C" {
 
 size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K, int64_t n_experts, int64_t top_k) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    if (n_experts > 0) return grouped_ws(M, top_k > 0 ? top_k : 1, n_experts).total;
+    if (n_experts > 0) {
+        const int64_t tk = top_k > 0 ? top_k : 1;
+        const size_t base = grouped_ws(M, tk, n_experts).total;
+        return tc_grouped_eligible(wt, N, K) ? grouped_tc_ws(base, M * tk, n_experts, K).total : base;
+    }
     return tc_workspace_bytes(wt, M, N, K);
 }
 
@@ -216,8 +257,9 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
     if (M * top_k > (int64_t)1 << 30) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: too many (token, slot) pairs");
     if (!aligned(ids, 4) || !aligned(y, 4)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm_grouped: ids/y must be 4-byte aligned");
     const GroupedWs L = grouped_ws(M, top_k, n_experts);
-    if (!workspace || ws_bytes < L.total)
-        return fail(KQ_ERR_WORKSPACE, "kq_gemm_grouped: workspace of %zu bytes needed, %zu given", L.total,
+    const size_t need = kq_gemm_workspace_bytes(wt, M, N, K, n_experts, top_k);
+    if (!workspace || ws_bytes < need)
+        return fail(KQ_ERR_WORKSPACE, "kq_gemm_grouped: workspace of %zu bytes needed, %zu given", need,
                     workspace ? ws_bytes : 0);
     if (!aligned(workspace, 256)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm_grouped: workspace must be 256-byte aligned");
     if (L.max_tiles > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: too many tiles");
@@ -236,6 +278,20 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
     s = check_launch("kq_gemm_grouped routing");
     if (s != KQ_OK) return s;
     count_launch(R_ROUTE, 3);
+    if (tc_grouped_eligible(wt, N, K)) {
+        const GroupedTcWs T = grouped_tc_ws(L.total, pairs, n_experts, K);
+        int *poff = reinterpret_cast<int *>(ws + T.off_poff);
+        int *tc_tiles = reinterpret_cast<int *>(ws + T.off_tiles);
+        int *tc_count = reinterpret_cast<int *>(ws + T.off_tile_count);
+        route_tc_tiles_kernel<<<1, 32, 0, st>>>(count, (int)n_experts, poff, tc_tiles, tc_count);
+        s = check_launch("kq_gemm_grouped tile table");
+        if (s != KQ_OK) return s;
+        count_launch(R_ROUTE, 1);
+        return tc_gemm_grouped(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq),
+                               (int)xq_rows_per_token, (int)top_k, pairs, n_experts, N, K, y, ws + T.off_panels,
+                               tc_tiles, tc_count, T.max_tiles, count, offset, poff, lists,
+                               reinterpret_cast<unsigned long long *>(flag), st);
+    }
     MmqExactArgs a{};
     a.w = static_cast<const uint8_t *>(w);
     a.xq = static_cast<const uint8_t *>(xq);
@@ -258,7 +314,8 @@ kq_status kq_read_device_flag(void *workspace, int64_t *n_bad, kq_stream_t strea
         e = cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, (cudaStream_t)stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
         if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_read_device_flag: %s", cudaGetErrorString(e));
-        return fail(KQ_ERR_DEVICE_FLAG, "kq_read_device_flag: %lld (token, slot) pairs had an expert id out of range", v);
+        return fail(KQ_ERR_DEVICE_FLAG,
+                    "kq_read_device_flag: device flag %lld (expert ids out of range, or tensor-core pipeline timeouts)", v);
     }
     return KQ_OK;
 }

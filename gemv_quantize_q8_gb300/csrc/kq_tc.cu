@@ -101,6 +101,11 @@ struct TcParams {
     int M, N, K, M_pad;
     int nsplit, sb_per_split;  // split-K: cluster rank z covers super-blocks [z*sb_per_split, ...)
     unsigned long long *err;   // device flag (workspace header)
+    // Routed experts (grouped != 0): blockIdx.y indexes a table of (expert e, 128-row tile j); the
+    // rows of expert e sit at panel rows poff[e] .. (padded to 4), its (token, slot) pair ids are
+    // lists[offset[e] .. offset[e] + count[e]), and its weights start at row group e * N/16.
+    int grouped;
+    const int *tiles, *tile_count, *count, *offset, *poff, *lists;
 };
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
@@ -188,13 +193,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * TC_ROWS, m0 = blockIdx.y * TC_TOK;
+    const int n0 = blockIdx.x * TC_ROWS;
+    int m0 = blockIdx.y * TC_TOK;   // first panel row of the token tile
+    int tok_valid = P.M - m0;       // token rows of the tile that are stored
+    int g_base = 0, list_base = 0;  // grouped: expert's first row group, first pair-list entry
+    if (P.grouped) {
+        const int ti = blockIdx.y;
+        if (ti >= *P.tile_count) return;  // a spare slot of the tile table: the whole CTA leaves at once
+        const int e = P.tiles[2 * ti], j = P.tiles[2 * ti + 1];
+        m0 = P.poff[e] + j * TC_TOK;
+        tok_valid = min(TC_TOK, P.count[e] - j * TC_TOK);
+        g_base = e * (P.N / 16);
+        list_base = P.offset[e] + j * TC_TOK;
+    }
     const int nchunk = P.K / 256;
     const int sb0 = blockIdx.z * P.sb_per_split;
     const int nsb = min(nchunk, sb0 + P.sb_per_split) - sb0;  // super-blocks of this CTA (t = sb - sb0)
     const int groups_total = (P.N + 15) / 16;
-    const int g0 = n0 / 16;
-    const int valid_groups = min(8, groups_total - g0);
+    const int valid_groups = min(8, groups_total - n0 / 16);
+    const int g0 = g_base + n0 / 16;
     const int rows_valid = valid_groups * 16;
 
     if (tid == 0) {
@@ -509,11 +526,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
         }
         if (ok && P.nsplit == 1 && n0 + row < P.N) {
-            float *yc = P.y + (int64_t)(m0 + tq * 32) * P.ldy + n0 + row;
-            const int mrem = P.M - (m0 + tq * 32);
+            const int mrem = tok_valid - tq * 32;
+            if (P.grouped) {
+                // token row -> its (token, slot) output row
+                const int *lp = P.lists + list_base + tq * 32;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < mrem) yc[(int64_t)i * P.ldy] = acc[i];
+                for (int i = 0; i < 32; ++i)
+                    if (i < mrem) P.y[(int64_t)lp[i] * P.ldy + n0 + row] = acc[i];
+            } else {
+                float *yc = P.y + (int64_t)(m0 + tq * 32) * P.ldy + n0 + row;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < mrem) yc[(int64_t)i * P.ldy] = acc[i];
+            }
         }
     }
 
@@ -581,6 +606,48 @@ __global__ void act_panel_kernel(const uint8_t *__restrict__ xq, int M, int M_pa
     *reinterpret_cast<uint4 *>(A + (int64_t)m * K + sb * 256 + lane * 8) = out;
     if (lane < 16) E[(int64_t)m * nsb * 16 + sb * 16 + lane] = bsv;
     if (lane == 0) D[(int64_t)sb * M_pad + m] = d;
+}
+
+// Routed-expert prologue: the routed rows of expert e, in routed order, into the f16 code panel, the
+// f16 bsum panel and the f32 scale panel at panel rows poff[e] .. poff[e] + roundup4(count[e]) (the
+// padding rows are zero).  Row i of the expert is pair lists[offset[e] + i], whose activation is Q8_K
+// row pair / top_k (one row per token) or row pair (one row per pair).  One block per expert, a warp
+// per (row, super-block).
+__global__ void act_panel_grouped_kernel(const uint8_t *__restrict__ xq, int rows_per_token, int top_k, int nsb,
+                                         const int *__restrict__ count, const int *__restrict__ offset,
+                                         const int *__restrict__ poff, const int *__restrict__ lists,
+                                         __half *__restrict__ A, __half *__restrict__ E, float *__restrict__ D,
+                                         int64_t dstride) {
+    const int e = blockIdx.x;
+    const int c = count[e], rows = (c + 3) & ~3, base = poff[e];
+    const int lane = threadIdx.x & 31;
+    const int64_t K = (int64_t)nsb * 256;
+    for (int64_t wi = threadIdx.x / 32; wi < (int64_t)rows * nsb; wi += blockDim.x / 32) {
+        const int i = (int)(wi / nsb), sb = (int)(wi % nsb);
+        const int64_t r = base + i;
+        uint4 out = make_uint4(0, 0, 0, 0);
+        __half bsv = __float2half(0.0f);
+        float d = 0.0f;
+        if (i < c) {
+            const int p = lists[offset[e] + i];
+            const int64_t src = rows_per_token == 1 ? p / top_k : p;
+            const uint8_t *blk = xq + (src * nsb + sb) * kQ8KBytes;
+            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(blk + 4 + lane * 8);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t *>(blk + 8 + lane * 8);
+            __half hv[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                hv[k] = __int2half_rn((int)(int8_t)((w0 >> (8 * k)) & 0xff));
+                hv[4 + k] = __int2half_rn((int)(int8_t)((w1 >> (8 * k)) & 0xff));
+            }
+            out = *reinterpret_cast<uint4 *>(hv);
+            if (lane < 16) bsv = __int2half_rn((int)reinterpret_cast<const int16_t *>(blk + 260)[lane]);
+            d = *reinterpret_cast<const float *>(blk);
+        }
+        *reinterpret_cast<uint4 *>(A + r * K + sb * 256 + lane * 8) = out;
+        if (lane < 16) E[r * nsb * 16 + sb * 16 + lane] = bsv;
+        if (lane == 0) D[(int64_t)sb * dstride + r] = d;
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -653,49 +720,67 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
+// One launch of the tensor-core kernel over activation panels built by a prologue.
+struct TcLaunch {
+    const uint8_t *w;
+    float *y;
+    int64_t ldy, M, N, K;
+    uint8_t *A, *E;       // f16 code panel [rows][K], f16 bsum panel [rows][K/16]
+    float *D;             // f32 scale panel [K/256][dstride]
+    int64_t rows;         // panel rows (tensor-map extent; tiles past it read zeros)
+    int64_t dstride;      // scale-panel row stride: >= any tile's first row + 128, a multiple of 4
+    unsigned grid_y;      // token tiles (dense) or tile-table slots (grouped)
+    int nsplit;
+    unsigned long long *err;
+    bool grouped;
+    const int *tiles, *tile_count, *count, *offset, *poff, *lists;
+};
+
 template <int DT>
-static kq_status launch_tc(const uint8_t *w, int64_t M, int64_t N, int64_t K, float *y, int64_t ldy, uint8_t *ws,
-                           const TcWs &L, cudaStream_t st) {
+static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     using Lay = TcLayout<DT>;
     auto encode = get_encode();
     if (!encode) return fail(KQ_ERR_CUDA, "kq_gemm: cuTensorMapEncodeTiled unavailable");
-    const int64_t nsb = K / 256;
+    const int64_t nsb = a.K / 256;
     CUtensorMap tmA, tmE;
     {
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)L.M_pad};
-        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.rows};
+        cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
         cuuint32_t box[2] = {TC_KB, TC_TOK};
         cuuint32_t es[2] = {1, 1};
-        CUresult r = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws + L.off_a, dims, strides, box, es,
+        CUresult r = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.A, dims, strides, box, es,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(KQ_ERR_CUDA, "kq_gemm: tensor map A encode failed (%d)", (int)r);
     }
     {
-        cuuint64_t dims[2] = {(cuuint64_t)nsb * 16, (cuuint64_t)L.M_pad};
+        cuuint64_t dims[2] = {(cuuint64_t)nsb * 16, (cuuint64_t)a.rows};
         cuuint64_t strides[1] = {(cuuint64_t)nsb * 32};
         cuuint32_t box[2] = {16, TC_TOK};
         cuuint32_t es[2] = {1, 1};
-        CUresult r = encode(&tmE, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws + L.off_e, dims, strides, box, es,
+        CUresult r = encode(&tmE, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.E, dims, strides, box, es,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(KQ_ERR_CUDA, "kq_gemm: tensor map E encode failed (%d)", (int)r);
     }
     TcParams p{};
-    p.w = w;
-    p.da = reinterpret_cast<const float *>(ws + L.off_d);
-    p.y = y;
-    p.ldy = ldy;
-    p.M = (int)M; p.N = (int)N; p.K = (int)K; p.M_pad = L.M_pad;
-    const int S = tc_splits((kq_dtype)DT, M, N, K);
+    p.w = a.w;
+    p.da = a.D;
+    p.y = a.y;
+    p.ldy = a.ldy;
+    p.M = (int)a.M; p.N = (int)a.N; p.K = (int)a.K; p.M_pad = (int)a.dstride;
+    const int S = a.nsplit;
     p.nsplit = S;
     p.sb_per_split = (int)((nsb + S - 1) / S);
-    p.err = reinterpret_cast<unsigned long long *>(ws + L.off_flag);
+    p.err = a.err;
+    p.grouped = a.grouped ? 1 : 0;
+    p.tiles = a.tiles; p.tile_count = a.tile_count; p.count = a.count;
+    p.offset = a.offset; p.poff = a.poff; p.lists = a.lists;
     auto kern = tc_gemm_kernel<DT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + TC_ROWS - 1) / TC_ROWS), (unsigned)(L.M_pad / TC_TOK), (unsigned)S);
+    cfg.gridDim = dim3((unsigned)((a.N + TC_ROWS - 1) / TC_ROWS), a.grid_y, (unsigned)S);
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Lay::ALLOC;
     cfg.stream = st;
@@ -711,6 +796,10 @@ static kq_status launch_tc(const uint8_t *w, int64_t M, int64_t N, int64_t K, fl
     return KQ_OK;
 }
 
+static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st) {
+    return wt == KQ_Q4_K ? launch_tc<KQ_Q4_K>(a, st) : launch_tc<KQ_Q6_K>(a, st);
+}
+
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, uint8_t *workspace, cudaStream_t st) {
     const TcWs L = tc_ws(M, K);
@@ -724,8 +813,58 @@ kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, i
         reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
     kq_status s = check_launch("kq_gemm (activation panel)");
     if (s != KQ_OK) return s;
-    s = wt == KQ_Q4_K ? launch_tc<KQ_Q4_K>(w, M, N, K, y, ldy, workspace, L, st)
-                      : launch_tc<KQ_Q6_K>(w, M, N, K, y, ldy, workspace, L, st);
+    TcLaunch a{};
+    a.w = w; a.y = y; a.ldy = ldy; a.M = M; a.N = N; a.K = K;
+    a.A = workspace + L.off_a; a.E = workspace + L.off_e; a.D = reinterpret_cast<float *>(workspace + L.off_d);
+    a.rows = L.M_pad; a.dstride = L.M_pad; a.grid_y = (unsigned)(L.M_pad / TC_TOK);
+    a.nsplit = tc_splits(wt, M, N, K);
+    a.err = reinterpret_cast<unsigned long long *>(workspace + L.off_flag);
+    s = launch_tc_dt(wt, a, st);
+    if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
+    return s;
+}
+
+// ---- routed experts on the tensor cores
+bool tc_grouped_eligible(kq_dtype wt, int64_t N, int64_t K) {
+    return (wt == KQ_Q4_K || wt == KQ_Q6_K) && N % 16 == 0 && K % 256 == 0 && K <= (1 << 20) && N <= (1 << 22);
+}
+
+TcGroupedPanels tc_grouped_panels(int64_t pairs, int64_t E, int64_t K) {
+    TcGroupedPanels g{};
+    const int64_t nsb = K / 256;
+    g.rows = pairs + 3 * E;                      // every expert's rows padded to a multiple of 4
+    g.dstride = ((g.rows + TC_TOK) + 3) & ~(int64_t)3;
+    size_t o = 0;
+    g.off_a = o; o += al256((size_t)g.rows * K * 2);
+    g.off_e = o; o += al256((size_t)g.rows * nsb * 32);
+    g.off_d = o; o += al256((size_t)nsb * g.dstride * 4);
+    g.bytes = o;
+    return g;
+}
+
+kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int rows_per_token, int top_k,
+                          int64_t pairs, int64_t E, int64_t N, int64_t K, float *y, uint8_t *panels,
+                          const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,
+                          const int *offset, const int *poff, const int *lists, unsigned long long *err,
+                          cudaStream_t st) {
+    const TcGroupedPanels G = tc_grouped_panels(pairs, E, K);
+    if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || max_tiles > 65535)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: shape too large for the tensor-core grid");
+    const int64_t nsb = K / 256;
+    act_panel_grouped_kernel<<<(unsigned)E, 256, 0, st>>>(
+        xq, rows_per_token, top_k, (int)nsb, count, offset, poff, lists, reinterpret_cast<__half *>(panels + G.off_a),
+        reinterpret_cast<__half *>(panels + G.off_e), reinterpret_cast<float *>(panels + G.off_d), G.dstride);
+    kq_status s = check_launch("kq_gemm_grouped (activation panel)");
+    if (s != KQ_OK) return s;
+    TcLaunch a{};
+    a.w = w; a.y = y; a.ldy = N; a.M = pairs; a.N = N; a.K = K;
+    a.A = panels + G.off_a; a.E = panels + G.off_e; a.D = reinterpret_cast<float *>(panels + G.off_d);
+    a.rows = G.rows; a.dstride = G.dstride; a.grid_y = (unsigned)max_tiles;
+    a.nsplit = 1;
+    a.err = err;
+    a.grouped = true;
+    a.tiles = tiles; a.tile_count = tile_count; a.count = count; a.offset = offset; a.poff = poff; a.lists = lists;
+    s = launch_tc_dt(wt, a, st);
     if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
     return s;
 }

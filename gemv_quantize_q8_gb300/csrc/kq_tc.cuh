@@ -11,4 +11,20 @@ size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, uint8_t *workspace, cudaStream_t st);
 
+// Routed experts on the tensor cores: 128-row tiles of each expert's routed rows (a tile table built
+// by the routing pass), activation panels gathered in routed order, outputs scattered back to their
+// (token, slot) rows.
+constexpr int kTcTileRows = 128;
+bool tc_grouped_eligible(kq_dtype wt, int64_t N, int64_t K);
+struct TcGroupedPanels {
+    int64_t rows, dstride;
+    size_t off_a, off_e, off_d, bytes;
+};
+TcGroupedPanels tc_grouped_panels(int64_t pairs, int64_t E, int64_t K);
+kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int rows_per_token, int top_k,
+                          int64_t pairs, int64_t E, int64_t N, int64_t K, float *y, uint8_t *panels,
+                          const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,
+                          const int *offset, const int *poff, const int *lists, unsigned long long *err,
+                          cudaStream_t st);
+
 }  // namespace kq

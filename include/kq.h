@@ -175,7 +175,10 @@ KQ_API kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, 
  * ids: int32 [M][top_k] expert of each (token, slot).  xq: activation rows; xq_rows_per_token = 1
  * ("broadcast": slot (t,k) reads row t) or top_k ("per-row": slot (t,k) reads row t*top_k+k).
  * y: fp32 [M][top_k][N]; y[t][k] = W_{ids[t][k]} . X_row.  Rows are gathered per expert in
- * (token, slot) order, so the result is deterministic.  An id outside [0, n_experts) is skipped
+ * (token, slot) order, so the result is deterministic.  Q4_K and Q6_K run on the tensor cores in
+ * 128-row tiles of each expert's rows (integer parts exact; fp32 promotion with fused multiply-adds,
+ * so outputs match the sequential CPU order to within rounding, not bit for bit); Q8_0 runs on the
+ * exact dp4a path in the CPU order.  An id outside [0, n_experts) is skipped
  * (its y row is not written) and recorded in the workspace's device flag: kq_read_device_flag
  * then returns KQ_ERR_DEVICE_FLAG.  workspace: kq_gemm_workspace_bytes(wt, M, N, K, n_experts,
  * top_k) bytes, 256-byte aligned. */
@@ -200,9 +203,9 @@ KQ_API kq_status kq_gemm_grouped_noalloc(kq_dtype wt, const void *w, int64_t n_e
                                          int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k,
                                          int64_t N, int64_t K, float *y, kq_stream_t stream);
 
-/* Read (and clear) the device flag of a grouped workspace.  Synchronises `stream`.
- * Returns KQ_OK, KQ_ERR_DEVICE_FLAG (an invalid expert id was seen; count in *n_bad if non-NULL),
- * or KQ_ERR_CUDA. */
+/* Read (and clear) the device flag of a kq_gemm / kq_gemm_grouped workspace.  Synchronises `stream`.
+ * Returns KQ_OK, KQ_ERR_DEVICE_FLAG (an invalid expert id was seen, or a tensor-core pipeline wait
+ * timed out; the count is in *n_bad if non-NULL), or KQ_ERR_CUDA. */
 KQ_API kq_status kq_read_device_flag(void *workspace, int64_t *n_bad, kq_stream_t stream);
 
 /* Weighted expert sum ([llama-18] weighted_expert_sum commit): out[t][n] = w[t][0]*y[t][0][n] +

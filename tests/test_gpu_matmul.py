@@ -228,6 +228,14 @@ def test_q8_0_swiglu_full_size_sampled():
 # ----------------------------------------------------------------------------- routed experts
 
 
+def _close(dtype, got, ref):
+    # Q4_K / Q6_K routed experts run on the tensor cores: integer parts exact, fp32 promotion in a
+    # different (fused) order, so near-exact; Q8_0 runs on the exact dp4a path in the CPU order
+    if dtype == kq.Q8_0:
+        return np.array_equal(got, ref)
+    return np.isfinite(got).all() and nmse(got, ref) <= 1e-10
+
+
 def _grouped(dtype, wn, E, xq, rpt, ids, M, top_k, N, K):
     y = torch.full((M, top_k, N), float("nan"), device=DEV)
     wsb = kq.gemm_workspace_bytes(dtype, M, N, K, E, top_k)
@@ -252,7 +260,24 @@ def test_grouped_small(dtype, rpt):
     ref, bad = oracle.gemm_grouped(dtype, w, E, _oracle_act(dtype, x), 1 if rpt == "broadcast" else top_k, ids, M,
                                    top_k, N, K)
     assert bad == 0
-    assert np.array_equal(host(y), ref)
+    assert _close(dtype, host(y), ref)
+
+
+@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K])
+def test_grouped_tensor_core_multi_tile(dtype):
+    # experts with more than one 128-row tile, several row tiles, a tail tile, an empty expert
+    g = synth.rng(405 + dtype)
+    E, M, top_k, N, K = 5, 300, 2, 256, 1024
+    w = synth.weights(dtype, E * N, K, g)
+    ids, _ = synth.routing(M, E, top_k, g)
+    ids[ids == 4] = 0  # expert 4 gets no rows, expert 0 gets many
+    x = synth.activations(M * top_k, K, g, outliers=True)
+    wn = repack(dtype, w, E * N, K)
+    xq = act_quant(dtype, dev(x), M * top_k, K)
+    y, ws = _grouped(dtype, wn, E, xq, top_k, ids, M, top_k, N, K)
+    assert kq.kq_read_device_flag(ws) == 0
+    ref, _ = oracle.gemm_grouped(dtype, w, E, oracle.quantize_q8_k(x), top_k, ids, M, top_k, N, K)
+    assert _close(dtype, host(y), ref)
 
 
 def test_grouped_invalid_ids_flag_and_untouched_rows():
@@ -273,7 +298,7 @@ def test_grouped_invalid_ids_flag_and_untouched_rows():
     ref, bad = oracle.gemm_grouped(kq.Q4_K, w, E, oracle.quantize_q8_k(x), 1, ids, M, top_k, N, K)
     assert bad == 2
     ok = np.isfinite(ref)
-    assert np.array_equal(yh[ok], ref[ok])
+    assert _close(kq.Q4_K, yh[ok], ref[ok])
 
 
 def test_grouped_top1_single_expert_equals_dense():
@@ -285,7 +310,7 @@ def test_grouped_top1_single_expert_equals_dense():
     xq = act_quant(kq.Q6_K, dev(x), M, K)
     y, _ = _grouped(kq.Q6_K, wn, E, xq, 1, np.zeros((M, 1), np.int32), M, 1, N, K)
     dense = gemm(kq.Q6_K, repack(kq.Q6_K, w[:N], N, K), xq, M, N, K)
-    assert np.array_equal(host(y)[:, 0], host(dense))
+    assert _close(kq.Q6_K, host(y)[:, 0], host(dense))
 
 
 def test_weighted_sum_bit_exact():
@@ -327,14 +352,15 @@ def test_moe_block_small_end_to_end():
     y_gu, h, hq, y_dn, out = _moe_pipeline(dev(x), repack(kq.Q4_K, w_gu, E * 2 * F, H),
                                            repack(kq.Q6_K, w_dn, E * H, F), ids, wts, E, top_k, H, F)
     ref_gu, _ = oracle.gemm_grouped(kq.Q4_K, w_gu, E, oracle.quantize_q8_k(x), 1, ids, M, top_k, 2 * F, H)
-    assert np.array_equal(host(y_gu), ref_gu)
+    assert _close(kq.Q4_K, host(y_gu), ref_gu)
     # downstream of exp(): the oracle continues from the GPU's h (ulp-level exp differences
     # are bounded separately), then every later stage must match bit for bit
     hq_ref = oracle.quantize_q8_k(host(h))
     assert np.array_equal(host(hq).reshape(M * top_k, -1), hq_ref)
     ref_dn, _ = oracle.gemm_grouped(kq.Q6_K, w_dn, E, hq_ref, top_k, ids, M, top_k, H, F)
-    assert np.array_equal(host(y_dn), ref_dn)
-    assert np.array_equal(host(out), oracle.moe_weighted_sum(ref_dn, wts))
+    assert _close(kq.Q6_K, host(y_dn), ref_dn)
+    # the weighted sum is exact: checked from the GPU's own slot outputs
+    assert np.array_equal(host(out), oracle.moe_weighted_sum(host(y_dn), wts))
     # and the whole block against the oracle's own SwiGLU
     h_ref = oracle.swiglu(ref_gu.reshape(-1, 2 * F)[:, :F], ref_gu.reshape(-1, 2 * F)[:, F:])
     dn2, _ = oracle.gemm_grouped(kq.Q6_K, w_dn, E, oracle.quantize_q8_k(h_ref), top_k, ids, M, top_k, H, F)
@@ -354,9 +380,9 @@ def test_moe_block_full_size_sampled():
     toks = g.choice(M, 12, replace=False)
     xq_ref = oracle.quantize_q8_k(x[toks])
     ref_gu, _ = oracle.gemm_grouped(kq.Q4_K, w_gu, E, xq_ref, 1, ids[toks], len(toks), top_k, 2 * F, H)
-    assert np.array_equal(host(y_gu)[toks], ref_gu)
+    assert _close(kq.Q4_K, host(y_gu)[toks], ref_gu)
     hh = host(h).reshape(M, top_k, F)[toks].reshape(-1, F)
     hq_ref = oracle.quantize_q8_k(hh)
     ref_dn, _ = oracle.gemm_grouped(kq.Q6_K, w_dn, E, hq_ref, top_k, ids[toks], len(toks), top_k, H, F)
-    assert np.array_equal(host(y_dn)[toks], ref_dn)
-    assert np.array_equal(host(out)[toks], oracle.moe_weighted_sum(ref_dn, wts[toks]))
+    assert _close(kq.Q6_K, host(y_dn)[toks], ref_dn)
+    assert np.array_equal(host(out)[toks], oracle.moe_weighted_sum(host(y_dn)[toks], wts[toks]))
