@@ -25,7 +25,7 @@ struct GroupedWs {
 
 // Regions the tensor-core grouped path appends to the routing workspace.
 struct GroupedTcWs {
-    size_t off_poff, off_tile_count, off_tiles, off_panels, total;
+    size_t off_poff, off_prow, off_tile_count, off_tiles, off_panels, total;
     int64_t max_tiles;
 };
 
@@ -34,6 +34,7 @@ static GroupedTcWs grouped_tc_ws(size_t base, int64_t pairs, int64_t E, int64_t 
     w.max_tiles = (pairs + kTcTileRows - 1) / kTcTileRows + E;
     size_t o = base;
     w.off_poff = o; o += align256(sizeof(int) * E);
+    w.off_prow = o; o += align256(sizeof(int) * pairs);
     w.off_tile_count = o; o += align256(sizeof(int));
     w.off_tiles = o; o += align256(sizeof(int) * 2 * w.max_tiles);
     w.off_panels = o; o += tc_grouped_panels(pairs, E, K).bytes;
@@ -84,64 +85,113 @@ __global__ void route_count_kernel(const int32_t *__restrict__ ids, int64_t pair
     }
 }
 
-// Single block: exclusive scan of the counts and the tile table (expert, first row) per expert.
-__global__ void route_scan_kernel(const int *__restrict__ count, int E, int *__restrict__ offset,
-                                  int *__restrict__ tiles, int *__restrict__ tile_count) {
-    if (threadIdx.x != 0) return;
-    int off = 0, nt = 0;
-    for (int e = 0; e < E; ++e) {
-        offset[e] = off;
-        const int c = count[e];
-        for (int s = 0; s < c; s += kTileM) {
-            tiles[2 * nt] = e;
-            tiles[2 * nt + 1] = s;
-            ++nt;
-        }
-        off += c;
+// Inclusive scan over the 1024 threads of a block (warp shuffles, then the 32 warp totals).
+__device__ __forceinline__ int block_scan_incl(int v, int *warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, s);
+        if (lane >= s) v += o;
     }
-    *tile_count = nt;
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, t, s);
+            if (lane >= s) t += o;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int r = v + (warp > 0 ? warp_tot[warp - 1] : 0);
+    __syncthreads();
+    return r;
 }
 
-// Tensor-core tile table (single thread): expert rows padded to a multiple of 4 in the activation
-// panels (poff), and one (expert, tile) entry per 128 routed rows of each expert.
-__global__ void route_tc_tiles_kernel(const int *__restrict__ count, int E, int *__restrict__ poff,
-                                      int *__restrict__ tiles, int *__restrict__ tile_count) {
-    if (threadIdx.x != 0) return;
-    int off = 0, nt = 0;
-    for (int e = 0; e < E; ++e) {
-        poff[e] = off;
-        const int c = count[e];
-        for (int j = 0; j * kTcTileRows < c; ++j) {
-            tiles[2 * nt] = e;
-            tiles[2 * nt + 1] = j;
-            ++nt;
+// One block of 1024 threads: exclusive scan of the expert counts (offset), the dp4a tile table of
+// 64-row tiles (expert, first row) and, when poff != NULL, the tensor-core table: expert rows padded
+// to a multiple of 4 (poff) and one (expert, 128-row tile index) entry per tile.
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int *__restrict__ count, int E, int *__restrict__ offset,
+                                                          int *__restrict__ tiles, int *__restrict__ tile_count,
+                                                          int *__restrict__ poff, int *__restrict__ tc_tiles,
+                                                          int *__restrict__ tc_tile_count) {
+    __shared__ int wt[32];
+    __shared__ int tot[4];
+    int carry_off = 0, carry_t = 0, carry_p = 0, carry_tc = 0;
+    for (int e0 = 0; e0 < E; e0 += 1024) {
+        const int e = e0 + threadIdx.x;
+        const int c = e < E ? count[e] : 0;
+        const int nt = (c + kTileM - 1) / kTileM, ntc = (c + kTcTileRows - 1) / kTcTileRows, cp = (c + 3) & ~3;
+        const int i_off = block_scan_incl(c, wt);
+        const int i_t = block_scan_incl(nt, wt);
+        const int i_p = block_scan_incl(cp, wt);
+        const int i_tc = block_scan_incl(ntc, wt);
+        if (e < E) {
+            offset[e] = carry_off + i_off - c;
+            const int t0 = carry_t + i_t - nt;
+            for (int j = 0; j < nt; ++j) { tiles[2 * (t0 + j)] = e; tiles[2 * (t0 + j) + 1] = j * kTileM; }
+            if (poff) {
+                poff[e] = carry_p + i_p - cp;
+                const int u0 = carry_tc + i_tc - ntc;
+                for (int j = 0; j < ntc; ++j) { tc_tiles[2 * (u0 + j)] = e; tc_tiles[2 * (u0 + j) + 1] = j; }
+            }
         }
-        off += (c + 3) & ~3;
+        // block totals: the last thread's inclusive values
+        if (threadIdx.x == 1023) { tot[0] = i_off; tot[1] = i_t; tot[2] = i_p; tot[3] = i_tc; }
+        __syncthreads();
+        carry_off += tot[0]; carry_t += tot[1]; carry_p += tot[2]; carry_tc += tot[3];
+        __syncthreads();
     }
-    *tile_count = nt;
+    if (threadIdx.x == 0) {
+        *tile_count = carry_t;
+        if (poff) *tc_tile_count = carry_tc;
+    }
 }
 
-// One block per expert: stable compaction of its pairs, in ascending pair order.
-__global__ void route_fill_kernel(const int32_t *__restrict__ ids, int64_t pairs, const int *__restrict__ offset,
-                                  int *__restrict__ lists) {
-    __shared__ int scan[256];
-    const int e = blockIdx.x;
-    int base = offset[e];
-    for (int64_t p0 = 0; p0 < pairs; p0 += blockDim.x) {
-        const int64_t p = p0 + threadIdx.x;
-        const int f = (p < pairs && ids[p] == e) ? 1 : 0;
-        scan[threadIdx.x] = f;
-        __syncthreads();
-        for (int s = 1; s < 256; s <<= 1) {  // inclusive Hillis-Steele scan
-            int v = threadIdx.x >= s ? scan[threadIdx.x - s] : 0;
-            __syncthreads();
-            scan[threadIdx.x] += v;
-            __syncthreads();
+// One warp per expert: stable compaction of its pairs, in ascending pair order.  A step covers 256
+// pairs: lane l holds pairs 8l .. 8l+7 of the step, an exclusive warp scan of the per-lane match
+// counts places them.  With prow != NULL also the tensor-core panel row of every list entry.
+__global__ void route_fill_kernel(const int32_t *__restrict__ ids, int64_t pairs, int E, const int *__restrict__ offset,
+                                  int *__restrict__ lists, const int *__restrict__ poff, int *__restrict__ prow) {
+    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (e >= E) return;
+    const int base0 = offset[e];
+    const int pbase = poff ? poff[e] : 0;
+    const bool vec = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
+    int n = 0;
+    for (int64_t p0 = 0; p0 < pairs; p0 += 256) {
+        const int64_t q = p0 + 8 * lane;
+        int v[8];
+        if (vec && q + 8 <= pairs) {
+            const int4 a = *reinterpret_cast<const int4 *>(ids + q);
+            const int4 b = *reinterpret_cast<const int4 *>(ids + q + 4);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = q + k < pairs ? ids[q + k] : -1;
         }
-        if (f) lists[base + scan[threadIdx.x] - 1] = (int)p;
-        const int tot = scan[255];
-        __syncthreads();
-        base += tot;
+        int c = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) c += v[k] == e;
+        int incl = c;
+#pragma unroll
+        for (int s2 = 1; s2 < 32; s2 <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, s2);
+            if (lane >= s2) incl += o;
+        }
+        int i = n + incl - c;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (v[k] == e) {
+                lists[base0 + i] = (int)(q + k);
+                if (prow) prow[base0 + i] = pbase + i;
+                ++i;
+            }
+        }
+        n += __shfl_sync(0xffffffffu, incl, 31);
     }
 }
 
@@ -273,25 +323,23 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
     int *lists = reinterpret_cast<int *>(ws + L.off_lists);
     const int64_t pairs = M * top_k;
     route_count_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, (int)n_experts, count, flag);
-    route_scan_kernel<<<1, 32, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count);
-    route_fill_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, offset, lists);
+    const bool tc = tc_grouped_eligible(wt, N, K);
+    const GroupedTcWs T = grouped_tc_ws(L.total, pairs, n_experts, K);
+    int *poff = tc ? reinterpret_cast<int *>(ws + T.off_poff) : nullptr;
+    int *prow = tc ? reinterpret_cast<int *>(ws + T.off_prow) : nullptr;
+    int *tc_tiles = tc ? reinterpret_cast<int *>(ws + T.off_tiles) : nullptr;
+    int *tc_count = tc ? reinterpret_cast<int *>(ws + T.off_tile_count) : nullptr;
+    route_scan_kernel<<<1, 1024, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count, poff, tc_tiles, tc_count);
+    route_fill_kernel<<<(unsigned)((n_experts + 7) / 8), 256, 0, st>>>(ids, pairs, (int)n_experts, offset, lists, poff,
+                                                                      prow);
     s = check_launch("kq_gemm_grouped routing");
     if (s != KQ_OK) return s;
     count_launch(R_ROUTE, 3);
-    if (tc_grouped_eligible(wt, N, K)) {
-        const GroupedTcWs T = grouped_tc_ws(L.total, pairs, n_experts, K);
-        int *poff = reinterpret_cast<int *>(ws + T.off_poff);
-        int *tc_tiles = reinterpret_cast<int *>(ws + T.off_tiles);
-        int *tc_count = reinterpret_cast<int *>(ws + T.off_tile_count);
-        route_tc_tiles_kernel<<<1, 32, 0, st>>>(count, (int)n_experts, poff, tc_tiles, tc_count);
-        s = check_launch("kq_gemm_grouped tile table");
-        if (s != KQ_OK) return s;
-        count_launch(R_ROUTE, 1);
+    if (tc)
         return tc_gemm_grouped(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq),
                                (int)xq_rows_per_token, (int)top_k, pairs, n_experts, N, K, y, ws + T.off_panels,
-                               tc_tiles, tc_count, T.max_tiles, count, offset, poff, lists,
+                               tc_tiles, tc_count, T.max_tiles, count, offset, poff, lists, prow,
                                reinterpret_cast<unsigned long long *>(flag), st);
-    }
     MmqExactArgs a{};
     a.w = static_cast<const uint8_t *>(w);
     a.xq = static_cast<const uint8_t *>(xq);
@@ -413,8 +461,9 @@ extern "C" kq_status kq_gemm_grouped_noalloc(kq_dtype wt, const void *w, int64_t
     // Every scratch field is fully rewritten below before it is read, so nothing left by an earlier
     // call needs clearing.
     route_count_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, (int)n_experts, count, flag);
-    route_scan_kernel<<<1, 32, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count);
-    route_fill_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, offset, lists);
+    route_scan_kernel<<<1, 1024, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count, nullptr, nullptr, nullptr);
+    route_fill_kernel<<<(unsigned)((n_experts + 7) / 8), 256, 0, st>>>(ids, pairs, (int)n_experts, offset, lists,
+                                                                      nullptr, nullptr);
     s = check_launch("kq_gemm_grouped_noalloc routing");
     if (s != KQ_OK) return s;
     count_launch(R_ROUTE, 3);

@@ -29,6 +29,7 @@
 // they do not steal issue slots or shared-memory bandwidth from the converter and epilogue warps.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records an error in the workspace's
 // device flag and leaves after draining its own copies and MMAs; it never spins forever.
+#include <algorithm>
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -106,7 +107,39 @@ struct TcParams {
     // lists[offset[e] .. offset[e] + count[e]), and its weights start at row group e * N/16.
     int grouped;
     const int *tiles, *tile_count, *count, *offset, *poff, *lists;
+    // Tile schedule: tiles are numbered token-tile-major (weight-row tile fastest): m_tiles x n_tiles
+    // (dense) or *tile_count x n_tiles (grouped), so CTAs running at the same time share activation
+    // tiles.  persistent: CTA b runs tiles b, b + gridDim.x, ...; otherwise CTA (x, y) runs tile
+    // y*n_tiles + x alone (the split-K launch).
+    int persistent, n_tiles, m_tiles;
 };
+
+struct TcTile {
+    int n0, m0, tok_valid, g0, valid_groups, list_base;
+};
+
+// Geometry of tile `tile`: weight rows n0.., first panel row m0, stored token rows, first weight row
+// group, row groups present, and (grouped) the first pair-list entry.
+__device__ __forceinline__ TcTile tc_tile(const TcParams &P, int tile, int m_tiles) {
+    TcTile T;
+    const int nt = tile % P.n_tiles, mt = tile / P.n_tiles;
+    (void)m_tiles;
+    T.n0 = nt * TC_ROWS;
+    T.valid_groups = min(8, (P.N + 15) / 16 - T.n0 / 16);
+    if (P.grouped) {
+        const int e = P.tiles[2 * mt], j = P.tiles[2 * mt + 1];
+        T.m0 = P.poff[e] + j * TC_TOK;
+        T.tok_valid = min(TC_TOK, P.count[e] - j * TC_TOK);
+        T.g0 = e * (P.N / 16) + T.n0 / 16;
+        T.list_base = P.offset[e] + j * TC_TOK;
+    } else {
+        T.m0 = mt * TC_TOK;
+        T.tok_valid = P.M - T.m0;
+        T.g0 = T.n0 / 16;
+        T.list_base = 0;
+    }
+    return T;
+}
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -193,26 +226,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * TC_ROWS;
-    int m0 = blockIdx.y * TC_TOK;   // first panel row of the token tile
-    int tok_valid = P.M - m0;       // token rows of the tile that are stored
-    int g_base = 0, list_base = 0;  // grouped: expert's first row group, first pair-list entry
-    if (P.grouped) {
-        const int ti = blockIdx.y;
-        if (ti >= *P.tile_count) return;  // a spare slot of the tile table: the whole CTA leaves at once
-        const int e = P.tiles[2 * ti], j = P.tiles[2 * ti + 1];
-        m0 = P.poff[e] + j * TC_TOK;
-        tok_valid = min(TC_TOK, P.count[e] - j * TC_TOK);
-        g_base = e * (P.N / 16);
-        list_base = P.offset[e] + j * TC_TOK;
-    }
     const int nchunk = P.K / 256;
     const int sb0 = blockIdx.z * P.sb_per_split;
-    const int nsb = min(nchunk, sb0 + P.sb_per_split) - sb0;  // super-blocks of this CTA (t = sb - sb0)
-    const int groups_total = (P.N + 15) / 16;
-    const int valid_groups = min(8, groups_total - n0 / 16);
-    const int g0 = g_base + n0 / 16;
-    const int rows_valid = valid_groups * 16;
+    const int nsb = min(nchunk, sb0 + P.sb_per_split) - sb0;  // super-blocks per tile
+    const int m_tiles = P.grouped ? *P.tile_count : P.m_tiles;
+    const int ntiles = P.n_tiles * m_tiles;
+    const int tile0 = P.persistent ? (int)blockIdx.x : (int)(blockIdx.y * P.n_tiles + blockIdx.x);
+    const int tstride = P.persistent ? (int)gridDim.x : ntiles;
+    if (tile0 >= ntiles) return;  // no tile for this CTA: it leaves before any setup
+    // One step = one (tile, super-block); every role walks steps 0 .. nsteps-1 in the same order, so
+    // the rings and accumulators run on across tile boundaries without draining.
+    const int nsteps = (ntiles - tile0 + tstride - 1) / tstride * nsb;
+    // roles keep (tile i, super-block t) counters along the steps instead of dividing by nsb
+    auto tile_of = [&](int i) { return tc_tile(P, tile0 + i * tstride, m_tiles); };
 
     if (tid == 0) {
         for (int i = 0; i < NPAIR; ++i) { mbar_init(&k_full[i], 32 * TC_CONV_WARPS + 1); mbar_init(&k_empty[i], 1); }
@@ -246,27 +272,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int i = 0; i < 2; ++i) { last_p[i] = -1; last_e[i] = -1; }
             for (int i = 0; i < 4; ++i) last_d[i] = -1;
             bool ok = true;
-            for (int t = 0; t < nsb && ok; ++t) {
-                const int gsb = sb0 + t;
-                const int p = t & 1, pph = (t >> 1) & 1;
+            TcTile T{};
+            for (int st = 0, ti = 0, tt = 0; st < nsteps && ok; ++st) {
+                if (tt == 0) T = tile_of(ti);
+                const int gsb = sb0 + tt;
+                if (++tt == nsb) { tt = 0; ++ti; }
+                const int p = st & 1, pph = (st >> 1) & 1;
                 if (!(ok = mbar_wait_sleep(&p_empty[p], pph ^ 1, abort_flag))) break;
-                mbar_arrive_expect_tx(&p_full[p], valid_groups * C::CB);
-                for (int gi = 0; gi < valid_groups; ++gi)
-                    bulk_load(sP + (p * 8 + gi) * C::CB, P.w + ((int64_t)(g0 + gi) * nchunk + gsb) * C::CB, C::CB,
+                mbar_arrive_expect_tx(&p_full[p], T.valid_groups * C::CB);
+                for (int gi = 0; gi < T.valid_groups; ++gi)
+                    bulk_load(sP + (p * 8 + gi) * C::CB, P.w + ((int64_t)(T.g0 + gi) * nchunk + gsb) * C::CB, C::CB,
                               &p_full[p]);
                 last_p[p] = pph;
                 if (C::EXT) {
-                    const int e = t & 1, eph = (t >> 1) & 1;
+                    const int e = st & 1, eph = (st >> 1) & 1;
                     if (!(ok = mbar_wait_sleep(&e_empty[e], eph ^ 1, abort_flag))) break;
                     mbar_arrive_expect_tx(&e_full[e], 4096);
-                    tma_load_2d(sEB + e * 4096, &tmE, &e_full[e], gsb * 16, m0);
+                    tma_load_2d(sEB + e * 4096, &tmE, &e_full[e], gsb * 16, T.m0);
                     last_e[e] = eph;
                 }
                 {
-                    const int h = t & 3, hph = (t >> 2) & 1;
+                    const int h = st & 3, hph = (st >> 2) & 1;
                     if (!(ok = mbar_wait_sleep(&h_empty[h], hph ^ 1, abort_flag))) break;
                     mbar_arrive_expect_tx(&da_full[h], TC_TOK * 4);
-                    bulk_load(sDA + h * TC_TOK * 4, P.da + (int64_t)gsb * P.M_pad + m0, TC_TOK * 4, &da_full[h]);
+                    bulk_load(sDA + h * TC_TOK * 4, P.da + (int64_t)gsb * P.M_pad + T.m0, TC_TOK * 4, &da_full[h]);
                     last_d[h] = hph;
                 }
             }
@@ -289,11 +318,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int last_k[NPAIR];
             for (int i = 0; i < NPAIR; ++i) last_k[i] = -1;
             bool ok = true;
-            for (int pp = 0; pp < nsb * 2 && ok; ++pp) {
+            int m0 = 0, ti = 0, tt = 0;
+            for (int pp = 0; pp < nsteps * 2 && ok; ++pp) {
+                if ((pp & 1) == 0 && tt == 0) m0 = tile_of(ti).m0;
                 const int s = pp % NPAIR, ph = (pp / NPAIR) & 1;
                 if (!(ok = mbar_wait_sleep(&k_empty[s], ph ^ 1, abort_flag))) break;
                 mbar_arrive_expect_tx(&k_full[s], 2 * ACT_TILE);
-                const int x = (sb0 + pp / 2) * 256 + (pp & 1) * 2 * TC_KB;
+                const int x = (sb0 + tt) * 256 + (pp & 1) * 2 * TC_KB;
+                if ((pp & 1) && ++tt == nsb) { tt = 0; ++ti; }
                 tma_load_2d(sAct + (2 * s) * ACT_TILE, &tmA, &k_full[s], x, m0);
                 tma_load_2d(sAct + (2 * s + 1) * ACT_TILE, &tmA, &k_full[s], x + TC_KB, m0);
                 last_k[s] = ph;
@@ -322,7 +354,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint64_t dEA = smem_desc(smem_u32(sEA), 256, 6), dEB = smem_desc(smem_u32(sEB), 256, 6);
             const uint32_t d1 = tbase + w * TC_TOK;
             bool ok = true;
-            for (int t = w; t < nsb && ok; t += 2) {
+            for (int t = w; t < nsteps && ok; t += 2) {  // t: step
                 if (!(ok = mbar_wait_sleep(&acc_empty[w], ((t >> 1) & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
                 for (int pr = 0; pr < 2 && ok; ++pr) {
@@ -366,10 +398,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // extension MMA -- both are needed only once the super-block's main MMAs are done.
         const int cw = warp - TC_EPI_WARPS, grp = cw >> 2, q = cw & 3;
         const int row = 32 * q + lane;
-        const bool rvalid = row < rows_valid;
         const uint32_t lane_base = tbase + ((uint32_t)(32 * q) << 16);
-        bool ok = true;
-        for (int t = 0; t < nsb && ok; ++t) {
+        bool ok = true, rvalid = false;
+        for (int t = 0, ti = 0, tt = 0; t < nsteps && ok; ++t) {  // t: step
+            if (tt == 0) rvalid = row < tile_of(ti).valid_groups * 16;
+            if (++tt == nsb) { tt = 0; ++ti; }
             const int p = t & 1;
             if (!(ok = mbar_wait_sleep(&p_full[p], (t >> 1) & 1, abort_flag))) break;
             // rows past N were not loaded: their scales are forced to 0, so they convert to zeros
@@ -482,11 +515,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int q = warp & 3, tq = warp >> 2;  // TMEM lane quarter (weight rows), token quarter
         const int row = 32 * q + lane;
         const uint32_t lane_base = tbase + ((uint32_t)(32 * q) << 16);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
         bool ok = true;
-        for (int t = 0; t < nsb && ok; ++t) {
+        for (int t = 0, ti = 0, tt = 0; t < nsteps && ok; ++t) {  // t: step
             const int buf = t & 1, h = t & 3;
+            const int tile_i = ti;
+            const bool first = tt == 0, last = tt == nsb - 1;
+            if (++tt == nsb) { tt = 0; ++ti; }
+            if (first) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+            }
             if (!(ok = mbar_wait_sleep(&acc_full[buf], (t >> 1) & 1, abort_flag))) break;
             if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag))) break;
             if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag))) break;
@@ -524,20 +562,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive(&acc_empty[buf]);
                 mbar_arrive(&h_empty[h]);
             }
-        }
-        if (ok && P.nsplit == 1 && n0 + row < P.N) {
-            const int mrem = tok_valid - tq * 32;
-            if (P.grouped) {
-                // token row -> its (token, slot) output row
-                const int *lp = P.lists + list_base + tq * 32;
+            if (!last || P.nsplit != 1) continue;
+            const TcTile T = tile_of(tile_i);
+            if (T.n0 + row < P.N) {
+                // the tile's last super-block: store (a split-K tile is reduced across the cluster below)
+                const int mrem = T.tok_valid - tq * 32;
+                if (P.grouped) {
+                    // token row -> its (token, slot) output row
+                    const int *lp = P.lists + T.list_base + tq * 32;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < mrem) P.y[(int64_t)lp[i] * P.ldy + n0 + row] = acc[i];
-            } else {
-                float *yc = P.y + (int64_t)(m0 + tq * 32) * P.ldy + n0 + row;
+                    for (int i = 0; i < 32; ++i)
+                        if (i < mrem) P.y[(int64_t)lp[i] * P.ldy + T.n0 + row] = acc[i];
+                } else {
+                    float *yc = P.y + (int64_t)(T.m0 + tq * 32) * P.ldy + T.n0 + row;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < mrem) yc[(int64_t)i * P.ldy] = acc[i];
+                    for (int i = 0; i < 32; ++i)
+                        if (i < mrem) yc[(int64_t)i * P.ldy] = acc[i];
+                }
             }
         }
     }
@@ -563,7 +604,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int ml = r0 + idx / TC_ROWS, nl = idx % TC_ROWS;
             float v = 0.0f;
             for (int k = 0; k < S; ++k) v += cluster.map_shared_rank(red, k)[ml * RS + nl];
-            const int mm = m0 + ml, nn = n0 + nl;
+            const TcTile T = tile_of(0);
+            const int mm = T.m0 + ml, nn = T.n0 + nl;
             if (mm < P.M && nn < P.N) P.y[(int64_t)mm * P.ldy + nn] = v;
         }
         cluster.sync();
@@ -608,46 +650,35 @@ __global__ void act_panel_kernel(const uint8_t *__restrict__ xq, int M, int M_pa
     if (lane == 0) D[(int64_t)sb * M_pad + m] = d;
 }
 
-// Routed-expert prologue: the routed rows of expert e, in routed order, into the f16 code panel, the
-// f16 bsum panel and the f32 scale panel at panel rows poff[e] .. poff[e] + roundup4(count[e]) (the
-// padding rows are zero).  Row i of the expert is pair lists[offset[e] + i], whose activation is Q8_K
-// row pair / top_k (one row per token) or row pair (one row per pair).  One block per expert, a warp
-// per (row, super-block).
+// Routed-expert prologue: list entry s (pair lists[s], routed order) goes to panel row prow[s] of the
+// f16 code panel, the f16 bsum panel and the f32 scale panel; its activation is Q8_K row pair / top_k
+// (one row per token) or row pair (one row per pair).  One warp per (list entry, super-block).  The
+// padding rows between experts are left unwritten: they only feed token columns that are discarded.
 __global__ void act_panel_grouped_kernel(const uint8_t *__restrict__ xq, int rows_per_token, int top_k, int nsb,
-                                         const int *__restrict__ count, const int *__restrict__ offset,
-                                         const int *__restrict__ poff, const int *__restrict__ lists,
+                                         int64_t pairs, const int *__restrict__ lists, const int *__restrict__ prow,
                                          __half *__restrict__ A, __half *__restrict__ E, float *__restrict__ D,
                                          int64_t dstride) {
-    const int e = blockIdx.x;
-    const int c = count[e], rows = (c + 3) & ~3, base = poff[e];
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
+    if (wid >= pairs * nsb) return;
+    const int64_t sidx = wid / nsb;
+    const int sb = (int)(wid % nsb);
+    const int p = lists[sidx];
+    const int64_t r = prow[sidx];
+    const int64_t src = rows_per_token == 1 ? p / top_k : p;
     const int64_t K = (int64_t)nsb * 256;
-    for (int64_t wi = threadIdx.x / 32; wi < (int64_t)rows * nsb; wi += blockDim.x / 32) {
-        const int i = (int)(wi / nsb), sb = (int)(wi % nsb);
-        const int64_t r = base + i;
-        uint4 out = make_uint4(0, 0, 0, 0);
-        __half bsv = __float2half(0.0f);
-        float d = 0.0f;
-        if (i < c) {
-            const int p = lists[offset[e] + i];
-            const int64_t src = rows_per_token == 1 ? p / top_k : p;
-            const uint8_t *blk = xq + (src * nsb + sb) * kQ8KBytes;
-            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(blk + 4 + lane * 8);
-            const uint32_t w1 = *reinterpret_cast<const uint32_t *>(blk + 8 + lane * 8);
-            __half hv[8];
+    const uint8_t *blk = xq + (src * nsb + sb) * kQ8KBytes;
+    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(blk + 4 + lane * 8);
+    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(blk + 8 + lane * 8);
+    __half hv[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                hv[k] = __int2half_rn((int)(int8_t)((w0 >> (8 * k)) & 0xff));
-                hv[4 + k] = __int2half_rn((int)(int8_t)((w1 >> (8 * k)) & 0xff));
-            }
-            out = *reinterpret_cast<uint4 *>(hv);
-            if (lane < 16) bsv = __int2half_rn((int)reinterpret_cast<const int16_t *>(blk + 260)[lane]);
-            d = *reinterpret_cast<const float *>(blk);
-        }
-        *reinterpret_cast<uint4 *>(A + r * K + sb * 256 + lane * 8) = out;
-        if (lane < 16) E[r * nsb * 16 + sb * 16 + lane] = bsv;
-        if (lane == 0) D[(int64_t)sb * dstride + r] = d;
+    for (int k = 0; k < 4; ++k) {
+        hv[k] = __int2half_rn((int)(int8_t)((w0 >> (8 * k)) & 0xff));
+        hv[4 + k] = __int2half_rn((int)(int8_t)((w1 >> (8 * k)) & 0xff));
     }
+    *reinterpret_cast<uint4 *>(A + r * K + sb * 256 + lane * 8) = *reinterpret_cast<uint4 *>(hv);
+    if (lane < 16) E[r * nsb * 16 + sb * 16 + lane] = __int2half_rn((int)reinterpret_cast<const int16_t *>(blk + 260)[lane]);
+    if (lane == 0) D[(int64_t)sb * dstride + r] = *reinterpret_cast<const float *>(blk);
 }
 
 // ------------------------------------------------------------------ host side
@@ -720,6 +751,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
+// Number of SMs of the current device (looked up once per device).
+static int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 // One launch of the tensor-core kernel over activation panels built by a prologue.
 struct TcLaunch {
     const uint8_t *w;
@@ -729,8 +773,8 @@ struct TcLaunch {
     float *D;             // f32 scale panel [K/256][dstride]
     int64_t rows;         // panel rows (tensor-map extent; tiles past it read zeros)
     int64_t dstride;      // scale-panel row stride: >= any tile's first row + 128, a multiple of 4
-    unsigned grid_y;      // token tiles (dense) or tile-table slots (grouped)
-    int nsplit;
+    int m_tiles;          // token tiles (dense) or tile-table slots (grouped, an upper bound)
+    int nsplit;           // > 1: split-K clusters, one CTA per (tile, split); else persistent CTAs
     unsigned long long *err;
     bool grouped;
     const int *tiles, *tile_count, *count, *offset, *poff, *lists;
@@ -776,11 +820,19 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     p.grouped = a.grouped ? 1 : 0;
     p.tiles = a.tiles; p.tile_count = a.tile_count; p.count = a.count;
     p.offset = a.offset; p.poff = a.poff; p.lists = a.lists;
+    p.n_tiles = (int)((a.N + TC_ROWS - 1) / TC_ROWS);
+    p.m_tiles = a.m_tiles;
+    p.persistent = S > 1 ? 0 : 1;
+    const int64_t tiles = (int64_t)p.n_tiles * a.m_tiles;
+    if (tiles > 0x7fffffff) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: too many tiles");
     auto kern = tc_gemm_kernel<DT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.N + TC_ROWS - 1) / TC_ROWS), a.grid_y, (unsigned)S);
+    if (S > 1)
+        cfg.gridDim = dim3((unsigned)p.n_tiles, (unsigned)a.m_tiles, (unsigned)S);
+    else
+        cfg.gridDim = dim3((unsigned)std::min<int64_t>(tiles, sm_count()), 1, 1);  // one CTA per SM, tiles strided
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Lay::ALLOC;
     cfg.stream = st;
@@ -816,7 +868,7 @@ kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, i
     TcLaunch a{};
     a.w = w; a.y = y; a.ldy = ldy; a.M = M; a.N = N; a.K = K;
     a.A = workspace + L.off_a; a.E = workspace + L.off_e; a.D = reinterpret_cast<float *>(workspace + L.off_d);
-    a.rows = L.M_pad; a.dstride = L.M_pad; a.grid_y = (unsigned)(L.M_pad / TC_TOK);
+    a.rows = L.M_pad; a.dstride = L.M_pad; a.m_tiles = (int)(L.M_pad / TC_TOK);
     a.nsplit = tc_splits(wt, M, N, K);
     a.err = reinterpret_cast<unsigned long long *>(workspace + L.off_flag);
     s = launch_tc_dt(wt, a, st);
@@ -845,21 +897,22 @@ TcGroupedPanels tc_grouped_panels(int64_t pairs, int64_t E, int64_t K) {
 kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int rows_per_token, int top_k,
                           int64_t pairs, int64_t E, int64_t N, int64_t K, float *y, uint8_t *panels,
                           const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,
-                          const int *offset, const int *poff, const int *lists, unsigned long long *err,
-                          cudaStream_t st) {
+                          const int *offset, const int *poff, const int *lists, const int *prow,
+                          unsigned long long *err, cudaStream_t st) {
     const TcGroupedPanels G = tc_grouped_panels(pairs, E, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || max_tiles > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: shape too large for the tensor-core grid");
     const int64_t nsb = K / 256;
-    act_panel_grouped_kernel<<<(unsigned)E, 256, 0, st>>>(
-        xq, rows_per_token, top_k, (int)nsb, count, offset, poff, lists, reinterpret_cast<__half *>(panels + G.off_a),
+    const int64_t warps = pairs * nsb;
+    act_panel_grouped_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+        xq, rows_per_token, top_k, (int)nsb, pairs, lists, prow, reinterpret_cast<__half *>(panels + G.off_a),
         reinterpret_cast<__half *>(panels + G.off_e), reinterpret_cast<float *>(panels + G.off_d), G.dstride);
     kq_status s = check_launch("kq_gemm_grouped (activation panel)");
     if (s != KQ_OK) return s;
     TcLaunch a{};
     a.w = w; a.y = y; a.ldy = N; a.M = pairs; a.N = N; a.K = K;
     a.A = panels + G.off_a; a.E = panels + G.off_e; a.D = reinterpret_cast<float *>(panels + G.off_d);
-    a.rows = G.rows; a.dstride = G.dstride; a.grid_y = (unsigned)max_tiles;
+    a.rows = G.rows; a.dstride = G.dstride; a.m_tiles = (int)max_tiles;
     a.nsplit = 1;
     a.err = err;
     a.grouped = true;
