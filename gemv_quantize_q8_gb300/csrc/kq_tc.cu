@@ -59,20 +59,37 @@ template <>
 struct TcCfg<KQ_Q4_K> {
     static constexpr int CB = kQ4KChunk;  // packed chunk bytes per 16-row group
     static constexpr bool EXT = true;     // min term through the extension MMA
+    static constexpr bool Q8 = false;     // per-32-block scales (Q8_0 x Q8_1)
     static constexpr int A_COLS = 32;     // TMEM columns of one converted kblock (64 f16)
+    static constexpr int NACC = 2;        // accumulator buffers
+    static constexpr int BPS = 1;         // accumulator read-outs per step (scale blocks per 256 K)
+    static constexpr int H_ROW = 8;       // bytes of row scales per step: f32 (d, -dmin)
     static constexpr uint32_t TM_S2 = 256, TM_A = 384;
 };
 template <>
 struct TcCfg<KQ_Q6_K> {
     static constexpr int CB = kQ6KChunk;
-    static constexpr bool EXT = false;
+    static constexpr bool EXT = false, Q8 = false;
     static constexpr int A_COLS = 64;     // lo tile (32 columns) then 16*hi tile (32 columns)
+    static constexpr int NACC = 2, BPS = 1, H_ROW = 8;  // f32 (d, 0)
     static constexpr uint32_t TM_S2 = 0, TM_A = 256;
 };
-// TMEM map: accumulator buffers at columns 0 and 128; Q4_K min-term tile at 256; converted kblock
-// stages from TM_A on (4 stages = one super-block).
+template <>
+struct TcCfg<KQ_Q8_0> {
+    static constexpr int CB = kQ80Chunk;
+    static constexpr bool EXT = false, Q8 = true;
+    static constexpr int A_COLS = 32;
+    // every 32-element block has its own weight and activation scale, so every block's integer
+    // dot P_b is read out of its own accumulator: three buffers rotate along the blocks
+    static constexpr int NACC = 3, BPS = 8, H_ROW = 16;  // the row's 8 f16 block scales
+    static constexpr uint32_t TM_S2 = 0, TM_A = 384;
+};
+// TMEM map: accumulator buffers at columns 0, 128 (and 256 for Q8_0); Q4_K min-term tile at 256;
+// converted kblock stages from TM_A on (4 stages = one super-block).
 static_assert(TcCfg<KQ_Q4_K>::TM_A + 4 * TcCfg<KQ_Q4_K>::A_COLS <= TMEM_COLS, "Q4_K TMEM map");
 static_assert(TcCfg<KQ_Q6_K>::TM_A + 4 * TcCfg<KQ_Q6_K>::A_COLS <= TMEM_COLS, "Q6_K TMEM map");
+static_assert(TcCfg<KQ_Q8_0>::NACC * 128 <= (int)TcCfg<KQ_Q8_0>::TM_A &&
+                  TcCfg<KQ_Q8_0>::TM_A + 4 * TcCfg<KQ_Q8_0>::A_COLS <= TMEM_COLS, "Q8_0 TMEM map");
 
 template <int DT>
 struct TcLayout {
@@ -82,15 +99,16 @@ struct TcLayout {
     static constexpr int EA_OFF = (P_OFF + 2 * 8 * C::CB + 1023) & ~1023;
     static constexpr int EB_OFF = EA_OFF + (C::EXT ? 2 * 4096 : 0);
     static constexpr int H_OFF = EB_OFF + (C::EXT ? 2 * 4096 : 0);
-    static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * 8;
-    static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4;
-    static constexpr int NBAR = 2 * NPAIR + 2 * 2 + 2 * 2 + 3 * 4 + 2 * 2 + 2;
+    static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * C::H_ROW;
+    static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4 * C::BPS;
+    static constexpr int NBAR = 2 * NPAIR + 2 * 2 + 2 * 2 + 3 * 4 + 2 * 3 + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = MISC_OFF + 16;
     static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment of the base
 };
 static_assert(TcLayout<KQ_Q4_K>::ALLOC <= 227 * 1024, "Q4_K tensor-core smem budget");
 static_assert(TcLayout<KQ_Q6_K>::ALLOC <= 227 * 1024, "Q6_K tensor-core smem budget");
+static_assert(TcLayout<KQ_Q8_0>::ALLOC <= 227 * 1024, "Q8_0 tensor-core smem budget");
 // the split-K reduction parks a 128 x (128 + 4) fp32 tile in the activation ring
 static_assert(TC_TOK * (TC_ROWS + 4) * 4 <= NACT * ACT_TILE, "split-K staging fits the activation ring");
 
@@ -220,8 +238,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t *p_full = k_empty + NPAIR, *p_empty = p_full + 2;
     uint64_t *e_full = p_empty + 2, *e_empty = e_full + 2;  // Q4_K: bsums (TMA) + mins (converters)
     uint64_t *h_full = e_empty + 2, *da_full = h_full + 4, *h_empty = da_full + 4;
-    uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 2;
-    uint64_t *mma_done = acc_empty + 2;  // one per MMA issuer
+    uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 3;
+    uint64_t *mma_done = acc_empty + 3;  // one per MMA issuer
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 4);
 
@@ -245,8 +263,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 32 * TC_CONV_WARPS);
             mbar_init(&e_full[i], 32 * TC_CONV_WARPS / 2 + 1); mbar_init(&e_empty[i], 1);
-            mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS);
         }
+        for (int i = 0; i < C::NACC; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS); }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&h_full[i], 32 * TC_CONV_WARPS / 2); mbar_init(&da_full[i], 1);
             mbar_init(&h_empty[i], TC_EPI_WARPS);
@@ -294,8 +312,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 {
                     const int h = st & 3, hph = (st >> 2) & 1;
                     if (!(ok = mbar_wait_sleep(&h_empty[h], hph ^ 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(&da_full[h], TC_TOK * 4);
-                    bulk_load(sDA + h * TC_TOK * 4, P.da + (int64_t)gsb * P.M_pad + T.m0, TC_TOK * 4, &da_full[h]);
+                    // the scale panel has one row of M_pad floats per scale block (256 or 32 K)
+                    mbar_arrive_expect_tx(&da_full[h], C::BPS * TC_TOK * 4);
+                    for (int b = 0; b < C::BPS; ++b)
+                        bulk_load(sDA + (h * C::BPS + b) * TC_TOK * 4,
+                                  P.da + (int64_t)(gsb * C::BPS + b) * P.M_pad + T.m0, TC_TOK * 4, &da_full[h]);
                     last_d[h] = hph;
                 }
             }
@@ -354,7 +375,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint64_t dEA = smem_desc(smem_u32(sEA), 256, 6), dEB = smem_desc(smem_u32(sEB), 256, 6);
             const uint32_t d1 = tbase + w * TC_TOK;
             bool ok = true;
-            for (int t = w; t < nsteps && ok; t += 2) {  // t: step
+            if (C::Q8) {
+                // Q8_0: each 32-element block (two K16 MMAs) fills its own accumulator buffer, the
+                // buffers rotating along the global block index g = 8*step + block.  One issuer takes
+                // every step: a parity wait only tells apart consecutive phases, so a buffer's user
+                // must never run more than one use ahead of its releases, which a single in-order
+                // issuer guarantees (a second issuer could reach use u while use u-2 is still held).
+                for (int t = 0; t < nsteps && ok && w == 0; ++t) {
+                    int g = 8 * t, buf = g % C::NACC, use = g / C::NACC;
+                    for (int pr = 0; pr < 2 && ok; ++pr) {
+                        const int pp = 2 * t + pr, s = pp % NPAIR;
+                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag))) break;
+                        for (int h = 0; h < 2 && ok; ++h) {
+                            const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
+                            const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
+                            for (int blk = 0; blk < 2; ++blk) {
+                                if (!(ok = mbar_wait_sleep(&acc_empty[buf], (use & 1) ^ 1, abort_flag))) break;
+                                tc_fence_after();
+                                const uint32_t dq = tbase + buf * TC_TOK;
+                                mma_f16_ts(dq, a0 + blk * 16, bd + (uint64_t)(blk * 4), idesc, 0);
+                                mma_f16_ts(dq, a0 + blk * 16 + 8, bd + (uint64_t)(blk * 4 + 2), idesc, 1);
+                                mma_commit(&acc_full[buf]);
+                                if (++buf == C::NACC) { buf = 0; ++use; }
+                            }
+                        }
+                        if (!ok) break;
+                        mma_commit(&k_empty[s]);
+                    }
+                }
+            }
+            for (int t = w; t < nsteps && ok && !C::Q8; t += 2) {  // t: step
                 if (!(ok = mbar_wait_sleep(&acc_empty[w], ((t >> 1) & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
                 for (int pr = 0; pr < 2 && ok; ++pr) {
@@ -408,6 +458,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // rows past N were not loaded: their scales are forced to 0, so they convert to zeros
             const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
             const int r16 = row & 15;
+            if (C::Q8) {
+                // Q8_0: the row's 64 codes of kblock kb sit at kb*1024 + r16*64; its 8 f16 block
+                // scales at 4096 + r16*16.  Codes go to f16 exactly: (0x6400 | (c ^ 0x80)) = 1152 + c.
+                uint4 cv[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        cv[j][i] = reinterpret_cast<const uint4 *>(chunk + (grp + 2 * j) * 1024 + r16 * 64)[i];
+                uint4 dv = *reinterpret_cast<const uint4 *>(chunk + 4096 + r16 * 16);
+                if (!rvalid) dv = make_uint4(0, 0, 0, 0);
+                const __half2 c1152 = __float2half2_rn(1152.0f);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (t > 0) {
+                        const int pq = 2 * (t - 1) + j;
+                        if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag))) break;
+                    }
+                    tc_fence_after();
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t wv[4] = {cv[j][i].x ^ 0x80808080u, cv[j][i].y ^ 0x80808080u,
+                                                cv[j][i].z ^ 0x80808080u, cv[j][i].w ^ 0x80808080u};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            r[8 * i + 2 * k] = h2u(__hsub2(u2h(__byte_perm(wv[k], 0x64646464u, 0x4140)), c1152));
+                            r[8 * i + 2 * k + 1] = h2u(__hsub2(u2h(__byte_perm(wv[k], 0x64646464u, 0x4342)), c1152));
+                        }
+                    }
+                    tmem_st32(lane_base + C::TM_A + (grp + 2 * j) * C::A_COLS, r);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&k_full[(2 * t + j) % NPAIR]);
+                }
+                if (!ok) break;
+                if (grp == 0) {
+                    const int h = t & 3;
+                    if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag))) break;
+                    reinterpret_cast<uint4 *>(sH + h * TC_ROWS * C::H_ROW)[row] = dv;
+                    mbar_arrive(&h_full[h]);
+                }
+                mbar_arrive(&p_empty[p]);
+                continue;
+            }
             // every shared-memory read of the super-block is issued up front
             uint4 cv[2][2], qh[2];
 #pragma unroll
@@ -525,6 +620,46 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
             }
+            if (C::Q8) {
+                // Q8_0: per 32-element block b, acc += (d_w*d_a)*P_b with each product rounded on its
+                // own and the blocks added in ascending K order -- the CPU oracle's arithmetic, so the
+                // result is bit-identical to it
+                if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag))) break;
+                const uint4 dwv = reinterpret_cast<const uint4 *>(sH + h * TC_ROWS * C::H_ROW)[row];
+                const uint32_t dww[4] = {dwv.x, dwv.y, dwv.z, dwv.w};
+                int g = 8 * t, qb = g % C::NACC, use = g / C::NACC;
+                for (int b = 0; b < 8 && ok; ++b) {
+                    if (!(ok = mbar_wait_sleep(&acc_full[qb], use & 1, abort_flag))) break;
+                    tc_fence_after();
+                    const float dw = half_bits_to_float((uint16_t)((dww[b >> 1] >> (16 * (b & 1))) & 0xffff));
+                    const float2 dw2 = make_float2(dw, dw);
+                    const float4 *dap = reinterpret_cast<const float4 *>(sDA + (h * 8 + b) * TC_TOK * 4) + tq * 8;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float pv[8];
+                        tmem_ld8(lane_base + qb * TC_TOK + tq * 32 + c * 8, pv);
+                        tmem_wait_ld();
+                        const float4 da0 = dap[2 * c], da1 = dap[2 * c + 1];
+                        const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
+#pragma unroll
+                        for (int i = 0; i < 8; i += 2) {
+                            const float2 sc = fmul2(dw2, make_float2(da[i], da[i + 1]));
+                            const float2 tv = fmul2(sc, make_float2(pv[i], pv[i + 1]));
+                            // the sum stays scalar __fadd_rn, which is never contracted with the product
+                            acc[c * 8 + i] = __fadd_rn(acc[c * 8 + i], tv.x);
+                            acc[c * 8 + i + 1] = __fadd_rn(acc[c * 8 + i + 1], tv.y);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[qb]);
+                    if (++qb == C::NACC) { qb = 0; ++use; }
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&h_empty[h]);
+            } else {
             if (!(ok = mbar_wait_sleep(&acc_full[buf], (t >> 1) & 1, abort_flag))) break;
             if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag))) break;
             if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag))) break;
@@ -561,6 +696,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (lane == 0) {
                 mbar_arrive(&acc_empty[buf]);
                 mbar_arrive(&h_empty[h]);
+            }
             }
             if (!last || P.nsplit != 1) continue;
             const TcTile T = tile_of(tile_i);
@@ -650,6 +786,37 @@ __global__ void act_panel_kernel(const uint8_t *__restrict__ xq, int M, int M_pa
     if (lane == 0) D[(int64_t)sb * M_pad + m] = d;
 }
 
+// Activation prologue for Q8_0 weights: Q8_1 rows -> f16 code panel [M_pad][K] and f32 scale panel
+// [K/32][M_pad] (the f16 block scale widened); rows past M are zero.  One warp per (row, 256
+// elements): lane l takes elements 8l .. 8l+7 of block l/4.  Also clears the workspace's device flag.
+__global__ void act_panel_q81_kernel(const uint8_t *__restrict__ xq, int M, int M_pad, int nsb, __half *__restrict__ A,
+                                     float *__restrict__ D, unsigned long long *__restrict__ err) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (int64_t)M_pad * nsb) return;
+    const int m = (int)(wid / nsb), sb = (int)(wid % nsb);
+    const int64_t K = (int64_t)nsb * 256;
+    const int blk = sb * 8 + (lane >> 2);
+    uint4 out = make_uint4(0, 0, 0, 0);
+    float d = 0.0f;
+    if (m < M) {
+        const uint8_t *b = xq + ((int64_t)m * nsb * 8 + blk) * kQ81Bytes;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(b + 4 + (lane & 3) * 8);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(b + 8 + (lane & 3) * 8);
+        __half hv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            hv[i] = __int2half_rn((int)(int8_t)((w0 >> (8 * i)) & 0xff));
+            hv[4 + i] = __int2half_rn((int)(int8_t)((w1 >> (8 * i)) & 0xff));
+        }
+        out = *reinterpret_cast<uint4 *>(hv);
+        d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(b));
+    }
+    *reinterpret_cast<uint4 *>(A + (int64_t)m * K + sb * 256 + lane * 8) = out;
+    if ((lane & 3) == 0) D[(int64_t)blk * M_pad + m] = d;
+}
+
 // Routed-expert prologue: list entry s (pair lists[s], routed order) goes to panel row prow[s] of the
 // f16 code panel, the f16 bsum panel and the f32 scale panel; its activation is Q8_K row pair / top_k
 // (one row per token) or row pair (one row per pair).  One warp per (list entry, super-block).  The
@@ -689,21 +856,24 @@ struct TcWs {
 
 static size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-static TcWs tc_ws(int64_t M, int64_t K) {
+// Workspace of the dense tensor-core GEMM: device flag, f16 code panel, (Q4_K/Q6_K) f16 bsum panel,
+// f32 scale panel with one row per scale block (256 elements for Q8_K, 32 for Q8_1).
+static TcWs tc_ws(kq_dtype wt, int64_t M, int64_t K) {
     TcWs w{};
     w.M_pad = (int)((M + TC_TOK - 1) / TC_TOK * TC_TOK);
     const int64_t nsb = K / 256;
+    const bool q8 = wt == KQ_Q8_0;
     size_t o = 0;
     w.off_flag = o; o += 256;
     w.off_a = o; o += al256((size_t)w.M_pad * K * 2);
-    w.off_e = o; o += al256((size_t)w.M_pad * nsb * 16 * 2);
-    w.off_d = o; o += al256((size_t)w.M_pad * nsb * 4);
+    w.off_e = o; o += q8 ? 0 : al256((size_t)w.M_pad * nsb * 16 * 2);
+    w.off_d = o; o += al256((size_t)w.M_pad * nsb * (q8 ? 8 : 1) * 4);
     w.total = o;
     return w;
 }
 
 bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
-    if (wt != KQ_Q4_K && wt != KQ_Q6_K) return false;
+    if (wt != KQ_Q4_K && wt != KQ_Q6_K && wt != KQ_Q8_0) return false;
     if (M < 128 || N < 128) return false;
     if (K % 256 || K > (1 << 20) || M > (1 << 22) || N > (1 << 22)) return false;
     return true;
@@ -715,6 +885,7 @@ bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
 // and clusters of S CTAs fill whole GPCs only in multiples of S -- over power-of-two splits that
 // leave at least two super-blocks per CTA.
 static int tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
+    if (wt == KQ_Q8_0) return 1;  // keeps every output's blocks in one ascending sum (bit-exact)
     const int64_t tiles = ((M + TC_TOK - 1) / TC_TOK) * ((N + TC_ROWS - 1) / TC_ROWS);
     const int nsb = (int)(K / 256);
     const double t_sb = wt == KQ_Q4_K ? 1.3 : 1.75, t_fill = 2.5, t_red = 1.0;
@@ -735,7 +906,7 @@ static int tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
 
 size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     if (!tc_eligible(wt, M, N, K)) return 0;
-    return tc_ws(M, K).total;
+    return tc_ws(wt, M, K).total;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -797,7 +968,9 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(KQ_ERR_CUDA, "kq_gemm: tensor map A encode failed (%d)", (int)r);
     }
-    {
+    if (!TcCfg<DT>::EXT) {
+        tmE = tmA;  // no bsum operand
+    } else {
         cuuint64_t dims[2] = {(cuuint64_t)nsb * 16, (cuuint64_t)a.rows};
         cuuint64_t strides[1] = {(cuuint64_t)nsb * 32};
         cuuint32_t box[2] = {16, TC_TOK};
@@ -849,20 +1022,25 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
 }
 
 static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st) {
-    return wt == KQ_Q4_K ? launch_tc<KQ_Q4_K>(a, st) : launch_tc<KQ_Q6_K>(a, st);
+    return wt == KQ_Q4_K ? launch_tc<KQ_Q4_K>(a, st) : wt == KQ_Q6_K ? launch_tc<KQ_Q6_K>(a, st) : launch_tc<KQ_Q8_0>(a, st);
 }
 
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, uint8_t *workspace, cudaStream_t st) {
-    const TcWs L = tc_ws(M, K);
+    const TcWs L = tc_ws(wt, M, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || L.M_pad / TC_TOK > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm: shape too large for the tensor-core grid");
     const int64_t nsb = K / 256;
     const int64_t warps = (int64_t)L.M_pad * nsb;
-    act_panel_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
-        xq, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
-        reinterpret_cast<__half *>(workspace + L.off_e), reinterpret_cast<float *>(workspace + L.off_d),
-        reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
+    if (wt == KQ_Q8_0)
+        act_panel_q81_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+            xq, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
+            reinterpret_cast<float *>(workspace + L.off_d), reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
+    else
+        act_panel_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+            xq, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
+            reinterpret_cast<__half *>(workspace + L.off_e), reinterpret_cast<float *>(workspace + L.off_d),
+            reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
     kq_status s = check_launch("kq_gemm (activation panel)");
     if (s != KQ_OK) return s;
     TcLaunch a{};

@@ -13,7 +13,7 @@ import torch
 import gemv_quantize_q8_gb300 as kq
 import oracle
 from gemv_quantize_q8_gb300 import synth
-from tests.gpu_util import DEV, act_quant, dev, gemm, host, nmse, repack
+from tests.gpu_util import DEV, act_quant, dev, gemm, host, nmse, q8_1, repack
 
 pytestmark = pytest.mark.gpu
 
@@ -130,6 +130,43 @@ def test_gemm_small_and_partials(dtype, M, N, K):
     assert np.array_equal(host(P), oracle.partials(dtype, w, xq_ref, M, N, K))
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (130, 200, 768), (300, 392, 1536), (384, 1040, 2560)])
+def test_gemm_q8_0_tensor_core_bit_exact(M, N, K):
+    """Q8_0 x Q8_1 on the tensor cores: every 32-block's integer dot comes out of its own
+    accumulator and is scaled and added in ascending K order, as the oracle does, so the result is
+    bit-identical -- across several 128 x 128 tiles, ragged in M and N."""
+    g = synth.rng(350 + M + N + K)
+    w = synth.weights(kq.Q8_0, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(kq.Q8_0, w, N, K)
+    xq = q8_1(dev(x), M, K)
+    before = kq.launch_count("mmq_tc")
+    y = host(gemm(kq.Q8_0, wn, xq, M, N, K))
+    assert kq.launch_count("mmq_tc") > before, "expected the tensor-core route"
+    ref = oracle.gemm(kq.Q8_0, w, oracle.quantize_q8_1(x), M, N, K)
+    assert np.array_equal(y, ref), (nmse(y, ref), np.abs(y - ref).max())
+
+
+def test_gemm_q8_0_tensor_core_integer_special_case():
+    """All weight and activation scales 1.0: the tensor-core Q8_0 GEMM must then return the exact
+    integer product W.X (K = 768 keeps every sum below 2^24), which pins the integer block dots
+    read out of TMEM independently of the fp32 scaling."""
+    M, N, K = 256, 384, 768
+    g = synth.rng(377)
+    wi = g.integers(-128, 128, (N, K)).astype(np.int8)
+    w = np.zeros((N, K // 32, 34), np.uint8)
+    w[:, :, 0:2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    w[:, :, 2:] = wi.reshape(N, K // 32, 32).view(np.uint8)
+    w = w.reshape(N, -1)
+    xi = g.integers(-127, 128, (M, K))
+    xi.reshape(M, K // 32, 32)[:, :, 5] = 127       # every block's amax is 127, so its d is 1
+    x = xi.astype(np.float32)
+    wn = repack(kq.Q8_0, w, N, K)
+    y = host(gemm(kq.Q8_0, wn, q8_1(dev(x), M, K), M, N, K))
+    ref = (xi.astype(np.int64) @ wi.astype(np.int64).T).astype(np.float32)
+    assert np.array_equal(y, ref)
+
+
 def test_tiny_config_bit_exact():
     """The tiny Q4_K workload (W [256, 1024], X [8, 1024], seed 0) end to end."""
     c = synth.TINY
@@ -222,7 +259,12 @@ def test_q8_0_swiglu_full_size_sampled():
     xq_ref = np.zeros((M, K // 32 * 36), np.uint8)
     xq_ref[rows] = oracle.quantize_q8_1(h_ref)
     ref = oracle.gemm_sampled(kq.Q8_0, w, xq_ref, K, mi, ni)
+    # the activation codes are compared bit for bit by the quantizer tests; the GEMM itself is
+    # bit-exact on identical codes (tensor-core path), so any difference comes from SwiGLU's exp
     assert nmse(y[mi, ni], ref) <= 1e-6
+    xq_gpu = host(xq).reshape(M, -1)
+    ref_gpu_codes = oracle.gemm_sampled(kq.Q8_0, w, xq_gpu, K, mi, ni)
+    assert np.array_equal(y[mi, ni], ref_gpu_codes)
 
 
 # ----------------------------------------------------------------------------- routed experts
