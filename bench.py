@@ -291,15 +291,24 @@ def _time_graph(fn, reps, warmup=2):
     return statistics.median(ts)
 
 
-def run_aux(args, device):
+def run_aux(args, device, which="all"):
     """The two other hot-path pipelines, timed whole from CUDA graphs (not part of `value`):
     Q8_0 GEMM behind the fused SwiGLU -> Q8_1 prologue, and the routed-expert MoE block."""
+    out = {}
+    if which in ("all", "q8_0"):
+        out.update(_aux_q8_0(device))
+    if which in ("all", "moe"):
+        out.update(_aux_moe(device))
+    return out
+
+
+def _aux_q8_0(device):
+    """SwiGLU -> Q8_1 prologue + Q8_0 GEMM, M=2048 N=2560 K=9728, each timed from a CUDA graph."""
     import torch
 
     import gemv_quantize_q8_gb300 as kq
     from gemv_quantize_q8_gb300 import synth
     out = {}
-    # --- SwiGLU -> Q8_1 prologue + Q8_0 GEMM, M=2048 N=2560 K=9728
     c = synth.SWIGLU_Q8_0
     M, N, K = c["M"], c["N"], c["K"]
     g = synth.rng(0)
@@ -321,7 +330,17 @@ def run_aux(args, device):
         "gemm_tops": round(2.0 * M * N * K / (t_gemm * 1e-3) / 1e12, 2),
         "total_us": round((t_pro + t_gemm) * 1e3, 1)}
     del gu, xq, y, ws, wn
-    # --- MoE block: quantize -> grouped Q4_K gate/up -> SwiGLU + Q8_K -> grouped Q6_K down -> weighted sum
+    return out
+
+
+def _aux_moe(device):
+    """MoE block: quantize -> grouped Q4_K gate/up -> SwiGLU + Q8_K -> grouped Q6_K down -> weighted
+    sum, timed whole from a CUDA graph."""
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    from gemv_quantize_q8_gb300 import synth
+    out = {}
     c = synth.MOE
     E, top_k, M, H, F = c["n_experts"], c["top_k"], c["M"], c["hidden"], c["ffn"]
     g = synth.rng(0)
@@ -480,6 +499,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-aux", action="store_true", help="skip the Q8_0+SwiGLU and MoE pipeline timings")
     ap.add_argument("--decode-only", action="store_true", help="time only the decode GEMV (for profiling)")
+    ap.add_argument("--aux-only", choices=["all", "q8_0", "moe"], default=None,
+                    help="time only the Q8_0+SwiGLU and/or MoE pipelines (for profiling)")
     ap.add_argument("--gemv-calls", type=int, default=1000, help="back-to-back GEMV calls per decode shape")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
@@ -507,6 +528,10 @@ def main():
         decode, decode_gbs = run_decode(args, device)
         if rank == 0:
             print(json.dumps({"decode_gemv_gbs": round(decode_gbs, 1), "shapes": decode}), flush=True)
+        return
+    if args.aux_only:
+        if rank == 0:
+            print(json.dumps(run_aux(args, device, args.aux_only)), flush=True)
         return
     res = run_prefill(args, device, rank, world)
     ms = res["ms"]

@@ -47,6 +47,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase: never suspends the thread, so it is the cheap first check for a
+// phase that has usually completed already.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // try_wait that lets the thread sleep up to `hint_ns` for the phase instead of returning at once.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
@@ -80,6 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // does not spin and take issue slots from the warps that are working.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, volatile int *abort,
                                                 uint64_t limit_ns = 2000000000ull) {
+    if (mbar_test_wait(bar, parity)) return true;
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {

@@ -627,12 +627,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag))) break;
                 if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag))) break;
                 const uint4 dwv = reinterpret_cast<const uint4 *>(sH + h * TC_ROWS * C::H_ROW)[row];
-                const uint32_t dww[4] = {dwv.x, dwv.y, dwv.z, dwv.w};
                 int g = 8 * t, qb = g % C::NACC, use = g / C::NACC;
                 for (int b = 0; b < 8 && ok; ++b) {
                     if (!(ok = mbar_wait_sleep(&acc_full[qb], use & 1, abort_flag))) break;
                     tc_fence_after();
-                    const float dw = half_bits_to_float((uint16_t)((dww[b >> 1] >> (16 * (b & 1))) & 0xffff));
+                    // block b's f16 scale, picked from the four words with selects (no local array)
+                    const uint32_t dword = (b & 4) ? ((b & 2) ? dwv.w : dwv.z) : ((b & 2) ? dwv.y : dwv.x);
+                    const float dw = half_bits_to_float((uint16_t)((b & 1) ? (dword >> 16) : (dword & 0xffff)));
                     const float2 dw2 = make_float2(dw, dw);
                     const float4 *dap = reinterpret_cast<const float4 *>(sDA + (h * 8 + b) * TC_TOK * 4) + tq * 8;
 #pragma unroll
@@ -646,7 +647,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int i = 0; i < 8; i += 2) {
                             const float2 sc = fmul2(dw2, make_float2(da[i], da[i + 1]));
                             const float2 tv = fmul2(sc, make_float2(pv[i], pv[i + 1]));
-                            // the sum stays scalar __fadd_rn, which is never contracted with the product
+                            // the sums are scalar adds with explicit rounding: the compiler fuses packed
+                            // f32x2 multiplies and adds into fused multiply-adds, which would round once
+                            // instead of twice and leave the CPU order
                             acc[c * 8 + i] = __fadd_rn(acc[c * 8 + i], tv.x);
                             acc[c * 8 + i + 1] = __fadd_rn(acc[c * 8 + i + 1], tv.y);
                         }
