@@ -36,14 +36,15 @@ __device__ __forceinline__ void warp_quantize_q8k_smem(const float *__restrict__
         float ax = fabsf(v[i]);
         if (ax > amax) { amax = ax; mx = v[i]; }
     }
-    int src = lane;
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        float oa = __shfl_xor_sync(0xffffffffu, amax, s);
-        float om = __shfl_xor_sync(0xffffffffu, mx, s);
-        int os = __shfl_xor_sync(0xffffffffu, src, s);
-        if (oa > amax || (oa == amax && os < src)) { amax = oa; mx = om; src = os; }
-    }
+    // Block amax and the signed value of its first occurrence: amax is never negative or NaN, so its
+    // bit pattern orders like its value; the lowest lane holding the maximum holds the first
+    // occurrence (within a lane the strict > above keeps the first).  One max-reduction, one ballot
+    // and one shuffle -- a short dependency chain on the decode call's critical path.
+    const uint32_t key = __float_as_uint(amax);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const int src = __ffs(__ballot_sync(0xffffffffu, key == kmax)) - 1;
+    mx = __shfl_sync(0xffffffffu, mx, src);
+    amax = __uint_as_float(kmax);
     int qv[8], sum = 0;
     float iscale = 0.0f;
     if (amax != 0.0f) iscale = __fdiv_rn(-127.0f, mx);

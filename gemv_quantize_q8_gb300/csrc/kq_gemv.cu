@@ -295,6 +295,19 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     }
 }
 
+// Number of SMs of the current device (looked up once per device).
+static int gemv_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 template <int DT, bool FUSED>
 static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq, int64_t N, int64_t K, float *y,
                              cudaStream_t st) {
@@ -302,16 +315,24 @@ static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq
     using WS = GemvWarpSmem<DT>;
     const int nchunk = (int)(K / 256);
     const int64_t rblocks = (N + kGemvRows - 1) / kGemvRows;
-    // Smallest power-of-two cluster split (at most 8) with at most 32 chunks per block; then split
-    // further while there are fewer than two blocks per SM and each block keeps >= 5 chunks.
+    // Smallest power-of-two cluster split (at most 8) with at most 32 chunks per block.
     int S = 1;
     while (S < 8 && (nchunk + S - 1) / S > kGemvMaxWarps) S *= 2;
     if ((nchunk + S - 1) / S > kGemvMaxWarps)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemv: K=%lld too large (at most %d)", (long long)K,
                     8 * kGemvMaxWarps * 256);
-    while (S < 8 && rblocks * S < 2 * 152 && (nchunk + 2 * S - 1) / (2 * S) >= 5) S *= 2;
+    // Then split further only while the blocks do not cover the SMs once, or a block needs more shared
+    // memory than lets two of them share an SM (measured on the decode shapes: fewer, larger blocks
+    // shorten each call's dependent chain, as long as the next call's blocks can still start beside
+    // them), keeping >= 5 chunks per block.
+    auto smem_for = [&](int s) {
+        const int c = (nchunk + s - 1) / s;
+        return (size_t)c * WS::BYTES + (size_t)s * kGemvRows * c * Tr::terms * 4;
+    };
+    while (S < 8 && (rblocks * S < gemv_sm_count() || smem_for(S) > 112 * 1024) && (nchunk + 2 * S - 1) / (2 * S) >= 5)
+        S *= 2;
     const int cpr = (nchunk + S - 1) / S;
-    const size_t smem = (size_t)cpr * WS::BYTES + (size_t)S * kGemvRows * cpr * Tr::terms * 4;
+    const size_t smem = smem_for(S);
     if (smem > 220 * 1024) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: K=%lld too large", (long long)K);
     if (rblocks > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: N=%lld too large", (long long)N);
     auto kern = gemv_kernel<DT, FUSED>;
