@@ -15,6 +15,11 @@
 namespace kq {
 
 constexpr int kTileM = 64;
+constexpr int kRouteChunk = 1024;   // chunked routing: pairs per block, 8 warps x 4 rows of 32
+constexpr int kRouteThreads = 256;
+constexpr int kRouteMaxE = 2048;    // chunked routing's shared counters: 8 warps x n_experts ints
+
+static bool chunked_routing(int64_t E) { return E <= kRouteMaxE; }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -38,6 +43,22 @@ static GroupedTcWs grouped_tc_ws(size_t base, int64_t pairs, int64_t E, int64_t 
     w.off_tile_count = o; o += align256(sizeof(int));
     w.off_tiles = o; o += align256(sizeof(int) * 2 * w.max_tiles);
     w.off_panels = o; o += tc_grouped_panels(pairs, E, K).bytes;
+    w.total = o;
+    return w;
+}
+
+// Chunked-routing region the workspace path appends after the routing base (n_experts <= kRouteMaxE).
+struct RouteHistWs {
+    size_t off_hist, off_bad, total;
+    int nchunks;
+};
+
+static RouteHistWs route_hist_ws(size_t base, int64_t pairs, int64_t E) {
+    RouteHistWs w{};
+    w.nchunks = chunked_routing(E) ? (int)((pairs + kRouteChunk - 1) / kRouteChunk) : 0;
+    size_t o = base;
+    w.off_hist = o; o += align256(sizeof(int) * (size_t)w.nchunks * E);
+    w.off_bad = o; o += align256(sizeof(int) * (size_t)w.nchunks);
     w.total = o;
     return w;
 }
@@ -113,16 +134,29 @@ __device__ __forceinline__ int block_scan_incl(int v, int *warp_tot) {
 // One block of 1024 threads: exclusive scan of the expert counts (offset), the dp4a tile table of
 // 64-row tiles (expert, first row) and, when poff != NULL, the tensor-core table: expert rows padded
 // to a multiple of 4 (poff) and one (expert, 128-row tile index) entry per tile.
-__global__ void __launch_bounds__(1024) route_scan_kernel(const int *__restrict__ count, int E, int *__restrict__ offset,
+// With hist != NULL (chunked routing) the counts are first summed from the per-chunk histograms and
+// written to count, the histograms are turned into per-chunk list bases (offset[e] + pairs of expert e
+// in earlier chunks), and the device flag gets the number of invalid ids.
+__global__ void __launch_bounds__(1024) route_scan_kernel(int *__restrict__ count, int E, int *__restrict__ offset,
                                                           int *__restrict__ tiles, int *__restrict__ tile_count,
                                                           int *__restrict__ poff, int *__restrict__ tc_tiles,
-                                                          int *__restrict__ tc_tile_count) {
+                                                          int *__restrict__ tc_tile_count, int *__restrict__ hist,
+                                                          int nchunks, const int *__restrict__ bad,
+                                                          long long *__restrict__ flag) {
     __shared__ int wt[32];
     __shared__ int tot[4];
     int carry_off = 0, carry_t = 0, carry_p = 0, carry_tc = 0;
     for (int e0 = 0; e0 < E; e0 += 1024) {
         const int e = e0 + threadIdx.x;
-        const int c = e < E ? count[e] : 0;
+        int c = 0;
+        if (e < E) {
+            if (hist) {
+                for (int k = 0; k < nchunks; ++k) c += hist[(int64_t)k * E + e];
+                count[e] = c;
+            } else {
+                c = count[e];
+            }
+        }
         const int nt = (c + kTileM - 1) / kTileM, ntc = (c + kTcTileRows - 1) / kTcTileRows, cp = (c + 3) & ~3;
         const int i_off = block_scan_incl(c, wt);
         const int i_t = block_scan_incl(nt, wt);
@@ -130,6 +164,14 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int *__restrict_
         const int i_tc = block_scan_incl(ntc, wt);
         if (e < E) {
             offset[e] = carry_off + i_off - c;
+            if (hist) {
+                int run = carry_off + i_off - c;
+                for (int k = 0; k < nchunks; ++k) {
+                    const int h = hist[(int64_t)k * E + e];
+                    hist[(int64_t)k * E + e] = run;
+                    run += h;
+                }
+            }
             const int t0 = carry_t + i_t - nt;
             for (int j = 0; j < nt; ++j) { tiles[2 * (t0 + j)] = e; tiles[2 * (t0 + j) + 1] = j * kTileM; }
             if (poff) {
@@ -147,6 +189,11 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int *__restrict_
     if (threadIdx.x == 0) {
         *tile_count = carry_t;
         if (poff) *tc_tile_count = carry_tc;
+        if (hist) {
+            long long nb = 0;
+            for (int k = 0; k < nchunks; ++k) nb += bad[k];
+            *flag = nb;
+        }
     }
 }
 
@@ -192,6 +239,83 @@ __global__ void route_fill_kernel(const int32_t *__restrict__ ids, int64_t pairs
             }
         }
         n += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
+// ---- chunked routing (workspace path, n_experts <= kRouteMaxE): a stable counting sort of the pairs by
+// expert.  Pairs are cut into chunks of kRouteChunk; route_hist_kernel counts each chunk's pairs per
+// expert, route_scan_kernel sums the chunk counts and turns them into per-chunk list bases, and
+// route_fill_chunk_kernel writes every pair at base + its rank among the chunk's pairs of the same
+// expert (ascending pair order), so the lists equal those of route_fill_kernel.
+// hist[chunk][e] = pairs of the chunk routed to expert e; bad[chunk] = ids outside [0, E).
+__global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(const int32_t *__restrict__ ids, int64_t pairs,
+                                                                   int E, int *__restrict__ hist, int *__restrict__ bad) {
+    extern __shared__ int cnt[];  // E
+    __shared__ int nbad;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    if (threadIdx.x == 0) nbad = 0;
+    __syncthreads();
+    const int64_t p0 = (int64_t)blockIdx.x * kRouteChunk;
+    int b = 0;
+    for (int i = threadIdx.x; i < kRouteChunk; i += blockDim.x) {
+        const int64_t p = p0 + i;
+        if (p < pairs) {
+            const int id = ids[p];
+            if (id >= 0 && id < E) atomicAdd(&cnt[id], 1);
+            else ++b;
+        }
+    }
+    if (b) atomicAdd(&nbad, b);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = cnt[e];
+    if (threadIdx.x == 0) bad[blockIdx.x] = nbad;
+}
+
+// One block per chunk.  Warp w takes the chunk's pairs w*128 .. w*128+127 in four rows of 32 (row k:
+// pairs w*128 + 32k + lane).  Within a row, lanes holding the same expert find each other with
+// __match_any_sync and rank by lane; a per-warp counter per expert carries the rank across rows; an
+// exclusive prefix over the warps carries it across warps.  base (= hist after the scan) carries it
+// across chunks.  With prow != NULL also the tensor-core panel row of every list entry.
+__global__ void __launch_bounds__(kRouteThreads) route_fill_chunk_kernel(
+    const int32_t *__restrict__ ids, int64_t pairs, int E, const int *__restrict__ base,
+    const int *__restrict__ offset, int *__restrict__ lists, const int *__restrict__ poff, int *__restrict__ prow) {
+    extern __shared__ int wcnt[];  // [8][E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const int64_t p0 = (int64_t)blockIdx.x * kRouteChunk + warp * 128;
+    const unsigned below = (1u << lane) - 1u;
+    int ev[4], rk[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t p = p0 + k * 32 + lane;
+        int e = p < pairs ? ids[p] : -1;
+        if (e < 0 || e >= E) e = -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        const int before = e >= 0 ? wcnt[warp * E + e] : 0;
+        rk[k] = before + __popc(m & below);
+        ev[k] = e;
+        __syncwarp();
+        if (e >= 0 && (m & below) == 0) wcnt[warp * E + e] = before + __popc(m);  // the group's lowest lane
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int e = ev[k];
+        if (e < 0) continue;
+        const int pos = base[(int64_t)blockIdx.x * E + e] + wcnt[warp * E + e] + rk[k];
+        lists[pos] = (int)(p0 + k * 32 + lane);
+        if (prow) prow[pos] = poff[e] + (pos - offset[e]);
     }
 }
 
@@ -249,7 +373,7 @@ size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K, int
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     if (n_experts > 0) {
         const int64_t tk = top_k > 0 ? top_k : 1;
-        const size_t base = grouped_ws(M, tk, n_experts).total;
+        const size_t base = route_hist_ws(grouped_ws(M, tk, n_experts).total, M * tk, n_experts).total;
         return tc_grouped_eligible(wt, N, K) ? grouped_tc_ws(base, M * tk, n_experts, K).total : base;
     }
     return tc_workspace_bytes(wt, M, N, K);
@@ -322,16 +446,35 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
     int *tiles = reinterpret_cast<int *>(ws + L.off_tiles);
     int *lists = reinterpret_cast<int *>(ws + L.off_lists);
     const int64_t pairs = M * top_k;
-    route_count_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, (int)n_experts, count, flag);
+    const RouteHistWs H = route_hist_ws(L.total, pairs, n_experts);
     const bool tc = tc_grouped_eligible(wt, N, K);
-    const GroupedTcWs T = grouped_tc_ws(L.total, pairs, n_experts, K);
+    const GroupedTcWs T = grouped_tc_ws(H.total, pairs, n_experts, K);
     int *poff = tc ? reinterpret_cast<int *>(ws + T.off_poff) : nullptr;
     int *prow = tc ? reinterpret_cast<int *>(ws + T.off_prow) : nullptr;
     int *tc_tiles = tc ? reinterpret_cast<int *>(ws + T.off_tiles) : nullptr;
     int *tc_count = tc ? reinterpret_cast<int *>(ws + T.off_tile_count) : nullptr;
-    route_scan_kernel<<<1, 1024, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count, poff, tc_tiles, tc_count);
-    route_fill_kernel<<<(unsigned)((n_experts + 7) / 8), 256, 0, st>>>(ids, pairs, (int)n_experts, offset, lists, poff,
-                                                                      prow);
+    if (H.nchunks > 0) {
+        int *hist = reinterpret_cast<int *>(ws + H.off_hist);
+        int *bad = reinterpret_cast<int *>(ws + H.off_bad);
+        const size_t fill_smem = sizeof(int) * 8 * (size_t)n_experts;
+        if (fill_smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(route_fill_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)fill_smem);
+            if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm_grouped: %s", cudaGetErrorString(e));
+        }
+        route_hist_kernel<<<(unsigned)H.nchunks, kRouteThreads, sizeof(int) * n_experts, st>>>(ids, pairs, (int)n_experts,
+                                                                                              hist, bad);
+        route_scan_kernel<<<1, 1024, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count, poff, tc_tiles, tc_count,
+                                              hist, H.nchunks, bad, flag);
+        route_fill_chunk_kernel<<<(unsigned)H.nchunks, kRouteThreads, fill_smem, st>>>(ids, pairs, (int)n_experts, hist,
+                                                                                       offset, lists, poff, prow);
+    } else {
+        route_count_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, (int)n_experts, count, flag);
+        route_scan_kernel<<<1, 1024, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count, poff, tc_tiles, tc_count,
+                                              nullptr, 0, nullptr, nullptr);
+        route_fill_kernel<<<(unsigned)((n_experts + 7) / 8), 256, 0, st>>>(ids, pairs, (int)n_experts, offset, lists,
+                                                                          poff, prow);
+    }
     s = check_launch("kq_gemm_grouped routing");
     if (s != KQ_OK) return s;
     count_launch(R_ROUTE, 3);
@@ -461,7 +604,8 @@ extern "C" kq_status kq_gemm_grouped_noalloc(kq_dtype wt, const void *w, int64_t
     // Every scratch field is fully rewritten below before it is read, so nothing left by an earlier
     // call needs clearing.
     route_count_kernel<<<(unsigned)n_experts, 256, 0, st>>>(ids, pairs, (int)n_experts, count, flag);
-    route_scan_kernel<<<1, 1024, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count, nullptr, nullptr, nullptr);
+    route_scan_kernel<<<1, 1024, 0, st>>>(count, (int)n_experts, offset, tiles, tile_count, nullptr, nullptr, nullptr,
+                                          nullptr, 0, nullptr, nullptr);
     route_fill_kernel<<<(unsigned)((n_experts + 7) / 8), 256, 0, st>>>(ids, pairs, (int)n_experts, offset, lists,
                                                                       nullptr, nullptr);
     s = check_launch("kq_gemm_grouped_noalloc routing");

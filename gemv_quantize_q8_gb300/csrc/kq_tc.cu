@@ -822,16 +822,20 @@ __global__ void act_panel_q81_kernel(const uint8_t *__restrict__ xq, int M, int 
 
 // Routed-expert prologue: list entry s (pair lists[s], routed order) goes to panel row prow[s] of the
 // f16 code panel, the f16 bsum panel and the f32 scale panel; its activation is Q8_K row pair / top_k
-// (one row per token) or row pair (one row per pair).  One warp per (list entry, super-block).  The
-// padding rows between experts are left unwritten: they only feed token columns that are discarded.
+// (one row per token) or row pair (one row per pair).  One warp per (list entry, super-block); only
+// the lists' valid entries (offset[E-1] + count[E-1]: pairs with an invalid expert id are in no list)
+// are read.  The padding rows between experts are left unwritten: they only feed token columns that
+// are discarded.
 __global__ void act_panel_grouped_kernel(const uint8_t *__restrict__ xq, int rows_per_token, int top_k, int nsb,
                                          int64_t pairs, const int *__restrict__ lists, const int *__restrict__ prow,
+                                         const int *__restrict__ count, const int *__restrict__ offset, int n_experts,
                                          __half *__restrict__ A, __half *__restrict__ E, float *__restrict__ D,
                                          int64_t dstride) {
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (wid >= pairs * nsb) return;
     const int64_t sidx = wid / nsb;
+    if (sidx >= (int64_t)offset[n_experts - 1] + count[n_experts - 1]) return;
     const int sb = (int)(wid % nsb);
     const int p = lists[sidx];
     const int64_t r = prow[sidx];
@@ -1086,7 +1090,8 @@ kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int 
     const int64_t nsb = K / 256;
     const int64_t warps = pairs * nsb;
     act_panel_grouped_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
-        xq, rows_per_token, top_k, (int)nsb, pairs, lists, prow, reinterpret_cast<__half *>(panels + G.off_a),
+        xq, rows_per_token, top_k, (int)nsb, pairs, lists, prow, count, offset, (int)E,
+        reinterpret_cast<__half *>(panels + G.off_a),
         reinterpret_cast<__half *>(panels + G.off_e), reinterpret_cast<float *>(panels + G.off_d), G.dstride);
     kq_status s = check_launch("kq_gemm_grouped (activation panel)");
     if (s != KQ_OK) return s;

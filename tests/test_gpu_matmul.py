@@ -343,6 +343,33 @@ def test_grouped_invalid_ids_flag_and_untouched_rows():
     assert _close(kq.Q4_K, yh[ok], ref[ok])
 
 
+@pytest.mark.parametrize("dtype", [kq.Q8_0, kq.Q4_K])
+def test_grouped_routing_spans_chunks(dtype):
+    """2760 (token, slot) pairs: the stable per-expert compaction runs in chunks of 1024 pairs, so
+    experts' rows continue across chunk boundaries; invalid ids sit on and next to the boundaries.
+    Rows are compared with the oracle (Q8_0 exactly), and the flag counts every invalid id."""
+    g = synth.rng(415 + dtype)
+    E, M, top_k, N, K = 37, 690, 4, 128, 512
+    w = synth.weights(dtype, E * N, K, g)
+    ids, _ = synth.routing(M, E, top_k, g)
+    flat = ids.reshape(-1)
+    bad_at = [0, 1023, 1024, 2047, 2048, 2759]
+    for i, p in enumerate(bad_at):
+        flat[p] = E + i if i % 2 == 0 else -1 - i
+    x = synth.activations(M, K, g)
+    wn = repack(dtype, w, E * N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    y, ws = _grouped(dtype, wn, E, xq, 1, ids, M, top_k, N, K)
+    assert kq.kq_read_device_flag(ws) == len(bad_at)
+    ref, bad = oracle.gemm_grouped(dtype, w, E, _oracle_act(dtype, x), 1, ids, M, top_k, N, K)
+    assert bad == len(bad_at)
+    yh = host(y).reshape(M * top_k, N)
+    ok = np.isfinite(ref.reshape(M * top_k, N)).all(axis=1)
+    assert ok.sum() == M * top_k - len(bad_at)
+    assert np.isnan(yh[~ok]).all()
+    assert _close(dtype, yh[ok], ref.reshape(M * top_k, N)[ok])
+
+
 def test_grouped_top1_single_expert_equals_dense():
     g = synth.rng(411)
     E, M, N, K = 3, 70, 64, 512
