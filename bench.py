@@ -358,7 +358,6 @@ def _aux_moe(device):
     xq = torch.empty(kq.q8k_bytes(M, H), dtype=torch.uint8, device=device)
     y_gu = torch.empty((M, top_k, 2 * F), device=device)
     hq = torch.empty(kq.q8k_bytes(M * top_k, F), dtype=torch.uint8, device=device)
-    h = torch.empty((M * top_k, F), device=device)
     y_dn = torch.empty((M, top_k, H), device=device)
     o = torch.empty((M, H), device=device)
     wsb = max(kq.gemm_workspace_bytes(synth.Q4_K, M, 2 * F, H, E, top_k),
@@ -369,7 +368,7 @@ def _aux_moe(device):
         kq.kq_quantize_q8k(x, M, H, H, xq)
         kq.kq_gemm_grouped(synth.Q4_K, w_gu, E, xq, 1, ids, M, top_k, 2 * F, H, y_gu, ws, wsb)
         flat = y_gu.view(M * top_k, 2 * F)
-        kq.kq_swiglu_quantize_q8k(flat, flat[:, F:], M * top_k, F, 2 * F, hq, h)
+        kq.kq_swiglu_quantize_q8k(flat, flat[:, F:], M * top_k, F, 2 * F, hq)  # only the Q8_K codes go on
         kq.kq_gemm_grouped(synth.Q6_K, w_dn, E, hq, top_k, ids, M, top_k, H, F, y_dn, ws, wsb)
         kq.kq_moe_weighted_sum(y_dn, wts, M, top_k, H, o)
 

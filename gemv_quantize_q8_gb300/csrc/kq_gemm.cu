@@ -34,7 +34,7 @@ struct GroupedTcWs {
     int64_t max_tiles;
 };
 
-static GroupedTcWs grouped_tc_ws(size_t base, int64_t pairs, int64_t E, int64_t K) {
+static GroupedTcWs grouped_tc_ws(kq_dtype wt, size_t base, int64_t pairs, int64_t E, int64_t K) {
     GroupedTcWs w{};
     w.max_tiles = (pairs + kTcTileRows - 1) / kTcTileRows + E;
     size_t o = base;
@@ -42,7 +42,7 @@ static GroupedTcWs grouped_tc_ws(size_t base, int64_t pairs, int64_t E, int64_t 
     w.off_prow = o; o += align256(sizeof(int) * pairs);
     w.off_tile_count = o; o += align256(sizeof(int));
     w.off_tiles = o; o += align256(sizeof(int) * 2 * w.max_tiles);
-    w.off_panels = o; o += tc_grouped_panels(pairs, E, K).bytes;
+    w.off_panels = o; o += tc_grouped_panels(wt, pairs, E, K).bytes;
     w.total = o;
     return w;
 }
@@ -374,7 +374,7 @@ size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K, int
     if (n_experts > 0) {
         const int64_t tk = top_k > 0 ? top_k : 1;
         const size_t base = route_hist_ws(grouped_ws(M, tk, n_experts).total, M * tk, n_experts).total;
-        return tc_grouped_eligible(wt, N, K) ? grouped_tc_ws(base, M * tk, n_experts, K).total : base;
+        return tc_grouped_eligible(wt, N, K) ? grouped_tc_ws(wt, base, M * tk, n_experts, K).total : base;
     }
     return tc_workspace_bytes(wt, M, N, K);
 }
@@ -448,7 +448,7 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
     const int64_t pairs = M * top_k;
     const RouteHistWs H = route_hist_ws(L.total, pairs, n_experts);
     const bool tc = tc_grouped_eligible(wt, N, K);
-    const GroupedTcWs T = grouped_tc_ws(H.total, pairs, n_experts, K);
+    const GroupedTcWs T = grouped_tc_ws(wt, H.total, pairs, n_experts, K);
     int *poff = tc ? reinterpret_cast<int *>(ws + T.off_poff) : nullptr;
     int *prow = tc ? reinterpret_cast<int *>(ws + T.off_prow) : nullptr;
     int *tc_tiles = tc ? reinterpret_cast<int *>(ws + T.off_tiles) : nullptr;

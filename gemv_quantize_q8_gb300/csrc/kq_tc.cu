@@ -64,6 +64,8 @@ struct TcCfg<KQ_Q4_K> {
     static constexpr int NACC = 2;        // accumulator buffers
     static constexpr int BPS = 1;         // accumulator read-outs per step (scale blocks per 256 K)
     static constexpr int H_ROW = 8;       // bytes of row scales per step: f32 (d, -dmin)
+    static constexpr int NP = 2;          // packed-weight ring slots (super-blocks in flight)
+    static constexpr int NE = 2;          // extension-operand ring slots (mins, bsums)
     static constexpr uint32_t TM_S2 = 256, TM_A = 384;
 };
 template <>
@@ -72,6 +74,7 @@ struct TcCfg<KQ_Q6_K> {
     static constexpr bool EXT = false, Q8 = false;
     static constexpr int A_COLS = 64;     // lo tile (32 columns) then 16*hi tile (32 columns)
     static constexpr int NACC = 2, BPS = 1, H_ROW = 8;  // f32 (d, 0)
+    static constexpr int NP = 2, NE = 2;
     static constexpr uint32_t TM_S2 = 0, TM_A = 256;
 };
 template <>
@@ -82,6 +85,7 @@ struct TcCfg<KQ_Q8_0> {
     // every 32-element block has its own weight and activation scale, so every block's integer
     // dot P_b is read out of its own accumulator: three buffers rotate along the blocks
     static constexpr int NACC = 3, BPS = 8, H_ROW = 16;  // the row's 8 f16 block scales
+    static constexpr int NP = 2, NE = 2;
     static constexpr uint32_t TM_S2 = 0, TM_A = 384;
 };
 // TMEM map: accumulator buffers at columns 0, 128 (and 256 for Q8_0); Q4_K min-term tile at 256;
@@ -96,12 +100,12 @@ struct TcLayout {
     using C = TcCfg<DT>;
     static constexpr int ACT_OFF = 0;
     static constexpr int P_OFF = ACT_OFF + NACT * ACT_TILE;
-    static constexpr int EA_OFF = (P_OFF + 2 * 8 * C::CB + 1023) & ~1023;
-    static constexpr int EB_OFF = EA_OFF + (C::EXT ? 2 * 4096 : 0);
-    static constexpr int H_OFF = EB_OFF + (C::EXT ? 2 * 4096 : 0);
+    static constexpr int EA_OFF = (P_OFF + C::NP * 8 * C::CB + 1023) & ~1023;
+    static constexpr int EB_OFF = EA_OFF + (C::EXT ? C::NE * 4096 : 0);
+    static constexpr int H_OFF = EB_OFF + (C::EXT ? C::NE * 4096 : 0);
     static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * C::H_ROW;
     static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4 * C::BPS;
-    static constexpr int NBAR = 2 * NPAIR + 2 * 2 + 2 * 2 + 3 * 4 + 2 * 3 + 2;
+    static constexpr int NBAR = 2 * NPAIR + 2 * 3 + 2 * 3 + 3 * 4 + 2 * 3 + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = MISC_OFF + 16;
     static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment of the base
@@ -235,9 +239,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // converted kblocks (TMEM, from both converter groups) complete the same phase, and a single MMA
     // commit frees both, so the MMA thread waits once per 128 K-elements.
     uint64_t *k_full = bars, *k_empty = k_full + NPAIR;
-    uint64_t *p_full = k_empty + NPAIR, *p_empty = p_full + 2;
-    uint64_t *e_full = p_empty + 2, *e_empty = e_full + 2;  // Q4_K: bsums (TMA) + mins (converters)
-    uint64_t *h_full = e_empty + 2, *da_full = h_full + 4, *h_empty = da_full + 4;
+    uint64_t *p_full = k_empty + NPAIR, *p_empty = p_full + 3;   // up to 3 packed-weight slots
+    uint64_t *e_full = p_empty + 3, *e_empty = e_full + 3;       // Q4_K: bsums (TMA) + mins (converters)
+    uint64_t *h_full = e_empty + 3, *da_full = h_full + 4, *h_empty = da_full + 4;
     uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 3;
     uint64_t *mma_done = acc_empty + 3;  // one per MMA issuer
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
@@ -260,10 +264,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (tid == 0) {
         for (int i = 0; i < NPAIR; ++i) { mbar_init(&k_full[i], 32 * TC_CONV_WARPS + 1); mbar_init(&k_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 32 * TC_CONV_WARPS);
-            mbar_init(&e_full[i], 32 * TC_CONV_WARPS / 2 + 1); mbar_init(&e_empty[i], 1);
-        }
+        for (int i = 0; i < C::NP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 32 * TC_CONV_WARPS); }
+        for (int i = 0; i < C::NE; ++i) { mbar_init(&e_full[i], 32 * TC_CONV_WARPS / 2 + 1); mbar_init(&e_empty[i], 1); }
         for (int i = 0; i < C::NACC; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS); }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&h_full[i], 32 * TC_CONV_WARPS / 2); mbar_init(&da_full[i], 1);
@@ -286,8 +288,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == TC_WARP_PROD) {
         // ------------------------------------------------------------ weight-side producer
         if (lane == 0) {
-            int last_p[2], last_e[2], last_d[4];
-            for (int i = 0; i < 2; ++i) { last_p[i] = -1; last_e[i] = -1; }
+            int last_p[3], last_e[3], last_d[4];
+            for (int i = 0; i < 3; ++i) { last_p[i] = -1; last_e[i] = -1; }
             for (int i = 0; i < 4; ++i) last_d[i] = -1;
             bool ok = true;
             TcTile T{};
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (tt == 0) T = tile_of(ti);
                 const int gsb = sb0 + tt;
                 if (++tt == nsb) { tt = 0; ++ti; }
-                const int p = st & 1, pph = (st >> 1) & 1;
+                const int p = st % C::NP, pph = (st / C::NP) & 1;
                 if (!(ok = mbar_wait_sleep(&p_empty[p], pph ^ 1, abort_flag))) break;
                 mbar_arrive_expect_tx(&p_full[p], T.valid_groups * C::CB);
                 for (int gi = 0; gi < T.valid_groups; ++gi)
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                               &p_full[p]);
                 last_p[p] = pph;
                 if (C::EXT) {
-                    const int e = st & 1, eph = (st >> 1) & 1;
+                    const int e = st % C::NE, eph = (st / C::NE) & 1;
                     if (!(ok = mbar_wait_sleep(&e_empty[e], eph ^ 1, abort_flag))) break;
                     mbar_arrive_expect_tx(&e_full[e], 4096);
                     tma_load_2d(sEB + e * 4096, &tmE, &e_full[e], gsb * 16, T.m0);
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // that also counts converter arrivals may never complete after an abort; the 100 ms bound
                 // still leaves the copy far more time than it needs to land.
                 volatile int no_abort = 0;
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < 3; ++i) {
                     if (last_p[i] >= 0) { no_abort = 0; mbar_wait(&p_full[i], last_p[i], &no_abort, 100000000ull); }
                     if (last_e[i] >= 0) { no_abort = 0; mbar_wait(&e_full[i], last_e[i], &no_abort, 100000000ull); }
                 }
@@ -425,8 +427,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 if (!ok) break;
                 if (C::EXT) {
-                    const int e = t & 1;
-                    if (!(ok = mbar_wait_sleep(&e_full[e], (t >> 1) & 1, abort_flag))) break;
+                    const int e = t % C::NE;
+                    if (!(ok = mbar_wait_sleep(&e_full[e], (t / C::NE) & 1, abort_flag))) break;
                     if (t > 0 && !(ok = mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) break;
                     tc_fence_after();
                     mma_f16(tbase + C::TM_S2, dEA + (uint64_t)(e * (4096 >> 4)), dEB + (uint64_t)(e * (4096 >> 4)),
@@ -453,8 +455,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int t = 0, ti = 0, tt = 0; t < nsteps && ok; ++t) {  // t: step
             if (tt == 0) rvalid = row < tile_of(ti).valid_groups * 16;
             if (++tt == nsb) { tt = 0; ++ti; }
-            const int p = t & 1;
-            if (!(ok = mbar_wait_sleep(&p_full[p], (t >> 1) & 1, abort_flag))) break;
+            const int p = t % C::NP;
+            if (!(ok = mbar_wait_sleep(&p_full[p], (t / C::NP) & 1, abort_flag))) break;
             // rows past N were not loaded: their scales are forced to 0, so they convert to zeros
             const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
             const int r16 = row & 15;
@@ -583,8 +585,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive(&h_full[h]);
             } else if (C::EXT) {
                 // extension A row: the 8 sub-block mins, each repeated for its two bsum groups
-                const int e = t & 1;
-                if (!(ok = mbar_wait_sleep(&e_empty[e], ((t >> 1) & 1) ^ 1, abort_flag))) break;
+                const int e = t % C::NE;
+                if (!(ok = mbar_wait_sleep(&e_empty[e], ((t / C::NE) & 1) ^ 1, abort_flag))) break;
                 uint8_t s12[12];
                 const uint32_t hw[3] = {hv.y, hv.z, hv.w};
 #pragma unroll
@@ -855,6 +857,38 @@ __global__ void act_panel_grouped_kernel(const uint8_t *__restrict__ xq, int row
     if (lane == 0) D[(int64_t)sb * dstride + r] = *reinterpret_cast<const float *>(blk);
 }
 
+// Routed-expert prologue for Q8_0 weights: as act_panel_grouped_kernel, from Q8_1 rows -- f16 codes
+// and the f32 (widened f16) scale of every 32-element block.  One warp per (list entry, 256 elements):
+// lane l takes elements 8l .. 8l+7 of block l/4.
+__global__ void act_panel_q81_grouped_kernel(const uint8_t *__restrict__ xq, int rows_per_token, int top_k, int nsb,
+                                             int64_t pairs, const int *__restrict__ lists,
+                                             const int *__restrict__ prow, const int *__restrict__ count,
+                                             const int *__restrict__ offset, int n_experts, __half *__restrict__ A,
+                                             float *__restrict__ D, int64_t dstride) {
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (wid >= pairs * nsb) return;
+    const int64_t sidx = wid / nsb;
+    if (sidx >= (int64_t)offset[n_experts - 1] + count[n_experts - 1]) return;
+    const int sb = (int)(wid % nsb);
+    const int p = lists[sidx];
+    const int64_t r = prow[sidx];
+    const int64_t src = rows_per_token == 1 ? p / top_k : p;
+    const int64_t K = (int64_t)nsb * 256;
+    const int blk = sb * 8 + (lane >> 2);
+    const uint8_t *b = xq + (src * nsb * 8 + blk) * kQ81Bytes;
+    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(b + 4 + (lane & 3) * 8);
+    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(b + 8 + (lane & 3) * 8);
+    __half hv[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        hv[i] = __int2half_rn((int)(int8_t)((w0 >> (8 * i)) & 0xff));
+        hv[4 + i] = __int2half_rn((int)(int8_t)((w1 >> (8 * i)) & 0xff));
+    }
+    *reinterpret_cast<uint4 *>(A + r * K + sb * 256 + lane * 8) = *reinterpret_cast<uint4 *>(hv);
+    if ((lane & 3) == 0) D[(int64_t)blk * dstride + r] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(b));
+}
+
 // ------------------------------------------------------------------ host side
 struct TcWs {
     size_t off_flag, off_a, off_e, off_d, total;
@@ -1063,18 +1097,22 @@ kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, i
 
 // ---- routed experts on the tensor cores
 bool tc_grouped_eligible(kq_dtype wt, int64_t N, int64_t K) {
-    return (wt == KQ_Q4_K || wt == KQ_Q6_K) && N % 16 == 0 && K % 256 == 0 && K <= (1 << 20) && N <= (1 << 22);
+    return (wt == KQ_Q4_K || wt == KQ_Q6_K || wt == KQ_Q8_0) && N % 16 == 0 && K % 256 == 0 && K <= (1 << 20) &&
+           N <= (1 << 22);
 }
 
-TcGroupedPanels tc_grouped_panels(int64_t pairs, int64_t E, int64_t K) {
+// Panels of the routed rows: f16 codes, (Q4_K/Q6_K) f16 bsums, f32 scales with one row per scale block
+// (256 elements for Q8_K activations, 32 for Q8_1).
+TcGroupedPanels tc_grouped_panels(kq_dtype wt, int64_t pairs, int64_t E, int64_t K) {
     TcGroupedPanels g{};
     const int64_t nsb = K / 256;
+    const bool q8 = wt == KQ_Q8_0;
     g.rows = pairs + 3 * E;                      // every expert's rows padded to a multiple of 4
     g.dstride = ((g.rows + TC_TOK) + 3) & ~(int64_t)3;
     size_t o = 0;
     g.off_a = o; o += al256((size_t)g.rows * K * 2);
-    g.off_e = o; o += al256((size_t)g.rows * nsb * 32);
-    g.off_d = o; o += al256((size_t)nsb * g.dstride * 4);
+    g.off_e = o; o += q8 ? 0 : al256((size_t)g.rows * nsb * 32);
+    g.off_d = o; o += al256((size_t)nsb * (q8 ? 8 : 1) * g.dstride * 4);
     g.bytes = o;
     return g;
 }
@@ -1084,15 +1122,20 @@ kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int 
                           const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,
                           const int *offset, const int *poff, const int *lists, const int *prow,
                           unsigned long long *err, cudaStream_t st) {
-    const TcGroupedPanels G = tc_grouped_panels(pairs, E, K);
+    const TcGroupedPanels G = tc_grouped_panels(wt, pairs, E, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || max_tiles > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: shape too large for the tensor-core grid");
     const int64_t nsb = K / 256;
     const int64_t warps = pairs * nsb;
-    act_panel_grouped_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
-        xq, rows_per_token, top_k, (int)nsb, pairs, lists, prow, count, offset, (int)E,
-        reinterpret_cast<__half *>(panels + G.off_a),
-        reinterpret_cast<__half *>(panels + G.off_e), reinterpret_cast<float *>(panels + G.off_d), G.dstride);
+    if (wt == KQ_Q8_0)
+        act_panel_q81_grouped_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+            xq, rows_per_token, top_k, (int)nsb, pairs, lists, prow, count, offset, (int)E,
+            reinterpret_cast<__half *>(panels + G.off_a), reinterpret_cast<float *>(panels + G.off_d), G.dstride);
+    else
+        act_panel_grouped_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+            xq, rows_per_token, top_k, (int)nsb, pairs, lists, prow, count, offset, (int)E,
+            reinterpret_cast<__half *>(panels + G.off_a),
+            reinterpret_cast<__half *>(panels + G.off_e), reinterpret_cast<float *>(panels + G.off_d), G.dstride);
     kq_status s = check_launch("kq_gemm_grouped (activation panel)");
     if (s != KQ_OK) return s;
     TcLaunch a{};

@@ -20,7 +20,7 @@ struct TcGroupedPanels {
     int64_t rows, dstride;
     size_t off_a, off_e, off_d, bytes;
 };
-TcGroupedPanels tc_grouped_panels(int64_t pairs, int64_t E, int64_t K);
+TcGroupedPanels tc_grouped_panels(kq_dtype wt, int64_t pairs, int64_t E, int64_t K);
 kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int rows_per_token, int top_k,
                           int64_t pairs, int64_t E, int64_t N, int64_t K, float *y, uint8_t *panels,
                           const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,

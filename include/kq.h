@@ -175,10 +175,11 @@ KQ_API kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, 
  * ids: int32 [M][top_k] expert of each (token, slot).  xq: activation rows; xq_rows_per_token = 1
  * ("broadcast": slot (t,k) reads row t) or top_k ("per-row": slot (t,k) reads row t*top_k+k).
  * y: fp32 [M][top_k][N]; y[t][k] = W_{ids[t][k]} . X_row.  Rows are gathered per expert in
- * (token, slot) order, so the result is deterministic.  Q4_K and Q6_K run on the tensor cores in
- * 128-row tiles of each expert's rows (integer parts exact; fp32 promotion with fused multiply-adds,
- * so outputs match the sequential CPU order to within rounding, not bit for bit); Q8_0 runs on the
- * exact dp4a path in the CPU order.  An id outside [0, n_experts) is skipped
+ * (token, slot) order, so the result is deterministic.  All three weight types run on the tensor
+ * cores in 128-row tiles of each expert's rows with exact integer parts; Q4_K and Q6_K promote to fp32
+ * with fused multiply-adds (outputs match the sequential CPU order to within rounding, not bit for
+ * bit), Q8_0 adds every 32-block's scaled dot in the CPU order (bit-exact).  An id outside
+ * [0, n_experts) is skipped
  * (its y row is not written) and recorded in the workspace's device flag: kq_read_device_flag
  * then returns KQ_ERR_DEVICE_FLAG.  workspace: kq_gemm_workspace_bytes(wt, M, N, K, n_experts,
  * top_k) bytes, 256-byte aligned. */

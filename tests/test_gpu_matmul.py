@@ -271,8 +271,8 @@ def test_q8_0_swiglu_full_size_sampled():
 
 
 def _close(dtype, got, ref):
-    # Q4_K / Q6_K routed experts run on the tensor cores: integer parts exact, fp32 promotion in a
-    # different (fused) order, so near-exact; Q8_0 runs on the exact dp4a path in the CPU order
+    # Q4_K / Q6_K routed experts: integer parts exact, fp32 promotion in a different (fused) order,
+    # so near-exact; Q8_0 (tensor cores or dp4a) adds its blocks in the CPU order, bit-exact
     if dtype == kq.Q8_0:
         return np.array_equal(got, ref)
     return np.isfinite(got).all() and nmse(got, ref) <= 1e-10
@@ -305,7 +305,7 @@ def test_grouped_small(dtype, rpt):
     assert _close(dtype, host(y), ref)
 
 
-@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K])
+@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K, kq.Q8_0])
 def test_grouped_tensor_core_multi_tile(dtype):
     # experts with more than one 128-row tile, several row tiles, a tail tile, an empty expert
     g = synth.rng(405 + dtype)
@@ -318,7 +318,7 @@ def test_grouped_tensor_core_multi_tile(dtype):
     xq = act_quant(dtype, dev(x), M * top_k, K)
     y, ws = _grouped(dtype, wn, E, xq, top_k, ids, M, top_k, N, K)
     assert kq.kq_read_device_flag(ws) == 0
-    ref, _ = oracle.gemm_grouped(dtype, w, E, oracle.quantize_q8_k(x), top_k, ids, M, top_k, N, K)
+    ref, _ = oracle.gemm_grouped(dtype, w, E, _oracle_act(dtype, x), top_k, ids, M, top_k, N, K)
     assert _close(dtype, host(y), ref)
 
 
