@@ -438,6 +438,47 @@ def run_decode(args, device, calls=None):
     return out, total_bytes / (total_ms * 1e-3) / 1e9
 
 
+def run_decode_batched(device, calls=200):
+    """Batched decode: kq_gemm with M = 2, 4, 8 quantised activation rows on the decode shapes, back to
+    back from a CUDA graph over rotating weight copies; us per call and algorithmic GB/s (weights +
+    Q8_K rows + fp32 outputs)."""
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    from gemv_quantize_q8_gb300 import synth
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    g = synth.rng(1)
+    out = {}
+    for cfg in synth.DECODE:
+        dtype, N, K = cfg["dtype"], cfg["N"], cfg["K"]
+        nb = kq.native_bytes(dtype, N, K)
+        copies = max(3, -(-3 * l2 // nb))
+        wc = torch.from_numpy(synth.weights(dtype, N, K, g).reshape(-1)).to(device)
+        ws = torch.empty((copies, nb), dtype=torch.uint8, device=device)
+        for c in range(copies):
+            kq.kq_repack_weights(dtype, wc, ws[c], N, K)
+        torch.cuda.synchronize()
+        res = {}
+        for M in (2, 4, 8):
+            x = torch.from_numpy(synth.activations(M, K, g)).to(device)
+            xq = torch.empty(kq.q8k_bytes(M, K), dtype=torch.uint8, device=device)
+            kq.kq_quantize_q8k(x, M, K, K, xq)
+            y = torch.empty((M, N), dtype=torch.float32, device=device)
+
+            def step():
+                for i in range(calls):
+                    kq.kq_gemm(dtype, ws[i % copies], xq, M, N, K, y, N)
+            ms = _time_graph(step, 5)
+            us = ms * 1e3 / calls
+            wbytes = N * (K // 256) * (144 if dtype == synth.Q4_K else 210)
+            algo = wbytes + M * (K // 256) * 292 + M * N * 4
+            res[f"M{M}"] = {"us_per_call": round(us, 2), "gbs": round(algo / (us * 1e-6) / 1e9, 1)}
+        out[cfg["name"]] = res
+        del ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def cpu_baseline(budget_s: float = 12.0):
     """The CPU oracle as it stands, all host threads, on a bounded sample of the prefill workload:
     the first `m` token rows of every (dtype, shape) GEMM (quantisation included)."""
@@ -526,7 +567,8 @@ def main():
     if args.decode_only:
         decode, decode_gbs = run_decode(args, device)
         if rank == 0:
-            print(json.dumps({"decode_gemv_gbs": round(decode_gbs, 1), "shapes": decode}), flush=True)
+            print(json.dumps({"decode_gemv_gbs": round(decode_gbs, 1), "shapes": decode,
+                              "decode_batched": run_decode_batched(device)}), flush=True)
         return
     if args.aux_only:
         if rank == 0:
@@ -542,6 +584,7 @@ def main():
     decode = None
     if not args.no_decode and not args.only:
         decode, decode_gbs = run_decode(args, device)
+        decode_batched = run_decode_batched(device)
     aux = run_aux(args, device) if rank == 0 and not args.only and not args.no_aux else None
     if rank == 0:
         pk, src = peaks()
@@ -572,6 +615,7 @@ def main():
             hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
             line["decode_gemv"] = {"gbs": round(decode_gbs, 1), "frac_of_hbm": round(decode_gbs / hbm, 4),
                                    "hbm_peak_gbs": hbm, "peak_source": src, "shapes": decode}
+            line["decode_batched"] = decode_batched
         if aux is not None:
             line.update(aux)
         if not args.no_cpu and not args.only:

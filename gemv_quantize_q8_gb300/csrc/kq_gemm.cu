@@ -394,6 +394,11 @@ kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t
     if (tc_eligible(wt, M, N, K))
         return tc_gemm(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
                        static_cast<uint8_t *>(workspace), st);
+    // batched decode: the weight-streaming GEMV kernel serves up to kGemvMaxBatch activation rows
+    if (M <= kGemvMaxBatch && aligned(w, 16) &&
+        gemv_batched(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy, st) ==
+            KQ_OK)
+        return KQ_OK;
     MmqExactArgs a{};
     a.w = static_cast<const uint8_t *>(w);
     a.xq = static_cast<const uint8_t *>(xq);

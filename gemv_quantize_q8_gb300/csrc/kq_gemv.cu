@@ -47,14 +47,16 @@ struct GemvTraits<KQ_Q8_0> { static constexpr int terms = 8; static constexpr bo
 
 __device__ __forceinline__ int sext8(uint32_t w, int i) { return (int)(int8_t)((w >> (8 * i)) & 0xff); }
 
-// Per-warp shared region: the chunk's codes for the block's two row groups, then its activation.
-template <int DT>
+// Per-warp shared region: the chunk's codes for the block's two row groups, then the chunk's
+// activation for each of the MC activation columns (320 bytes each: q[256], d, bsums).
+template <int DT, int MC>
 struct GemvWarpSmem {
     static constexpr int CB = chunk_bytes(DT);
-    static constexpr int Q_OFF = 2 * CB;          // int8 q[256]
+    static constexpr int Q_OFF = 2 * CB;          // column m at Q_OFF + m*XB: int8 q[256]
     static constexpr int D_OFF = Q_OFF + 256;     // f32 d: 1 (Q8_K) or 8 (Q8_1)
     static constexpr int B_OFF = D_OFF + 32;      // int16 bsums[16]
-    static constexpr int BYTES = B_OFF + 32;      // multiple of 16
+    static constexpr int XB = 320;                // one column's activation (multiple of 16)
+    static constexpr int BYTES = Q_OFF + MC * XB;
 };
 
 // One lane = one row: the exact fp32 term(s) of (row, chunk) from the integer sub-block dots.
@@ -166,15 +168,19 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
 // rank k owns chunk k*cpr + w for all 32 rows of the block (lane = row): it bulk-copies that chunk's
 // codes for the block's two row groups into its own shared region, quantises (or copies) the
 // chunk's activation there, and forms the 32 rows' terms.  No warp waits for another until the
-// final ordered reduction.
-template <int DT, bool FUSED>
+// final ordered reduction.  MC > 1 (batched decode, M <= MC activation rows given quantised): the
+// staged weight chunk serves every activation column; each (row, column) output is formed exactly as
+// for one column.  y[m*ldy + n].
+template <int DT, bool FUSED, int MC>
 __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const uint8_t *__restrict__ w,
                                                                          const float *__restrict__ x,
                                                                          const uint8_t *__restrict__ xq,
                                                                          int64_t N, int nchunk, int cpr,
-                                                                         float *__restrict__ y) {
+                                                                         float *__restrict__ y, int M,
+                                                                         int64_t ldy) {
+    static_assert(!FUSED || MC == 1, "the fused quantise prologue takes one activation column");
     using Tr = GemvTraits<DT>;
-    using WS = GemvWarpSmem<DT>;
+    using WS = GemvWarpSmem<DT, MC>;
     constexpr int CB = chunk_bytes(DT);
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t bars[kGemvMaxWarps];
@@ -189,8 +195,8 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     const int c_begin = rank * cpr;
     const int nloc = max(0, min(nchunk, c_begin + cpr) - c_begin);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tstride = cpr * Tr::terms;
-    // shared layout: per-warp buffers [cpr][WS] | terms [32][cpr*terms] | (S > 1) gather [S-1][32][cpr*terms]
+    const int tstride = MC * cpr * Tr::terms;  // a row's terms: [column][local chunk][term]
+    // shared layout: per-warp buffers [cpr][WS] | terms [32][tstride] | (S > 1) gather [S-1][32][tstride]
     float *terms = reinterpret_cast<float *>(smem + (size_t)cpr * WS::BYTES);
     float *gather = terms + kGemvRows * tstride;
 
@@ -221,7 +227,27 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
         int8_t *q_s = reinterpret_cast<int8_t *>(ws + WS::Q_OFF);
         float *da_s = reinterpret_cast<float *>(ws + WS::D_OFF);
         int16_t *bs_s = reinterpret_cast<int16_t *>(ws + WS::B_OFF);
-        if (FUSED) {
+        if (MC > 1) {
+            // batched decode: column m's chunk c is block (m, c) of the quantised activation rows
+            for (int m = 0; m < M; ++m) {
+                int8_t *qm = q_s + m * WS::XB;
+                float *dm = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(da_s) + m * WS::XB);
+                int16_t *bm = reinterpret_cast<int16_t *>(reinterpret_cast<uint8_t *>(bs_s) + m * WS::XB);
+                if (!Tr::q81) {
+                    const uint8_t *blk = xq + ((int64_t)m * nchunk + c) * kQ8KBytes;
+                    const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4);
+                    reinterpret_cast<uint2 *>(qm)[lane] = make_uint2(src[2 * lane], src[2 * lane + 1]);
+                    if (lane < 16) bm[lane] = reinterpret_cast<const int16_t *>(blk + 260)[lane];
+                    if (lane == 0) dm[0] = *reinterpret_cast<const float *>(blk);
+                } else {
+                    const int b = lane >> 2, part = lane & 3;  // 8 blocks x 4 lanes
+                    const uint8_t *blk = xq + (((int64_t)m * nchunk + c) * 8 + b) * kQ81Bytes;
+                    const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4 + 8 * part);
+                    reinterpret_cast<uint2 *>(qm + 32 * b)[part] = make_uint2(src[0], src[1]);
+                    if (part == 0) dm[b] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+                }
+            }
+        } else if (FUSED) {
             if (!Tr::q81) {
                 warp_quantize_q8k_smem(x + (int64_t)c * 256, q_s, da_s, bs_s);
             } else {
@@ -245,7 +271,11 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
         if (mbar_wait_sleep(&bars[warp], 0, &abort_flag)) {
             const int gi = lane >> 4;
             if (gi < ngroups)
-                gemv_row_chunk<DT>(ws + gi * CB, lane & 15, q_s, da_s, bs_s, terms + lane * tstride + warp * Tr::terms);
+                for (int m = 0; m < (MC > 1 ? M : 1); ++m)
+                    gemv_row_chunk<DT>(ws + gi * CB, lane & 15, q_s + m * WS::XB,
+                                       reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(da_s) + m * WS::XB),
+                                       reinterpret_cast<const int16_t *>(reinterpret_cast<const uint8_t *>(bs_s) + m * WS::XB),
+                                       terms + lane * tstride + (m * cpr + warp) * Tr::terms);
         } else if (lane == 0) {
             int no_abort = 0;  // drain this warp's copies (bounded) before the block may exit
             mbar_wait(&bars[warp], 0, &no_abort, 100000000ull);
@@ -253,13 +283,16 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     }
 
     // ---- ordered reduction: one thread per row adds the row's terms in ascending K order
+    const int ncol = MC > 1 ? M : 1;
     if (S == 1) {
         __syncthreads();
-        if (threadIdx.x < kGemvRows) {
-            const int64_t n = rb * kGemvRows + threadIdx.x;
+        for (int t = threadIdx.x; t < kGemvRows * ncol; t += blockDim.x) {
+            const int r = t & (kGemvRows - 1), m = t / kGemvRows;
+            const int64_t n = rb * kGemvRows + r;
+            const float *tr = terms + r * tstride + m * cpr * Tr::terms;
             float acc = 0.0f;
-            for (int i = 0; i < nloc * Tr::terms; ++i) acc = __fadd_rn(acc, terms[threadIdx.x * tstride + i]);
-            if (n < N) y[n] = abort_flag ? __int_as_float(0x7fc00000) : acc;
+            for (int i = 0; i < nloc * Tr::terms; ++i) acc = __fadd_rn(acc, tr[i]);
+            if (n < N) y[m * ldy + n] = abort_flag ? __int_as_float(0x7fc00000) : acc;
         }
     } else {
         // Every rank pushes its terms into rank 0's gather buffer and signals rank 0's barrier; only
@@ -280,16 +313,17 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
             }
         } else {
             const bool got = mbar_wait_sleep(&gather_bar, 0, &abort_flag);
-            if (threadIdx.x < kGemvRows) {
-                const int64_t n = rb * kGemvRows + threadIdx.x;
+            for (int t = threadIdx.x; t < kGemvRows * ncol; t += blockDim.x) {
+                const int r = t & (kGemvRows - 1), m = t / kGemvRows;
+                const int64_t n = rb * kGemvRows + r;
                 float acc = 0.0f;
                 for (int k = 0; k < S; ++k) {
                     const int kb = k * cpr, ke = min(nchunk, kb + cpr);
                     const int cnt = max(0, ke - kb) * Tr::terms;
-                    const float *src = (k == 0 ? terms : gather + (size_t)(k - 1) * per) + threadIdx.x * tstride;
+                    const float *src = (k == 0 ? terms : gather + (size_t)(k - 1) * per) + r * tstride + m * cpr * Tr::terms;
                     for (int i = 0; i < cnt; ++i) acc = __fadd_rn(acc, src[i]);
                 }
-                if (n < N) y[n] = (!got || abort_flag) ? __int_as_float(0x7fc00000) : acc;
+                if (n < N) y[m * ldy + n] = (!got || abort_flag) ? __int_as_float(0x7fc00000) : acc;
             }
         }
     }
@@ -308,11 +342,11 @@ static int gemv_sm_count() {
     return cache[dev];
 }
 
-template <int DT, bool FUSED>
+template <int DT, bool FUSED, int MC>
 static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq, int64_t N, int64_t K, float *y,
-                             cudaStream_t st) {
+                             cudaStream_t st, int M = 1, int64_t ldy = 0) {
     using Tr = GemvTraits<DT>;
-    using WS = GemvWarpSmem<DT>;
+    using WS = GemvWarpSmem<DT, MC>;
     const int nchunk = (int)(K / 256);
     const int64_t rblocks = (N + kGemvRows - 1) / kGemvRows;
     // Smallest power-of-two cluster split (at most 8) with at most 32 chunks per block.
@@ -327,15 +361,17 @@ static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq
     // them), keeping >= 5 chunks per block.
     auto smem_for = [&](int s) {
         const int c = (nchunk + s - 1) / s;
-        return (size_t)c * WS::BYTES + (size_t)s * kGemvRows * c * Tr::terms * 4;
+        return (size_t)c * WS::BYTES + (size_t)s * kGemvRows * c * Tr::terms * MC * 4;
     };
     while (S < 8 && (rblocks * S < gemv_sm_count() || smem_for(S) > 112 * 1024) && (nchunk + 2 * S - 1) / (2 * S) >= 5)
         S *= 2;
+    while (S < 8 && smem_for(S) > 220 * 1024) S *= 2;  // several activation columns need more room
     const int cpr = (nchunk + S - 1) / S;
     const size_t smem = smem_for(S);
     if (smem > 220 * 1024) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: K=%lld too large", (long long)K);
+    if (ldy == 0) ldy = N;
     if (rblocks > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: N=%lld too large", (long long)N);
-    auto kern = gemv_kernel<DT, FUSED>;
+    auto kern = gemv_kernel<DT, FUSED, MC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
@@ -357,10 +393,32 @@ static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, kern, w, x, xq, N, nchunk, cpr, y);
+    e = cudaLaunchKernelEx(&cfg, kern, w, x, xq, N, nchunk, cpr, y, M, ldy);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: launch failed: %s", cudaGetErrorString(e));
     count_launch(R_GEMV);
     return KQ_OK;
+}
+
+template <int DT>
+static kq_status gemv_batched_dt(const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
+                                 int64_t ldy, cudaStream_t st) {
+    if (M == 1) return launch_gemv<DT, false, 1>(w, nullptr, xq, N, K, y, st, 1, ldy);
+    if (M == 2) return launch_gemv<DT, false, 2>(w, nullptr, xq, N, K, y, st, (int)M, ldy);
+    if (M <= 4) return launch_gemv<DT, false, 4>(w, nullptr, xq, N, K, y, st, (int)M, ldy);
+    return launch_gemv<DT, false, 8>(w, nullptr, xq, N, K, y, st, (int)M, ldy);
+}
+
+// Batched decode (1 <= M <= kGemvMaxBatch quantised activation rows): the GEMV with every staged
+// weight chunk serving all M columns.  Returns KQ_ERR_INVALID_ARG when the shape does not fit the
+// kernel's shared memory (the caller then takes the general path).
+kq_status gemv_batched(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
+                       int64_t ldy, cudaStream_t st) {
+    if (M < 1 || M > kGemvMaxBatch) return fail(KQ_ERR_INVALID_ARG, "gemv_batched: M=%lld", (long long)M);
+    switch (wt) {
+    case KQ_Q4_K: return gemv_batched_dt<KQ_Q4_K>(w, xq, M, N, K, y, ldy, st);
+    case KQ_Q6_K: return gemv_batched_dt<KQ_Q6_K>(w, xq, M, N, K, y, ldy, st);
+    default: return gemv_batched_dt<KQ_Q8_0>(w, xq, M, N, K, y, ldy, st);
+    }
 }
 
 }  // namespace kq
@@ -382,8 +440,8 @@ extern "C" kq_status kq_gemv(kq_dtype wt, const void *w, const float *x, const v
     const uint8_t *wb = static_cast<const uint8_t *>(w);
     const uint8_t *xb = static_cast<const uint8_t *>(xq);
     switch (wt) {
-    case KQ_Q4_K: return x ? launch_gemv<KQ_Q4_K, true>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q4_K, false>(wb, x, xb, N, K, y, st);
-    case KQ_Q6_K: return x ? launch_gemv<KQ_Q6_K, true>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q6_K, false>(wb, x, xb, N, K, y, st);
-    default: return x ? launch_gemv<KQ_Q8_0, true>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q8_0, false>(wb, x, xb, N, K, y, st);
+    case KQ_Q4_K: return x ? launch_gemv<KQ_Q4_K, true, 1>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q4_K, false, 1>(wb, x, xb, N, K, y, st);
+    case KQ_Q6_K: return x ? launch_gemv<KQ_Q6_K, true, 1>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q6_K, false, 1>(wb, x, xb, N, K, y, st);
+    default: return x ? launch_gemv<KQ_Q8_0, true, 1>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q8_0, false, 1>(wb, x, xb, N, K, y, st);
     }
 }

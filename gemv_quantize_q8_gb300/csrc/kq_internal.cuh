@@ -44,6 +44,13 @@ __host__ __device__ inline int64_t chunk_offset(int dtype, int64_t g, int64_t c,
 constexpr int kQ8KBytes = 292;  // f32 d, int8 q[256], int16 bsums[16]
 constexpr int kQ81Bytes = 36;   // f16 d, f16 s, int8 q[32]
 
+// ---------------------------------------------------------------- batched decode (kq_gemv.cu)
+constexpr int kGemvMaxBatch = 8;
+// y[m*ldy + n] for m < M <= kGemvMaxBatch quantised activation rows, bit-identical to the CPU order;
+// KQ_ERR_INVALID_ARG when the shape does not fit (the caller then takes the general path).
+kq_status gemv_batched(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
+                       int64_t ldy, cudaStream_t st);
+
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ int dp4a(int a, int b, int c) { return __dp4a(a, b, c); }
 

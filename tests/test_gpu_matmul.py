@@ -167,6 +167,31 @@ def test_gemm_q8_0_tensor_core_integer_special_case():
     assert np.array_equal(y, ref)
 
 
+@pytest.mark.parametrize("dtype", DTS)
+@pytest.mark.parametrize("M,N,K", [(2, 100, 1024), (3, 256, 2560), (5, 48, 9728), (8, 130, 4096), (8, 64, 16384)])
+def test_gemm_batched_decode_bit_exact(dtype, M, N, K):
+    """Batched decode (M <= 8) runs the weight-streaming GEMV kernel with every staged chunk serving all
+    M activation rows; each output is the oracle's sequential sum, so the result is bit-identical --
+    also with K split across a cluster, ragged N and an output row stride larger than N."""
+    g = synth.rng(360 + M + N + K + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    ldy = N + 8
+    y = torch.full((M, ldy), float("nan"), device=DEV)
+    before = kq.launch_count("gemv")
+    kq.kq_gemm(dtype, wn, xq, M, N, K, y, ldy, None, 0)
+    # Q8_0 keeps 8 terms per chunk and column; with many columns and long K those do not fit the
+    # kernel's shared memory and the dp4a kernel (also bit-exact) takes the call
+    if not (dtype == kq.Q8_0 and M * K >= 40000):
+        assert kq.launch_count("gemv") > before, "expected the batched-decode kernel"
+    yh = host(y)
+    ref = oracle.gemm(dtype, w, _oracle_act(dtype, x), M, N, K)
+    assert np.array_equal(yh[:, :N], ref), (nmse(yh[:, :N], ref), np.abs(yh[:, :N] - ref).max())
+    assert np.isnan(yh[:, N:]).all()
+
+
 def test_tiny_config_bit_exact():
     """The tiny Q4_K workload (W [256, 1024], X [8, 1024], seed 0) end to end."""
     c = synth.TINY
