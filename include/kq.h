@@ -165,6 +165,10 @@ KQ_API size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t
  *   Q6_K x Q8_K: per super-block d_a*d_w*sum_j sc_j*P_j, P_j = sum of (c-32)*q over 16 elements
  *   Q8_0 x Q8_1: per 32-block d_w*d_a*P_b
  * w: native [N][K]; xq: M activation rows (Q8_K or Q8_1 per wt); y: fp32 rows of stride ldy >= N.
+ * Paths: M <= 8 (batched decode) the weight-streaming GEMV kernel, bit-exact with the sequential CPU
+ * order; M >= 9 with N >= 128 the tensor-core kernel (Q8_0 bit-exact; Q4_K/Q6_K integer parts exact,
+ * fp32 promotion fused, NMSE ~1e-14); otherwise, or when a shape does not fit the GEMV kernel, the
+ * exact dp4a kernel.
  * workspace: device buffer of at least kq_gemm_workspace_bytes(wt, M, N, K, 0, 0) bytes (may be
  * NULL when that is 0), 256-byte aligned. */
 KQ_API kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
