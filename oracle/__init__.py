@@ -66,6 +66,7 @@ def lib():
             L.orc_quantize_q8_k.argtypes = [P, I64, I64, I64, P]
             L.orc_quantize_q8_1.argtypes = [P, I64, I64, I64, P]
             L.orc_swiglu.argtypes = [P, P, I64, I64, I64, P, I64]
+            L.orc_rmsnorm.argtypes = [P, P, ctypes.c_float, I64, I64, I64, P, I64]
             L.orc_partials_row.argtypes = [I32, P, P, I64, P]
             L.orc_dot_row.argtypes = [I32, P, P, I64]
             L.orc_dot_row.restype = ctypes.c_float
@@ -132,6 +133,23 @@ def quantize_q8_1(x: np.ndarray) -> np.ndarray:
     out = np.empty((M, K // 32 * 36), dtype=np.uint8)
     lib().orc_quantize_q8_1(_ptr(x), M, K, K, _ptr(out))
     return out
+
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """y = (x * r) * gamma, r = 1 / sqrt(sum(x^2) / K + eps), fp32, sum in the fixed row-reduction order."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    M, K = x.shape
+    assert gamma.shape == (K,)
+    y = np.empty((M, K), dtype=np.float32)
+    lib().orc_rmsnorm(_ptr(x), _ptr(gamma), float(np.float32(eps)), M, K, K, _ptr(y), K)
+    return y
+
+
+def rmsnorm_quantize_q8_k(x: np.ndarray, gamma: np.ndarray, eps: float):
+    """The fused norm-quant producer: (Q8_K bytes of the normalized rows, the normalized rows)."""
+    y = rmsnorm(x, gamma, eps)
+    return quantize_q8_k(y), y
 
 
 def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:

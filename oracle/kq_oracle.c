@@ -318,6 +318,40 @@ ORC_API void orc_swiglu(const float *g, const float *u, int64_t M, int64_t K, in
         }
 }
 
+/* RMSNorm producer (vllm.cpp PR #2890, the fused norm-quant epilogue commit: the norm row kernel
+ * emits the row's Q8_K blocks beside its normalized output, byte-identical to quantizing that output
+ * with the standalone quantizer).  The pages give no formula; the reading is the usual one:
+ *   ss = sum_i x_i^2,  r = 1 / sqrt(ss / K + eps),  y_i = (x_i * r) * gamma_i        (all fp32)
+ * with the sum in the fixed order of a 256-thread row reduction, because the quantised codes of y
+ * depend on every rounding of r: thread t adds x[t]^2, x[t+256]^2, ... in ascending order; the 32
+ * thread sums of each group of 32 combine in xor-butterfly order (butterfly_sum32); the 8 group sums
+ * are added in ascending order.  Division and square root are the IEEE ones (sqrtf, /).
+ * Parity pinned: f64 RMSNorm within the fp32 error bound, a constant row (exact), the zero row,
+ * invariance under scaling x by a power of two, position independence of x_i*gamma_i. */
+ORC_API void orc_rmsnorm(const float *x, const float *gamma, float eps, int64_t M, int64_t K, int64_t ldx, float *y,
+                         int64_t ldy) {
+    for (int64_t m = 0; m < M; ++m) {
+        const float *xr = x + m * ldx;
+        float th[256];
+        for (int t = 0; t < 256; ++t) {
+            float s = 0.0f;
+            for (int64_t i = t; i < K; i += 256) {
+                float sq = xr[i] * xr[i];
+                s = s + sq;
+            }
+            th[t] = s;
+        }
+        float total = 0.0f;
+        for (int w = 0; w < 8; ++w) total = total + butterfly_sum32(th + 32 * w);
+        float mean = total / (float)K;
+        float r = 1.0f / sqrtf(mean + eps);
+        for (int64_t i = 0; i < K; ++i) {
+            float a = xr[i] * r;
+            y[m * ldy + i] = a * gamma[i];
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Integer block dots.                                                       */
 /* ------------------------------------------------------------------------ */

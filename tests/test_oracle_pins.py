@@ -498,3 +498,69 @@ def test_q8_k_half_way_ties_go_to_even():
     assert d == 1.0
     want = [math.floor(v) + (math.floor(v) % 2) for v in halves]   # the even neighbour of each tie
     assert list(q[1:1 + halves.size]) == want
+
+
+# ----------------------------------------------------------------------------- RMSNorm producer
+
+
+def test_rmsnorm_against_f64():
+    # y = x / sqrt(mean(x^2) + eps) * gamma in f64; the fp32 oracle differs by a few roundings only
+    g = synth.rng(700)
+    for K in (256, 2560, 9728):
+        x = synth.activations(3, K, g, outliers=True)
+        gamma = (g.standard_normal(K) * 0.5 + 1.0).astype(np.float32)
+        eps = 1e-6
+        y = oracle.rmsnorm(x, gamma, eps)
+        xd = x.astype(np.float64)
+        ref = xd / np.sqrt((xd * xd).mean(axis=1, keepdims=True) + eps) * gamma.astype(np.float64)
+        assert np.all(np.abs(y - ref) <= 1e-5 * np.abs(ref) + 1e-30), np.abs((y - ref) / ref).max()
+
+
+def test_rmsnorm_constant_row_is_exact():
+    # x = 3: sum of squares 9K is exact, r = fl(1/3), y = fl(3 * fl(1/3)) = 1 exactly; the Q8_K block of
+    # an all-ones row: first maximum at element 0, iscale = -127, every code -127, d = 1/(-127)
+    K = 512
+    x = np.full((1, K), 3.0, np.float32)
+    q, y = oracle.rmsnorm_quantize_q8_k(x, np.ones(K, np.float32), 0.0)
+    assert np.array_equal(y, np.ones((1, K), np.float32))
+    blk = q[0, :292]
+    assert np.frombuffer(blk[:4].tobytes(), np.float32)[0] == np.float32(1.0) / np.float32(-127.0)
+    assert (blk[4:260].view(np.int8) == -127).all()
+    assert (np.frombuffer(blk[260:292].tobytes(), np.int16) == -127 * 16).all()
+
+
+def test_rmsnorm_zero_row_gives_zero_block():
+    K = 256
+    q, y = oracle.rmsnorm_quantize_q8_k(np.zeros((2, K), np.float32), np.ones(K, np.float32), 1e-6)
+    assert (y == 0).all() and (q == 0).all()
+
+
+def test_rmsnorm_scale_invariance_by_powers_of_two():
+    # with eps = 0, scaling x by 2^k scales every square and the sum by 4^k exactly and r by 2^-k,
+    # so y is unchanged bit for bit -- a misplaced mean, square root or eps would break this
+    g = synth.rng(701)
+    K = 2560
+    x = synth.activations(2, K, g, outliers=True)
+    gamma = (g.standard_normal(K) + 1.0).astype(np.float32)
+    y = oracle.rmsnorm(x, gamma, 0.0)
+    for k in (-3, 2, 5):
+        assert np.array_equal(oracle.rmsnorm(x * np.float32(2.0 ** k), gamma, 0.0), y)
+
+
+def test_rmsnorm_elementwise_positions():
+    # y_i = (x_i * r) * gamma_i: with gamma_3 = 1, y_3 is x_3 * r itself; swapping gamma_3 and
+    # gamma_700 (r does not depend on gamma) gives y_3 = (x_3 * r) * gamma_700 and leaves every other
+    # position unchanged -- an index slip between x, gamma and y breaks this
+    g = synth.rng(702)
+    K = 1024
+    x = synth.activations(1, K, g)
+    gamma = (g.standard_normal(K) + 1.0).astype(np.float32)
+    gamma[3] = 1.0
+    y = oracle.rmsnorm(x, gamma, 1e-5)
+    gs = gamma.copy()
+    gs[[3, 700]] = gs[[700, 3]]
+    ys = oracle.rmsnorm(x, gs, 1e-5)
+    assert ys[0, 3] == np.float32(y[0, 3] * gamma[700])
+    keep = np.ones(K, bool)
+    keep[[3, 700]] = False
+    assert np.array_equal(ys[0, keep], y[0, keep])
