@@ -299,7 +299,33 @@ def run_aux(args, device, which="all"):
         out.update(_aux_q8_0(device))
     if which in ("all", "moe"):
         out.update(_aux_moe(device))
+    if which in ("all", "rmsnorm"):
+        out.update(_aux_rmsnorm(device))
     return out
+
+
+def _aux_rmsnorm(device):
+    """Fused RMSNorm -> Q8_K producer: one decode row (K = 2560, 9728) and a 2048-row prefill block
+    (K = 4096); us per call from a CUDA graph and GB/s of x + gamma read and Q8_K written."""
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    from gemv_quantize_q8_gb300 import synth
+    g = synth.rng(3)
+    res = {}
+    for M, K in ((1, 2560), (1, 9728), (2048, 4096)):
+        x = torch.from_numpy(synth.activations(M, K, g)).to(device)
+        gamma = torch.from_numpy((g.standard_normal(K) * 0.3 + 1.0).astype("float32")).to(device)
+        xq = torch.empty(kq.q8k_bytes(M, K), dtype=torch.uint8, device=device)
+        calls = 100 if M == 1 else 20
+
+        def step():
+            for _ in range(calls):
+                kq.kq_rmsnorm_quantize_q8k(x, gamma, 1e-6, M, K, K, xq)
+        us = _time_graph(step, 5) * 1e3 / calls
+        nbytes = M * K * 4 + K * 4 + kq.q8k_bytes(M, K)
+        res[f"m{M}_k{K}"] = {"us_per_call": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    return {"rmsnorm_q8k": res}
 
 
 def _aux_q8_0(device):
@@ -539,7 +565,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-aux", action="store_true", help="skip the Q8_0+SwiGLU and MoE pipeline timings")
     ap.add_argument("--decode-only", action="store_true", help="time only the decode GEMV (for profiling)")
-    ap.add_argument("--aux-only", choices=["all", "q8_0", "moe"], default=None,
+    ap.add_argument("--aux-only", choices=["all", "q8_0", "moe", "rmsnorm"], default=None,
                     help="time only the Q8_0+SwiGLU and/or MoE pipelines (for profiling)")
     ap.add_argument("--gemv-calls", type=int, default=1000, help="back-to-back GEMV calls per decode shape")
     ap.add_argument("--no-cpu", action="store_true")

@@ -53,6 +53,7 @@ _SIGS = {
     "kq_quantize_q8_1": ([_P, _I64, _I64, _I64, _P, _P], _I32),
     "kq_swiglu_quantize_q8_1": ([_P, _P, _I64, _I64, _I64, _P, _P, _P], _I32),
     "kq_swiglu_quantize_q8k": ([_P, _P, _I64, _I64, _I64, _P, _P, _P], _I32),
+    "kq_rmsnorm_quantize_q8k": ([_P, _P, ctypes.c_float, _I64, _I64, _I64, _P, _P, _P], _I32),
     "kq_gemv": ([_I32, _P, _P, _P, _I64, _I64, _P, _P], _I32),
     "kq_gemm_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64, _I64], _SZ),
     "kq_gemm": ([_I32, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I32),
@@ -159,6 +160,11 @@ def kq_swiglu_quantize_q8_1(g, u, M, K, ld, xq, h_out=None, stream=None):
 
 def kq_swiglu_quantize_q8k(g, u, M, K, ld, xq, h_out=None, stream=None):
     _check(lib().kq_swiglu_quantize_q8k(_ptr(g), _ptr(u), M, K, ld, _ptr(xq), _ptr(h_out), _stream(stream)))
+
+
+def kq_rmsnorm_quantize_q8k(x, gamma, eps, M, K, ldx, xq, y_out=None, stream=None):
+    _check(lib().kq_rmsnorm_quantize_q8k(_ptr(x), _ptr(gamma), float(eps), M, K, ldx, _ptr(xq), _ptr(y_out),
+                                         _stream(stream)))
 
 
 def kq_gemv(wt, w, x, xq, N, K, y, stream=None):

@@ -42,6 +42,47 @@ __device__ __forceinline__ void load8(const float *p, float v[8]) {
     }
 }
 
+// The Q8_K block body shared by every producer of Q8_K rows (the standalone and SwiGLU quantizers and
+// the RMSNorm producer), so their blocks are byte-identical by construction.  One warp, lane l holding
+// elements 8l..8l+7 of the block; o: the 292-byte block (f32 d, int8 q[256], int16 bsums[16]).
+__device__ __forceinline__ void q8k_block_store(const float (&v)[8], uint8_t *__restrict__ o) {
+    const int lane = threadIdx.x & 31;
+    // lane-local ascending scan, first occurrence wins (strict >)
+    float amax = 0.0f, mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float ax = fabsf(v[i]);
+        if (ax > amax) { amax = ax; mx = v[i]; }
+    }
+    // block amax and its first occurrence: amax is never negative or NaN, so its bits order like its
+    // value, and the lowest lane holding the maximum holds the first occurrence
+    const uint32_t key = __float_as_uint(amax);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const int src = __ffs(__ballot_sync(0xffffffffu, key == kmax)) - 1;
+    mx = __shfl_sync(0xffffffffu, mx, src);
+    if (kmax == 0u) {  // zero block
+        uint32_t *o32 = reinterpret_cast<uint32_t *>(o);
+        for (int i = lane; i < kQ8KBytes / 4; i += 32) o32[i] = 0u;
+        return;
+    }
+    const float iscale = __fdiv_rn(-127.0f, mx);
+    int q[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q[i] = q8k_code(__fmul_rn(iscale, v[i]));
+        sum += q[i];
+    }
+    uint32_t w0 = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
+    uint32_t w1 = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | ((uint32_t)(q[7] & 0xff) << 24);
+    uint32_t *qs = reinterpret_cast<uint32_t *>(o + 4 + lane * 8);
+    qs[0] = w0;
+    qs[1] = w1;
+    int pair = sum + __shfl_xor_sync(0xffffffffu, sum, 1);
+    if ((lane & 1) == 0) reinterpret_cast<int16_t *>(o + 260)[lane >> 1] = (int16_t)pair;
+    if (lane == 0) *reinterpret_cast<float *>(o) = __fdiv_rn(1.0f, iscale);
+}
+
 // One warp quantizes one 256-element block; lane l holds elements 8l..8l+7.
 // SWIGLU: the block's inputs are h = silu(g)*u computed here (optionally stored to h_out).
 template <bool VEC, bool SWIGLU>
@@ -65,43 +106,7 @@ __global__ void quantize_q8k_kernel(const float *__restrict__ x, const float *__
             for (int i = 0; i < 8; ++i) hp[i] = v[i];
         }
     }
-    // lane-local ascending scan, first occurrence wins (strict >)
-    float amax = 0.0f, mx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float ax = fabsf(v[i]);
-        if (ax > amax) { amax = ax; mx = v[i]; }
-    }
-    int src = lane;  // chunk index holding the current maximum
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        float oa = __shfl_xor_sync(0xffffffffu, amax, s);
-        float om = __shfl_xor_sync(0xffffffffu, mx, s);
-        int os = __shfl_xor_sync(0xffffffffu, src, s);
-        if (oa > amax || (oa == amax && os < src)) { amax = oa; mx = om; src = os; }
-    }
-    uint8_t *o = out + blk * kQ8KBytes;
-    if (amax == 0.0f) {  // zero block
-        uint32_t *o32 = reinterpret_cast<uint32_t *>(o);
-        for (int i = lane; i < kQ8KBytes / 4; i += 32) o32[i] = 0u;
-        return;
-    }
-    const float iscale = __fdiv_rn(-127.0f, mx);
-    int q[8];
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q[i] = q8k_code(__fmul_rn(iscale, v[i]));
-        sum += q[i];
-    }
-    uint32_t w0 = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
-    uint32_t w1 = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | ((uint32_t)(q[7] & 0xff) << 24);
-    uint32_t *qs = reinterpret_cast<uint32_t *>(o + 4 + lane * 8);
-    qs[0] = w0;
-    qs[1] = w1;
-    int pair = sum + __shfl_xor_sync(0xffffffffu, sum, 1);
-    if ((lane & 1) == 0) reinterpret_cast<int16_t *>(o + 260)[lane >> 1] = (int16_t)pair;
-    if (lane == 0) *reinterpret_cast<float *>(o) = __fdiv_rn(1.0f, iscale);
+    q8k_block_store(v, out + blk * kQ8KBytes);
 }
 
 __device__ __forceinline__ uint16_t f16_bits(float f) {
@@ -174,6 +179,55 @@ __global__ void quantize_q8_1_kernel(const float *__restrict__ x, const float *_
     }
 }
 
+// Fused RMSNorm + Q8_K producer (vllm.cpp PR #2890, fused norm-quant epilogue: the norm row kernel
+// emits the row's Q8_K blocks beside its normalized output).  One block of 256 threads per row:
+//   ss = sum_i x_i^2 -- thread t adds x[t]^2, x[t+256]^2, ... in order, each warp combines its 32 sums
+//        in xor-butterfly order (strides 16 .. 1), thread 0 adds the 8 warp sums in order;
+//   r  = 1 / sqrt(ss / K + eps) (IEEE division and square root);  y_i = (x_i * r) * gamma_i;
+// then warp w quantises blocks w, w+8, ... of y with the standalone Q8_K body (and stores y when
+// y_out != NULL).  Every operation is rounded on its own, so codes and y match the CPU oracle's.
+template <bool VEC>
+__global__ void __launch_bounds__(256) rmsnorm_q8k_kernel(const float *__restrict__ x, const float *__restrict__ gamma,
+                                                          float eps, int64_t K, int64_t ldx, uint8_t *__restrict__ out,
+                                                          float *__restrict__ y_out) {
+    __shared__ float wsum[8];
+    __shared__ float rs;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;
+    const float *xr = x + row * ldx;
+    float s = 0.0f;
+    for (int64_t i = tid; i < K; i += 256) {
+        const float v = xr[i];
+        s = __fadd_rn(s, __fmul_rn(v, v));
+    }
+#pragma unroll
+    for (int st = 16; st >= 1; st >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, st));
+    if (lane == 0) wsum[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+        float total = 0.0f;
+        for (int w = 0; w < 8; ++w) total = __fadd_rn(total, wsum[w]);
+        const float mean = __fdiv_rn(total, (float)K);
+        rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+    }
+    __syncthreads();
+    const float r = rs;
+    const int64_t nb = K / 256;
+    for (int64_t b = warp; b < nb; b += 8) {
+        float v[8], gv[8];
+        load8<VEC>(xr + b * 256 + lane * 8, v);
+        load8<VEC>(gamma + b * 256 + lane * 8, gv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], r), gv[i]);
+        if (y_out) {
+            float *yp = y_out + row * K + b * 256 + lane * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) yp[i] = v[i];
+        }
+        q8k_block_store(v, out + (row * nb + b) * kQ8KBytes);
+    }
+}
+
 static kq_status quant_common(const char *name, const float *x, const float *u, int64_t M, int64_t K, int64_t ld,
                               void *xq, float *h_out, int block, bool swiglu, cudaStream_t st) {
     if (!x || !xq || (swiglu && !u)) return fail(KQ_ERR_INVALID_ARG, "%s: null pointer", name);
@@ -235,6 +289,27 @@ kq_status kq_swiglu_quantize_q8_1(const float *g, const float *u, int64_t M, int
 kq_status kq_swiglu_quantize_q8k(const float *g, const float *u, int64_t M, int64_t K, int64_t ld, void *xq,
                                  float *h_out, kq_stream_t stream) {
     return quant_common("kq_swiglu_quantize_q8k", g, u, M, K, ld, xq, h_out, 256, true, (cudaStream_t)stream);
+}
+
+kq_status kq_rmsnorm_quantize_q8k(const float *x, const float *gamma, float eps, int64_t M, int64_t K, int64_t ldx,
+                                  void *xq, float *y_out, kq_stream_t stream) {
+    const char *name = "kq_rmsnorm_quantize_q8k";
+    if (!x || !gamma || !xq) return fail(KQ_ERR_INVALID_ARG, "%s: null pointer", name);
+    if (M <= 0 || K <= 0 || K % 256 || M > 0x7fffffff)
+        return fail(KQ_ERR_INVALID_ARG, "%s: need M > 0 and K a positive multiple of 256 (M=%lld K=%lld)", name,
+                    (long long)M, (long long)K);
+    if (ldx < K) return fail(KQ_ERR_INVALID_ARG, "%s: leading dimension %lld < K %lld", name, (long long)ldx, (long long)K);
+    if (!(eps >= 0.0f) || !isfinite(eps)) return fail(KQ_ERR_INVALID_ARG, "%s: eps must be finite and >= 0", name);
+    if (!aligned(x, 4) || !aligned(gamma, 4) || !aligned(xq, 4) || (y_out && !aligned(y_out, 4)))
+        return fail(KQ_ERR_ALIGNMENT, "%s: pointers must be 4-byte aligned", name);
+    const bool vec = aligned(x, 16) && aligned(gamma, 16) && ldx % 4 == 0 && (!y_out || aligned(y_out, 16));
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *o = static_cast<uint8_t *>(xq);
+    if (vec) rmsnorm_q8k_kernel<true><<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ldx, o, y_out);
+    else rmsnorm_q8k_kernel<false><<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ldx, o, y_out);
+    kq_status s = check_launch(name);
+    if (s == KQ_OK) count_launch(R_QUANT);
+    return s;
 }
 
 }  // extern "C"

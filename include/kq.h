@@ -136,6 +136,16 @@ KQ_API kq_status kq_quantize_q8_1(const float *x, int64_t M, int64_t K, int64_t 
 KQ_API kq_status kq_swiglu_quantize_q8_1(const float *g, const float *u, int64_t M, int64_t K, int64_t ld, void *xq,
                                   float *h_out, kq_stream_t stream);
 
+/* Fused RMSNorm + Q8_K producer ([vllm-2890], fused norm-quant epilogue): per row,
+ *   r = 1 / sqrt(sum_i x_i^2 / K + eps),  y_i = (x_i * r) * gamma_i   (fp32, each operation rounded),
+ * with the sum in a fixed order (256 partial sums: thread t takes x[t], x[t+256], ...; groups of 32
+ * combined in xor-butterfly order; the 8 group sums added in order), then y quantised exactly as
+ * kq_quantize_q8k does (byte-identical).  x: fp32 [M][ldx]; gamma: fp32 [K]; xq: Q8_K [M][K/256];
+ * y_out: optional fp32 [M][K] copy of y (NULL to skip).  One launch replaces norm + quantize; its
+ * output feeds kq_gemv (xq) or kq_gemm. */
+KQ_API kq_status kq_rmsnorm_quantize_q8k(const float *x, const float *gamma, float eps, int64_t M, int64_t K,
+                                         int64_t ldx, void *xq, float *y_out, kq_stream_t stream);
+
 /* Fused SwiGLU + Q8_K: as kq_swiglu_quantize_q8_1 but the quantizer is kq_quantize_q8k's
  * (used between the routed gate/up and down projections). */
 KQ_API kq_status kq_swiglu_quantize_q8k(const float *g, const float *u, int64_t M, int64_t K, int64_t ld, void *xq,

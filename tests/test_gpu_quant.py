@@ -123,3 +123,73 @@ def test_quantizer_rejects_bad_args():
     with pytest.raises(kq.KqError) as e:
         kq.kq_quantize_q8k(x, 1, 300, 300, out)
     assert e.value.status == 1
+
+
+# ----------------------------------------------------------------------------- RMSNorm -> Q8_K producer
+
+
+def _rmsnorm_gpu(x, gamma, eps, ld=None, with_y=True):
+    M, K = x.shape[0], gamma.shape[0]
+    ld = ld or K
+    xd = torch.zeros((M, ld), device=DEV)
+    xd[:, :K] = dev(np.ascontiguousarray(x[:, :K]))
+    xq = torch.full((kq.q8k_bytes(M, K),), 0xAB, dtype=torch.uint8, device=DEV)
+    y = torch.full((M, K), float("nan"), device=DEV) if with_y else None
+    kq.kq_rmsnorm_quantize_q8k(xd, dev(gamma), eps, M, K, ld, xq, y)
+    return host(xq).reshape(M, -1), (host(y) if with_y else None)
+
+
+@pytest.mark.parametrize("M,K", [(1, 256), (1, 2560), (1, 9728), (3, 4096), (64, 2048), (5, 16384)])
+def test_rmsnorm_q8k_bit_exact(M, K):
+    """Codes, scales, bsums and the normalized rows equal the oracle's byte for byte: the kernel's sum of
+    squares follows the oracle's fixed reduction order and every other step is one IEEE operation."""
+    g = synth.rng(720 + M + K)
+    x = synth.activations(M, K, g, outliers=True)
+    gamma = (g.standard_normal(K) * 0.3 + 1.0).astype(np.float32)
+    q, y = _rmsnorm_gpu(x, gamma, 1e-6)
+    q_ref, y_ref = oracle.rmsnorm_quantize_q8_k(x, gamma, 1e-6)
+    assert np.array_equal(y, y_ref)
+    assert np.array_equal(q, q_ref)
+
+
+def test_rmsnorm_q8k_special_rows_and_stride():
+    # zero row (r = 1/sqrt(eps), y = 0: the zero block), a constant row, huge/tiny magnitudes, a row
+    # stride larger than K (scalar loads), and no y output
+    K = 512
+    rows = [np.zeros(K, np.float32), np.full(K, 3.0, np.float32), np.full(K, -1e-20, np.float32),
+            (np.arange(K) - 256).astype(np.float32) * 1e15]
+    x = np.stack(rows)
+    gamma = np.linspace(0.5, 1.5, K, dtype=np.float32)
+    q_ref, y_ref = oracle.rmsnorm_quantize_q8_k(x, gamma, 1e-5)
+    q, y = _rmsnorm_gpu(x, gamma, 1e-5, ld=K + 3)
+    assert np.array_equal(q, q_ref) and np.array_equal(y, y_ref)
+    q2, _ = _rmsnorm_gpu(x, gamma, 1e-5, with_y=False)
+    assert np.array_equal(q2, q_ref)
+
+
+def test_rmsnorm_q8k_feeds_decode_gemv():
+    # the producer's Q8_K row drives the decode GEMV directly (no separate quantize launch); the result
+    # equals the oracle's GEMV on the oracle's own normalized-and-quantised row, bit for bit
+    g = synth.rng(730)
+    N, K = 640, 2560
+    x = synth.activations(1, K, g, outliers=True)
+    gamma = (g.standard_normal(K) * 0.3 + 1.0).astype(np.float32)
+    w = synth.weights(kq.Q4_K, N, K, g)
+    wn = torch.empty(kq.native_bytes(kq.Q4_K, N, K), dtype=torch.uint8, device=DEV)
+    kq.kq_repack_weights(kq.Q4_K, dev(w.reshape(-1)), wn, N, K)
+    xq = torch.empty(kq.q8k_bytes(1, K), dtype=torch.uint8, device=DEV)
+    kq.kq_rmsnorm_quantize_q8k(dev(x), dev(gamma), 1e-6, 1, K, K, xq)
+    y = torch.full((N,), float("nan"), device=DEV)
+    kq.kq_gemv(kq.Q4_K, wn, None, xq, N, K, y)
+    q_ref, _ = oracle.rmsnorm_quantize_q8_k(x, gamma, 1e-6)
+    assert np.array_equal(host(y), oracle.gemm(kq.Q4_K, w, q_ref, 1, N, K)[0])
+
+
+def test_rmsnorm_q8k_rejects_bad_args():
+    K = 256
+    x = torch.zeros((1, K), device=DEV)
+    gm = torch.ones(K, device=DEV)
+    xq = torch.empty(kq.q8k_bytes(1, K), dtype=torch.uint8, device=DEV)
+    for args in [(x, gm, 1e-6, 1, 300, K), (x, gm, -1.0, 1, K, K), (x, gm, 1e-6, 1, K, K - 1), (x, gm, 1e-6, 0, K, K)]:
+        with pytest.raises(kq.KqError):
+            kq.kq_rmsnorm_quantize_q8k(*args, xq)
