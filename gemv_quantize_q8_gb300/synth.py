@@ -14,6 +14,8 @@ Distributions (the five workloads of this library's benchmark and tests):
     in 0..63 and 4-bit codes uniform in 0..15.  Every bit of the 12 scale/min
     bytes and of the 128 code bytes is used by exactly one field, so uniform
     fields are uniform random bytes.
+  * Q5_K: as Q4_K, with d, dmin = |N(0,1)| * 0.005 and 32 uniform high-bit bytes (5-bit codes
+    uniform in 0..31).
   * Q6_K: d = |N(0,1)| * 0.002 (f16); int8 scales uniform in -128..127;
     6-bit codes uniform in 0..63 (stored with an offset of 32): again uniform
     random ql/qh bytes.
@@ -29,10 +31,10 @@ from __future__ import annotations
 
 import numpy as np
 
-Q4_K, Q6_K, Q8_0, Q8_K, Q8_1 = 1, 2, 3, 4, 5
-NAMES = {Q4_K: "q4_k", Q6_K: "q6_k", Q8_0: "q8_0", Q8_K: "q8_k", Q8_1: "q8_1"}
-BLOCK_ELEMS = {Q4_K: 256, Q6_K: 256, Q8_0: 32, Q8_K: 256, Q8_1: 32}
-BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q8_0: 34, Q8_K: 292, Q8_1: 36}
+Q4_K, Q6_K, Q8_0, Q8_K, Q8_1, Q5_K = 1, 2, 3, 4, 5, 6
+NAMES = {Q4_K: "q4_k", Q5_K: "q5_k", Q6_K: "q6_k", Q8_0: "q8_0", Q8_K: "q8_k", Q8_1: "q8_1"}
+BLOCK_ELEMS = {Q4_K: 256, Q5_K: 256, Q6_K: 256, Q8_0: 32, Q8_K: 256, Q8_1: 32}
+BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210, Q8_0: 34, Q8_K: 292, Q8_1: 36}
 
 
 def rng(seed: int = 0) -> np.random.Generator:
@@ -85,8 +87,26 @@ def q8_0_weights(N: int, K: int, g: np.random.Generator) -> np.ndarray:
     return blk.reshape(N, nb * 34)
 
 
+def q5_k_weights(N: int, K: int, g: np.random.Generator) -> np.ndarray:
+    """Canonical Q5_K bytes [N, K/256*176]: d, dmin, 12 scale/min bytes, 32 high-bit bytes, 128 code bytes."""
+    assert K % 256 == 0
+    nsb = K // 256
+    d = np.abs(g.standard_normal((N, nsb))) * 0.005
+    dmin = np.abs(g.standard_normal((N, nsb))) * 0.005
+    sm = g.integers(0, 256, size=(N, nsb, 12), dtype=np.uint8)
+    qh = g.integers(0, 256, size=(N, nsb, 32), dtype=np.uint8)
+    codes = g.integers(0, 256, size=(N, nsb, 128), dtype=np.uint8)
+    blk = np.empty((N, nsb, 176), dtype=np.uint8)
+    blk[..., 0:2] = _f16_bytes(d)
+    blk[..., 2:4] = _f16_bytes(dmin)
+    blk[..., 4:16] = sm
+    blk[..., 16:48] = qh
+    blk[..., 48:176] = codes
+    return blk.reshape(N, nsb * 176)
+
+
 def weights(dtype: int, N: int, K: int, g: np.random.Generator) -> np.ndarray:
-    return {Q4_K: q4_k_weights, Q6_K: q6_k_weights, Q8_0: q8_0_weights}[dtype](N, K, g)
+    return {Q4_K: q4_k_weights, Q5_K: q5_k_weights, Q6_K: q6_k_weights, Q8_0: q8_0_weights}[dtype](N, K, g)
 
 
 def activations(M: int, K: int, g: np.random.Generator, outliers: bool = False) -> np.ndarray:

@@ -23,11 +23,11 @@ SRC = os.path.join(HERE, "kq_oracle.c")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "libkq_oracle.so")
 
-Q4_K, Q6_K, Q8_0, Q8_K, Q8_1 = 1, 2, 3, 4, 5
-BLOCK_ELEMS = {Q4_K: 256, Q6_K: 256, Q8_0: 32, Q8_K: 256, Q8_1: 32}
-BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q8_0: 34, Q8_K: 292, Q8_1: 36}
-ACT_DTYPE = {Q4_K: Q8_K, Q6_K: Q8_K, Q8_0: Q8_1}
-SUBBLOCK = {Q4_K: 32, Q6_K: 16, Q8_0: 32}
+Q4_K, Q6_K, Q8_0, Q8_K, Q8_1, Q5_K = 1, 2, 3, 4, 5, 6
+BLOCK_ELEMS = {Q4_K: 256, Q5_K: 256, Q6_K: 256, Q8_0: 32, Q8_K: 256, Q8_1: 32}
+BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210, Q8_0: 34, Q8_K: 292, Q8_1: 36}
+ACT_DTYPE = {Q4_K: Q8_K, Q5_K: Q8_K, Q6_K: Q8_K, Q8_0: Q8_1}
+SUBBLOCK = {Q4_K: 32, Q5_K: 32, Q6_K: 16, Q8_0: 32}
 
 _lock = threading.Lock()
 _lib = None
@@ -59,8 +59,8 @@ def lib():
             L.orc_half_to_float.restype = ctypes.c_float
             L.orc_float_to_half.argtypes = [ctypes.c_float]
             L.orc_float_to_half.restype = ctypes.c_uint16
-            for name in ("orc_dequant_q4_k", "orc_dequant_q6_k", "orc_dequant_q8_0", "orc_dequant_q8_k",
-                         "orc_dequant_q8_1"):
+            for name in ("orc_dequant_q4_k", "orc_dequant_q5_k", "orc_dequant_q6_k", "orc_dequant_q8_0",
+                         "orc_dequant_q8_k", "orc_dequant_q8_1"):
                 getattr(L, name).argtypes = [P, P]
                 getattr(L, name).restype = None
             L.orc_quantize_q8_k.argtypes = [P, I64, I64, I64, P]
@@ -105,8 +105,8 @@ def dequant(dtype: int, blocks: np.ndarray) -> np.ndarray:
     nb = blocks.size // bb
     assert nb * bb == blocks.size
     out = np.empty(nb * be, dtype=np.float64)
-    fn = {Q4_K: "orc_dequant_q4_k", Q6_K: "orc_dequant_q6_k", Q8_0: "orc_dequant_q8_0", Q8_K: "orc_dequant_q8_k",
-          Q8_1: "orc_dequant_q8_1"}[dtype]
+    fn = {Q4_K: "orc_dequant_q4_k", Q5_K: "orc_dequant_q5_k", Q6_K: "orc_dequant_q6_k", Q8_0: "orc_dequant_q8_0",
+          Q8_K: "orc_dequant_q8_k", Q8_1: "orc_dequant_q8_1"}[dtype]
     f = getattr(lib(), fn)
     base = _ptr(blocks)
     obase = _ptr(out)

@@ -39,7 +39,7 @@
 
 #define ORC_API __attribute__((visibility("default")))
 
-enum { ORC_Q4_K = 1, ORC_Q6_K = 2, ORC_Q8_0 = 3, ORC_Q8_K = 4, ORC_Q8_1 = 5 };
+enum { ORC_Q4_K = 1, ORC_Q6_K = 2, ORC_Q8_0 = 3, ORC_Q8_K = 4, ORC_Q8_1 = 5, ORC_Q5_K = 6 };
 
 /* ------------------------------------------------------------------------ */
 /* IEEE binary16 <-> binary32, written from the IEEE 754 definition.         */
@@ -114,7 +114,7 @@ static int16_t rd_i16(const uint8_t *p) {
 
 ORC_API int64_t orc_block_elems(int dtype) {
     switch (dtype) {
-    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
+    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
     case ORC_Q8_0: case ORC_Q8_1: return 32;
     default: return 0;
     }
@@ -122,6 +122,7 @@ ORC_API int64_t orc_block_elems(int dtype) {
 ORC_API int64_t orc_block_bytes(int dtype) {
     switch (dtype) {
     case ORC_Q4_K: return 144;  /* d, dmin, 12 scale bytes, 128 nibble bytes */
+    case ORC_Q5_K: return 176;  /* d, dmin, 12 scale bytes, 32 high-bit bytes, 128 nibble bytes */
     case ORC_Q6_K: return 210;  /* ql[128], qh[64], int8 scales[16], d */
     case ORC_Q8_0: return 34;   /* d, int8[32] */
     case ORC_Q8_K: return 292;  /* f32 d, int8[256], int16 bsums[16] */
@@ -150,6 +151,15 @@ static int q4k_code(const uint8_t *qs, int i) {
     int c = i / 64, r = i % 64;
     uint8_t b = qs[32 * c + (r % 32)];
     return r < 32 ? (b & 0x0f) : (b >> 4);
+}
+
+/* Q5_K: 5-bit code (0..31) of element i: the Q4_K nibble (same 64-element chunk layout, nibbles at
+ * byte 48 of the block) plus 16 times a high bit from qh[32] (byte 16 of the block): for element
+ * 64c + l (l < 32) bit 2c of qh[l], for element 64c + 32 + l bit 2c+1 of qh[l]. */
+static int q5k_code(const uint8_t *blk, int i) {
+    int c = i / 64, r = i % 64, l = r % 32;
+    int hb = (blk[16 + l] >> (2 * c + (r >= 32))) & 1;
+    return q4k_code(blk + 48, i) | (hb << 4);
 }
 
 /* Q6_K: 6-bit code (0..63, stored with an offset of 32) of element i.
@@ -181,6 +191,19 @@ ORC_API void orc_dequant_q4_k(const uint8_t *blk, double *out) {
         int sc, mn;
         q4k_scale_min(s12, i / 32, &sc, &mn);
         out[i] = d * sc * q4k_code(qs, i) - dmin * mn;
+    }
+}
+
+/* Q5_K: x = d*sc*c - dmin*m with the 5-bit code c.  Pinned by single-element position sweeps and the
+ * unit-scale integer reduction. */
+ORC_API void orc_dequant_q5_k(const uint8_t *blk, double *out) {
+    double d = orc_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+    double dmin = orc_half_to_float((uint16_t)(blk[2] | (blk[3] << 8)));
+    const uint8_t *s12 = blk + 4;
+    for (int i = 0; i < 256; ++i) {
+        int sc, mn;
+        q4k_scale_min(s12, i / 32, &sc, &mn);
+        out[i] = d * sc * q5k_code(blk, i) - dmin * mn;
     }
 }
 
@@ -358,9 +381,10 @@ ORC_API void orc_rmsnorm(const float *x, const float *gamma, float eps, int64_t 
 
 /* Partial integer dots of one weight block row against one activation row.
  * Q4_K x Q8_K: P_j = sum_{i<32} c*q over sub-block j (8 per super-block).
+ * Q5_K x Q8_K: the same over the 5-bit codes.
  * Q6_K x Q8_K: P_j = sum_{i<16} (c-32)*q over sub-block j (16 per super-block).
  * Q8_0 x Q8_1: P_b = sum_{i<32} w*q over block b.
- * Output: K/32 (Q4_K, Q8_0) or K/16 (Q6_K) int32 values. */
+ * Output: K/32 (Q4_K, Q5_K, Q8_0) or K/16 (Q6_K) int32 values. */
 ORC_API void orc_partials_row(int dtype, const uint8_t *wrow, const uint8_t *xrow, int64_t K, int32_t *out) {
     if (dtype == ORC_Q4_K) {
         for (int64_t b = 0; b < K / 256; ++b) {
@@ -369,6 +393,16 @@ ORC_API void orc_partials_row(int dtype, const uint8_t *wrow, const uint8_t *xro
             for (int j = 0; j < 8; ++j) {
                 int32_t acc = 0;
                 for (int i = 32 * j; i < 32 * j + 32; ++i) acc += q4k_code(wb + 16, i) * q[i];
+                out[8 * b + j] = acc;
+            }
+        }
+    } else if (dtype == ORC_Q5_K) {
+        for (int64_t b = 0; b < K / 256; ++b) {
+            const uint8_t *wb = wrow + 176 * b;
+            const int8_t *q = (const int8_t *)(xrow + 292 * b + 4);
+            for (int j = 0; j < 8; ++j) {
+                int32_t acc = 0;
+                for (int i = 32 * j; i < 32 * j + 32; ++i) acc += q5k_code(wb, i) * q[i];
                 out[8 * b + j] = acc;
             }
         }
@@ -403,12 +437,14 @@ ORC_API void orc_partials_row(int dtype, const uint8_t *wrow, const uint8_t *xro
  * independent brute force on tiny inputs. */
 ORC_API float orc_dot_row(int dtype, const uint8_t *wrow, const uint8_t *xrow, int64_t K) {
     float acc = 0.0f;
-    if (dtype == ORC_Q4_K) {
+    if (dtype == ORC_Q4_K || dtype == ORC_Q5_K) {
+        /* Q5_K: the Q4_K formula over 5-bit codes (same header: d, dmin, packed scales and mins) */
+        const int64_t bb = dtype == ORC_Q4_K ? 144 : 176;
         for (int64_t b = 0; b < K / 256; ++b) {
-            const uint8_t *wb = wrow + 144 * b;
+            const uint8_t *wb = wrow + bb * b;
             const uint8_t *xb = xrow + 292 * b;
             int32_t P[8];
-            orc_partials_row(ORC_Q4_K, wb, xb, 256, P);
+            orc_partials_row(dtype, wb, xb, 256, P);
             int64_t sumi = 0, summ = 0;
             for (int j = 0; j < 8; ++j) {
                 int sc, mn;

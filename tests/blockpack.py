@@ -30,6 +30,21 @@ def pack_q4_k(d, dmin, sc, mn, codes):
     return b
 
 
+def pack_q5_k(d, dmin, sc, mn, codes):
+    """sc, mn: 8 ints in 0..63; codes: 256 ints in 0..31 -> 176 bytes (header as Q4_K, then 32 high-bit
+    bytes -- element 64c + l takes bit 2c of byte l, element 64c + 32 + l bit 2c + 1 -- then the low
+    nibbles in the Q4_K arrangement)."""
+    q4 = pack_q4_k(d, dmin, sc, mn, [c & 15 for c in codes])
+    b = np.zeros(176, dtype=np.uint8)
+    b[0:16] = q4[0:16]
+    for c in range(4):
+        for l in range(32):
+            b[16 + l] |= ((codes[64 * c + l] >> 4) & 1) << (2 * c)
+            b[16 + l] |= ((codes[64 * c + 32 + l] >> 4) & 1) << (2 * c + 1)
+    b[48:176] = q4[16:144]
+    return b
+
+
 def pack_q6_k(d, sc, codes):
     """sc: 16 ints in -128..127; codes: 256 ints in 0..63 -> 210 bytes."""
     b = np.zeros(210, dtype=np.uint8)

@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 from gemv_quantize_q8_gb300 import synth
-from tests.blockpack import pack_q4_k, pack_q6_k, pack_q8_0, parse_fixture
+from tests.blockpack import pack_q4_k, pack_q5_k, pack_q6_k, pack_q8_0, parse_fixture
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -88,6 +88,53 @@ def test_q4_k_scale_min_fields():
         x = oracle.dequant(oracle.Q4_K, blk)
         want = np.array([d * sc[i // 32] * codes[i] - dmin * mn[i // 32] for i in range(256)])
         assert np.array_equal(x, want)
+
+
+def test_q5_k_every_element_position_and_high_bit():
+    """A single nonzero 5-bit code at element i dequantises at i only; codes >= 16 exercise the high
+    bit's byte and bit position (byte i % 32, bit 2*(i // 64) + (i % 64 >= 32))."""
+    for i in range(256):
+        codes = [0] * 256
+        codes[i] = 16 + (i % 16) if i % 2 else 1 + (i % 15)
+        sc = [j + 1 for j in range(8)]
+        blk = pack_q5_k(1.0, 0.0, sc, [0] * 8, codes)
+        x = oracle.dequant(oracle.Q5_K, blk)
+        want = np.zeros(256)
+        want[i] = sc[i // 32] * codes[i]
+        assert np.array_equal(x, want), i
+
+
+def test_q5_k_all_codes_and_fields():
+    g = np.random.default_rng(6)
+    for _ in range(40):
+        sc = g.integers(0, 64, 8)
+        mn = g.integers(0, 64, 8)
+        codes = g.integers(0, 32, 256)
+        blk = pack_q5_k(0.5, 0.25, sc, mn, codes)
+        x = oracle.dequant(oracle.Q5_K, blk)
+        want = np.array([0.5 * sc[i // 32] * codes[i] - 0.25 * mn[i // 32] for i in range(256)])
+        assert np.array_equal(x, want)
+
+
+def test_q5_k_unit_scales_is_integer_matmul():
+    g = np.random.default_rng(11)
+    M, N, K = 3, 4, 512
+    codes = g.integers(0, 32, size=(N, K))
+    wb = np.concatenate([np.concatenate([pack_q5_k(1.0, 0.0, [1] * 8, [0] * 8, codes[n, 256 * b:256 * b + 256])
+                                         for b in range(K // 256)]) for n in range(N)])
+    x = _integer_acts(M, K, g)
+    y = oracle.gemm(oracle.Q5_K, wb, oracle.quantize_q8_k(x), M, N, K)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ codes.T)
+
+
+def test_q5_k_min_term_sign():
+    """d = 0, dmin = 1, every min 1: y = -sum(q) over the row."""
+    g = np.random.default_rng(12)
+    M, N, K = 2, 3, 256
+    wb = np.concatenate([pack_q5_k(0.0, 1.0, [5] * 8, [1] * 8, g.integers(0, 32, 256)) for _ in range(N)])
+    x = _integer_acts(M, K, g)
+    y = oracle.gemm(oracle.Q5_K, wb, oracle.quantize_q8_k(x), M, N, K)
+    assert np.array_equal(y, np.repeat(-x.sum(axis=1, keepdims=True), N, axis=1).astype(np.float32))
 
 
 def test_q6_k_every_element_position():
@@ -343,18 +390,21 @@ def _brute_force_f64(dtype, w, x_blocks, M, N, K):
                 d = float(blk[0:2].view(np.float16)[0])
                 vals += [d * int(v) for v in blk[2:34].view(np.int8)]
             return vals
-        bb = 144 if dtype == oracle.Q4_K else 210
+        bb = {oracle.Q4_K: 144, oracle.Q5_K: 176, oracle.Q6_K: 210}[dtype]
         for b in range(K // 256):
             blk = row[bb * b:bb * b + bb]
-            if dtype == oracle.Q4_K:
+            if dtype in (oracle.Q4_K, oracle.Q5_K):
                 d = float(blk[0:2].view(np.float16)[0]); dm = float(blk[2:4].view(np.float16)[0])
                 s = [int(v) for v in blk[4:16]]
+                qs = 16 if dtype == oracle.Q4_K else 48
                 for i in range(256):
                     j, c, r = i // 32, i // 64, i % 64
                     sc = s[j] & 63 if j < 4 else (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4)
                     mn = s[j + 4] & 63 if j < 4 else (s[j + 4] >> 4) | ((s[j] >> 6) << 4)
-                    byte = int(blk[16 + 32 * c + r % 32])
+                    byte = int(blk[qs + 32 * c + r % 32])
                     code = byte & 15 if r < 32 else byte >> 4
+                    if dtype == oracle.Q5_K:
+                        code += 16 * ((int(blk[16 + r % 32]) >> (2 * c + (r >= 32))) & 1)
                     vals.append(d * sc * code - dm * mn)
             else:
                 d = float(blk[208:210].view(np.float16)[0])
@@ -386,7 +436,7 @@ def _brute_force_f64(dtype, w, x_blocks, M, N, K):
     return np.array([[math.fsum(a * b for a, b in zip(X[m], W[n])) for n in range(N)] for m in range(M)])
 
 
-@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0])
 def test_brute_force_tiny(dtype):
     g = np.random.default_rng(20 + dtype)
     M, N, K = 3, 4, 512
@@ -399,7 +449,7 @@ def test_brute_force_tiny(dtype):
     assert np.abs(y - ref).max() <= 1e-5 * scale
 
 
-@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0])
 def test_f64_band_and_zero_input(dtype):
     g = np.random.default_rng(30 + dtype)
     M, N, K = 8, 64, 1024
