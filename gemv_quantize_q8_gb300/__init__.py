@@ -20,8 +20,8 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libkq.so")
 
-Q4_K, Q6_K, Q8_0, Q8_K, Q8_1 = 1, 2, 3, 4, 5
-DTYPES = {"q4_k": Q4_K, "q6_k": Q6_K, "q8_0": Q8_0, "q8_k": Q8_K, "q8_1": Q8_1}
+Q4_K, Q6_K, Q8_0, Q8_K, Q8_1, Q5_K = 1, 2, 3, 4, 5, 6
+DTYPES = {"q4_k": Q4_K, "q5_k": Q5_K, "q6_k": Q6_K, "q8_0": Q8_0, "q8_k": Q8_K, "q8_1": Q8_1}
 STATUS = {0: "KQ_OK", 1: "KQ_ERR_INVALID_ARG", 2: "KQ_ERR_UNSUPPORTED_DTYPE", 3: "KQ_ERR_ALIGNMENT",
           4: "KQ_ERR_WORKSPACE", 5: "KQ_ERR_CUDA", 6: "KQ_ERR_DEVICE_FLAG"}
 

@@ -38,6 +38,7 @@ kq_status check_launch(const char *what) {
 const char *dtype_name(kq_dtype d) {
     switch (d) {
     case KQ_Q4_K: return "Q4_K";
+    case KQ_Q5_K: return "Q5_K";
     case KQ_Q6_K: return "Q6_K";
     case KQ_Q8_0: return "Q8_0";
     case KQ_Q8_K: return "Q8_K";
@@ -58,12 +59,17 @@ __global__ void repack_kernel(int dtype, const uint8_t *__restrict__ src, uint8_
     const int r = tid >> 2, kb = tid & 3;
     const int64_t n = g * kRowGroup + r;
     const bool valid = n < N;
-    if (dtype == KQ_Q4_K) {
-        const uint8_t *blk = src + n * (nchunk * 144) + c * 144;
+    if (dtype == KQ_Q4_K || dtype == KQ_Q5_K) {
+        // Q5_K canonical block: header 16 | high bits 32 | nibbles 128; the native chunk keeps the Q4_K
+        // arrangement and appends each row's 32 high-bit bytes at 2304 + r*32
+        const int bb = dtype == KQ_Q4_K ? 144 : 176, qs = dtype == KQ_Q4_K ? 16 : 48;
+        const uint8_t *blk = src + n * (nchunk * bb) + c * bb;
         uint8_t *codes = out + kb * 512 + r * 32;
-        for (int l = 0; l < 32; ++l) codes[l] = valid ? blk[16 + 32 * kb + l] : 0;
+        for (int l = 0; l < 32; ++l) codes[l] = valid ? blk[qs + 32 * kb + l] : 0;
         if (kb == 0)
             for (int i = 0; i < 16; ++i) out[2048 + r * 16 + i] = valid ? blk[i] : 0;
+        if (dtype == KQ_Q5_K && kb == 1)
+            for (int i = 0; i < 32; ++i) out[2304 + r * 32 + i] = valid ? blk[16 + i] : 0;
     } else if (dtype == KQ_Q6_K) {
         const uint8_t *blk = src + n * (nchunk * 210) + c * 210;
         uint8_t code[64];
@@ -139,7 +145,7 @@ int64_t kq_launch_count(const char *route) {
 
 int64_t kq_block_elems(kq_dtype d) {
     switch (d) {
-    case KQ_Q4_K: case KQ_Q6_K: case KQ_Q8_K: return 256;
+    case KQ_Q4_K: case KQ_Q5_K: case KQ_Q6_K: case KQ_Q8_K: return 256;
     case KQ_Q8_0: case KQ_Q8_1: return 32;
     default: return 0;
     }
@@ -148,6 +154,7 @@ int64_t kq_block_elems(kq_dtype d) {
 int64_t kq_block_bytes(kq_dtype d) {
     switch (d) {
     case KQ_Q4_K: return 144;
+    case KQ_Q5_K: return 176;
     case KQ_Q6_K: return 210;
     case KQ_Q8_0: return 34;
     case KQ_Q8_K: return 292;
@@ -170,8 +177,8 @@ int64_t kq_native_bytes(kq_dtype d, int64_t N, int64_t K) {
 
 kq_status kq_repack_weights(kq_dtype dtype, const void *w_canon, void *w_native, int64_t N, int64_t K,
                             kq_stream_t stream) {
-    if (dtype != KQ_Q4_K && dtype != KQ_Q6_K && dtype != KQ_Q8_0)
-        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_repack_weights: weight dtype %s is not Q4_K, Q6_K or Q8_0",
+    if (dtype != KQ_Q4_K && dtype != KQ_Q5_K && dtype != KQ_Q6_K && dtype != KQ_Q8_0)
+        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_repack_weights: weight dtype %s is not Q4_K, Q5_K, Q6_K or Q8_0",
                     dtype_name(dtype));
     if (!w_canon || !w_native) return fail(KQ_ERR_INVALID_ARG, "kq_repack_weights: null pointer");
     if (N <= 0 || K <= 0 || K % kChunkK)

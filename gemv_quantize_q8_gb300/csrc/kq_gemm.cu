@@ -352,8 +352,9 @@ __global__ void weighted_sum_kernel(const float *__restrict__ ys, const float *_
 
 static kq_status check_matmul_args(const char *name, kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N,
                                    int64_t K) {
-    if (wt != KQ_Q4_K && wt != KQ_Q6_K && wt != KQ_Q8_0)
-        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "%s: weight dtype %s is not Q4_K, Q6_K or Q8_0", name, dtype_name(wt));
+    if (wt != KQ_Q4_K && wt != KQ_Q5_K && wt != KQ_Q6_K && wt != KQ_Q8_0)
+        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "%s: weight dtype %s is not Q4_K, Q5_K, Q6_K or Q8_0", name,
+                    dtype_name(wt));
     if (!w || !xq) return fail(KQ_ERR_INVALID_ARG, "%s: null pointer", name);
     if (M <= 0 || N <= 0 || K <= 0 || K % 256)
         return fail(KQ_ERR_INVALID_ARG, "%s: need M, N > 0 and K a positive multiple of 256 (M=%lld N=%lld K=%lld)",

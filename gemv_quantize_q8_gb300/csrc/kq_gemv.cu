@@ -41,6 +41,8 @@ struct GemvTraits;
 template <>
 struct GemvTraits<KQ_Q4_K> { static constexpr int terms = 1; static constexpr bool q81 = false; };
 template <>
+struct GemvTraits<KQ_Q5_K> { static constexpr int terms = 1; static constexpr bool q81 = false; };
+template <>
 struct GemvTraits<KQ_Q6_K> { static constexpr int terms = 1; static constexpr bool q81 = false; };
 template <>
 struct GemvTraits<KQ_Q8_0> { static constexpr int terms = 8; static constexpr bool q81 = true; };
@@ -60,14 +62,21 @@ struct GemvWarpSmem {
 };
 
 // One lane = one row: the exact fp32 term(s) of (row, chunk) from the integer sub-block dots.
-// Q4_K: term = (d_a*d_w)*sumi - (d_a*dmin)*summ; Q6_K: term = (d_a*d_w)*sumi;
+// Q4_K, Q5_K: term = (d_a*d_w)*sumi - (d_a*dmin)*summ; Q6_K: term = (d_a*d_w)*sumi;
 // Q8_0: 8 terms (d_w*d_a)*P_b, one per 32-element block.
 template <int DT>
 __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk, int r,
                                                const int8_t *__restrict__ q, const float *__restrict__ da,
                                                const int16_t *__restrict__ bs, float *__restrict__ term) {
-    if (DT == KQ_Q4_K || DT == KQ_Q6_K) {
-        int P[16];  // Q4_K: 8 sub-blocks of 32; Q6_K: 16 sub-blocks of 16
+    if (DT == KQ_Q4_K || DT == KQ_Q5_K || DT == KQ_Q6_K) {
+        constexpr bool K4 = DT == KQ_Q4_K || DT == KQ_Q5_K;  // 8 sub-blocks of 32 with (d, dmin, scales, mins)
+        int P[16];  // Q4_K/Q5_K: 8 sub-blocks of 32; Q6_K: 16 sub-blocks of 16
+        uint32_t q5h[8];  // Q5_K: the row's 32 high-bit bytes (byte l pairs with code byte l of every kblock)
+        if (DT == KQ_Q5_K) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(chunk + 2304 + r * 32);
+            const uint4 b = *reinterpret_cast<const uint4 *>(chunk + 2304 + r * 32 + 16);
+            q5h[0] = a.x; q5h[1] = a.y; q5h[2] = a.z; q5h[3] = a.w; q5h[4] = b.x; q5h[5] = b.y; q5h[6] = b.z; q5h[7] = b.w;
+        }
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
             const uint4 v0 = *reinterpret_cast<const uint4 *>(chunk + kb * 512 + r * 32);
@@ -89,6 +98,10 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
             for (int i = 0; i < 8; ++i) {
                 const int seg = i >> 2;  // elements 64kb+16seg+.. (low nibbles) / 64kb+32+16seg+.. (high)
                 uint32_t lo = w[i] & 0x0f0f0f0fu, hi = (w[i] >> 4) & 0x0f0f0f0fu;
+                if (DT == KQ_Q5_K) {  // fifth bit: bit 2kb of byte l (low nibbles), bit 2kb+1 (high)
+                    lo |= ((q5h[i] >> (2 * kb)) & 0x01010101u) << 4;
+                    hi |= ((q5h[i] >> (2 * kb + 1)) & 0x01010101u) << 4;
+                }
                 if (DT == KQ_Q6_K) {
                     lo = __vsub4(lo | (((hb[i & 3] >> (2 * seg)) & 0x03030303u) << 4), 0x20202020u);
                     hi = __vsub4(hi | (((hb[i & 3] >> (4 + 2 * seg)) & 0x03030303u) << 4), 0x20202020u);
@@ -96,7 +109,7 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
                 plo[seg] = dp4a((int)lo, ql[i], plo[seg]);
                 phi[seg] = dp4a((int)hi, qh[i], phi[seg]);
             }
-            if (DT == KQ_Q4_K) {
+            if (K4) {
                 P[2 * kb] = plo[0] + plo[1];      // sub-block 2kb   (elements 64kb .. 64kb+31)
                 P[2 * kb + 1] = phi[0] + phi[1];  // sub-block 2kb+1 (elements 64kb+32 .. 64kb+63)
             } else {
@@ -106,7 +119,7 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
                 P[4 * kb + 3] = phi[1];  // sub-block 4kb+3 (64kb+48 .. +63)
             }
         }
-        if (DT == KQ_Q4_K) {
+        if (K4) {
             const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + 2048 + r * 16);
             uint8_t s12[12];
             const uint32_t hw[3] = {hv.y, hv.z, hv.w};
@@ -416,6 +429,7 @@ kq_status gemv_batched(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t
     if (M < 1 || M > kGemvMaxBatch) return fail(KQ_ERR_INVALID_ARG, "gemv_batched: M=%lld", (long long)M);
     switch (wt) {
     case KQ_Q4_K: return gemv_batched_dt<KQ_Q4_K>(w, xq, M, N, K, y, ldy, st);
+    case KQ_Q5_K: return gemv_batched_dt<KQ_Q5_K>(w, xq, M, N, K, y, ldy, st);
     case KQ_Q6_K: return gemv_batched_dt<KQ_Q6_K>(w, xq, M, N, K, y, ldy, st);
     default: return gemv_batched_dt<KQ_Q8_0>(w, xq, M, N, K, y, ldy, st);
     }
@@ -427,8 +441,9 @@ using namespace kq;
 
 extern "C" kq_status kq_gemv(kq_dtype wt, const void *w, const float *x, const void *xq, int64_t N, int64_t K,
                              float *y, kq_stream_t stream) {
-    if (wt != KQ_Q4_K && wt != KQ_Q6_K && wt != KQ_Q8_0)
-        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemv: weight dtype %s is not Q4_K, Q6_K or Q8_0", dtype_name(wt));
+    if (wt != KQ_Q4_K && wt != KQ_Q5_K && wt != KQ_Q6_K && wt != KQ_Q8_0)
+        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemv: weight dtype %s is not Q4_K, Q5_K, Q6_K or Q8_0",
+                    dtype_name(wt));
     if (!w || !y || (!x && !xq) || (x && xq))
         return fail(KQ_ERR_INVALID_ARG, "kq_gemv: need w, y and exactly one of x / xq");
     if (N <= 0 || K <= 0 || K % 256)
@@ -441,6 +456,7 @@ extern "C" kq_status kq_gemv(kq_dtype wt, const void *w, const float *x, const v
     const uint8_t *xb = static_cast<const uint8_t *>(xq);
     switch (wt) {
     case KQ_Q4_K: return x ? launch_gemv<KQ_Q4_K, true, 1>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q4_K, false, 1>(wb, x, xb, N, K, y, st);
+    case KQ_Q5_K: return x ? launch_gemv<KQ_Q5_K, true, 1>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q5_K, false, 1>(wb, x, xb, N, K, y, st);
     case KQ_Q6_K: return x ? launch_gemv<KQ_Q6_K, true, 1>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q6_K, false, 1>(wb, x, xb, N, K, y, st);
     default: return x ? launch_gemv<KQ_Q8_0, true, 1>(wb, x, xb, N, K, y, st) : launch_gemv<KQ_Q8_0, false, 1>(wb, x, xb, N, K, y, st);
     }

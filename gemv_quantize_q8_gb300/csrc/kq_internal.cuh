@@ -30,9 +30,13 @@ constexpr int kQ4KChunk = kRowGroup * (kQ4KCodeBytes + kQ4KHdrBytes);        // 
 constexpr int kQ6KCodeBytes = 192, kQ6KScaleBytes = 16;
 constexpr int kQ6KChunk = kRowGroup * (kQ6KCodeBytes + kQ6KScaleBytes + 2);  // 3360
 constexpr int kQ80Chunk = kRowGroup * (256 + 8 * 2);                          // 4352
+// Q5_K: the Q4_K chunk (nibbles of 4 kblocks, then 16-byte row headers) followed by each row's 32
+// high-bit bytes: 2048 + 256 + 512
+constexpr int kQ5KChunk = kRowGroup * (kQ4KCodeBytes + kQ4KHdrBytes + 32);     // 2816
 
 __host__ __device__ constexpr int chunk_bytes(int dtype) {
-    return dtype == KQ_Q4_K ? kQ4KChunk : dtype == KQ_Q6_K ? kQ6KChunk : dtype == KQ_Q8_0 ? kQ80Chunk : 0;
+    return dtype == KQ_Q4_K ? kQ4KChunk : dtype == KQ_Q5_K ? kQ5KChunk : dtype == KQ_Q6_K ? kQ6KChunk
+           : dtype == KQ_Q8_0 ? kQ80Chunk : 0;
 }
 
 // Byte offset of chunk (row group g, K-chunk c) for a weight with nchunk chunks per row.

@@ -49,9 +49,10 @@ __device__ __forceinline__ void stage_weights(ExactSmem &s, const uint8_t *__res
             for (int j = 0; j < 8; ++j) { s.wmn[row][j] = 0; s.wd[row][j] = 0.0f; }
         }
     }
-    if (DT == KQ_Q4_K || DT == KQ_Q6_K) {
+    if (DT == KQ_Q4_K || DT == KQ_Q5_K || DT == KQ_Q6_K) {
         // unit = (row, kblock kb, 16-byte half seg): low nibbles -> elements 64kb+16seg+i,
-        // high nibbles -> 64kb+32+16seg+i; Q6_K adds two high bits per element and the -32 offset.
+        // high nibbles -> 64kb+32+16seg+i; Q5_K adds one high bit per element (bits 2kb / 2kb+1 of the
+        // row's high-bit bytes), Q6_K two high bits and the -32 offset.
         for (int u = tid; u < rows_valid * 8; u += 256) {
             const int row = u >> 3, kb = (u >> 1) & 3, seg = u & 1;
             const uint8_t *ch = wtile + ((row >> 4) * nchunk + c) * (int64_t)cb;
@@ -68,10 +69,15 @@ __device__ __forceinline__ void stage_weights(ExactSmem &s, const uint8_t *__res
                                     0x20202020u);
                 }
             } else {
+                uint32_t hq[4] = {0u, 0u, 0u, 0u};
+                if (DT == KQ_Q5_K) {
+                    const uint4 h = __ldg(reinterpret_cast<const uint4 *>(ch + 2304 + (row & 15) * 32 + seg * 16));
+                    hq[0] = h.x; hq[1] = h.y; hq[2] = h.z; hq[3] = h.w;
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    lo[i] = w[i] & 0x0f0f0f0fu;
-                    hi[i] = (w[i] >> 4) & 0x0f0f0f0fu;
+                    lo[i] = (w[i] & 0x0f0f0f0fu) | (((hq[i] >> (2 * kb)) & 0x01010101u) << 4);
+                    hi[i] = ((w[i] >> 4) & 0x0f0f0f0fu) | (((hq[i] >> (2 * kb + 1)) & 0x01010101u) << 4);
                 }
             }
             *reinterpret_cast<uint4 *>(&s.wq[row][64 * kb + 16 * seg]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -79,7 +85,7 @@ __device__ __forceinline__ void stage_weights(ExactSmem &s, const uint8_t *__res
         }
         if (tid < rows_valid) {
             const uint8_t *ch = wtile + ((tid >> 4) * nchunk + c) * (int64_t)cb;
-            if (DT == KQ_Q4_K) {
+            if (DT == KQ_Q4_K || DT == KQ_Q5_K) {
                 const uint8_t *h = ch + 2048 + (tid & 15) * 16;
                 s.wd[tid][0] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(h));
                 s.wd[tid][1] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(h + 2));
@@ -277,7 +283,7 @@ __global__ void __launch_bounds__(256) mmq_exact_kernel(MmqExactArgs a) {
                     const int ni = tx + 16 * j;
                     const float t1 = __fmul_rn(da, s.wd[ni][0]);
                     float term = __fmul_rn(t1, (float)sumi[i][j]);
-                    if (DT == KQ_Q4_K) {
+                    if (DT == KQ_Q4_K || DT == KQ_Q5_K) {
                         int summ = 0;
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) summ += s.wmn[ni][jj] * (s.abs_[mi][2 * jj] + s.abs_[mi][2 * jj + 1]);
@@ -327,6 +333,7 @@ kq_status launch_mmq_exact(int dt, int mode, bool grouped, const MmqExactArgs &a
         return mode == 1 ? launch_one<DTV, 1, false>(a, grid_y, st) : launch_one<DTV, 0, false>(a, grid_y, st); \
     }
     KQ_DISPATCH(KQ_Q4_K)
+    KQ_DISPATCH(KQ_Q5_K)
     KQ_DISPATCH(KQ_Q6_K)
     KQ_DISPATCH(KQ_Q8_0)
 #undef KQ_DISPATCH

@@ -60,6 +60,7 @@ struct TcCfg<KQ_Q4_K> {
     static constexpr int CB = kQ4KChunk;  // packed chunk bytes per 16-row group
     static constexpr bool EXT = true;     // min term through the extension MMA
     static constexpr bool Q8 = false;     // per-32-block scales (Q8_0 x Q8_1)
+    static constexpr bool Q5 = false;     // fifth code bit from the row's high-bit bytes (Q5_K)
     static constexpr int A_COLS = 32;     // TMEM columns of one converted kblock (64 f16)
     static constexpr int NACC = 2;        // accumulator buffers
     static constexpr int BPS = 1;         // accumulator read-outs per step (scale blocks per 256 K)
@@ -69,9 +70,16 @@ struct TcCfg<KQ_Q4_K> {
     static constexpr uint32_t TM_S2 = 256, TM_A = 384;
 };
 template <>
+struct TcCfg<KQ_Q5_K> {  // Q4_K's header and min term; 5-bit codes, sc*c <= 63*31 exact in f16
+    static constexpr int CB = kQ5KChunk;
+    static constexpr bool EXT = true, Q8 = false, Q5 = true;
+    static constexpr int A_COLS = 32, NACC = 2, BPS = 1, H_ROW = 8, NP = 2, NE = 2;
+    static constexpr uint32_t TM_S2 = 256, TM_A = 384;
+};
+template <>
 struct TcCfg<KQ_Q6_K> {
     static constexpr int CB = kQ6KChunk;
-    static constexpr bool EXT = false, Q8 = false;
+    static constexpr bool EXT = false, Q8 = false, Q5 = false;
     static constexpr int A_COLS = 64;     // lo tile (32 columns) then 16*hi tile (32 columns)
     static constexpr int NACC = 2, BPS = 1, H_ROW = 8;  // f32 (d, 0)
     static constexpr int NP = 2, NE = 2;
@@ -80,7 +88,7 @@ struct TcCfg<KQ_Q6_K> {
 template <>
 struct TcCfg<KQ_Q8_0> {
     static constexpr int CB = kQ80Chunk;
-    static constexpr bool EXT = false, Q8 = true;
+    static constexpr bool EXT = false, Q8 = true, Q5 = false;
     static constexpr int A_COLS = 32;
     // every 32-element block has its own weight and activation scale, so every block's integer
     // dot P_b is read out of its own accumulator: three buffers rotate along the blocks
@@ -112,6 +120,7 @@ struct TcLayout {
 };
 static_assert(TcLayout<KQ_Q4_K>::ALLOC <= 227 * 1024, "Q4_K tensor-core smem budget");
 static_assert(TcLayout<KQ_Q6_K>::ALLOC <= 227 * 1024, "Q6_K tensor-core smem budget");
+static_assert(TcLayout<KQ_Q5_K>::ALLOC <= 227 * 1024, "Q5_K tensor-core smem budget");
 static_assert(TcLayout<KQ_Q8_0>::ALLOC <= 227 * 1024, "Q8_0 tensor-core smem budget");
 // the split-K reduction parks a 128 x (128 + 4) fp32 tile in the activation ring
 static_assert(TC_TOK * (TC_ROWS + 4) * 4 <= NACT * ACT_TILE, "split-K staging fits the activation ring");
@@ -197,6 +206,27 @@ __device__ __forceinline__ void convert_q4k_kblock(uint4 v0, uint4 v1, int sc_lo
         r[2 * i + 1] = h2u(__hfma2(u2h((d23 & 0x000F000Fu) | 0x64006400u), slo, nlo));
         r[16 + 2 * i] = h2u(__hfma2(u2h((d01 & 0x00F000F0u) | 0x54005400u), shi, nhi));
         r[16 + 2 * i + 1] = h2u(__hfma2(u2h((d23 & 0x00F000F0u) | 0x54005400u), shi, nhi));
+    }
+}
+
+// Q5_K kblock kb of one row: the Q4_K conversion with each code's fifth bit taken from the row's
+// high-bit words hq (byte l pairs with code byte l: bit 2kb for the low nibble, bit 2kb+1 for the high
+// one) and placed above the nibble: (0x6400 | (n + 16h)) = 1024 + c and (0x5400 | 16(n + 16h)) = 64 + c.
+__device__ __forceinline__ void convert_q5k_kblock(uint4 v0, uint4 v1, const uint32_t (&hq)[8], int kb, int sc_lo,
+                                                   int sc_hi, uint32_t (&r)[32]) {
+    const __half2 slo = __float2half2_rn((float)sc_lo), shi = __float2half2_rn((float)sc_hi);
+    const __half2 nlo = __float2half2_rn(-1024.0f * sc_lo), nhi = __float2half2_rn(-64.0f * sc_hi);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t d01 = __byte_perm(w[i], 0u, 0x4140), d23 = __byte_perm(w[i], 0u, 0x4342);
+        const uint32_t h01 = __byte_perm(hq[i], 0u, 0x4140), h23 = __byte_perm(hq[i], 0u, 0x4342);
+        const uint32_t l01 = ((h01 >> (2 * kb)) & 0x00010001u) << 4, l23 = ((h23 >> (2 * kb)) & 0x00010001u) << 4;
+        const uint32_t u01 = ((h01 >> (2 * kb + 1)) & 0x00010001u) << 8, u23 = ((h23 >> (2 * kb + 1)) & 0x00010001u) << 8;
+        r[2 * i] = h2u(__hfma2(u2h((d01 & 0x000F000Fu) | l01 | 0x64006400u), slo, nlo));
+        r[2 * i + 1] = h2u(__hfma2(u2h((d23 & 0x000F000Fu) | l23 | 0x64006400u), slo, nlo));
+        r[16 + 2 * i] = h2u(__hfma2(u2h((d01 & 0x00F000F0u) | u01 | 0x54005400u), shi, nhi));
+        r[16 + 2 * i + 1] = h2u(__hfma2(u2h((d23 & 0x00F000F0u) | u23 | 0x54005400u), shi, nhi));
     }
 }
 
@@ -514,8 +544,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 cv[j][1] = *reinterpret_cast<const uint4 *>(codes + 16);
                 if (!C::EXT) qh[j] = *reinterpret_cast<const uint4 *>(chunk + 2048 + (grp + 2 * j) * 256 + r16 * 16);
             }
-            // Q4_K: d, dmin and the 12 packed scale bytes; Q6_K: the 16 int8 sub-block scales
+            // Q4_K/Q5_K: d, dmin and the 12 packed scale bytes; Q6_K: the 16 int8 sub-block scales
             uint4 hv = *reinterpret_cast<const uint4 *>(chunk + (C::EXT ? 2048 : 3072) + r16 * 16);
+
             if (!rvalid) hv = make_uint4(0, 0, 0, 0);
             int ksc[2][4];  // sub-block scales of kblocks grp and grp+2
             if (C::EXT) {
@@ -549,7 +580,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t ta = lane_base + C::TM_A + kb * C::A_COLS;
                 if (C::EXT) {
                     uint32_t r[32];
-                    convert_q4k_kblock(cv[j][0], cv[j][1], ksc[j][0], ksc[j][1], r);
+                    if (C::Q5) {
+                        // the row's 32 high-bit bytes, loaded per kblock to keep them out of the wait
+                        const uint4 a = *reinterpret_cast<const uint4 *>(chunk + 2304 + r16 * 32);
+                        const uint4 b = *reinterpret_cast<const uint4 *>(chunk + 2304 + r16 * 32 + 16);
+                        const uint32_t q5w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                        convert_q5k_kblock(cv[j][0], cv[j][1], q5w, kb, ksc[j][0], ksc[j][1], r);
+                    } else {
+                        convert_q4k_kblock(cv[j][0], cv[j][1], ksc[j][0], ksc[j][1], r);
+                    }
                     tmem_st32(ta, r);
                 } else {
                     const uint32_t hb[4] = {qh[j].x, qh[j].y, qh[j].z, qh[j].w};
@@ -914,7 +953,7 @@ static TcWs tc_ws(kq_dtype wt, int64_t M, int64_t K) {
 }
 
 bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
-    if (wt != KQ_Q4_K && wt != KQ_Q6_K && wt != KQ_Q8_0) return false;
+    if (wt != KQ_Q4_K && wt != KQ_Q5_K && wt != KQ_Q6_K && wt != KQ_Q8_0) return false;
     // M <= 8 belongs to the batched-decode GEMV; from 9 rows on, a mostly empty 128-token tile still
     // beats the dp4a kernel (measured 3-10x at M = 16..64 on the decode and prefill shapes)
     if (M <= kGemvMaxBatch || N < 128) return false;
@@ -931,7 +970,7 @@ static int tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     if (wt == KQ_Q8_0) return 1;  // keeps every output's blocks in one ascending sum (bit-exact)
     const int64_t tiles = ((M + TC_TOK - 1) / TC_TOK) * ((N + TC_ROWS - 1) / TC_ROWS);
     const int nsb = (int)(K / 256);
-    const double t_sb = wt == KQ_Q4_K ? 1.3 : 1.75, t_fill = 2.5, t_red = 1.0;
+    const double t_sb = wt == KQ_Q4_K ? 1.3 : wt == KQ_Q5_K ? 1.5 : 1.75, t_fill = 2.5, t_red = 1.0;
     const int num_sms = 152, gpcs = 8, sms_per_gpc = 19;
     int best = 1;
     double best_t = 1e30;
@@ -1065,7 +1104,12 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
 }
 
 static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st) {
-    return wt == KQ_Q4_K ? launch_tc<KQ_Q4_K>(a, st) : wt == KQ_Q6_K ? launch_tc<KQ_Q6_K>(a, st) : launch_tc<KQ_Q8_0>(a, st);
+    switch (wt) {
+    case KQ_Q4_K: return launch_tc<KQ_Q4_K>(a, st);
+    case KQ_Q5_K: return launch_tc<KQ_Q5_K>(a, st);
+    case KQ_Q6_K: return launch_tc<KQ_Q6_K>(a, st);
+    default: return launch_tc<KQ_Q8_0>(a, st);
+    }
 }
 
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
@@ -1099,7 +1143,8 @@ kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, i
 
 // ---- routed experts on the tensor cores
 bool tc_grouped_eligible(kq_dtype wt, int64_t N, int64_t K) {
-    return (wt == KQ_Q4_K || wt == KQ_Q6_K || wt == KQ_Q8_0) && N % 16 == 0 && K % 256 == 0 && K <= (1 << 20) &&
+    return (wt == KQ_Q4_K || wt == KQ_Q5_K || wt == KQ_Q6_K || wt == KQ_Q8_0) && N % 16 == 0 && K % 256 == 0 &&
+           K <= (1 << 20) &&
            N <= (1 << 22);
 }
 

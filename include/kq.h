@@ -76,7 +76,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *kq_stream_t; /* same handle as cudaStream_t */
 
-typedef enum { KQ_Q4_K = 1, KQ_Q6_K = 2, KQ_Q8_0 = 3, KQ_Q8_K = 4, KQ_Q8_1 = 5 } kq_dtype;
+typedef enum { KQ_Q4_K = 1, KQ_Q6_K = 2, KQ_Q8_0 = 3, KQ_Q8_K = 4, KQ_Q8_1 = 5, KQ_Q5_K = 6 } kq_dtype;
 
 typedef enum {
     KQ_OK = 0,

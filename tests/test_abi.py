@@ -46,6 +46,8 @@ def test_binding_covers_every_symbol_and_loads(built):
     assert kq.row_bytes(kq.Q4_K, 2560) == 10 * 144
     assert kq.native_bytes(kq.Q4_K, 9728, 2560) == 9728 * 10 * 144
     assert kq.native_bytes(kq.Q6_K, 17, 256) == 2 * 3360          # rows padded to a multiple of 16
+    assert kq.block_bytes(kq.Q5_K) == 176 and kq.row_bytes(kq.Q5_K, 512) == 2 * 176
+    assert kq.native_bytes(kq.Q5_K, 17, 256) == 2 * 2816          # Q4_K chunk + 32 high-bit bytes per row
     assert kq.native_bytes(kq.Q8_0, 16, 1024) == 4 * 4352
     assert kq.native_bytes(kq.Q8_0, 16, 100) == 0
 

@@ -17,7 +17,7 @@ from tests.gpu_util import DEV, act_quant, dev, gemm, host, nmse, q8_1, repack
 
 pytestmark = pytest.mark.gpu
 
-DTS = [kq.Q4_K, kq.Q6_K, kq.Q8_0]
+DTS = [kq.Q4_K, kq.Q5_K, kq.Q6_K, kq.Q8_0]
 
 
 def _oracle_act(dtype, x):
@@ -223,11 +223,11 @@ def test_gemm_adversarial_max_magnitudes(M):
     """All codes and scales at their extremes: integer sums reach their largest values
     (M = 4 takes the batched-decode GEMV, M = 256 the tensor-core kernel)."""
     N, K = 256, 512
-    for dtype in (kq.Q4_K, kq.Q6_K):
-        bb = 144 if dtype == kq.Q4_K else 210
+    for dtype in (kq.Q4_K, kq.Q5_K, kq.Q6_K):
+        bb = {kq.Q4_K: 144, kq.Q5_K: 176, kq.Q6_K: 210}[dtype]
         w = np.full((N, K // 256 * bb), 0xFF, dtype=np.uint8)
         for b in range(K // 256):     # keep d finite: f16 1.0 (Q4_K: d and dmin, Q6_K: d)
-            if dtype == kq.Q4_K:
+            if dtype in (kq.Q4_K, kq.Q5_K):
                 w[:, b * bb:b * bb + 4] = np.frombuffer(np.array([1.0, 1.0], np.float16).tobytes(), np.uint8)
             else:
                 w[:, b * bb + 208:b * bb + 210] = np.frombuffer(np.array([1.0], np.float16).tobytes(), np.uint8)
@@ -244,7 +244,7 @@ def test_gemm_adversarial_max_magnitudes(M):
         assert nmse(y, ref) <= 1e-10
 
 
-@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K])
+@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q5_K, kq.Q6_K])
 @pytest.mark.parametrize("shape", synth.PREFILL_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
 def test_gemm_prefill_full_size_sampled(dtype, shape):
     N, K = shape
@@ -330,7 +330,7 @@ def test_grouped_small(dtype, rpt):
     assert _close(dtype, host(y), ref)
 
 
-@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K, kq.Q8_0])
+@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q5_K, kq.Q6_K, kq.Q8_0])
 def test_grouped_tensor_core_multi_tile(dtype):
     # experts with more than one 128-row tile, several row tiles, a tail tile, an empty expert
     g = synth.rng(405 + dtype)
