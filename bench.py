@@ -301,7 +301,56 @@ def run_aux(args, device, which="all"):
         out.update(_aux_moe(device))
     if which in ("all", "rmsnorm"):
         out.update(_aux_rmsnorm(device))
+    if which in ("all", "q5_k"):
+        out.update(_aux_q5k(device))
     return out
+
+
+def _aux_q5k(device):
+    """Q5_K weights: the prefill shapes at M = 512 through kq_gemm (tensor cores; TOPS from graph
+    replays, quantisation excluded) and the two Q4_K decode shapes as Q5_K fused-quant GEMVs
+    (1000 calls over rotating weight copies; weight GB/s)."""
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    from gemv_quantize_q8_gb300 import synth
+    g = synth.rng(5)
+    out = {"prefill_tops": {}, "decode": {}}
+    M = 512
+    for N, K in synth.PREFILL_SHAPES:
+        wc = torch.from_numpy(synth.weights(synth.Q5_K, N, K, g).reshape(-1)).to(device)
+        wn = torch.empty(kq.native_bytes(synth.Q5_K, N, K), dtype=torch.uint8, device=device)
+        kq.kq_repack_weights(synth.Q5_K, wc, wn, N, K)
+        del wc
+        x = torch.from_numpy(synth.activations(M, K, g)).to(device)
+        xq = torch.empty(kq.q8k_bytes(M, K), dtype=torch.uint8, device=device)
+        kq.kq_quantize_q8k(x, M, K, K, xq)
+        y = torch.empty((M, N), device=device)
+        wsb = kq.gemm_workspace_bytes(synth.Q5_K, M, N, K)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
+        ms = _time_graph(lambda: kq.kq_gemm(synth.Q5_K, wn, xq, M, N, K, y, N, ws, wsb), 10)
+        out["prefill_tops"][f"{N}x{K}_m{M}"] = round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    for N, K in ((9728, 2560), (2560, 9728)):
+        nb = kq.native_bytes(synth.Q5_K, N, K)
+        copies = max(3, -(-3 * l2 // nb))
+        wc = torch.from_numpy(synth.weights(synth.Q5_K, N, K, g).reshape(-1)).to(device)
+        ws = torch.empty((copies, nb), dtype=torch.uint8, device=device)
+        for c in range(copies):
+            kq.kq_repack_weights(synth.Q5_K, wc, ws[c], N, K)
+        x = torch.from_numpy(synth.activations(1, K, g)).to(device)
+        y = torch.empty(N, device=device)
+        calls = 1000
+
+        def step():
+            for i in range(calls):
+                kq.kq_gemv(synth.Q5_K, ws[i % copies], x, None, N, K, y)
+        us = _time_graph(step, 5) * 1e3 / calls
+        wbytes = N * (K // 256) * 176
+        out["decode"][f"{N}x{K}"] = {"us_per_call": round(us, 2), "gbs": round(wbytes / (us * 1e-6) / 1e9, 1)}
+        del ws
+        torch.cuda.empty_cache()
+    return {"q5_k": out}
 
 
 def _aux_rmsnorm(device):
@@ -565,7 +614,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-aux", action="store_true", help="skip the Q8_0+SwiGLU and MoE pipeline timings")
     ap.add_argument("--decode-only", action="store_true", help="time only the decode GEMV (for profiling)")
-    ap.add_argument("--aux-only", choices=["all", "q8_0", "moe", "rmsnorm"], default=None,
+    ap.add_argument("--aux-only", choices=["all", "q8_0", "moe", "rmsnorm", "q5_k"], default=None,
                     help="time only the Q8_0+SwiGLU and/or MoE pipelines (for profiling)")
     ap.add_argument("--gemv-calls", type=int, default=1000, help="back-to-back GEMV calls per decode shape")
     ap.add_argument("--no-cpu", action="store_true")
