@@ -170,10 +170,8 @@ def run_prefill(args, device, rank, world):
     weights, x_host = build_prefill_inputs(device, only=cases if args.only else None)
     Mmax, Kmax = x_host.shape
     x_dev = torch.from_numpy(x_host).to(device)
-    x_pin = torch.from_numpy(x_host).pin_memory()
     max_y = max(M * N for (M, _, N, _) in cases)
     y = torch.empty(max_y, dtype=torch.float32, device=device)
-    y_pin = torch.empty(max_y, dtype=torch.float32).pin_memory()
     xq = torch.empty(max(kq.q8k_bytes(M, K) for (M, _, _, K) in cases), dtype=torch.uint8, device=device)
     ws_need = max(kq.gemm_workspace_bytes(dt, M, N, K) for (M, dt, N, K) in cases)
     ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=device)
@@ -189,13 +187,43 @@ def run_prefill(args, device, rank, world):
             if events is not None:
                 events[i][1].record(stream)
 
+    # End to end as a serving loop runs it: every GEMM's activation comes from its own pinned host
+    # buffer and its output goes back to one, each step.  Copies run on their own streams against
+    # double-buffered device buffers, ordered by events, so the copy engines overlap the kernels; the
+    # whole step is one CUDA graph.
+    max_x = max(M * K for (M, _, _, K) in cases)
+    xh = [torch.from_numpy(np.ascontiguousarray(x_host[:M, :K]).reshape(-1)).pin_memory() for (M, _, _, K) in cases]
+    yh = [torch.empty(M * N, dtype=torch.float32).pin_memory() for (M, _, N, _) in cases]
+    xbuf = [torch.empty(max_x, dtype=torch.float32, device=device) for _ in range(2)]
+    ybuf = [torch.empty(max_y, dtype=torch.float32, device=device) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    nc = len(cases)
+    ev_in, ev_q, ev_c, ev_out = ([torch.cuda.Event() for _ in range(nc)] for _ in range(4))
+
     def step_e2e():
-        for (M, dt, N, K) in cases:
-            xd = x_dev[:M, :K]
-            xd.copy_(x_pin[:M, :K], non_blocking=True)           # host -> device, pinned
-            kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)
-            kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, y, N, ws, ws_need)
-            y_pin[:M * N].copy_(y[:M * N], non_blocking=True)     # device -> host, pinned
+        cs = torch.cuda.current_stream()
+        s_in.wait_stream(cs)
+        s_out.wait_stream(cs)
+        for i, (M, dt, N, K) in enumerate(cases):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_q[i - 2])                  # buffer b no longer read by quantize
+                xbuf[b][:M * K].copy_(xh[i], non_blocking=True)   # host -> device, pinned
+                ev_in[i].record(s_in)
+            cs.wait_event(ev_in[i])
+            if i >= 2:
+                cs.wait_event(ev_out[i - 2])                      # output buffer b copied out
+            kq.kq_quantize_q8k(xbuf[b], M, K, K, xq)
+            ev_q[i].record(cs)
+            kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, ybuf[b], N, ws, ws_need)
+            ev_c[i].record(cs)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c[i])
+                yh[i].copy_(ybuf[b][:M * N], non_blocking=True)   # device -> host, pinned
+                ev_out[i].record(s_out)
+        cs.wait_stream(s_in)
+        cs.wait_stream(s_out)
 
     for _ in range(args.warmup):
         step()
@@ -254,14 +282,27 @@ def run_prefill(args, device, rank, world):
     for _ in range(max(1, args.warmup // 2)):
         step_e2e()
     torch.cuda.synchronize()
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e):
+        step_e2e()
+    for _ in range(max(1, args.warmup // 2)):
+        g_e2e.replay()
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step_e2e()
+        g_e2e.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    # the pipelined step computed what the plain one computes (last GEMM, bit for bit)
+    M, dt, N, K = cases[-1]
+    kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)
+    kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, y, N, ws, ws_need)
+    torch.cuda.synchronize()
+    assert torch.equal(y[:M * N].cpu(), yh[-1]), "end-to-end step output differs from the device step"
+
     h2d = sum(M * K * 4 for (M, _, _, K) in cases)
     d2h = sum(M * N * 4 for (M, _, N, _) in cases)
     return dict(ops=ops, ms=ms, gemm_ms=gemm_ms, per_case=per_case, clocks=clk, launches=launches,
