@@ -477,7 +477,8 @@ def _aux_moe(device):
     y_dn = torch.empty((M, top_k, H), device=device)
     o = torch.empty((M, H), device=device)
     wsb = max(kq.gemm_workspace_bytes(synth.Q4_K, M, 2 * F, H, E, top_k),
-              kq.gemm_workspace_bytes(synth.Q6_K, M, H, F, E, top_k))
+              kq.gemm_workspace_bytes(synth.Q6_K, M, H, F, E, top_k),
+              kq.kq_gemm_grouped_swiglu_workspace_bytes(synth.Q4_K, M, F, H, E, top_k))
     ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
 
     def moe():
@@ -488,11 +489,37 @@ def _aux_moe(device):
         kq.kq_gemm_grouped(synth.Q6_K, w_dn, E, hq, top_k, ids, M, top_k, H, F, y_dn, ws, wsb)
         kq.kq_moe_weighted_sum(y_dn, wts, M, top_k, H, o)
 
+    def gate_up():
+        kq.kq_gemm_grouped(synth.Q4_K, w_gu, E, xq, 1, ids, M, top_k, 2 * F, H, y_gu, ws, wsb)
+        flat = y_gu.view(M * top_k, 2 * F)
+        kq.kq_swiglu_quantize_q8k(flat, flat[:, F:], M * top_k, F, 2 * F, hq)
+
+    def gate_up_fused():
+        # SwiGLU and the Q8_K quantisation in the gate/up GEMM's epilogue: no fp32 gate/up rows
+        kq.kq_gemm_grouped_swiglu_q8k(synth.Q4_K, w_gu, E, xq, 1, ids, M, top_k, F, H, hq, ws, wsb)
+
+    def moe_fused():
+        kq.kq_quantize_q8k(x, M, H, H, xq)
+        gate_up_fused()
+        kq.kq_gemm_grouped(synth.Q6_K, w_dn, E, hq, top_k, ids, M, top_k, H, F, y_dn, ws, wsb)
+        kq.kq_moe_weighted_sum(y_dn, wts, M, top_k, H, o)
+
     t = _time_graph(moe, 5)
+    moe()
+    o_ref = o.clone()
+    t_f = _time_graph(moe_fused, 5)
+    moe_fused()
+    assert torch.equal(o, o_ref), "fused SwiGLU epilogue changed the MoE block's output"
+    t_gu = _time_graph(gate_up, 5)
+    t_guf = _time_graph(gate_up_fused, 5)
     ops = 2.0 * M * top_k * (2 * F * H + H * F)
     out["moe_mul_mat_id"] = {"workload": c["name"], "block_us": round(t * 1e3, 1),
                              "tops": round(ops / (t * 1e-3) / 1e12, 2),
-                             "weight_gbs": round((w_gu.numel() + w_dn.numel()) / (t * 1e-3) / 1e9, 1)}
+                             "weight_gbs": round((w_gu.numel() + w_dn.numel()) / (t * 1e-3) / 1e9, 1),
+                             "block_us_fused_swiglu": round(t_f * 1e3, 1),
+                             "tops_fused_swiglu": round(ops / (t_f * 1e-3) / 1e12, 2),
+                             "gate_up_swiglu_us": round(t_gu * 1e3, 1),
+                             "gate_up_swiglu_fused_us": round(t_guf * 1e3, 1)}
     assert kq.kq_read_device_flag(ws) == 0, "MoE routing reported bad expert ids"
     return out
 

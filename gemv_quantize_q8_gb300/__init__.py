@@ -63,6 +63,8 @@ _SIGS = {
     "kq_debug_partials": ([_I32, _P, _P, _I64, _I64, _I64, _P, _P], _I32),
     "kq_launch_count": ([ctypes.c_char_p], _I64),
     "kq_gemm_grouped_noalloc": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P], _I32),
+    "kq_gemm_grouped_swiglu_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64, _I64], _SZ),
+    "kq_gemm_grouped_swiglu_q8k": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _SZ, _P], _I32),
 }
 
 
@@ -179,6 +181,17 @@ def kq_gemm_grouped(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K
                     stream=None):
     _check(lib().kq_gemm_grouped(wt, _ptr(w), n_experts, _ptr(xq), xq_rows_per_token, _ptr(ids), M, top_k, N, K,
                                  _ptr(y), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def kq_gemm_grouped_swiglu_workspace_bytes(wt, M, F, K, n_experts, top_k) -> int:
+    return int(lib().kq_gemm_grouped_swiglu_workspace_bytes(wt, M, F, K, n_experts, top_k))
+
+
+def kq_gemm_grouped_swiglu_q8k(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, F, K, hq, workspace, ws_bytes,
+                               stream=None):
+    """Routed gate/up GEMM whose epilogue writes Q8_K rows of silu(gate)*up to hq (no fp32 rows)."""
+    _check(lib().kq_gemm_grouped_swiglu_q8k(wt, _ptr(w), n_experts, _ptr(xq), xq_rows_per_token, _ptr(ids), M, top_k,
+                                            F, K, _ptr(hq), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def kq_gemm_grouped_noalloc(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K, y, stream=None):

@@ -6,16 +6,9 @@
 // quantizes the activation once per thread block instead of launching a separate kernel
 // (strix-llama.cpp PR #18 "Optimize ROCM Prefill and Decode", fused-quant MMVQ commit).
 #pragma once
-#include "kq_internal.cuh"
+#include "kq_q8k_block.cuh"
 
 namespace kq {
-
-__device__ __forceinline__ int q8k_code_dev(float p) {
-    if (isnan(p)) return 0;
-    if (p >= 127.0f) return 127;
-    if (p <= -127.0f) return -127;
-    return __float2int_rn(p);
-}
 
 // One warp quantizes 256 fp32 values at x (any 4-byte alignment) into Q8_K fields.
 __device__ __forceinline__ void warp_quantize_q8k_smem(const float *__restrict__ x, int8_t *q, float *d,
@@ -50,7 +43,7 @@ __device__ __forceinline__ void warp_quantize_q8k_smem(const float *__restrict__
     if (amax != 0.0f) iscale = __fdiv_rn(-127.0f, mx);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        qv[i] = amax == 0.0f ? 0 : q8k_code_dev(__fmul_rn(iscale, v[i]));
+        qv[i] = amax == 0.0f ? 0 : q8k_code(__fmul_rn(iscale, v[i]));
         sum += qv[i];
     }
     uint32_t w0 = (qv[0] & 0xff) | ((qv[1] & 0xff) << 8) | ((qv[2] & 0xff) << 16) | ((uint32_t)(qv[3] & 0xff) << 24);

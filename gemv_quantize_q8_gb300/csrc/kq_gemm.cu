@@ -423,21 +423,32 @@ kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, int64_t 
     return launch_mmq_exact(wt, 1, false, a, (unsigned)gy, (cudaStream_t)stream);
 }
 
-kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const void *xq, int64_t xq_rows_per_token,
-                          const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y, void *workspace,
-                          size_t ws_bytes, kq_stream_t stream) {
+}  // extern "C"
+
+namespace kq {
+
+static size_t swq_scratch_offset(size_t base) { return (base + 255) & ~(size_t)255; }
+
+// The routed GEMM behind kq_gemm_grouped (hq == NULL: fp32 rows to y) and kq_gemm_grouped_swiglu_q8k
+// (hq != NULL: N = 2F gate/up rows, Q8_K rows of silu(gate)*up to hq; the caller has checked the
+// fused preconditions and sized the workspace with the scratch after need_base bytes).
+static kq_status grouped_run(kq_dtype wt, const void *w, int64_t n_experts, const void *xq, int64_t xq_rows_per_token,
+                             const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y, uint8_t *hq,
+                             void *workspace, size_t ws_bytes, kq_stream_t stream) {
     kq_status s = check_matmul_args("kq_gemm_grouped", wt, w, xq, M, N, K);
     if (s != KQ_OK) return s;
-    if (!ids || !y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: null ids or y");
+    if (!ids || (!y && !hq)) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: null ids or y");
     if (n_experts <= 0 || top_k <= 0 || n_experts > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: need 0 < n_experts <= 65535 and top_k > 0");
     if (xq_rows_per_token != 1 && xq_rows_per_token != top_k)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: xq_rows_per_token must be 1 or top_k");
     if (N % 16) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: N=%lld must be a multiple of 16", (long long)N);
     if (M * top_k > (int64_t)1 << 30) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: too many (token, slot) pairs");
-    if (!aligned(ids, 4) || !aligned(y, 4)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm_grouped: ids/y must be 4-byte aligned");
+    if (!aligned(ids, 4) || !aligned(y, 4) || !aligned(hq, 4))
+        return fail(KQ_ERR_ALIGNMENT, "kq_gemm_grouped: ids/y must be 4-byte aligned");
     const GroupedWs L = grouped_ws(M, top_k, n_experts);
-    const size_t need = kq_gemm_workspace_bytes(wt, M, N, K, n_experts, top_k);
+    const size_t need_base = kq_gemm_workspace_bytes(wt, M, N, K, n_experts, top_k);
+    const size_t need = hq ? swq_scratch_offset(need_base) + tc_swq_scratch_bytes() : need_base;
     if (!workspace || ws_bytes < need)
         return fail(KQ_ERR_WORKSPACE, "kq_gemm_grouped: workspace of %zu bytes needed, %zu given", need,
                     workspace ? ws_bytes : 0);
@@ -488,7 +499,9 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
         return tc_gemm_grouped(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq),
                                (int)xq_rows_per_token, (int)top_k, pairs, n_experts, N, K, y, ws + T.off_panels,
                                tc_tiles, tc_count, T.max_tiles, count, offset, poff, lists, prow,
-                               reinterpret_cast<unsigned long long *>(flag), st);
+                               reinterpret_cast<unsigned long long *>(flag), hq,
+                               hq ? reinterpret_cast<float *>(ws + swq_scratch_offset(need_base)) : nullptr, st);
+    if (hq) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_swiglu_q8k: shape not served by the tensor cores");
     MmqExactArgs a{};
     a.w = static_cast<const uint8_t *>(w);
     a.xq = static_cast<const uint8_t *>(xq);
@@ -497,6 +510,39 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
     a.rows_per_token = (int)xq_rows_per_token;
     a.top_k = (int)top_k;
     return launch_mmq_exact(wt, 0, true, a, (unsigned)L.max_tiles, st);
+}
+
+}  // namespace kq
+
+extern "C" {
+
+kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const void *xq, int64_t xq_rows_per_token,
+                          const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y, void *workspace,
+                          size_t ws_bytes, kq_stream_t stream) {
+    if (!y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: null ids or y");
+    return grouped_run(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K, y, nullptr, workspace, ws_bytes,
+                       stream);
+}
+
+size_t kq_gemm_grouped_swiglu_workspace_bytes(kq_dtype wt, int64_t M, int64_t F, int64_t K, int64_t n_experts,
+                                              int64_t top_k) {
+    if (M <= 0 || F <= 0 || K <= 0 || n_experts <= 0) return 0;
+    return swq_scratch_offset(kq_gemm_workspace_bytes(wt, M, 2 * F, K, n_experts, top_k)) + tc_swq_scratch_bytes();
+}
+
+kq_status kq_gemm_grouped_swiglu_q8k(kq_dtype wt, const void *w, int64_t n_experts, const void *xq,
+                                     int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k, int64_t F,
+                                     int64_t K, void *hq, void *workspace, size_t ws_bytes, kq_stream_t stream) {
+    const char *name = "kq_gemm_grouped_swiglu_q8k";
+    if (!hq) return fail(KQ_ERR_INVALID_ARG, "%s: null hq", name);
+    if (F <= 0 || F % 256 || F > (1 << 21))
+        return fail(KQ_ERR_INVALID_ARG, "%s: F=%lld must be a positive multiple of 256 (at most 2^21)", name,
+                    (long long)F);
+    if (!tc_grouped_eligible(wt, 2 * F, K) || K % 256)
+        return fail(KQ_ERR_INVALID_ARG, "%s: weight type %s with K=%lld is not served by the tensor cores", name,
+                    dtype_name(wt), (long long)K);
+    return grouped_run(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, 2 * F, K, nullptr,
+                       static_cast<uint8_t *>(hq), workspace, ws_bytes, stream);
 }
 
 kq_status kq_read_device_flag(void *workspace, int64_t *n_bad, kq_stream_t stream) {

@@ -11,23 +11,9 @@
 // commit): d = amax/127 with IEEE division, q = roundf(x/d), and the block sum taken in xor-butterfly
 // order.  Eight lanes own one 32-element block (4 elements each); the butterfly strides 16, 8, 4
 // cross lanes and strides 2, 1 stay inside a lane, which reproduces the 32-lane order exactly.
-#include "kq_internal.cuh"
+#include "kq_q8k_block.cuh"
 
 namespace kq {
-
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    float e = expf(-g);
-    float den = __fadd_rn(1.0f, e);
-    float s = __fdiv_rn(g, den);
-    return __fmul_rn(s, u);
-}
-
-__device__ __forceinline__ int q8k_code(float p) {
-    if (isnan(p)) return 0;
-    if (p >= 127.0f) return 127;
-    if (p <= -127.0f) return -127;
-    return __float2int_rn(p);
-}
 
 template <bool VEC>
 __device__ __forceinline__ void load8(const float *p, float v[8]) {
@@ -40,47 +26,6 @@ __device__ __forceinline__ void load8(const float *p, float v[8]) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = p[i];
     }
-}
-
-// The Q8_K block body shared by every producer of Q8_K rows (the standalone and SwiGLU quantizers and
-// the RMSNorm producer), so their blocks are byte-identical by construction.  One warp, lane l holding
-// elements 8l..8l+7 of the block; o: the 292-byte block (f32 d, int8 q[256], int16 bsums[16]).
-__device__ __forceinline__ void q8k_block_store(const float (&v)[8], uint8_t *__restrict__ o) {
-    const int lane = threadIdx.x & 31;
-    // lane-local ascending scan, first occurrence wins (strict >)
-    float amax = 0.0f, mx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float ax = fabsf(v[i]);
-        if (ax > amax) { amax = ax; mx = v[i]; }
-    }
-    // block amax and its first occurrence: amax is never negative or NaN, so its bits order like its
-    // value, and the lowest lane holding the maximum holds the first occurrence
-    const uint32_t key = __float_as_uint(amax);
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-    const int src = __ffs(__ballot_sync(0xffffffffu, key == kmax)) - 1;
-    mx = __shfl_sync(0xffffffffu, mx, src);
-    if (kmax == 0u) {  // zero block
-        uint32_t *o32 = reinterpret_cast<uint32_t *>(o);
-        for (int i = lane; i < kQ8KBytes / 4; i += 32) o32[i] = 0u;
-        return;
-    }
-    const float iscale = __fdiv_rn(-127.0f, mx);
-    int q[8];
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q[i] = q8k_code(__fmul_rn(iscale, v[i]));
-        sum += q[i];
-    }
-    uint32_t w0 = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
-    uint32_t w1 = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | ((uint32_t)(q[7] & 0xff) << 24);
-    uint32_t *qs = reinterpret_cast<uint32_t *>(o + 4 + lane * 8);
-    qs[0] = w0;
-    qs[1] = w1;
-    int pair = sum + __shfl_xor_sync(0xffffffffu, sum, 1);
-    if ((lane & 1) == 0) reinterpret_cast<int16_t *>(o + 260)[lane >> 1] = (int16_t)pair;
-    if (lane == 0) *reinterpret_cast<float *>(o) = __fdiv_rn(1.0f, iscale);
 }
 
 // One warp quantizes one 256-element block; lane l holds elements 8l..8l+7.

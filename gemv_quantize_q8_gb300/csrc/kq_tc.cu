@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "kq_q8k_block.cuh"
 #include "kq_sm100.cuh"
 #include "kq_tc.cuh"
 
@@ -113,7 +114,7 @@ struct TcLayout {
     static constexpr int H_OFF = EB_OFF + (C::EXT ? C::NE * 4096 : 0);
     static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * C::H_ROW;
     static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4 * C::BPS;
-    static constexpr int NBAR = 2 * NPAIR + 2 * 3 + 2 * 3 + 3 * 4 + 2 * 3 + 2;
+    static constexpr int NBAR = 2 * NPAIR + 2 * 3 + 2 * 3 + 3 * 4 + 2 * 3 + 2 + 4;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = MISC_OFF + 16;
     static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment of the base
@@ -143,6 +144,16 @@ struct TcParams {
     // tiles.  persistent: CTA b runs tiles b, b + gridDim.x, ...; otherwise CTA (x, y) runs tile
     // y*n_tiles + x alone (the split-K launch).
     int persistent, n_tiles, m_tiles;
+    // Fused SwiGLU -> Q8_K (swq != 0; routed gate/up weights: N = 2F rows per expert, gate rows [0, F),
+    // up rows [F, 2F)).  The scheduled unit is four tiles of one token tile: gate rows 256b..256b+255
+    // as two 128-row tiles, then the up rows of the same columns.  The epilogue parks the gate tiles
+    // in this CTA's slice of scr, replaces them by h = silu(gate)*up when the up tiles arrive (each
+    // thread meets its own gate values again), and after the fourth tile quantizes every token's 256
+    // h values into Q8_K block b of its pair's row of hq.  scr is rewritten by every unit, so it
+    // stays in L2; the fp32 gate/up rows never reach HBM.
+    int swq;
+    float *scr;    // [gridDim.x][2][TC_TOK][256] fp32 (units alternate halves)
+    uint8_t *hq;   // [pairs][F/256] Q8_K blocks
 };
 
 struct TcTile {
@@ -151,11 +162,13 @@ struct TcTile {
 
 // Geometry of tile `tile`: weight rows n0.., first panel row m0, stored token rows, first weight row
 // group, row groups present, and (grouped) the first pair-list entry.
+template <bool SWQ>
 __device__ __forceinline__ TcTile tc_tile(const TcParams &P, int tile, int m_tiles) {
     TcTile T;
     const int nt = tile % P.n_tiles, mt = tile / P.n_tiles;
     (void)m_tiles;
-    T.n0 = nt * TC_ROWS;
+    // fused SwiGLU units: weight-row tile nt = 4b + s is gate (s < 2) or up (s >= 2) half s & 1 of block b
+    T.n0 = SWQ ? ((nt & 2) ? P.N / 2 : 0) + 256 * (nt >> 2) + TC_ROWS * (nt & 1) : nt * TC_ROWS;
     T.valid_groups = min(8, (P.N + 15) / 16 - T.n0 / 16);
     if (P.grouped) {
         const int e = P.tiles[2 * mt], j = P.tiles[2 * mt + 1];
@@ -251,7 +264,9 @@ __device__ __forceinline__ void convert_q6k_sub(const uint32_t (&nib)[4], const 
     }
 }
 
-template <int DT>
+// SWQ: fused SwiGLU -> Q8_K epilogue (routed gate/up); a separate instantiation, so the plain GEMM's
+// register allocation is untouched by it.
+template <int DT, bool SWQ>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE, TcParams P) {
     using C = TcCfg<DT>;
@@ -274,6 +289,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t *h_full = e_empty + 3, *da_full = h_full + 4, *h_empty = da_full + 4;
     uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 3;
     uint64_t *mma_done = acc_empty + 3;  // one per MMA issuer
+    uint64_t *sw_bar = mma_done + 2;     // fused SwiGLU: the four epilogue warps of each token quarter
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 4);
 
@@ -283,14 +299,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int nsb = min(nchunk, sb0 + P.sb_per_split) - sb0;  // super-blocks per tile
     const int m_tiles = P.grouped ? *P.tile_count : P.m_tiles;
     const int ntiles = P.n_tiles * m_tiles;
-    const int tile0 = P.persistent ? (int)blockIdx.x : (int)(blockIdx.y * P.n_tiles + blockIdx.x);
-    const int tstride = P.persistent ? (int)gridDim.x : ntiles;
-    if (tile0 >= ntiles) return;  // no tile for this CTA: it leaves before any setup
+    // scheduled units: single tiles, or (fused SwiGLU) runs of four consecutive tiles
+    const int nunits = SWQ ? ntiles >> 2 : ntiles;
+    const int unit0 = P.persistent ? (int)blockIdx.x : (int)(blockIdx.y * P.n_tiles + blockIdx.x);
+    const int ustride = P.persistent ? (int)gridDim.x : nunits;
+    if (unit0 >= nunits) return;  // no tile for this CTA: it leaves before any setup
     // One step = one (tile, super-block); every role walks steps 0 .. nsteps-1 in the same order, so
     // the rings and accumulators run on across tile boundaries without draining.
-    const int nsteps = (ntiles - tile0 + tstride - 1) / tstride * nsb;
+    const int nsteps = (nunits - unit0 + ustride - 1) / ustride * (SWQ ? 4 : 1) * nsb;
     // roles keep (tile i, super-block t) counters along the steps instead of dividing by nsb
-    auto tile_of = [&](int i) { return tc_tile(P, tile0 + i * tstride, m_tiles); };
+    auto tile_of = [&](int i) {
+        return tc_tile<SWQ>(P, SWQ ? (unit0 + (i >> 2) * ustride) * 4 + (i & 3) : unit0 + i * ustride, m_tiles);
+    };
 
     if (tid == 0) {
         for (int i = 0; i < NPAIR; ++i) { mbar_init(&k_full[i], 32 * TC_CONV_WARPS + 1); mbar_init(&k_empty[i], 1); }
@@ -303,6 +323,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&sw_bar[i], 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -652,6 +673,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int row = 32 * q + lane;
         const uint32_t lane_base = tbase + ((uint32_t)(32 * q) << 16);
         bool ok = true;
+        // fused SwiGLU: the previous unit's h rows are quantized while the next unit runs, one token per
+        // warp per step, from the other half of this CTA's double-buffered scratch
+        int sw_u = 0;                 // units this warp has finished: the pending one is sw_u - 1
+        int pj = 0, pend = -1;        // pending unit: next token of this quarter, end (-1: none)
+        int plist = 0, pb = 0;        // its pair-list offset (token quarter included), its column block
+        bool pwait = true;            // its barrier phase has been waited for
+        auto swq_token = [&](int j) {  // quantize token j of the pending unit into its hq block
+            const float *hs = P.scr + ((int64_t)blockIdx.x * 2 + ((sw_u - 1) & 1)) * (TC_TOK * 256) + (tq * 32 + j) * 256;
+            const float4 *hv = reinterpret_cast<const float4 *>(hs) + 2 * lane;
+            const float4 h0 = hv[0], h1 = hv[1];
+            const float v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+            q8k_block_store(v, P.hq + ((int64_t)P.lists[plist + j] * (P.N / 512) + pb) * kQ8KBytes);
+        };
         for (int t = 0, ti = 0, tt = 0; t < nsteps && ok; ++t) {  // t: step
             const int buf = t & 1, h = t & 3;
             const int tile_i = ti;
@@ -742,8 +776,56 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive(&h_empty[h]);
             }
             }
+            if (SWQ && pend >= 0) {
+                // the accumulator is released; one token of the pending unit (after its four warps met)
+                if (!pwait) {
+                    if (!(ok = mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag))) break;
+                    pwait = true;
+                }
+                if (pj < pend) { swq_token(pj); pj += 4; }
+            }
             if (!last || P.nsplit != 1) continue;
             const TcTile T = tile_of(tile_i);
+            if (SWQ) {
+                // fused SwiGLU -> Q8_K.  Tile s of the unit holds column 128*(s & 1) + row of the block
+                // for this thread's 32 tokens: gate (s < 2) is parked, up (s >= 2) turns it into h.
+                const int s = tile_i & 3;
+                const int mrem = T.tok_valid - tq * 32;
+                float *sc = P.scr + ((int64_t)blockIdx.x * 2 + (sw_u & 1)) * (TC_TOK * 256) + tq * 32 * 256 +
+                            TC_ROWS * (s & 1) + row;
+                if (s < 2) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < mrem) sc[i * 256] = acc[i];
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {  // eight gate loads in flight, then their h
+                        float gv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) gv[i] = c + i < mrem ? sc[(c + i) * 256] : 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (c + i < mrem) sc[(c + i) * 256] = silu_mul(gv[i], acc[c + i]);
+                    }
+                }
+                if (s != 3) continue;
+                // finish the pending unit, then publish this one: its four warps' h columns complete
+                // every token's block once all four have arrived
+                if (pend >= 0) {
+                    if (!pwait && !(ok = mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag))) break;
+                    for (; pj < pend; pj += 4) swq_token(pj);
+                }
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sw_bar[tq]);
+                pj = q;
+                pend = max(0, min(32, mrem));
+                plist = T.list_base + tq * 32;
+                pb = (T.n0 - P.N / 2) >> 8;
+                pwait = false;
+                ++sw_u;
+                continue;
+            }
             if (T.n0 + row < P.N) {
                 // the tile's last super-block: store (a split-K tile is reduced across the cluster below)
                 const int mrem = T.tok_valid - tq * 32;
@@ -760,6 +842,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         if (i < mrem) yc[(int64_t)i * P.ldy] = acc[i];
                 }
             }
+        }
+        if (SWQ && ok && pend >= 0) {  // the last unit's tokens
+            if (pwait || mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag))
+                for (; pj < pend; pj += 4) swq_token(pj);
         }
     }
 
@@ -1031,6 +1117,8 @@ struct TcLaunch {
     unsigned long long *err;
     bool grouped;
     const int *tiles, *tile_count, *count, *offset, *poff, *lists;
+    uint8_t *hq;          // non-NULL: fused SwiGLU -> Q8_K output (grouped gate/up only), y unused
+    float *scr;           // its scratch: tc_swq_scratch_bytes()
 };
 
 template <int DT>
@@ -1078,16 +1166,22 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     p.n_tiles = (int)((a.N + TC_ROWS - 1) / TC_ROWS);
     p.m_tiles = a.m_tiles;
     p.persistent = S > 1 ? 0 : 1;
+    p.swq = a.hq ? 1 : 0;
+    p.hq = a.hq;
+    p.scr = a.scr;
+    if (p.swq && (S != 1 || !a.grouped || a.N % 512 || !a.scr))
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm (tensor core): fused SwiGLU needs a routed, unsplit launch");
     const int64_t tiles = (int64_t)p.n_tiles * a.m_tiles;
+    const int64_t units = p.swq ? tiles / 4 : tiles;
     if (tiles > 0x7fffffff) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: too many tiles");
-    auto kern = tc_gemm_kernel<DT>;
+    auto kern = p.swq ? tc_gemm_kernel<DT, true> : tc_gemm_kernel<DT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
     if (S > 1)
         cfg.gridDim = dim3((unsigned)p.n_tiles, (unsigned)a.m_tiles, (unsigned)S);
     else
-        cfg.gridDim = dim3((unsigned)std::min<int64_t>(tiles, sm_count()), 1, 1);  // one CTA per SM, tiles strided
+        cfg.gridDim = dim3((unsigned)std::min<int64_t>(units, sm_count()), 1, 1);  // one CTA per SM, units strided
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Lay::ALLOC;
     cfg.stream = st;
@@ -1148,6 +1242,9 @@ bool tc_grouped_eligible(kq_dtype wt, int64_t N, int64_t K) {
            N <= (1 << 22);
 }
 
+// Fused SwiGLU scratch: two 128-token x 256-column fp32 tiles per persistent CTA.
+size_t tc_swq_scratch_bytes() { return (size_t)sm_count() * 2 * TC_TOK * 256 * sizeof(float); }
+
 // Panels of the routed rows: f16 codes, (Q4_K/Q6_K) f16 bsums, f32 scales with one row per scale block
 // (256 elements for Q8_K activations, 32 for Q8_1).
 TcGroupedPanels tc_grouped_panels(kq_dtype wt, int64_t pairs, int64_t E, int64_t K) {
@@ -1168,7 +1265,7 @@ kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int 
                           int64_t pairs, int64_t E, int64_t N, int64_t K, float *y, uint8_t *panels,
                           const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,
                           const int *offset, const int *poff, const int *lists, const int *prow,
-                          unsigned long long *err, cudaStream_t st) {
+                          unsigned long long *err, uint8_t *hq, float *scr, cudaStream_t st) {
     const TcGroupedPanels G = tc_grouped_panels(wt, pairs, E, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || max_tiles > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: shape too large for the tensor-core grid");
@@ -1193,6 +1290,7 @@ kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int 
     a.err = err;
     a.grouped = true;
     a.tiles = tiles; a.tile_count = tile_count; a.count = count; a.offset = offset; a.poff = poff; a.lists = lists;
+    a.hq = hq; a.scr = scr;
     s = launch_tc_dt(wt, a, st);
     if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
     return s;

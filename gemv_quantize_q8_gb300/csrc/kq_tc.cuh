@@ -25,6 +25,9 @@ kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int 
                           int64_t pairs, int64_t E, int64_t N, int64_t K, float *y, uint8_t *panels,
                           const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,
                           const int *offset, const int *poff, const int *lists, const int *prow,
-                          unsigned long long *err, cudaStream_t st);
+                          unsigned long long *err, uint8_t *hq, float *scr, cudaStream_t st);
+// Scratch bytes of the fused SwiGLU -> Q8_K epilogue (hq != NULL above, N = 2F, F % 256 == 0): one
+// pair of 128 KB tiles per SM of the current device.
+size_t tc_swq_scratch_bytes();
 
 }  // namespace kq

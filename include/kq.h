@@ -201,6 +201,25 @@ KQ_API kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, 
                           const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y,
                           void *workspace, size_t ws_bytes, kq_stream_t stream);
 
+/* Routed gate/up GEMM with SwiGLU and Q8_K quantisation fused into its epilogue ([vllm-2890] "fuse
+ * silu-mul with Q8_K quant epilogue", moved from the quantizer into the routed GEMM).
+ * w: n_experts native gate/up weights repacked together as [n_experts*2F][K], each expert's gate rows
+ * [0, F) followed by its up rows [F, 2F).  ids, xq, xq_rows_per_token, M, top_k, K: as for
+ * kq_gemm_grouped.  hq: Q8_K [M][top_k][F/256] blocks of h = silu(gate)*up, where gate and up are the
+ * rows kq_gemm_grouped would write to y (N = 2F).  The result is byte-identical to kq_gemm_grouped
+ * followed by kq_swiglu_quantize_q8k(y, y + F, M*top_k, F, 2F, hq): each 128-token tile's gate and up
+ * values meet in an L2-resident scratch tile of the workspace and never reach device memory as fp32.
+ * F: a positive multiple of 256 (at most 2^21); K: a multiple of 256 up to 2^20; all four weight types.
+ * An id outside [0, n_experts) is skipped (its hq row is not written) and recorded in the workspace's
+ * device flag (kq_read_device_flag).  workspace: kq_gemm_grouped_swiglu_workspace_bytes(wt, M, F, K,
+ * n_experts, top_k) bytes, 256-byte aligned; the size depends on the current device's SM count. */
+KQ_API size_t kq_gemm_grouped_swiglu_workspace_bytes(kq_dtype wt, int64_t M, int64_t F, int64_t K, int64_t n_experts,
+                                                     int64_t top_k);
+KQ_API kq_status kq_gemm_grouped_swiglu_q8k(kq_dtype wt, const void *w, int64_t n_experts, const void *xq,
+                                            int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k,
+                                            int64_t F, int64_t K, void *hq, void *workspace, size_t ws_bytes,
+                                            kq_stream_t stream);
+
 /* kq_gemm_grouped without a workspace, for callers that cannot allocate device memory when they
  * run this layer (for example a plug-in that is handed only its input and output buffers, or code
  * that must not call cudaMalloc after start-up).  The pages have no counterpart to this entry
