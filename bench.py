@@ -279,6 +279,12 @@ def run_prefill(args, device, rank, world):
         per_case[f"{'q4_k' if dt == 1 else 'q6_k'}_{N}x{K}_m{M}"] = round(2.0 * M * N * K / (t * 1e-3) / 1e12, 2)
         del gc
 
+    # the step's 18 activation quantisations alone (excluded from the GEMM TOPS, reported beside them)
+    def quant_all():
+        for (M, dt, N, K) in cases:
+            kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)
+    quant_ms = _time_graph(quant_all, 5)
+
     # end to end through the C ABI with host buffers
     for _ in range(max(1, args.warmup // 2)):
         step_e2e()
@@ -307,7 +313,27 @@ def run_prefill(args, device, rank, world):
     h2d = sum(M * K * 4 for (M, _, _, K) in cases)
     d2h = sum(M * N * 4 for (M, _, N, _) in cases)
     return dict(ops=ops, ms=ms, gemm_ms=gemm_ms, per_case=per_case, clocks=clk, launches=launches,
-                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, cases=cases)
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, cases=cases, quant_ms=quant_ms)
+
+
+def int8_mma_sync_peak(device):
+    """Measured ceiling of the warp-level int8 tensor path (mma.sync s8), the legacy route to int8
+    MMAs on sm_103a: TOPS of the probe kernel, median of 5 timed launches after a warm-up."""
+    import torch
+
+    import gemv_quantize_q8_gb300 as kq
+    sink = torch.zeros(1, dtype=torch.int32, device=device)
+    kq.kq_probe_int8_mma_sync(2000, sink)
+    torch.cuda.synchronize()
+    ts, ops = [], 0.0
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ops = kq.kq_probe_int8_mma_sync(40000, sink)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return ops / (statistics.median(ts) * 1e-3) / 1e12
 
 
 def _time_graph(fn, reps, warmup=2):
@@ -646,9 +672,28 @@ def cpu_baseline(budget_s: float = 12.0):
         if dt_ * 2.2 > budget_s or m >= 64:
             break
         m *= 2
-    return {"value": ops / el / 1e12, "unit": "TOPS", "cores": threads, "kind": "oracle",
-            "sample": f"first {m} token rows of each of the 6 Q4_K/Q6_K prefill GEMMs, quantize included "
-                      f"({ops:.3g} int8 ops in {el:.2f} s)"}
+    out = {"value": ops / el / 1e12, "unit": "TOPS", "cores": threads, "kind": "oracle",
+           "sample": f"first {m} token rows of each of the 6 Q4_K/Q6_K prefill GEMMs, quantize included "
+                     f"({ops:.3g} int8 ops in {el:.2f} s)"}
+    # one thread, one token row of every prefill GEMM
+    t = time.perf_counter()
+    ops1 = 0.0
+    for (dt, N, K), w in ws.items():
+        oracle.gemm(dt, w, oracle.quantize_q8_k(x[:1, :K]), 1, N, K, threads=1)
+        ops1 += 2.0 * N * K
+    out["single_thread_value"] = ops1 / (time.perf_counter() - t) / 1e12
+    # the decode GEMVs in full (one call per shape, quantisation included), all threads: weight GB/s
+    el_d, wbytes = 0.0, 0
+    for cfg in synth.DECODE:
+        dt, N, K = cfg["dtype"], cfg["N"], cfg["K"]
+        w = synth.weights(dt, N, K, g)
+        xv = synth.activations(1, K, g)
+        t0 = time.perf_counter()
+        oracle.gemm(dt, w, oracle.quantize_q8_k(xv), 1, N, K, threads=threads)
+        el_d += time.perf_counter() - t0
+        wbytes += w.nbytes
+    out["decode_gemv_gbs"] = wbytes / el_d / 1e9
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -753,8 +798,15 @@ def main():
                          "kernel": "kq_gemm = activation-panel prologue + tcgen05 GEMM, 18 prefill GEMMs",
                          "peak_source": f"{src} bf16_tflops burst (f16 tensor rate = bf16 rate)"},
             "per_gemm_tops": res["per_case"],
+            "quantize_us_per_step": round(res["quant_ms"] * 1e3, 1),
             "clocks": res["clocks"],
         }
+        if not args.only:
+            p8 = int8_mma_sync_peak(device)
+            line["int8_mma_sync_peak"] = {
+                "tops": round(p8, 1), "value_over_peak": round(value / p8, 3),
+                "kq_gemm_over_peak": round(gemm_tops / p8, 3),
+                "source": "measured live: mma.sync m16n8k32 s8 on every SM, register operands, 32 warps per SM"}
         if decode is not None:
             hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
             line["decode_gemv"] = {"gbs": round(decode_gbs, 1), "frac_of_hbm": round(decode_gbs / hbm, 4),

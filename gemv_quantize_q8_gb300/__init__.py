@@ -63,6 +63,7 @@ _SIGS = {
     "kq_debug_partials": ([_I32, _P, _P, _I64, _I64, _I64, _P, _P], _I32),
     "kq_launch_count": ([ctypes.c_char_p], _I64),
     "kq_gemm_grouped_noalloc": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P], _I32),
+    "kq_probe_int8_mma_sync": ([_I64, _P, ctypes.POINTER(ctypes.c_double), _P], _I32),
     "kq_gemm_grouped_swiglu_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64, _I64], _SZ),
     "kq_gemm_grouped_swiglu_q8k": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _SZ, _P], _I32),
 }
@@ -198,6 +199,13 @@ def kq_gemm_grouped_noalloc(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top
     """kq_gemm_grouped for callers that cannot allocate: routing scratch is a fixed array inside the library."""
     _check(lib().kq_gemm_grouped_noalloc(wt, _ptr(w), n_experts, _ptr(xq), xq_rows_per_token, _ptr(ids), M, top_k,
                                          N, K, _ptr(y), _stream(stream)))
+
+
+def kq_probe_int8_mma_sync(iters, sink, stream=None) -> float:
+    """Launch the int8 mma.sync throughput probe; returns the int8 ops it issues (time it with events)."""
+    ops = ctypes.c_double(0.0)
+    _check(lib().kq_probe_int8_mma_sync(iters, _ptr(sink), ctypes.byref(ops), _stream(stream)))
+    return ops.value
 
 
 def kq_read_device_flag(workspace, stream=None) -> int:

@@ -237,6 +237,14 @@ KQ_API kq_status kq_gemm_grouped_noalloc(kq_dtype wt, const void *w, int64_t n_e
                                          int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k,
                                          int64_t N, int64_t K, float *y, kq_stream_t stream);
 
+/* Measurement aid, not on the hot path: the throughput ceiling of the warp-level int8 tensor path
+ * (mma.sync m16n8k32 s8 x s8 -> s32), the only integer MMA sm_103a code can issue.  Launches one kernel
+ * on `stream` in which every warp of 32 per SM issues `iters` x 4 independent MMAs on register
+ * operands; the caller times it (CUDA events around the call).  *ops (host) receives the int8 ops
+ * issued (2*16*8*32 per MMA).  sink: one int32 of device memory the kernel may write (keeps the work
+ * live).  Returns KQ_ERR_INVALID_ARG for iters <= 0 or NULL pointers. */
+KQ_API kq_status kq_probe_int8_mma_sync(int64_t iters, int32_t *sink, double *ops, kq_stream_t stream);
+
 /* Read (and clear) the device flag of a kq_gemm / kq_gemm_grouped workspace.  Synchronises `stream`.
  * Returns KQ_OK, KQ_ERR_DEVICE_FLAG (an invalid expert id was seen, or a tensor-core pipeline wait
  * timed out; the count is in *n_bad if non-NULL), or KQ_ERR_CUDA. */

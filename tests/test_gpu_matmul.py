@@ -480,3 +480,14 @@ def test_moe_block_full_size_sampled():
     ref_dn, _ = oracle.gemm_grouped(kq.Q6_K, w_dn, E, hq_ref, top_k, ids[toks], len(toks), top_k, H, F)
     assert _close(kq.Q6_K, host(y_dn)[toks], ref_dn)
     assert np.array_equal(host(out)[toks], oracle.moe_weighted_sum(host(y_dn)[toks], wts[toks]))
+
+
+def test_int8_mma_sync_probe_counts_its_ops():
+    # the measurement aid behind the bench's int8 ceiling: one launch, ops reported on the host
+    sink = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ops = kq.kq_probe_int8_mma_sync(10, sink)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert ops == sms * 4 * 8 * 10 * 4 * (2 * 16 * 8 * 32)
+    with pytest.raises(kq.KqError):
+        kq.kq_probe_int8_mma_sync(0, sink)
