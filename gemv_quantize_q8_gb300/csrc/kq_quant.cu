@@ -12,6 +12,7 @@
 // order.  Eight lanes own one 32-element block (4 elements each); the butterfly strides 16, 8, 4
 // cross lanes and strides 2, 1 stay inside a lane, which reproduces the 32-lane order exactly.
 #include "kq_q8k_block.cuh"
+#include "kq_sm100.cuh"
 
 namespace kq {
 
@@ -125,29 +126,49 @@ __global__ void quantize_q8_1_kernel(const float *__restrict__ x, const float *_
 }
 
 // Fused RMSNorm + Q8_K producer (vllm.cpp PR #2890, fused norm-quant epilogue: the norm row kernel
-// emits the row's Q8_K blocks beside its normalized output).  One block of 256 threads per row:
-//   ss = sum_i x_i^2 -- thread t adds x[t]^2, x[t+256]^2, ... in order, each warp combines its 32 sums
-//        in xor-butterfly order (strides 16 .. 1), thread 0 adds the 8 warp sums in order;
+// emits the row's Q8_K blocks beside its normalized output).  One block per row:
+//   ss = sum_i x_i^2 -- thread t < 256 adds x[t]^2, x[t+256]^2, ... in order, each of the first 8
+//        warps combines its 32 sums in xor-butterfly order (strides 16 .. 1), thread 0 adds the 8
+//        warp sums in order;
 //   r  = 1 / sqrt(ss / K + eps) (IEEE division and square root);  y_i = (x_i * r) * gamma_i;
-// then warp w quantises blocks w, w+8, ... of y with the standalone Q8_K body (and stores y when
+// then warp w quantises blocks w, w+NW, ... of y with the standalone Q8_K body (and stores y when
 // y_out != NULL).  Every operation is rounded on its own, so codes and y match the CPU oracle's.
-template <bool VEC>
-__global__ void __launch_bounds__(256) rmsnorm_q8k_kernel(const float *__restrict__ x, const float *__restrict__ gamma,
-                                                          float eps, int64_t K, int64_t ldx, uint8_t *__restrict__ out,
-                                                          float *__restrict__ y_out) {
+// With few rows (THREADS = 1024) the x and gamma values of each warp's first two blocks, which do not
+// depend on r, are loaded before the reduction, so a decode row pays one memory round trip for them;
+// with many rows (THREADS = 256) the rows in flight hide the latency and registers stay free.
+// The few-row launch allows programmatic dependent launch, as the decode GEMV does: gamma (a weight,
+// never written by the kernel before this one) is read before the dependency wait, x after it.
+template <bool VEC, int THREADS>
+__global__ void __launch_bounds__(THREADS) rmsnorm_q8k_kernel(const float *__restrict__ x, const float *__restrict__ gamma,
+                                                              float eps, int64_t K, int64_t ldx, uint8_t *__restrict__ out,
+                                                              float *__restrict__ y_out) {
+    constexpr int NW = THREADS / 32;
+    constexpr int PF = THREADS >= 1024 ? 2 : 0;  // blocks per warp loaded before the reduction
     __shared__ float wsum[8];
     __shared__ float rs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = blockIdx.x;
     const float *xr = x + row * ldx;
-    float s = 0.0f;
-    for (int64_t i = tid; i < K; i += 256) {
-        const float v = xr[i];
-        s = __fadd_rn(s, __fmul_rn(v, v));
-    }
+    const int64_t nb = K / 256;
+    float pv[PF > 0 ? PF : 1][8], pg[PF > 0 ? PF : 1][8];
+    if (PF > 0) sm100::grid_launch_dependents();
 #pragma unroll
-    for (int st = 16; st >= 1; st >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, st));
-    if (lane == 0) wsum[warp] = s;
+    for (int j = 0; j < PF; ++j)
+        if (warp + j * NW < nb) load8<VEC>(gamma + (warp + j * NW) * 256 + lane * 8, pg[j]);
+    if (PF > 0) sm100::grid_dependency_wait();
+#pragma unroll
+    for (int j = 0; j < PF; ++j)
+        if (warp + j * NW < nb) load8<VEC>(xr + (warp + j * NW) * 256 + lane * 8, pv[j]);
+    if (tid < 256) {
+        float s = 0.0f;
+        for (int64_t i = tid; i < K; i += 256) {
+            const float v = xr[i];
+            s = __fadd_rn(s, __fmul_rn(v, v));
+        }
+#pragma unroll
+        for (int st = 16; st >= 1; st >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, st));
+        if (lane == 0) wsum[warp] = s;
+    }
     __syncthreads();
     if (tid == 0) {
         float total = 0.0f;
@@ -157,11 +178,7 @@ __global__ void __launch_bounds__(256) rmsnorm_q8k_kernel(const float *__restric
     }
     __syncthreads();
     const float r = rs;
-    const int64_t nb = K / 256;
-    for (int64_t b = warp; b < nb; b += 8) {
-        float v[8], gv[8];
-        load8<VEC>(xr + b * 256 + lane * 8, v);
-        load8<VEC>(gamma + b * 256 + lane * 8, gv);
+    auto emit = [&](int64_t b, float (&v)[8], const float (&gv)[8]) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], r), gv[i]);
         if (y_out) {
@@ -170,6 +187,15 @@ __global__ void __launch_bounds__(256) rmsnorm_q8k_kernel(const float *__restric
             for (int i = 0; i < 8; ++i) yp[i] = v[i];
         }
         q8k_block_store(v, out + (row * nb + b) * kQ8KBytes);
+    };
+#pragma unroll
+    for (int j = 0; j < PF; ++j)
+        if (warp + j * NW < nb) emit(warp + j * NW, pv[j], pg[j]);
+    for (int64_t b = warp + PF * NW; b < nb; b += NW) {
+        float v[8], gv[8];
+        load8<VEC>(xr + b * 256 + lane * 8, v);
+        load8<VEC>(gamma + b * 256 + lane * 8, gv);
+        emit(b, v, gv);
     }
 }
 
@@ -250,8 +276,25 @@ kq_status kq_rmsnorm_quantize_q8k(const float *x, const float *gamma, float eps,
     const bool vec = aligned(x, 16) && aligned(gamma, 16) && ldx % 4 == 0 && (!y_out || aligned(y_out, 16));
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t *o = static_cast<uint8_t *>(xq);
-    if (vec) rmsnorm_q8k_kernel<true><<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ldx, o, y_out);
-    else rmsnorm_q8k_kernel<false><<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ldx, o, y_out);
+    // a few rows (decode): 32 warps per row so the Q8_K blocks are quantised in one round; many rows:
+    // 8 warps per row, several rows per SM
+    if (M <= 64) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)M, 1, 1);
+        cfg.blockDim = dim3(1024, 1, 1);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, rmsnorm_q8k_kernel<true, 1024>, x, gamma, eps, K, ldx, o, y_out)
+                            : cudaLaunchKernelEx(&cfg, rmsnorm_q8k_kernel<false, 1024>, x, gamma, eps, K, ldx, o, y_out);
+        if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
+    } else {
+        if (vec) rmsnorm_q8k_kernel<true, 256><<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ldx, o, y_out);
+        else rmsnorm_q8k_kernel<false, 256><<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ldx, o, y_out);
+    }
     kq_status s = check_launch(name);
     if (s == KQ_OK) count_launch(R_QUANT);
     return s;

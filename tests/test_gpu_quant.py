@@ -139,7 +139,8 @@ def _rmsnorm_gpu(x, gamma, eps, ld=None, with_y=True):
     return host(xq).reshape(M, -1), (host(y) if with_y else None)
 
 
-@pytest.mark.parametrize("M,K", [(1, 256), (1, 2560), (1, 9728), (3, 4096), (64, 2048), (5, 16384)])
+@pytest.mark.parametrize("M,K", [(1, 256), (1, 2560), (1, 9728), (3, 4096), (64, 2048), (5, 16384), (2, 24576),
+                                 (65, 1024), (70, 20480)])
 def test_rmsnorm_q8k_bit_exact(M, K):
     """Codes, scales, bsums and the normalized rows equal the oracle's byte for byte: the kernel's sum of
     squares follows the oracle's fixed reduction order and every other step is one IEEE operation."""
