@@ -40,10 +40,10 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # DRAM bytes (read + write) per tcgen05 GEMM launch, averaged over the 36 launches of two timed step
 # replays, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum).  Valid only for the
 # kernel sources it was taken on: reported as null once their hash differs.
-TC_TRAFFIC = {"bytes_per_launch": 64.92e6,
+TC_TRAFFIC = {"bytes_per_launch": 64.88e6,
               "sources": ("gemv_quantize_q8_gb300/csrc/kq_tc.cu", "gemv_quantize_q8_gb300/csrc/kq_sm100.cuh",
                           "gemv_quantize_q8_gb300/csrc/kq_q8k_block.cuh"),
-              "sha256": "4009c59bb0f22f59b60eb1a679f974f053bd70a1deb7dc301bfd990dd878f2a2"}
+              "sha256": "31589cf860193af5fb3f7ca3f92c74aefe4b0776c0af53de3828f2f47ea57884"}
 
 
 def max_over_ranks(vals, world, device=None):

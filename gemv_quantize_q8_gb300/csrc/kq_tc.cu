@@ -114,7 +114,7 @@ struct TcLayout {
     static constexpr int H_OFF = EB_OFF + (C::EXT ? C::NE * 4096 : 0);
     static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * C::H_ROW;
     static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4 * C::BPS;
-    static constexpr int NBAR = 2 * NPAIR + 2 * 3 + 2 * 3 + 3 * 4 + 2 * 3 + 2 + 4;
+    static constexpr int NBAR = 2 * NPAIR + 2 * 3 + 2 * 3 + 3 * 4 + 2 * 3 + 2 + 4 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = MISC_OFF + 16;
     static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment of the base
@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 3;
     uint64_t *mma_done = acc_empty + 3;  // one per MMA issuer
     uint64_t *sw_bar = mma_done + 2;     // fused SwiGLU: the four epilogue warps of each token quarter
+    uint64_t *s2_empty = sw_bar + 4;     // Q5_K: phase t completes once super-block t's min term is read
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 4);
 
@@ -324,6 +325,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
         for (int i = 0; i < 4; ++i) mbar_init(&sw_bar[i], 4);
+        mbar_init(s2_empty, TC_EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -420,7 +422,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // accumulators, so no ordering between the issuers is needed beyond the barriers.
         // Lean issue loop: descriptors are built once and stepped by adding to their address field,
         // one wait and one commit cover a pair of kblocks.  Q4_K's min-term tile is single: the
-        // extension MMA of super-block t waits until the epilogue is done with t-1.
+        // extension MMA of super-block t waits until the epilogue is done with t-1 (Q5_K: until it has
+        // read t-1's min term).
         if (lane == 0) {
             const int w = warp == TC_WARP_MMA ? 0 : 1;
             constexpr uint32_t idesc = idesc_f16_f32(TC_ROWS, TC_TOK);
@@ -480,7 +483,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (C::EXT) {
                     const int e = t % C::NE;
                     if (!(ok = mbar_wait_sleep(&e_full[e], (t / C::NE) & 1, abort_flag))) break;
-                    if (t > 0 && !(ok = mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) break;
+                    if (t > 0 && !(ok = C::Q5 ? mbar_wait_sleep(s2_empty, (t - 1) & 1, abort_flag)
+                                              : mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag)))
+                        break;
                     tc_fence_after();
                     mma_f16(tbase + C::TM_S2, dEA + (uint64_t)(e * (4096 >> 4)), dEB + (uint64_t)(e * (4096 >> 4)),
                             idesc, 0);
@@ -745,12 +750,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const float2 rs = reinterpret_cast<const float2 *>(sH + h * TC_ROWS * 8)[row];  // (d, -dmin)
             const float4 *dap = reinterpret_cast<const float4 *>(sDA + h * TC_TOK * 4) + tq * 8;
             const float2 dw2 = make_float2(rs.x, rs.x), nm2 = make_float2(rs.y, rs.y);
+            if (C::Q5) {
+                // Q5_K: the min-term tile is single and the next super-block's extension MMA waits for
+                // it, so it is read first, folded in as acc += da*(-dmin*S2) and released on its own
+                // barrier before the main accumulator (acc += da*(d*S1)).  With Q5_K's heavier
+                // conversion this takes the epilogue's second half off the chain that paces the steps
+                // (measured faster for Q5_K only; Q4_K reads both tiles together below).
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float s2[8];
+                    tmem_ld8(lane_base + C::TM_S2 + tq * 32 + c * 8, s2);
+                    tmem_wait_ld();
+                    const float4 da0 = dap[2 * c], da1 = dap[2 * c + 1];
+                    const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        float2 &a = *reinterpret_cast<float2 *>(&acc[c * 8 + i]);
+                        a = ffma2(fmul2(make_float2(s2[i], s2[i + 1]), nm2), make_float2(da[i], da[i + 1]), a);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s2_empty);
+            }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t col = tq * 32 + c * 8;
                 float s1[8], s2[8];
                 tmem_ld8(lane_base + buf * TC_TOK + col, s1);
-                if (C::EXT) tmem_ld8(lane_base + C::TM_S2 + col, s2);
+                if (C::EXT && !C::Q5) tmem_ld8(lane_base + C::TM_S2 + col, s2);
                 tmem_wait_ld();
                 const float4 da0 = dap[2 * c], da1 = dap[2 * c + 1];
                 const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
@@ -758,7 +786,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int i = 0; i < 8; i += 2) {
                     float2 &a = *reinterpret_cast<float2 *>(&acc[c * 8 + i]);
                     const float2 dap2 = make_float2(da[i], da[i + 1]);
-                    if (C::EXT) {
+                    if (C::Q5) {
+                        a = ffma2(fmul2(make_float2(s1[i], s1[i + 1]), dw2), dap2, a);  // acc += da*(d*S1)
+                    } else if (C::EXT) {
                         // acc += da * (d*S1 - dmin*S2)
                         const float2 u = fmul2(make_float2(s2[i], s2[i + 1]), nm2);
                         const float2 v = ffma2(make_float2(s1[i], s1[i + 1]), dw2, u);
