@@ -68,3 +68,17 @@ def test_host_validation_errors_without_gpu(built):
     st = L.kq_gemm_grouped(kq.Q4_K, 16, 4, 16, 1, 16, 8, 2, 256, 1024, 16, 256, 16, None)
     assert st == 4
     assert L.kq_status_string(6) == b"device reported invalid input"
+    # fused SwiGLU epilogue: F must be a positive multiple of 256, hq non-NULL (checked before any launch)
+    st = L.kq_gemm_grouped_swiglu_q8k(kq.Q4_K, 16, 4, 16, 1, 16, 8, 2, 128, 1024, 16, 16, 1 << 20, None)
+    assert st == 1 and b"multiple of 256" in L.kq_last_error()
+    st = L.kq_gemm_grouped_swiglu_q8k(kq.Q4_K, 16, 4, 16, 1, 16, 8, 2, 256, 1024, None, 16, 1 << 20, None)
+    assert st == 1 and b"null hq" in L.kq_last_error()
+    st = L.kq_gemm_grouped_swiglu_q8k(kq.Q8_K, 16, 4, 16, 1, 16, 8, 2, 256, 1024, 16, 16, 1 << 20, None)
+    assert st in (1, 2)
+    # RMSNorm producer: K a multiple of 256, eps finite and >= 0
+    st = L.kq_rmsnorm_quantize_q8k(16, 16, 1e-6, 1, 300, 300, 16, None, None)
+    assert st == 1
+    st = L.kq_rmsnorm_quantize_q8k(16, 16, -1.0, 1, 256, 256, 16, None, None)
+    assert st == 1 and b"eps" in L.kq_last_error()
+    # int8 probe: iters must be positive
+    assert L.kq_probe_int8_mma_sync(0, 16, None, None) == 1
