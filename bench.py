@@ -3,9 +3,11 @@
 
 Default workload ("prefill"): the six Q4_K/Q6_K weight shapes [4096x4096],
 [14336x4096], [4096x14336] at M = 128, 512 and 2048 tokens (18 GEMMs per
-step).  One step = for every (M, dtype, shape): quantise X[M, K] (fp32, N(0,1)
-with 1% x10 outliers) to Q8_K, then the GEMM Y = X . W^T.  `value` is the
-whole-step int8-equivalent throughput, sum(2*M*N*K) / step time, in TOPS.
+step).  One step = for every (M, dtype, shape): the GEMM Y = X . W^T from the
+fp32 rows X[M, K] (N(0,1) with 1% x10 outliers), quantised to Q8_K inside the
+GEMM's prologue (kq_gemm_f32; bit-identical to kq_quantize_q8k + kq_gemm).
+`value` is the whole-step int8-equivalent throughput, sum(2*M*N*K) / step time,
+in TOPS.
 
 The same JSON line carries the decode GEMV (M = 1, fused activation quant) on
 Q4_K [9728x2560], Q4_K [2560x9728] and Q6_K [2560x9728]: 1000 back-to-back
@@ -41,9 +43,8 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # replays, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum).  Valid only for the
 # kernel sources it was taken on: reported as null once their hash differs.
 TC_TRAFFIC = {"bytes_per_launch": 64.88e6,
-              "sources": ("gemv_quantize_q8_gb300/csrc/kq_tc.cu", "gemv_quantize_q8_gb300/csrc/kq_sm100.cuh",
-                          "gemv_quantize_q8_gb300/csrc/kq_q8k_block.cuh"),
-              "sha256": "31589cf860193af5fb3f7ca3f92c74aefe4b0776c0af53de3828f2f47ea57884"}
+              "sources": ("gemv_quantize_q8_gb300/csrc/kq_tc.cu", "gemv_quantize_q8_gb300/csrc/kq_sm100.cuh"),
+              "sha256": "fd66ae8097811b34ff92e0f2bb5c20698c8de0e6ff045b3ef43e6d6dbdc4d18d"}
 
 
 def max_over_ranks(vals, world, device=None):
@@ -63,13 +64,22 @@ def whole_job_tops(ops_per_rank, world, ms):
     return world * ops_per_rank / (ms * 1e-3) / 1e12
 
 
+TC_KERNEL_END = b"// Activation prologue: Q8_K rows"
+
+
 def tc_traffic():
+    """The recorded traffic while the GEMM kernel's sources are the ones it was measured on: the headers,
+    and kq_tc.cu up to the first prologue kernel (host code and the prologues after it do not enter
+    the tcgen05 kernel)."""
     import hashlib
     h = hashlib.sha256()
     root = os.path.dirname(os.path.abspath(__file__))
     for f in TC_TRAFFIC["sources"]:
         with open(os.path.join(root, f), "rb") as fh:
-            h.update(fh.read())
+            data = fh.read()
+        if f.endswith("kq_tc.cu"):
+            data = data.split(TC_KERNEL_END, 1)[0]
+        h.update(data)
     return TC_TRAFFIC["bytes_per_launch"] if h.hexdigest() == TC_TRAFFIC["sha256"] else None
 METRIC = "Q4_K/Q6_K GEMM int8 TOPS at prefill; GEMV weight GB/s vs HBM peak"
 
@@ -193,27 +203,28 @@ def run_prefill(args, device, rank, world):
     xq = torch.empty(max(kq.q8k_bytes(M, K) for (M, _, _, K) in cases), dtype=torch.uint8, device=device)
     ws_need = max(kq.gemm_workspace_bytes(dt, M, N, K) for (M, dt, N, K) in cases)
     ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=device)
+    # the step runs every GEMM from its fp32 activation rows: kq_gemm_f32 quantises them to Q8_K
+    # inside the GEMM's prologue (bit-identical to kq_quantize_q8k + kq_gemm, one launch fewer)
+    wsf_need = max(kq.kq_gemm_f32_workspace_bytes(dt, M, N, K) for (M, dt, N, K) in cases)
+    wsf = torch.zeros(wsf_need, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
     ops = sum(2.0 * M * N * K for (M, _, N, K) in cases)
 
-    def step(events=None):
-        for i, (M, dt, N, K) in enumerate(cases):
-            kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)           # X[:M, :K] (row stride Kmax)
-            if events is not None:
-                events[i][0].record(stream)
-            kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, y, N, ws, ws_need)
-            if events is not None:
-                events[i][1].record(stream)
+    def step():
+        for (M, dt, N, K) in cases:
+            # X[:M, :K] (row stride Kmax), quantised in the GEMM's prologue
+            kq.kq_gemm_f32(dt, weights[(dt, N, K)], x_dev, Kmax, M, N, K, y, N, wsf, wsf_need)
 
     # End to end as a serving loop runs it: every GEMM's activation comes from its own pinned host
     # buffer and its output goes back to one, each step.  Copies run on their own streams against
-    # double-buffered device buffers, ordered by events, so the copy engines overlap the kernels; the
+    # triple-buffered device buffers, ordered by events, so the copy engines overlap the kernels; the
     # whole step is one CUDA graph.
     max_x = max(M * K for (M, _, _, K) in cases)
     xh = [torch.from_numpy(np.ascontiguousarray(x_host[:M, :K]).reshape(-1)).pin_memory() for (M, _, _, K) in cases]
     yh = [torch.empty(M * N, dtype=torch.float32).pin_memory() for (M, _, N, _) in cases]
-    xbuf = [torch.empty(max_x, dtype=torch.float32, device=device) for _ in range(2)]
-    ybuf = [torch.empty(max_y, dtype=torch.float32, device=device) for _ in range(2)]
+    NB = 3  # device buffers per direction: the copies of GEMMs i+1, i+2 overlap GEMM i
+    xbuf = [torch.empty(max_x, dtype=torch.float32, device=device) for _ in range(NB)]
+    ybuf = [torch.empty(max_y, dtype=torch.float32, device=device) for _ in range(NB)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     nc = len(cases)
     ev_in, ev_q, ev_c, ev_out = ([torch.cuda.Event() for _ in range(nc)] for _ in range(4))
@@ -223,18 +234,17 @@ def run_prefill(args, device, rank, world):
         s_in.wait_stream(cs)
         s_out.wait_stream(cs)
         for i, (M, dt, N, K) in enumerate(cases):
-            b = i % 2
+            b = i % NB
             with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_q[i - 2])                  # buffer b no longer read by quantize
+                if i >= NB:
+                    s_in.wait_event(ev_q[i - NB])                 # buffer b no longer read
                 xbuf[b][:M * K].copy_(xh[i], non_blocking=True)   # host -> device, pinned
                 ev_in[i].record(s_in)
             cs.wait_event(ev_in[i])
-            if i >= 2:
-                cs.wait_event(ev_out[i - 2])                      # output buffer b copied out
-            kq.kq_quantize_q8k(xbuf[b], M, K, K, xq)
+            if i >= NB:
+                cs.wait_event(ev_out[i - NB])                     # output buffer b copied out
+            kq.kq_gemm_f32(dt, weights[(dt, N, K)], xbuf[b], K, M, N, K, ybuf[b], N, wsf, wsf_need)
             ev_q[i].record(cs)
-            kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, ybuf[b], N, ws, ws_need)
             ev_c[i].record(cs)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_c[i])
@@ -246,7 +256,7 @@ def run_prefill(args, device, rank, world):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    # The step (quantize + GEMM for every case) is captured once as a CUDA graph and replayed, as a
+    # The step (every case's GEMM from fp32 rows) is captured once as a CUDA graph and replayed, as a
     # serving loop would run a layer: the timed region then holds GPU work, not Python launch time.
     launches0 = kq.launch_count()
     g_step = torch.cuda.CUDAGraph()
@@ -320,7 +330,8 @@ def run_prefill(args, device, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    # the pipelined step computed what the plain one computes (last GEMM, bit for bit)
+    # the pipelined step (kq_gemm_f32 from the host rows) computed what kq_quantize_q8k + kq_gemm
+    # compute (last GEMM, bit for bit)
     M, dt, N, K = cases[-1]
     kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)
     kq.kq_gemm(dt, weights[(dt, N, K)], xq, M, N, K, y, N, ws, ws_need)

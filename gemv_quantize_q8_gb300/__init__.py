@@ -64,6 +64,8 @@ _SIGS = {
     "kq_launch_count": ([ctypes.c_char_p], _I64),
     "kq_gemm_grouped_noalloc": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P], _I32),
     "kq_probe_int8_mma_sync": ([_I64, _P, ctypes.POINTER(ctypes.c_double), _P], _I32),
+    "kq_gemm_f32_workspace_bytes": ([_I32, _I64, _I64, _I64], _SZ),
+    "kq_gemm_f32": ([_I32, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I32),
     "kq_gemm_grouped_swiglu_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64, _I64], _SZ),
     "kq_gemm_grouped_swiglu_q8k": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _SZ, _P], _I32),
 }
@@ -176,6 +178,16 @@ def kq_gemv(wt, w, x, xq, N, K, y, stream=None):
 
 def kq_gemm(wt, w, xq, M, N, K, y, ldy, workspace=None, ws_bytes=0, stream=None):
     _check(lib().kq_gemm(wt, _ptr(w), _ptr(xq), M, N, K, _ptr(y), ldy, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def kq_gemm_f32_workspace_bytes(wt, M, N, K) -> int:
+    return int(lib().kq_gemm_f32_workspace_bytes(wt, M, N, K))
+
+
+def kq_gemm_f32(wt, w, x, ldx, M, N, K, y, ldy, workspace, ws_bytes, stream=None):
+    """kq_gemm from fp32 rows: the activation quantiser runs inside the GEMM's prologue."""
+    _check(lib().kq_gemm_f32(wt, _ptr(w), _ptr(x), ldx, M, N, K, _ptr(y), ldy, _ptr(workspace), ws_bytes,
+                             _stream(stream)))
 
 
 def kq_gemm_grouped(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K, y, workspace, ws_bytes,

@@ -8,6 +8,8 @@
 // order -- and the result -- is deterministic.
 #include <mutex>
 
+#include <algorithm>
+
 #include "kq_internal.cuh"
 #include "kq_mmq_exact.cuh"
 #include "kq_tc.cuh"
@@ -407,6 +409,43 @@ kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t
     const int64_t gy = (M + kTileM - 1) / kTileM;
     if (gy > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: M=%lld too large", (long long)M);
     return launch_mmq_exact(wt, 0, false, a, (unsigned)gy, st);
+}
+
+size_t kq_gemm_f32_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % 256) return 0;
+    // kq_gemm's workspace first (at least the 256-byte header holding the device flag, so
+    // kq_read_device_flag applies), then room for the quantised rows, which the paths other than the
+    // tensor-core prologue need
+    const size_t g = std::max<size_t>(256, (kq_gemm_workspace_bytes(wt, M, N, K, 0, 0) + 255) & ~(size_t)255);
+    const size_t xq = wt == KQ_Q8_0 ? (size_t)M * (K / 32) * kQ81Bytes : (size_t)M * (K / 256) * kQ8KBytes;
+    return g + xq;
+}
+
+kq_status kq_gemm_f32(kq_dtype wt, const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                      float *y, int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream) {
+    kq_status s = check_matmul_args("kq_gemm_f32", wt, w, x, M, N, K);
+    if (s != KQ_OK) return s;
+    if (!y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_f32: null y");
+    if (ldy < N || ldx < K)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_f32: ldy %lld < N %lld or ldx %lld < K %lld", (long long)ldy,
+                    (long long)N, (long long)ldx, (long long)K);
+    if (!aligned(y, 4)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm_f32: y must be 4-byte aligned");
+    const size_t need = kq_gemm_f32_workspace_bytes(wt, M, N, K);
+    if (!workspace || ws_bytes < need)
+        return fail(KQ_ERR_WORKSPACE, "kq_gemm_f32: workspace of %zu bytes needed, %zu given", need,
+                    workspace ? ws_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm_f32: workspace must be 256-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (wt != KQ_Q8_0 && tc_eligible(wt, M, N, K))
+        return tc_gemm_f32(wt, static_cast<const uint8_t *>(w), x, ldx, M, N, K, y, ldy, ws, st);
+    // other paths: quantise into the workspace's tail, then the plain GEMM
+    const size_t gneed = kq_gemm_workspace_bytes(wt, M, N, K, 0, 0);
+    const size_t g = std::max<size_t>(256, (gneed + 255) & ~(size_t)255);
+    uint8_t *xq = ws + g;
+    s = wt == KQ_Q8_0 ? kq_quantize_q8_1(x, M, K, ldx, xq, stream) : kq_quantize_q8k(x, M, K, ldx, xq, stream);
+    if (s != KQ_OK) return s;
+    return kq_gemm(wt, w, xq, M, N, K, y, ldy, gneed ? workspace : nullptr, gneed, stream);
 }
 
 kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,

@@ -1,9 +1,10 @@
 // kq_q8k_block.cuh -- the Q8_K block arithmetic shared by every kernel that writes Q8_K rows.
 //
-// silu_mul is the SwiGLU element h = silu(g)*u; q8k_block_store quantizes one 256-element block
-// held by a warp.  The standalone and SwiGLU quantizers, the RMSNorm producer and the routed
-// gate/up GEMM's fused SwiGLU epilogue all call these, so the blocks they write are
-// byte-identical by construction.
+// silu_mul is the SwiGLU element h = silu(g)*u; q8k_block_codes quantizes one 256-element block
+// held by a warp and q8k_block_store writes it as Q8_K bytes.  The standalone and SwiGLU quantizers,
+// the RMSNorm producer, the routed gate/up GEMM's fused SwiGLU epilogue and the fp32-input GEMM's
+// prologue (codes straight into the tensor-core panel) all call these, so their blocks are identical
+// by construction.
 #pragma once
 #include "kq_internal.cuh"
 
@@ -23,10 +24,10 @@ __device__ __forceinline__ int q8k_code(float p) {
     return __float2int_rn(p);
 }
 
-// The Q8_K block body.  One warp, lane l holding elements 8l..8l+7 of the block; o: the 292-byte
-// block (f32 d, int8 q[256], int16 bsums[16]).
-__device__ __forceinline__ void q8k_block_store(const float (&v)[8], uint8_t *__restrict__ o) {
-    const int lane = threadIdx.x & 31;
+// The Q8_K block arithmetic.  One warp, lane l holding elements 8l..8l+7 of the block: q receives
+// lane l's eight codes, pair the sum of the codes of lanes l and l^1 (bsum l/2 of the block, valid
+// on even lanes) and d the block scale.  An all-zero (or all-NaN) block gives q = 0, pair = 0, d = 0.
+__device__ __forceinline__ void q8k_block_codes(const float (&v)[8], int (&q)[8], int &pair, float &d) {
     // lane-local ascending scan, first occurrence wins (strict >)
     float amax = 0.0f, mx = 0.0f;
 #pragma unroll
@@ -41,26 +42,36 @@ __device__ __forceinline__ void q8k_block_store(const float (&v)[8], uint8_t *__
     const int src = __ffs(__ballot_sync(0xffffffffu, key == kmax)) - 1;
     mx = __shfl_sync(0xffffffffu, mx, src);
     if (kmax == 0u) {  // zero block
-        uint32_t *o32 = reinterpret_cast<uint32_t *>(o);
-        for (int i = lane; i < kQ8KBytes / 4; i += 32) o32[i] = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0;
+        pair = 0;
+        d = 0.0f;
         return;
     }
     const float iscale = __fdiv_rn(-127.0f, mx);
-    int q[8];
     int sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         q[i] = q8k_code(__fmul_rn(iscale, v[i]));
         sum += q[i];
     }
+    pair = sum + __shfl_xor_sync(0xffffffffu, sum, 1);
+    d = __fdiv_rn(1.0f, iscale);
+}
+
+// The 292-byte Q8_K block (f32 d, int8 q[256], int16 bsums[16]) of the warp's 256 values at o.
+__device__ __forceinline__ void q8k_block_store(const float (&v)[8], uint8_t *__restrict__ o) {
+    const int lane = threadIdx.x & 31;
+    int q[8], pair;
+    float d;
+    q8k_block_codes(v, q, pair, d);
     uint32_t w0 = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
     uint32_t w1 = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | ((uint32_t)(q[7] & 0xff) << 24);
     uint32_t *qs = reinterpret_cast<uint32_t *>(o + 4 + lane * 8);
     qs[0] = w0;
     qs[1] = w1;
-    int pair = sum + __shfl_xor_sync(0xffffffffu, sum, 1);
     if ((lane & 1) == 0) reinterpret_cast<int16_t *>(o + 260)[lane >> 1] = (int16_t)pair;
-    if (lane == 0) *reinterpret_cast<float *>(o) = __fdiv_rn(1.0f, iscale);
+    if (lane == 0) *reinterpret_cast<float *>(o) = d;
 }
 
 }  // namespace kq

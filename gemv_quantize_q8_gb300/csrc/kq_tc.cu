@@ -946,6 +946,43 @@ __global__ void act_panel_kernel(const uint8_t *__restrict__ xq, int M, int M_pa
     if (lane == 0) D[(int64_t)sb * M_pad + m] = d;
 }
 
+// Activation prologue straight from fp32 rows (kq_gemm_f32): each warp quantises one 256-element
+// block of row m with the Q8_K block arithmetic (q8k_block_codes, the standalone quantizer's) and
+// writes the codes, the 16 bsums and d into the panels as act_panel_kernel would from the Q8_K block
+// -- the same panels, without the Q8_K round trip through memory.  One warp per (row, super-block);
+// rows past M are zero.  Also clears the workspace's device flag.
+template <bool VEC>
+__global__ void act_panel_f32_kernel(const float *__restrict__ x, int64_t ldx, int M, int M_pad, int nsb,
+                                     __half *__restrict__ A, __half *__restrict__ E, float *__restrict__ D,
+                                     unsigned long long *__restrict__ err) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (int64_t)M_pad * nsb) return;
+    const int m = (int)(wid / nsb), sb = (int)(wid % nsb);
+    const int64_t K = (int64_t)nsb * 256;
+    int q[8] = {0, 0, 0, 0, 0, 0, 0, 0}, pair = 0;
+    float d = 0.0f;
+    if (m < M) {
+        const float *p = x + (int64_t)m * ldx + sb * 256 + lane * 8;
+        float v[8];
+        if (VEC) {
+            const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = p[i];
+        }
+        q8k_block_codes(v, q, pair, d);
+    }
+    __half hv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hv[i] = __int2half_rn(q[i]);
+    *reinterpret_cast<uint4 *>(A + (int64_t)m * K + sb * 256 + lane * 8) = *reinterpret_cast<uint4 *>(hv);
+    if ((lane & 1) == 0) E[(int64_t)m * nsb * 16 + sb * 16 + (lane >> 1)] = __int2half_rn(pair);
+    if (lane == 0) D[(int64_t)sb * M_pad + m] = d;
+}
+
 // Activation prologue for Q8_0 weights: Q8_1 rows -> f16 code panel [M_pad][K] and f32 scale panel
 // [K/32][M_pad] (the f16 block scale widened); rows past M are zero.  One warp per (row, 256
 // elements): lane l takes elements 8l .. 8l+7 of block l/4.  Also clears the workspace's device flag.
@@ -1236,14 +1273,24 @@ static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st) {
     }
 }
 
-kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
-                  int64_t ldy, uint8_t *workspace, cudaStream_t st) {
+// The tensor-core GEMM from quantised rows xq, or (xf != NULL, Q4_K/Q5_K/Q6_K) from fp32 rows xf of
+// stride ldx quantised to Q8_K inside the prologue.
+static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, const float *xf, int64_t ldx, int64_t M,
+                              int64_t N, int64_t K, float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st) {
     const TcWs L = tc_ws(wt, M, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || L.M_pad / TC_TOK > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm: shape too large for the tensor-core grid");
     const int64_t nsb = K / 256;
     const int64_t warps = (int64_t)L.M_pad * nsb;
-    if (wt == KQ_Q8_0)
+    if (xf) {
+        if (wt == KQ_Q8_0) return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_f32: Q8_0 weights take Q8_1 activations");
+        const bool vec = (reinterpret_cast<uintptr_t>(xf) & 15) == 0 && ldx % 4 == 0;
+        auto kern = vec ? act_panel_f32_kernel<true> : act_panel_f32_kernel<false>;
+        kern<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+            xf, ldx, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
+            reinterpret_cast<__half *>(workspace + L.off_e), reinterpret_cast<float *>(workspace + L.off_d),
+            reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
+    } else if (wt == KQ_Q8_0)
         act_panel_q81_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
             xq, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
             reinterpret_cast<float *>(workspace + L.off_d), reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
@@ -1263,6 +1310,16 @@ kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, i
     s = launch_tc_dt(wt, a, st);
     if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
     return s;
+}
+
+kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
+                  int64_t ldy, uint8_t *workspace, cudaStream_t st) {
+    return tc_gemm_impl(wt, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st);
+}
+
+kq_status tc_gemm_f32(kq_dtype wt, const uint8_t *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                      float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st) {
+    return tc_gemm_impl(wt, w, nullptr, x, ldx, M, N, K, y, ldy, workspace, st);
 }
 
 // ---- routed experts on the tensor cores

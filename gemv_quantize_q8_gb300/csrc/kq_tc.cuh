@@ -10,6 +10,10 @@ bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, uint8_t *workspace, cudaStream_t st);
+// The same GEMM from fp32 activation rows (stride ldx), quantised to Q8_K inside the prologue with the
+// standalone quantizer's arithmetic (Q4_K, Q5_K, Q6_K weights).
+kq_status tc_gemm_f32(kq_dtype wt, const uint8_t *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                      float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st);
 
 // Routed experts on the tensor cores: 128-row tiles of each expert's routed rows (a tile table built
 // by the routing pass), activation panels gathered in routed order, outputs scattered back to their

@@ -184,6 +184,20 @@ KQ_API size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t
 KQ_API kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream);
 
+/* kq_gemm from fp32 activations, with the activation quantizer moved into the GEMM that consumes it
+ * ([vllm-2890]: a standalone quantizer launch costs a noticeable share of a step, so it belongs in its
+ * consumer): x is fp32 [M][ldx] (ldx >= K, 4-byte aligned).  On the tensor-core
+ * path (Q4_K/Q5_K/Q6_K weights, M >= 9, N >= 128) the prologue quantises each 256-element block with
+ * the Q8_K quantizer's own arithmetic and writes the codes, bsums and scale straight into the GEMM's
+ * f16 panels, so the Q8_K rows never travel through memory and one launch is saved; on the other paths
+ * x is quantised into the workspace (Q8_K, or Q8_1 for Q8_0 weights) and kq_gemm runs on it.  Either
+ * way y is bit-identical to kq_quantize_q8k (or kq_quantize_q8_1) followed by kq_gemm.
+ * workspace: kq_gemm_f32_workspace_bytes(wt, M, N, K) bytes, 256-byte aligned; it begins with
+ * kq_gemm's workspace, so kq_read_device_flag applies to it. */
+KQ_API size_t kq_gemm_f32_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K);
+KQ_API kq_status kq_gemm_f32(kq_dtype wt, const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                             float *y, int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream);
+
 /* Routed-expert GEMM (MUL_MAT_ID; [llama-18] routed-compact MMQ and per-expert tile width).
  * w: n_experts native weights, repacked together as one [n_experts*N][K] matrix (N % 16 == 0).
  * ids: int32 [M][top_k] expert of each (token, slot).  xq: activation rows; xq_rows_per_token = 1
