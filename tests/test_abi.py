@@ -80,5 +80,14 @@ def test_host_validation_errors_without_gpu(built):
     assert st == 1
     st = L.kq_rmsnorm_quantize_q8k(16, 16, -1.0, 1, 256, 256, 16, None, None)
     assert st == 1 and b"eps" in L.kq_last_error()
+    # fp32-input GEMM: ldx >= K, a supported weight type, a workspace of the size it asks for
+    st = L.kq_gemm_f32(kq.Q4_K, 16, 16, 1000, 160, 256, 1024, 16, 256, 16, 1 << 30, None)
+    assert st == 1 and b"ldx" in L.kq_last_error()
+    st = L.kq_gemm_f32(kq.Q8_K, 16, 16, 1024, 160, 256, 1024, 16, 256, 16, 1 << 30, None)
+    assert st == 2
+    need = L.kq_gemm_f32_workspace_bytes(kq.Q4_K, 160, 256, 1024)
+    assert need >= 256 + 160 * 4 * 292
+    st = L.kq_gemm_f32(kq.Q4_K, 16, 16, 1024, 160, 256, 1024, 16, 256, 256, need - 1, None)
+    assert st == 4
     # int8 probe: iters must be positive
     assert L.kq_probe_int8_mma_sync(0, 16, None, None) == 1
