@@ -286,8 +286,9 @@ ORC_API void orc_quantize_q8_k(const float *x, int64_t M, int64_t K, int64_t ldx
 
 /* Sum of 32 values in xor-butterfly order: at each stride (16, 8, 4, 2, 1)
  * every slot i becomes p[i] + p[i ^ stride]; the result is slot 0.
- * Parity: self-consistent only (the order is a definition); its value is
- * bounded against an exact sum in the tests. */
+ * Parity pinned: bounded against an exact sum, and the stride order by inputs
+ * whose large parts cancel exactly only at the right stage (the sum is then a
+ * closed-form exact value that a differently ordered tree misses). */
 static float butterfly_sum32(const float *v) {
     float p[32], t[32];
     for (int i = 0; i < 32; ++i) p[i] = v[i];

@@ -268,6 +268,41 @@ def test_q8_1_bounds_zero_block_and_sum():
             assert abs(float(s16) - exact) <= bound + abs(float(s16)) * 2.0 ** -11
 
 
+def test_q8_1_block_sum_follows_the_butterfly_order():
+    """Pins the order of the Q8_1 block sum s without restating it.  x_i = B*sign_i + r_i with the sign
+    taken from one index bit and B = 2**(21 - k): in the xor-butterfly order (strides 16, 8, 4, 2, 1)
+    the slots paired before stage k share a sign, so their large parts stay at or below 2**21 (every
+    partial sum exact), and stage k cancels them exactly; s is then exactly the sum of the small parts
+    r_i (multiples of 1/4), known in closed form.  An order that pairs one more same-sign bit first has
+    to hold 2**22 and loses the quarter bits: the butterfly with stages k and k+1 swapped misses the
+    exact value, checked below so the pin can fail.  The GPU quantizer is compared with the oracle byte
+    for byte, so this pins its order too."""
+    g = np.random.default_rng(81)
+    strides = [16, 8, 4, 2, 1]
+
+    def xor_tree(x, order):  # a differently ordered tree, only to show the construction separates orders
+        p = x.astype(np.float32)
+        for st in order:
+            p = (p + p[np.arange(32) ^ st]).astype(np.float32)
+        return float(p[0])
+
+    wrong = [0] * 4
+    for k, st in enumerate(strides):                  # stage k of the butterfly pairs indices i, i ^ st
+        B = 2.0 ** (21 - k)
+        sign = np.array([-1.0 if i & st else 1.0 for i in range(32)])
+        for _ in range(16):
+            r = g.integers(-8, 9, 32) * 0.25
+            x64 = B * sign + r
+            x = x64.astype(np.float32)
+            assert np.array_equal(x.astype(np.float64), x64)        # every input exactly representable
+            s16 = oracle.quantize_q8_1(x[None, :])[0][2:4].view(np.float16)[0]
+            assert float(s16) == r.sum(), (k, float(s16), r.sum())  # exact: large parts cancel at stage k
+            if k < 4:
+                swapped = strides[:k] + [strides[k + 1], strides[k]] + strides[k + 2:]
+                wrong[k] += xor_tree(x, swapped) != r.sum()
+    assert all(w > 0 for w in wrong), wrong
+
+
 def test_q8_1_roundf_half_away():
     # amax = 127 -> d = 1 exactly; x = 2.5 -> roundf gives 3 (half away from zero), -0.5 -> -1
     x = np.zeros((1, 32), dtype=np.float32)
