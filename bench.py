@@ -677,7 +677,7 @@ def run_decode_batched(device, calls=200):
     return out
 
 
-def cpu_baseline(budget_s: float = 12.0):
+def cpu_baseline(budget_s: float = 12.0, extras: bool = True):
     """The CPU oracle as it stands, all host threads, on a bounded sample of the prefill workload:
     the first `m` token rows of every (dtype, shape) GEMM (quantisation included)."""
     import oracle
@@ -703,6 +703,8 @@ def cpu_baseline(budget_s: float = 12.0):
     out = {"value": ops / el / 1e12, "unit": "TOPS", "cores": threads, "kind": "oracle",
            "sample": f"first {m} token rows of each of the 6 Q4_K/Q6_K prefill GEMMs, quantize included "
                      f"({ops:.3g} int8 ops in {el:.2f} s)"}
+    if not extras:
+        return out
     # one thread, one token row of every prefill GEMM
     t = time.perf_counter()
     ops1 = 0.0
@@ -730,9 +732,9 @@ def run_reference(args, rank, world):
         return
     vals = []
     for _ in range(args.warmup):
-        cpu_baseline(budget_s=4.0)
+        cpu_baseline(budget_s=4.0, extras=False)
     for _ in range(args.steps):
-        vals.append(cpu_baseline(budget_s=4.0))
+        vals.append(cpu_baseline(budget_s=4.0, extras=False))
     v = statistics.median(b["value"] for b in vals)
     last = vals[-1]
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS", "n_gpus": args.gpus,
