@@ -1,7 +1,7 @@
 /*
  * kq.h -- C ABI of the keep-quant int8 matmul library for GB300 (sm_103a).
  *
- * Block-quantised weights (Q4_K, Q6_K, Q8_0) stay packed in device memory;
+ * Block-quantised weights (Q4_K, Q5_K, Q6_K, Q8_0) stay packed in device memory;
  * activations are quantised on the fly to Q8_K (256-element blocks) or Q8_1
  * (32-element blocks) and multiplied with integer dot products, scaled into
  * fp32.  Sources of the operations (prose descriptions on three pages):
@@ -35,6 +35,10 @@
  *        scales and mins (8 each), 128 bytes of 4-bit codes; element 64c+l is
  *        the low nibble and 64c+32+l the high nibble of code byte 32c+l.
  *        x = d*sc_j*c - dmin*m_j, j = sub-block of 32.
+ *   Q5_K (176 B / 256): f16 d, f16 dmin, the 12 Q4_K scale/min bytes, qh[32]
+ *        (high code bits), 128 bytes of 4-bit codes in the Q4_K arrangement;
+ *        element 64c+l takes bit 2c of qh[l] and 64c+32+l bit 2c+1 as its
+ *        fifth bit (c = 0..31); x = d*sc_j*c - dmin*m_j.
  *   Q6_K (210 B / 256): ql[128], qh[64], int8 scales[16], f16 d;
  *        x = d*sc_j*(c - 32), j = sub-block of 16.
  *   Q8_0 (34 B / 32):   f16 d, int8 w[32]; x = d*w.
@@ -54,6 +58,8 @@
  *        Q4_K); high 2 code bits [kb][16][16 B] (byte j: elements 64kb+j,
  *        +16+j, +32+j, +48+j in bits 0-1, 2-3, 4-5, 6-7); int8 scales
  *        [16][16]; f16 d [16].
+ *   Q5_K chunk (2816 B): the Q4_K chunk, then each row's 32 high-bit bytes
+ *        [16][32 B] (canonical order).
  *   Q8_0 chunk (4352 B): codes [kb][16][64 B]; f16 d [16][8].
  * Every chunk starts on a 16-byte boundary when the buffer does.
  */
@@ -111,7 +117,7 @@ KQ_API int64_t kq_native_bytes(kq_dtype dtype, int64_t N, int64_t K);
  * (w_native, kq_native_bytes bytes, 16-byte aligned).  This is the stage-once step of the keep-quant
  * provider ([vllm-2890], keep-quant provider commit: weights are staged once and dispatched many
  * times).  For routed experts, repack [E*N][K] at once: with N a multiple of 16 each expert's rows
- * stay in their own row groups.  Padding rows are written as zeros.  Dtypes: Q4_K, Q6_K, Q8_0. */
+ * stay in their own row groups.  Padding rows are written as zeros.  Dtypes: Q4_K, Q5_K, Q6_K, Q8_0. */
 KQ_API kq_status kq_repack_weights(kq_dtype dtype, const void *w_canon, void *w_native, int64_t N, int64_t K,
                             kq_stream_t stream);
 
@@ -172,11 +178,12 @@ KQ_API size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t
  * by every warp).  Y[m][n] = sum_sb blockdot(W row n, X row m):
  *   Q4_K x Q8_K: per super-block d_a*(d_w*sum_j sc_j*P_j - dmin*sum_j m_j*(bs_2j + bs_2j+1)),
  *                P_j = sum of c*q over sub-block j (32 elements)
+ *   Q5_K x Q8_K: the Q4_K formula over the 5-bit codes c
  *   Q6_K x Q8_K: per super-block d_a*d_w*sum_j sc_j*P_j, P_j = sum of (c-32)*q over 16 elements
  *   Q8_0 x Q8_1: per 32-block d_w*d_a*P_b
  * w: native [N][K]; xq: M activation rows (Q8_K or Q8_1 per wt); y: fp32 rows of stride ldy >= N.
  * Paths: M <= 8 (batched decode) the weight-streaming GEMV kernel, bit-exact with the sequential CPU
- * order; M >= 9 with N >= 128 the tensor-core kernel (Q8_0 bit-exact; Q4_K/Q6_K integer parts exact,
+ * order; M >= 9 with N >= 128 the tensor-core kernel (Q8_0 bit-exact; Q4_K/Q5_K/Q6_K integer parts exact,
  * fp32 promotion fused, NMSE ~1e-14); otherwise, or when a shape does not fit the GEMV kernel, the
  * exact dp4a kernel.
  * workspace: device buffer of at least kq_gemm_workspace_bytes(wt, M, N, K, 0, 0) bytes (may be
@@ -203,8 +210,8 @@ KQ_API kq_status kq_gemm_f32(kq_dtype wt, const void *w, const float *x, int64_t
  * ids: int32 [M][top_k] expert of each (token, slot).  xq: activation rows; xq_rows_per_token = 1
  * ("broadcast": slot (t,k) reads row t) or top_k ("per-row": slot (t,k) reads row t*top_k+k).
  * y: fp32 [M][top_k][N]; y[t][k] = W_{ids[t][k]} . X_row.  Rows are gathered per expert in
- * (token, slot) order, so the result is deterministic.  All three weight types run on the tensor
- * cores in 128-row tiles of each expert's rows with exact integer parts; Q4_K and Q6_K promote to fp32
+ * (token, slot) order, so the result is deterministic.  All four weight types run on the tensor
+ * cores in 128-row tiles of each expert's rows with exact integer parts; Q4_K, Q5_K and Q6_K promote to fp32
  * with fused multiply-adds (outputs match the sequential CPU order to within rounding, not bit for
  * bit), Q8_0 adds every 32-block's scaled dot in the CPU order (bit-exact).  An id outside
  * [0, n_experts) is skipped
