@@ -588,6 +588,26 @@ def test_q8_k_half_way_ties_go_to_even():
 # ----------------------------------------------------------------------------- RMSNorm producer
 
 
+def test_rmsnorm_sum_of_squares_order():
+    """Pins the order of the sum of squares (thread t adds x[t]^2, x[t+256]^2, ... in sequence) with a
+    closed form: x[0] = 4096, x[256] = x[512] = 1, the rest 0, K = 768.  Thread 0 adds 2^24 + 1, which
+    rounds to 2^24 (a tie, to even), then + 1 again: the total is exactly 2^24; the other partial sums
+    are 0.  An order that adds the two 1s first keeps 2^24 + 2 and gives another r (checked, so the pin
+    can fail).  Expected y_0 = (4096 * r) * 1 with r = 1 / sqrt(2^24 / 768), each an IEEE fp32 step."""
+    K = 768
+    x = np.zeros((1, K), np.float32)
+    x[0, 0], x[0, 256], x[0, 512] = 4096.0, 1.0, 1.0
+    gamma = np.ones(K, np.float32)
+    y = oracle.rmsnorm(x, gamma, 0.0)
+
+    def r_of(total):
+        return np.float32(np.float32(1.0) / np.sqrt(np.float32(np.float32(total) / np.float32(K))))
+
+    r = r_of(2.0 ** 24)
+    assert y[0, 0] == np.float32(np.float32(4096.0) * r) and y[0, 256] == r and y[0, 512] == r
+    assert np.float32(np.float32(4096.0) * r) != np.float32(np.float32(4096.0) * r_of(2.0 ** 24 + 2))
+
+
 def test_rmsnorm_against_f64():
     # y = x / sqrt(mean(x^2) + eps) * gamma in f64; the fp32 oracle differs by a few roundings only
     g = synth.rng(700)
