@@ -572,6 +572,30 @@ def test_routing_generator_shapes():
     assert np.allclose(w.sum(1), 1.0, atol=1e-6) and (ids >= 0).all() and (ids < 256).all()
 
 
+def test_input_recipe_is_seeded_and_matches_its_description():
+    """The synthetic inputs follow the stated recipe: N(0,1) activations with each element scaled by 10
+    with probability 1%, routing draws distinct experts per token uniformly, and a seed fixes every
+    byte (weights, activations and routing)."""
+    x = synth.activations(512, 1024, np.random.default_rng(0), outliers=True)
+    x0 = synth.activations(512, 1024, np.random.default_rng(0))   # the same N(0,1) draws, unscaled
+    ratio = x / x0
+    scaled = ratio == np.float32(10.0)
+    assert np.all(scaled | (ratio == np.float32(1.0)))              # each element x1 or x10
+    assert 0.008 < float(scaled.mean()) < 0.012                      # with probability 1%
+    xn = synth.activations(512, 1024, np.random.default_rng(1))
+    assert abs(float(xn.mean())) < 0.01 and abs(float(xn.std()) - 1.0) < 0.01
+    ids, _ = synth.routing(2048, 256, 8, np.random.default_rng(2))
+    counts = np.bincount(ids.reshape(-1), minlength=256)
+    assert counts.sum() == 2048 * 8 and counts.min() > 20 and counts.max() < 120   # mean 64
+    for dt in (synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.Q8_0):
+        a = synth.weights(dt, 32, 512, synth.rng(7))
+        b = synth.weights(dt, 32, 512, synth.rng(7))
+        assert np.array_equal(a, b) and a.nbytes == 32 * (512 // oracle.BLOCK_ELEMS[dt]) * oracle.BLOCK_BYTES[dt]
+    r1 = synth.routing(16, 64, 4, synth.rng(3))
+    r2 = synth.routing(16, 64, 4, synth.rng(3))
+    assert np.array_equal(r1[0], r2[0]) and np.array_equal(r1[1], r2[1])
+
+
 def test_q8_k_half_way_ties_go_to_even():
     """mx = -127 gives iscale = 1 exactly, so x = n + 1/2 is an exact tie:
     the nearest-integer reading is round-half-to-even (2.5 -> 2, 3.5 -> 4)."""
