@@ -578,9 +578,8 @@ def test_input_recipe_is_seeded_and_matches_its_description():
     byte (weights, activations and routing)."""
     x = synth.activations(512, 1024, np.random.default_rng(0), outliers=True)
     x0 = synth.activations(512, 1024, np.random.default_rng(0))   # the same N(0,1) draws, unscaled
-    ratio = x / x0
-    scaled = ratio == np.float32(10.0)
-    assert np.all(scaled | (ratio == np.float32(1.0)))              # each element x1 or x10
+    scaled = x == x0 * np.float32(10.0)
+    assert np.all(scaled | (x == x0))                                # each element x1 or x10
     assert 0.008 < float(scaled.mean()) < 0.012                      # with probability 1%
     xn = synth.activations(512, 1024, np.random.default_rng(1))
     assert abs(float(xn.mean())) < 0.01 and abs(float(xn.std()) - 1.0) < 0.01
