@@ -723,7 +723,55 @@ def cpu_baseline(budget_s: float = 12.0, extras: bool = True):
         el_d += time.perf_counter() - t0
         wbytes += w.nbytes
     out["decode_gemv_gbs"] = wbytes / el_d / 1e9
+    out["other_configs"] = cpu_other_configs(threads)
     return out
+
+
+def cpu_other_configs(threads: int):
+    """The oracle on the remaining workloads, all threads: the tiny Q4_K GEMM in full, and bounded
+    token samples of the Q8_0 + SwiGLU GEMM and of the MoE block (the experts a sample routes to are
+    generated and renumbered; every (token, slot) pair does the full per-pair work)."""
+    import oracle
+    from gemv_quantize_q8_gb300 import synth
+    res = {}
+    g = synth.rng(5)
+    c = synth.TINY
+    w = synth.weights(c["dtype"], c["N"], c["K"], g)
+    x = synth.activations(c["M"], c["K"], g)
+    t = time.perf_counter()
+    oracle.gemm(c["dtype"], w, oracle.quantize_q8_k(x), c["M"], c["N"], c["K"], threads=threads)
+    el = time.perf_counter() - t
+    res[c["name"]] = {"tops": 2.0 * c["M"] * c["N"] * c["K"] / el / 1e12, "sample": "in full"}
+    c = synth.SWIGLU_Q8_0
+    ms = 16
+    w = synth.weights(synth.Q8_0, c["N"], c["K"], g)
+    gu = synth.activations(ms, 2 * c["K"], g)
+    t = time.perf_counter()
+    h = oracle.swiglu(gu[:, :c["K"]], gu[:, c["K"]:])
+    oracle.gemm(synth.Q8_0, w, oracle.quantize_q8_1(h), ms, c["N"], c["K"], threads=threads)
+    el = time.perf_counter() - t
+    res[c["name"]] = {"tops": 2.0 * ms * c["N"] * c["K"] / el / 1e12,
+                      "sample": f"{ms} of {c['M']} rows, SwiGLU and Q8_1 quantisation included"}
+    c = synth.MOE
+    ts, E, top_k, H, F = 16, c["n_experts"], c["top_k"], c["hidden"], c["ffn"]
+    ids, wts = synth.routing(ts, E, top_k, g)
+    used, local = np.unique(ids, return_inverse=True)
+    ids_l = local.reshape(ids.shape).astype(np.int32)
+    El = used.size
+    w_gu = synth.weights(synth.Q4_K, El * 2 * F, H, g)
+    w_dn = synth.weights(synth.Q6_K, El * H, F, g)
+    x = synth.activations(ts, H, g)
+    t = time.perf_counter()
+    y_gu, _ = oracle.gemm_grouped(synth.Q4_K, w_gu, El, oracle.quantize_q8_k(x), 1, ids_l, ts, top_k, 2 * F, H,
+                                  threads=threads)
+    flat = y_gu.reshape(ts * top_k, 2 * F)
+    hq = oracle.quantize_q8_k(oracle.swiglu(flat[:, :F], flat[:, F:]))
+    y_dn, _ = oracle.gemm_grouped(synth.Q6_K, w_dn, El, hq, top_k, ids_l, ts, top_k, H, F, threads=threads)
+    oracle.moe_weighted_sum(y_dn, wts)
+    el = time.perf_counter() - t
+    res[c["name"]] = {"tops": 2.0 * ts * top_k * (2 * F * H + H * F) / el / 1e12,
+                      "sample": f"{ts} of {c['M']} tokens ({El} experts routed to), the whole block"}
+    return res
 
 
 # ----------------------------------------------------------------------------- reference arm
