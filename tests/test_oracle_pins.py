@@ -52,6 +52,7 @@ def test_float_to_half_round_to_nearest_even():
 
 
 @pytest.mark.parametrize("fname,dtype,nbytes", [("q4_k_blocks.txt", oracle.Q4_K, 144),
+                                                ("q5_k_blocks.txt", oracle.Q5_K, 176),
                                                 ("q6_k_blocks.txt", oracle.Q6_K, 210)])
 def test_hand_derived_blocks(fname, dtype, nbytes):
     cases = list(parse_fixture(os.path.join(GOLDEN, fname), nbytes))
