@@ -51,15 +51,16 @@ def test_float_to_half_round_to_nearest_even():
 # --------------------------------------------------------------------------- layouts
 
 
-@pytest.mark.parametrize("fname,dtype,nbytes", [("q4_k_blocks.txt", oracle.Q4_K, 144),
-                                                ("q5_k_blocks.txt", oracle.Q5_K, 176),
-                                                ("q6_k_blocks.txt", oracle.Q6_K, 210)])
-def test_hand_derived_blocks(fname, dtype, nbytes):
+@pytest.mark.parametrize("fname,dtype,nbytes,nelem", [("q4_k_blocks.txt", oracle.Q4_K, 144, 256),
+                                                      ("q5_k_blocks.txt", oracle.Q5_K, 176, 256),
+                                                      ("q6_k_blocks.txt", oracle.Q6_K, 210, 256),
+                                                      ("q8_0_blocks.txt", oracle.Q8_0, 34, 32)])
+def test_hand_derived_blocks(fname, dtype, nbytes, nelem):
     cases = list(parse_fixture(os.path.join(GOLDEN, fname), nbytes))
     assert cases
     for name, blk, exp in cases:
         x = oracle.dequant(dtype, blk)
-        want = np.zeros(256)
+        want = np.zeros(nelem)
         for i, v in exp.items():
             want[i] = v
         assert np.array_equal(x, want), name
