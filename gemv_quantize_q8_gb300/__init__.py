@@ -68,6 +68,10 @@ _SIGS = {
     "kq_gemm_f32": ([_I32, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I32),
     "kq_gemm_grouped_swiglu_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64, _I64], _SZ),
     "kq_gemm_grouped_swiglu_q8k": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _SZ, _P], _I32),
+    "kq_debug_tc_splits": ([_I32, _I64, _I64, _I64], _I32),
+    "kq_debug_tc_sums": ([_I32, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _SZ, _P], _I32),
+    "kq_debug_tc_sums_grouped": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _SZ, _P], _I32),
+    "kq_debug_tc_wait_timeout": ([_I32, _P, _P, _I64, _I64, _I64, _P, _I64, _I64, _P, _SZ, _P], _I32),
 }
 
 
@@ -235,3 +239,27 @@ def kq_moe_weighted_sum(y_slots, w, M, top_k, N, out, stream=None):
 
 def kq_debug_partials(wt, w, xq, M, N, K, partials, stream=None):
     _check(lib().kq_debug_partials(wt, _ptr(w), _ptr(xq), M, N, K, _ptr(partials), _stream(stream)))
+
+
+def kq_debug_tc_splits(wt, M, N, K) -> int:
+    """Split-K factor of the tensor-core path for this shape on the current device (0: not that path)."""
+    return int(lib().kq_debug_tc_splits(wt, M, N, K))
+
+
+def kq_debug_tc_sums(wt, w, xq, M, N, K, y, ldy, sums, workspace=None, ws_bytes=0, stream=None):
+    """kq_gemm's tensor-core kernel, also writing the integer sums of every scale block (int32 [M][N][nblk][2])."""
+    _check(lib().kq_debug_tc_sums(wt, _ptr(w), _ptr(xq), M, N, K, _ptr(y), ldy, _ptr(sums), _ptr(workspace), ws_bytes,
+                                  _stream(stream)))
+
+
+def kq_debug_tc_sums_grouped(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K, y, sums, workspace,
+                             ws_bytes, stream=None):
+    """kq_gemm_grouped's tensor-core kernel, also writing the integer block sums of every (token, slot) row."""
+    _check(lib().kq_debug_tc_sums_grouped(wt, _ptr(w), n_experts, _ptr(xq), xq_rows_per_token, _ptr(ids), M, top_k,
+                                          N, K, _ptr(y), _ptr(sums), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def kq_debug_tc_wait_timeout(wt, w, xq, M, N, K, y, ldy, wait_limit_ns, workspace, ws_bytes, stream=None):
+    """The tensor-core kernel with its activation producer idle and every wait limited to wait_limit_ns."""
+    _check(lib().kq_debug_tc_wait_timeout(wt, _ptr(w), _ptr(xq), M, N, K, _ptr(y), ldy, wait_limit_ns,
+                                          _ptr(workspace), ws_bytes, _stream(stream)))

@@ -8,6 +8,9 @@
 // order -- and the result -- is deterministic.
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 
 #include "kq_internal.cuh"
@@ -366,6 +369,23 @@ static kq_status check_matmul_args(const char *name, kq_dtype wt, const void *w,
     return KQ_OK;
 }
 
+// Argument checks shared by kq_gemm and its debug twins: matmul arguments, output, workspace.
+static kq_status check_gemm_call(const char *name, kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N,
+                                 int64_t K, const float *y, int64_t ldy, const void *workspace, size_t ws_bytes) {
+    kq_status s = check_matmul_args(name, wt, w, xq, M, N, K);
+    if (s != KQ_OK) return s;
+    if (!y) return fail(KQ_ERR_INVALID_ARG, "%s: null y", name);
+    if (ldy < N) return fail(KQ_ERR_INVALID_ARG, "%s: ldy %lld < N %lld", name, (long long)ldy, (long long)N);
+    if (!aligned(y, 4)) return fail(KQ_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", name);
+    const size_t need = kq_gemm_workspace_bytes(wt, M, N, K, 0, 0);
+    if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(KQ_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, need,
+                    workspace ? ws_bytes : 0);
+    if (workspace && !aligned(workspace, 256))
+        return fail(KQ_ERR_ALIGNMENT, "%s: workspace must be 256-byte aligned", name);
+    return KQ_OK;
+}
+
 }  // namespace kq
 
 using namespace kq;
@@ -384,15 +404,8 @@ size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K, int
 
 kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
                   void *workspace, size_t ws_bytes, kq_stream_t stream) {
-    kq_status s = check_matmul_args("kq_gemm", wt, w, xq, M, N, K);
+    kq_status s = check_gemm_call("kq_gemm", wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes);
     if (s != KQ_OK) return s;
-    if (!y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: null y");
-    if (ldy < N) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: ldy %lld < N %lld", (long long)ldy, (long long)N);
-    if (!aligned(y, 4)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm: y must be 4-byte aligned");
-    const size_t need = kq_gemm_workspace_bytes(wt, M, N, K, 0, 0);
-    if (need > 0 && (!workspace || ws_bytes < need))
-        return fail(KQ_ERR_WORKSPACE, "kq_gemm: workspace of %zu bytes needed, %zu given", need, workspace ? ws_bytes : 0);
-    if (workspace && !aligned(workspace, 256)) return fail(KQ_ERR_ALIGNMENT, "kq_gemm: workspace must be 256-byte aligned");
     cudaStream_t st = (cudaStream_t)stream;
     if (tc_eligible(wt, M, N, K))
         return tc_gemm(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
@@ -462,6 +475,42 @@ kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, int64_t 
     return launch_mmq_exact(wt, 1, false, a, (unsigned)gy, (cudaStream_t)stream);
 }
 
+int kq_debug_tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % 256) return 0;
+    return tc_split_factor(wt, M, N, K);
+}
+
+kq_status kq_debug_tc_sums(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
+                           int64_t ldy, int32_t *sums, void *workspace, size_t ws_bytes, kq_stream_t stream) {
+    kq_status s = check_gemm_call("kq_debug_tc_sums", wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes);
+    if (s != KQ_OK) return s;
+    if (!sums || !aligned(sums, 4)) return fail(KQ_ERR_INVALID_ARG, "kq_debug_tc_sums: null or misaligned sums");
+    if (!tc_eligible(wt, M, N, K))
+        return fail(KQ_ERR_INVALID_ARG, "kq_debug_tc_sums: %s M=%lld N=%lld K=%lld does not take the tensor-core path",
+                    dtype_name(wt), (long long)M, (long long)N, (long long)K);
+    TcDebug d;
+    d.sums = sums;
+    return tc_gemm(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
+                   static_cast<uint8_t *>(workspace), (cudaStream_t)stream, &d);
+}
+
+kq_status kq_debug_tc_wait_timeout(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,
+                                   float *y, int64_t ldy, int64_t wait_limit_ns, void *workspace, size_t ws_bytes,
+                                   kq_stream_t stream) {
+    kq_status s = check_gemm_call("kq_debug_tc_wait_timeout", wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes);
+    if (s != KQ_OK) return s;
+    if (wait_limit_ns < 1000 || wait_limit_ns > 1000000000)
+        return fail(KQ_ERR_INVALID_ARG, "kq_debug_tc_wait_timeout: wait_limit_ns must be in [1e3, 1e9]");
+    if (!tc_eligible(wt, M, N, K))
+        return fail(KQ_ERR_INVALID_ARG, "kq_debug_tc_wait_timeout: %s M=%lld N=%lld K=%lld does not take the "
+                    "tensor-core path", dtype_name(wt), (long long)M, (long long)N, (long long)K);
+    TcDebug d;
+    d.wait_ns = (unsigned long long)wait_limit_ns;
+    d.withhold_act = true;
+    return tc_gemm(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
+                   static_cast<uint8_t *>(workspace), (cudaStream_t)stream, &d);
+}
+
 }  // extern "C"
 
 namespace kq {
@@ -473,7 +522,7 @@ static size_t swq_scratch_offset(size_t base) { return (base + 255) & ~(size_t)2
 // fused preconditions and sized the workspace with the scratch after need_base bytes).
 static kq_status grouped_run(kq_dtype wt, const void *w, int64_t n_experts, const void *xq, int64_t xq_rows_per_token,
                              const int32_t *ids, int64_t M, int64_t top_k, int64_t N, int64_t K, float *y, uint8_t *hq,
-                             void *workspace, size_t ws_bytes, kq_stream_t stream) {
+                             void *workspace, size_t ws_bytes, kq_stream_t stream, const TcDebug *dbg = nullptr) {
     kq_status s = check_matmul_args("kq_gemm_grouped", wt, w, xq, M, N, K);
     if (s != KQ_OK) return s;
     if (!ids || (!y && !hq)) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: null ids or y");
@@ -504,6 +553,7 @@ static kq_status grouped_run(kq_dtype wt, const void *w, int64_t n_experts, cons
     const int64_t pairs = M * top_k;
     const RouteHistWs H = route_hist_ws(L.total, pairs, n_experts);
     const bool tc = tc_grouped_eligible(wt, N, K);
+    if (dbg && !tc) return fail(KQ_ERR_INVALID_ARG, "kq_debug_tc_sums_grouped: shape not served by the tensor cores");
     const GroupedTcWs T = grouped_tc_ws(wt, H.total, pairs, n_experts, K);
     int *poff = tc ? reinterpret_cast<int *>(ws + T.off_poff) : nullptr;
     int *prow = tc ? reinterpret_cast<int *>(ws + T.off_prow) : nullptr;
@@ -539,7 +589,7 @@ static kq_status grouped_run(kq_dtype wt, const void *w, int64_t n_experts, cons
                                (int)xq_rows_per_token, (int)top_k, pairs, n_experts, N, K, y, ws + T.off_panels,
                                tc_tiles, tc_count, T.max_tiles, count, offset, poff, lists, prow,
                                reinterpret_cast<unsigned long long *>(flag), hq,
-                               hq ? reinterpret_cast<float *>(ws + swq_scratch_offset(need_base)) : nullptr, st);
+                               hq ? reinterpret_cast<float *>(ws + swq_scratch_offset(need_base)) : nullptr, st, dbg);
     if (hq) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped_swiglu_q8k: shape not served by the tensor cores");
     MmqExactArgs a{};
     a.w = static_cast<const uint8_t *>(w);
@@ -561,6 +611,17 @@ kq_status kq_gemm_grouped(kq_dtype wt, const void *w, int64_t n_experts, const v
     if (!y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: null ids or y");
     return grouped_run(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K, y, nullptr, workspace, ws_bytes,
                        stream);
+}
+
+kq_status kq_debug_tc_sums_grouped(kq_dtype wt, const void *w, int64_t n_experts, const void *xq,
+                                   int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k, int64_t N,
+                                   int64_t K, float *y, int32_t *sums, void *workspace, size_t ws_bytes,
+                                   kq_stream_t stream) {
+    if (!sums || !aligned(sums, 4)) return fail(KQ_ERR_INVALID_ARG, "kq_debug_tc_sums_grouped: null or misaligned sums");
+    TcDebug d;
+    d.sums = sums;
+    return grouped_run(wt, w, n_experts, xq, xq_rows_per_token, ids, M, top_k, N, K, y, nullptr, workspace, ws_bytes,
+                       stream, &d);
 }
 
 size_t kq_gemm_grouped_swiglu_workspace_bytes(kq_dtype wt, int64_t M, int64_t F, int64_t K, int64_t n_experts,
@@ -636,21 +697,57 @@ constexpr size_t kStaticScratchBytes = (size_t)1 << 20;  // 1 MiB: up to ~250k (
 static __device__ __align__(256) uint8_t g_grouped_scratch[kStaticScratchBytes];
 
 static std::mutex g_scratch_mu;
-static void *g_scratch_addr[256];  // device address of g_grouped_scratch, per device ordinal
+// Device address of g_grouped_scratch per device ordinal, with the id of the CUDA context it was
+// looked up in: the address belongs to the module loaded into that context, and a reset of the device
+// (cudaDeviceReset, or any teardown of its primary context) unloads the module, so a cached address
+// whose context id differs from the current one is looked up again.
+static void *g_scratch_addr[256];
+static unsigned long long g_scratch_ctx[256];
 
-// Device address of the static scratch on the current device; looked up once per device.
+// Unique id of the current thread's CUDA context (driver cuCtxGetCurrent + cuCtxGetId, reached through
+// the runtime's entry-point query, so no driver library is linked); 0 if it cannot be read.
+static unsigned long long current_ctx_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+        cudaGetLastError();
+        looked_up = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the static scratch on the current device, looked up once per device (with that
+// device current, the first call does cudaGetSymbolAddress) and again after the device's context
+// changed.
 static kq_status static_scratch(void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm_grouped_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 256) return fail(KQ_ERR_CUDA, "kq_gemm_grouped_noalloc: device ordinal %d out of range", dev);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    // cudaGetSymbolAddress makes the device's primary context current if none is; the context id is
+    // read after it, so the first lookup records the context the address belongs to
+    const unsigned long long ctx = current_ctx_id();
+    if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_grouped_scratch);
         if (e != cudaSuccess || !p)
             return fail(KQ_ERR_CUDA, "kq_gemm_grouped_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_ctx_id();
     }
     *out = g_scratch_addr[dev];
     return KQ_OK;

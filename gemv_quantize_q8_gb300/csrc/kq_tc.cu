@@ -154,6 +154,16 @@ struct TcParams {
     int swq;
     float *scr;    // [gridDim.x][2][TC_TOK][256] fp32 (units alternate halves)
     uint8_t *hq;   // [pairs][F/256] Q8_K blocks
+    // Debug instantiation only (DBG): the integer sums every super-block (Q8_0: every 32-block)
+    // accumulates in TMEM, read out before the fp32 promotion: dbg[out row][n][block][2] int32 =
+    // (sum_j sc_j*P_j, Q4_K/Q5_K min term sum_j m_j*(bs_2j + bs_2j+1) or 0), out row = token row
+    // (dense) or (token, slot) pair (routed).
+    int *dbg;
+    int dbg_nblk;
+    // Wall-time limit of every pipeline wait (ns), and a test hook: withhold != 0 keeps the activation
+    // producer idle, so the first wait for an activation tile cannot complete and runs into the limit.
+    unsigned long long wait_ns;
+    int withhold;
 };
 
 struct TcTile {
@@ -264,9 +274,9 @@ __device__ __forceinline__ void convert_q6k_sub(const uint32_t (&nib)[4], const 
     }
 }
 
-// SWQ: fused SwiGLU -> Q8_K epilogue (routed gate/up); a separate instantiation, so the plain GEMM's
-// register allocation is untouched by it.
-template <int DT, bool SWQ>
+// SWQ: fused SwiGLU -> Q8_K epilogue (routed gate/up); DBG: the debug read-out of the integer sums
+// (P.dbg).  Each is a separate instantiation, so the plain GEMM's register allocation is untouched.
+template <int DT, bool SWQ, bool DBG>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE, TcParams P) {
     using C = TcCfg<DT>;
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int gsb = sb0 + tt;
                 if (++tt == nsb) { tt = 0; ++ti; }
                 const int p = st % C::NP, pph = (st / C::NP) & 1;
-                if (!(ok = mbar_wait_sleep(&p_empty[p], pph ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&p_empty[p], pph ^ 1, abort_flag, P.wait_ns))) break;
                 mbar_arrive_expect_tx(&p_full[p], T.valid_groups * C::CB);
                 for (int gi = 0; gi < T.valid_groups; ++gi)
                     bulk_load(sP + (p * 8 + gi) * C::CB, P.w + ((int64_t)(T.g0 + gi) * nchunk + gsb) * C::CB, C::CB,
@@ -359,14 +369,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 last_p[p] = pph;
                 if (C::EXT) {
                     const int e = st % C::NE, eph = (st / C::NE) & 1;
-                    if (!(ok = mbar_wait_sleep(&e_empty[e], eph ^ 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&e_empty[e], eph ^ 1, abort_flag, P.wait_ns))) break;
                     mbar_arrive_expect_tx(&e_full[e], 4096);
                     tma_load_2d(sEB + e * 4096, &tmE, &e_full[e], gsb * 16, T.m0);
                     last_e[e] = eph;
                 }
                 {
                     const int h = st & 3, hph = (st >> 2) & 1;
-                    if (!(ok = mbar_wait_sleep(&h_empty[h], hph ^ 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&h_empty[h], hph ^ 1, abort_flag, P.wait_ns))) break;
                     // the scale panel has one row of M_pad floats per scale block (256 or 32 K)
                     mbar_arrive_expect_tx(&da_full[h], C::BPS * TC_TOK * 4);
                     for (int b = 0; b < C::BPS; ++b)
@@ -395,10 +405,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int i = 0; i < NPAIR; ++i) last_k[i] = -1;
             bool ok = true;
             int m0 = 0, ti = 0, tt = 0;
-            for (int pp = 0; pp < nsteps * 2 && ok; ++pp) {
+            for (int pp = 0; pp < nsteps * 2 && ok && !P.withhold; ++pp) {
                 if ((pp & 1) == 0 && tt == 0) m0 = tile_of(ti).m0;
                 const int s = pp % NPAIR, ph = (pp / NPAIR) & 1;
-                if (!(ok = mbar_wait_sleep(&k_empty[s], ph ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&k_empty[s], ph ^ 1, abort_flag, P.wait_ns))) break;
                 mbar_arrive_expect_tx(&k_full[s], 2 * ACT_TILE);
                 const int x = (sb0 + tt) * 256 + (pp & 1) * 2 * TC_KB;
                 if ((pp & 1) && ++tt == nsb) { tt = 0; ++ti; }
@@ -441,12 +451,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     int g = 8 * t, buf = g % C::NACC, use = g / C::NACC;
                     for (int pr = 0; pr < 2 && ok; ++pr) {
                         const int pp = 2 * t + pr, s = pp % NPAIR;
-                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
                         for (int h = 0; h < 2 && ok; ++h) {
                             const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
                             const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
                             for (int blk = 0; blk < 2; ++blk) {
-                                if (!(ok = mbar_wait_sleep(&acc_empty[buf], (use & 1) ^ 1, abort_flag))) break;
+                                if (!(ok = mbar_wait_sleep(&acc_empty[buf], (use & 1) ^ 1, abort_flag, P.wait_ns))) break;
                                 tc_fence_after();
                                 const uint32_t dq = tbase + buf * TC_TOK;
                                 mma_f16_ts(dq, a0 + blk * 16, bd + (uint64_t)(blk * 4), idesc, 0);
@@ -461,11 +471,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
             for (int t = w; t < nsteps && ok && !C::Q8; t += 2) {  // t: step
-                if (!(ok = mbar_wait_sleep(&acc_empty[w], ((t >> 1) & 1) ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&acc_empty[w], ((t >> 1) & 1) ^ 1, abort_flag, P.wait_ns))) break;
                 tc_fence_after();
                 for (int pr = 0; pr < 2 && ok; ++pr) {
                     const int pp = 2 * t + pr, s = pp % NPAIR;
-                    if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -482,9 +492,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!ok) break;
                 if (C::EXT) {
                     const int e = t % C::NE;
-                    if (!(ok = mbar_wait_sleep(&e_full[e], (t / C::NE) & 1, abort_flag))) break;
-                    if (t > 0 && !(ok = C::Q5 ? mbar_wait_sleep(s2_empty, (t - 1) & 1, abort_flag)
-                                              : mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag)))
+                    if (!(ok = mbar_wait_sleep(&e_full[e], (t / C::NE) & 1, abort_flag, P.wait_ns))) break;
+                    if (t > 0 && !(ok = C::Q5 ? mbar_wait_sleep(s2_empty, (t - 1) & 1, abort_flag, P.wait_ns)
+                                              : mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, P.wait_ns)))
                         break;
                     tc_fence_after();
                     mma_f16(tbase + C::TM_S2, dEA + (uint64_t)(e * (4096 >> 4)), dEB + (uint64_t)(e * (4096 >> 4)),
@@ -512,7 +522,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (tt == 0) rvalid = row < tile_of(ti).valid_groups * 16;
             if (++tt == nsb) { tt = 0; ++ti; }
             const int p = t % C::NP;
-            if (!(ok = mbar_wait_sleep(&p_full[p], (t / C::NP) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait_sleep(&p_full[p], (t / C::NP) & 1, abort_flag, P.wait_ns))) break;
             // rows past N were not loaded: their scales are forced to 0, so they convert to zeros
             const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
             const int r16 = row & 15;
@@ -532,7 +542,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int j = 0; j < 2; ++j) {
                     if (t > 0) {
                         const int pq = 2 * (t - 1) + j;
-                        if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag, P.wait_ns))) break;
                     }
                     tc_fence_after();
                     uint32_t r[32];
@@ -554,7 +564,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!ok) break;
                 if (grp == 0) {
                     const int h = t & 3;
-                    if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag, P.wait_ns))) break;
                     reinterpret_cast<uint4 *>(sH + h * TC_ROWS * C::H_ROW)[row] = dv;
                     mbar_arrive(&h_full[h]);
                 }
@@ -600,7 +610,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int kb = grp + 2 * j;
                 if (t > 0) {
                     const int pq = 2 * (t - 1) + j;
-                    if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag, P.wait_ns))) break;
                 }
                 tc_fence_after();
                 const uint32_t ta = lane_base + C::TM_A + kb * C::A_COLS;
@@ -638,7 +648,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (grp == 0) {
                 // the row's (d, -dmin) for the epilogue
                 const int h = t & 3;
-                if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag, P.wait_ns))) break;
                 float2 dpair = make_float2(0.0f, 0.0f);
                 if (C::EXT)
                     dpair = make_float2(half_bits_to_float((uint16_t)(hv.x & 0xffff)),
@@ -651,7 +661,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             } else if (C::EXT) {
                 // extension A row: the 8 sub-block mins, each repeated for its two bsum groups
                 const int e = t % C::NE;
-                if (!(ok = mbar_wait_sleep(&e_empty[e], ((t / C::NE) & 1) ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&e_empty[e], ((t / C::NE) & 1) ^ 1, abort_flag, P.wait_ns))) break;
                 uint8_t s12[12];
                 const uint32_t hw[3] = {hv.y, hv.z, hv.w};
 #pragma unroll
@@ -691,9 +701,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const float v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
             q8k_block_store(v, P.hq + ((int64_t)P.lists[plist + j] * (P.N / 512) + pb) * kQ8KBytes);
         };
+        // DBG: component `comp` of block `blk` for this thread's row and the 8 tokens j0 .. j0+7 of the
+        // tile, converted from the fp32 accumulator (an exact integer) to int32
+        auto dbg_put = [&](const TcTile &T, int j0, int blk, int comp, const float (&v)[8]) {
+            const int n = T.n0 + row;
+            if (n >= P.N) return;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = j0 + i;
+                if (j >= T.tok_valid) break;
+                const int64_t mrow = P.grouped ? (int64_t)P.lists[T.list_base + j] : (int64_t)(T.m0 + j);
+                P.dbg[((mrow * P.N + n) * P.dbg_nblk + blk) * 2 + comp] = __float2int_rn(v[i]);
+            }
+        };
         for (int t = 0, ti = 0, tt = 0; t < nsteps && ok; ++t) {  // t: step
             const int buf = t & 1, h = t & 3;
             const int tile_i = ti;
+            const int gsb = sb0 + tt;  // this step's super-block along K
             const bool first = tt == 0, last = tt == nsb - 1;
             if (++tt == nsb) { tt = 0; ++ti; }
             if (first) {
@@ -704,12 +728,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // Q8_0: per 32-element block b, acc += (d_w*d_a)*P_b with each product rounded on its
                 // own and the blocks added in ascending K order -- the CPU oracle's arithmetic, so the
                 // result is bit-identical to it
-                if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag))) break;
-                if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag, P.wait_ns))) break;
+                if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag, P.wait_ns))) break;
                 const uint4 dwv = reinterpret_cast<const uint4 *>(sH + h * TC_ROWS * C::H_ROW)[row];
                 int g = 8 * t, qb = g % C::NACC, use = g / C::NACC;
                 for (int b = 0; b < 8 && ok; ++b) {
-                    if (!(ok = mbar_wait_sleep(&acc_full[qb], use & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&acc_full[qb], use & 1, abort_flag, P.wait_ns))) break;
                     tc_fence_after();
                     // block b's f16 scale, picked from the four words with selects (no local array)
                     const uint32_t dword = (b & 4) ? ((b & 2) ? dwv.w : dwv.z) : ((b & 2) ? dwv.y : dwv.x);
@@ -721,6 +745,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         float pv[8];
                         tmem_ld8(lane_base + qb * TC_TOK + tq * 32 + c * 8, pv);
                         tmem_wait_ld();
+                        if (DBG) {
+                            const TcTile T = tile_of(tile_i);
+                            const float zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                            dbg_put(T, tq * 32 + c * 8, gsb * 8 + b, 0, pv);
+                            dbg_put(T, tq * 32 + c * 8, gsb * 8 + b, 1, zero);
+                        }
                         const float4 da0 = dap[2 * c], da1 = dap[2 * c + 1];
                         const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
 #pragma unroll
@@ -743,9 +773,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&h_empty[h]);
             } else {
-            if (!(ok = mbar_wait_sleep(&acc_full[buf], (t >> 1) & 1, abort_flag))) break;
-            if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag))) break;
-            if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait_sleep(&acc_full[buf], (t >> 1) & 1, abort_flag, P.wait_ns))) break;
+            if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag, P.wait_ns))) break;
+            if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag, P.wait_ns))) break;
             tc_fence_after();
             const float2 rs = reinterpret_cast<const float2 *>(sH + h * TC_ROWS * 8)[row];  // (d, -dmin)
             const float4 *dap = reinterpret_cast<const float4 *>(sDA + h * TC_TOK * 4) + tq * 8;
@@ -761,6 +791,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     float s2[8];
                     tmem_ld8(lane_base + C::TM_S2 + tq * 32 + c * 8, s2);
                     tmem_wait_ld();
+                    if (DBG) dbg_put(tile_of(tile_i), tq * 32 + c * 8, gsb, 1, s2);
                     const float4 da0 = dap[2 * c], da1 = dap[2 * c + 1];
                     const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
 #pragma unroll
@@ -780,6 +811,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tmem_ld8(lane_base + buf * TC_TOK + col, s1);
                 if (C::EXT && !C::Q5) tmem_ld8(lane_base + C::TM_S2 + col, s2);
                 tmem_wait_ld();
+                if (DBG) {
+                    const TcTile T = tile_of(tile_i);
+                    dbg_put(T, (int)col, gsb, 0, s1);
+                    if (!C::EXT) {
+                        const float zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        dbg_put(T, (int)col, gsb, 1, zero);
+                    } else if (!C::Q5) {
+                        dbg_put(T, (int)col, gsb, 1, s2);
+                    }
+                }
                 const float4 da0 = dap[2 * c], da1 = dap[2 * c + 1];
                 const float da[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
 #pragma unroll
@@ -809,7 +850,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (SWQ && pend >= 0) {
                 // the accumulator is released; one token of the pending unit (after its four warps met)
                 if (!pwait) {
-                    if (!(ok = mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag, P.wait_ns))) break;
                     pwait = true;
                 }
                 if (pj < pend) { swq_token(pj); pj += 4; }
@@ -842,7 +883,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // finish the pending unit, then publish this one: its four warps' h columns complete
                 // every token's block once all four have arrived
                 if (pend >= 0) {
-                    if (!pwait && !(ok = mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag))) break;
+                    if (!pwait && !(ok = mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag, P.wait_ns))) break;
                     for (; pj < pend; pj += 4) swq_token(pj);
                 }
                 __threadfence_block();
@@ -874,7 +915,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
         }
         if (SWQ && ok && pend >= 0) {  // the last unit's tokens
-            if (pwait || mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag))
+            if (pwait || mbar_wait_sleep(&sw_bar[tq], (sw_u - 1) & 1, abort_flag, P.wait_ns))
                 for (; pj < pend; pj += 4) swq_token(pj);
         }
     }
@@ -1114,29 +1155,104 @@ bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     return true;
 }
 
+// Number of SMs of the current device (looked up once per device).
+static int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 152;
+    }
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 152;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// CTAs of the tensor-core kernel that the current device runs at once when they are launched in
+// clusters of S (S = 1: one per SM, the shared-memory budget allows no more).  Clusters fill a GPC
+// only in whole multiples of their size, so the count comes from the device's own cluster occupancy;
+// without a device it falls back to GB300's 8 GPCs of 19 SMs.  Cached per device and S.
+template <int DT>
+static int resident_ctas(int S) {
+    static int cache[64][4] = {};
+    const int si = S == 1 ? 0 : S == 2 ? 1 : S == 4 ? 2 : 3;
+    const int fallback = S == 1 ? 152 : 8 * (19 / S) * S;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fallback;
+    }
+    if (cache[dev][si]) return cache[dev][si];
+    int n = 0;
+    if (S == 1) {
+        n = sm_count();
+    } else {
+        auto kern = tc_gemm_kernel<DT, false, false>;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, (unsigned)S);
+        cfg.blockDim = dim3(TC_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = TcLayout<DT>::ALLOC;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)S;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout<DT>::ALLOC) ==
+                cudaSuccess &&
+            cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess)
+            n = clusters * S;
+        else
+            cudaGetLastError();  // leave no error behind for the next launch check
+    }
+    if (n <= 0) n = fallback;
+    cache[dev][si] = n;
+    return n;
+}
+
+static int resident_ctas_dt(kq_dtype wt, int S) {
+    switch (wt) {
+    case KQ_Q4_K: return resident_ctas<KQ_Q4_K>(S);
+    case KQ_Q5_K: return resident_ctas<KQ_Q5_K>(S);
+    case KQ_Q6_K: return resident_ctas<KQ_Q6_K>(S);
+    default: return resident_ctas<KQ_Q8_0>(S);
+    }
+}
+
 // Split-K factor: the number of CTAs per output tile (a cluster along z).  Chosen with a small
 // cost model measured on GB300 -- every CTA pays a pipeline fill and drain (~2.5 us) and each
-// super-block costs ~1.3 us (Q4_K) or ~1.75 us (Q6_K); a split adds a cluster reduction (~1 us)
-// and clusters of S CTAs fill whole GPCs only in multiples of S -- over power-of-two splits that
-// leave at least two super-blocks per CTA.
+// super-block costs ~1.3 us (Q4_K) or ~1.75 us (Q6_K); a split adds a cluster reduction (~1 us),
+// and only as many clusters run at once as the device holds (resident_ctas) -- over power-of-two
+// splits that leave at least two super-blocks per CTA.
 static int tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     if (wt == KQ_Q8_0) return 1;  // keeps every output's blocks in one ascending sum (bit-exact)
     const int64_t tiles = ((M + TC_TOK - 1) / TC_TOK) * ((N + TC_ROWS - 1) / TC_ROWS);
     const int nsb = (int)(K / 256);
     const double t_sb = wt == KQ_Q4_K ? 1.3 : wt == KQ_Q5_K ? 1.5 : 1.75, t_fill = 2.5, t_red = 1.0;
-    const int num_sms = 152, gpcs = 8, sms_per_gpc = 19;
     int best = 1;
     double best_t = 1e30;
     for (int S = 1; S <= 8; S *= 2) {
         const int per = (nsb + S - 1) / S;
         if (S > 1 && per < 2) break;
         if ((nsb + per - 1) / per != S) continue;  // S must be exactly realisable
-        const int64_t usable = S == 1 ? num_sms : (int64_t)gpcs * (sms_per_gpc / S) * S;
+        const int64_t usable = resident_ctas_dt(wt, S);
         const int64_t waves = (tiles * S + usable - 1) / usable;
         const double t = (double)waves * (t_fill + per * t_sb + (S > 1 ? t_red : 0.0));
         if (t < best_t - 1e-9) { best_t = t; best = S; }
     }
     return best;
+}
+
+int tc_split_factor(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
+    return tc_eligible(wt, M, N, K) ? tc_splits(wt, M, N, K) : 0;
 }
 
 size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
@@ -1157,18 +1273,6 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// Number of SMs of the current device (looked up once per device).
-static int sm_count() {
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-    if (!cache[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-        cache[dev] = n;
-    }
-    return cache[dev];
-}
 
 // One launch of the tensor-core kernel over activation panels built by a prologue.
 struct TcLaunch {
@@ -1186,6 +1290,7 @@ struct TcLaunch {
     const int *tiles, *tile_count, *count, *offset, *poff, *lists;
     uint8_t *hq;          // non-NULL: fused SwiGLU -> Q8_K output (grouped gate/up only), y unused
     float *scr;           // its scratch: tc_swq_scratch_bytes()
+    const TcDebug *dbg;   // NULL, or the debug read-out / wait-limit hooks
 };
 
 template <int DT>
@@ -1236,12 +1341,19 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     p.swq = a.hq ? 1 : 0;
     p.hq = a.hq;
     p.scr = a.scr;
+    p.wait_ns = a.dbg ? a.dbg->wait_ns : kTcWaitNs;
+    p.withhold = a.dbg && a.dbg->withhold_act ? 1 : 0;
+    const bool dbg_sums = a.dbg && a.dbg->sums;
+    p.dbg = dbg_sums ? a.dbg->sums : nullptr;
+    p.dbg_nblk = (int)(TcCfg<DT>::Q8 ? a.K / 32 : a.K / 256);
     if (p.swq && (S != 1 || !a.grouped || a.N % 512 || !a.scr))
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm (tensor core): fused SwiGLU needs a routed, unsplit launch");
+    if (p.swq && dbg_sums) return fail(KQ_ERR_INVALID_ARG, "kq_gemm (tensor core): no debug read-out with fused SwiGLU");
     const int64_t tiles = (int64_t)p.n_tiles * a.m_tiles;
     const int64_t units = p.swq ? tiles / 4 : tiles;
     if (tiles > 0x7fffffff) return fail(KQ_ERR_INVALID_ARG, "kq_gemm: too many tiles");
-    auto kern = p.swq ? tc_gemm_kernel<DT, true> : tc_gemm_kernel<DT, false>;
+    auto kern = p.swq ? tc_gemm_kernel<DT, true, false>
+                      : dbg_sums ? tc_gemm_kernel<DT, false, true> : tc_gemm_kernel<DT, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
@@ -1276,7 +1388,8 @@ static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st) {
 // The tensor-core GEMM from quantised rows xq, or (xf != NULL, Q4_K/Q5_K/Q6_K) from fp32 rows xf of
 // stride ldx quantised to Q8_K inside the prologue.
 static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, const float *xf, int64_t ldx, int64_t M,
-                              int64_t N, int64_t K, float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st) {
+                              int64_t N, int64_t K, float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st,
+                              const TcDebug *dbg) {
     const TcWs L = tc_ws(wt, M, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || L.M_pad / TC_TOK > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm: shape too large for the tensor-core grid");
@@ -1307,19 +1420,20 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
     a.rows = L.M_pad; a.dstride = L.M_pad; a.m_tiles = (int)(L.M_pad / TC_TOK);
     a.nsplit = tc_splits(wt, M, N, K);
     a.err = reinterpret_cast<unsigned long long *>(workspace + L.off_flag);
+    a.dbg = dbg;
     s = launch_tc_dt(wt, a, st);
     if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
     return s;
 }
 
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
-                  int64_t ldy, uint8_t *workspace, cudaStream_t st) {
-    return tc_gemm_impl(wt, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st);
+                  int64_t ldy, uint8_t *workspace, cudaStream_t st, const TcDebug *dbg) {
+    return tc_gemm_impl(wt, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st, dbg);
 }
 
 kq_status tc_gemm_f32(kq_dtype wt, const uint8_t *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
                       float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st) {
-    return tc_gemm_impl(wt, w, nullptr, x, ldx, M, N, K, y, ldy, workspace, st);
+    return tc_gemm_impl(wt, w, nullptr, x, ldx, M, N, K, y, ldy, workspace, st, nullptr);
 }
 
 // ---- routed experts on the tensor cores
@@ -1352,7 +1466,7 @@ kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int 
                           int64_t pairs, int64_t E, int64_t N, int64_t K, float *y, uint8_t *panels,
                           const int *tiles, const int *tile_count, int64_t max_tiles, const int *count,
                           const int *offset, const int *poff, const int *lists, const int *prow,
-                          unsigned long long *err, uint8_t *hq, float *scr, cudaStream_t st) {
+                          unsigned long long *err, uint8_t *hq, float *scr, cudaStream_t st, const TcDebug *dbg) {
     const TcGroupedPanels G = tc_grouped_panels(wt, pairs, E, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || max_tiles > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm_grouped: shape too large for the tensor-core grid");
@@ -1378,6 +1492,7 @@ kq_status tc_gemm_grouped(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int 
     a.grouped = true;
     a.tiles = tiles; a.tile_count = tile_count; a.count = count; a.offset = offset; a.poff = poff; a.lists = lists;
     a.hq = hq; a.scr = scr;
+    a.dbg = dbg;
     s = launch_tc_dt(wt, a, st);
     if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
     return s;

@@ -250,7 +250,9 @@ KQ_API kq_status kq_gemm_grouped_swiglu_q8k(kq_dtype wt, const void *w, int64_t 
  * holds it until the process exits), which allows about 250k (token, slot) pairs; larger
  * M*top_k (or n_experts) is rejected with KQ_ERR_INVALID_ARG before anything is launched.
  * The first call on a device looks the array's address up (cudaGetSymbolAddress, once per
- * device, with that device current); make that first call before any stream capture.  The call
+ * device, with that device current); make that first call before any stream capture.  The address
+ * belongs to the device's CUDA context: after a reset of the device (cudaDeviceReset) the next call
+ * sees a new context and looks the address up again, so make that call outside a capture too.  The call
  * allocates nothing.  All calls share the one array, so calls that overlap on the GPU (other
  * streams, other host threads) race: serialise them.  Ids outside [0, n_experts) are skipped (their
  * y rows are not written) but, unlike kq_gemm_grouped, their number is not reported. */
@@ -282,11 +284,50 @@ KQ_API kq_status kq_moe_weighted_sum(const float *y_slots, const float *w, int64
  * "mmq_tc", "route", "weighted_sum".  Unknown route names return -1.  Thread-safe. */
 KQ_API int64_t kq_launch_count(const char *route);
 
-/* Debug: the integer sub-block dots of kq_gemm, partials[m][n][j] (int32):
- * Q4_K: K/32 per (m,n), P_j = sum c*q; Q6_K: K/16, P_j = sum (c-32)*q; Q8_0: K/32, P_b = sum w*q.
- * Computed by the same integer machinery as kq_gemm's exact path; bit-exact by contract. */
+/* Debug: the integer sub-block dots of kq_gemm, partials[m][n][j] (int32)
+ * ([vllm-2890] keep-quant provider commit: the integer dots are taken in the CPU accumulation order and
+ * gated bit-exact against the CPU tier):
+ * Q4_K/Q5_K: K/32 per (m,n), P_j = sum c*q; Q6_K: K/16, P_j = sum (c-32)*q; Q8_0: K/32, P_b = sum w*q.
+ * Computed by the exact dp4a kernel, one integer dot per sub-block; bit-exact by contract. */
 KQ_API kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,
                             int32_t *partials, kq_stream_t stream);
+
+/* Debug: the split-K factor (CTAs of a thread-block cluster per 128 x 128 output tile, 1 = no split)
+ * that kq_gemm's tensor-core path takes for this shape on the current device, or 0 when the shape does
+ * not take the tensor-core path.  Host only; launches nothing. */
+KQ_API int kq_debug_tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K);
+
+/* Debug twin of kq_gemm's tensor-core path ([vllm-2890] keep-quant provider commit: integer dots
+ * bit-exact against the CPU tier).  Runs the very kernel kq_gemm runs for this shape (same tiles, same
+ * split-K clusters, same TMEM accumulation), with a debug epilogue that also writes, before the fp32
+ * promotion, the integer sums each scale block accumulated in tensor memory:
+ *   sums[m][n][b][0] = sum_j sc_j*P_j over block b (Q4_K, Q5_K, Q6_K: 256 elements), P_b (Q8_0: 32)
+ *   sums[m][n][b][1] = sum_j m_j*(bs_2j + bs_2j+1) (Q4_K, Q5_K min term), else 0
+ * as int32 [M][N][nblk][2], nblk = K/256 (K/32 for Q8_0).  y is written as by kq_gemm.  Arguments and
+ * workspace as kq_gemm; KQ_ERR_INVALID_ARG when the shape does not take the tensor-core path (M <= 8 or
+ * N < 128). */
+KQ_API kq_status kq_debug_tc_sums(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,
+                                  float *y, int64_t ldy, int32_t *sums, void *workspace, size_t ws_bytes,
+                                  kq_stream_t stream);
+
+/* Debug twin of kq_gemm_grouped's tensor-core path: sums as kq_debug_tc_sums, one row per (token, slot)
+ * pair, int32 [M*top_k][N][nblk][2]; rows of invalid ids are not written.  Arguments and workspace as
+ * kq_gemm_grouped. */
+KQ_API kq_status kq_debug_tc_sums_grouped(kq_dtype wt, const void *w, int64_t n_experts, const void *xq,
+                                          int64_t xq_rows_per_token, const int32_t *ids, int64_t M, int64_t top_k,
+                                          int64_t N, int64_t K, float *y, int32_t *sums, void *workspace,
+                                          size_t ws_bytes, kq_stream_t stream);
+
+/* Test hook of the tensor-core pipeline's bounded waits: runs kq_gemm's tensor-core kernel with its
+ * activation-tile producer kept idle, so the first wait for an activation tile can never complete,
+ * and with every pipeline wait limited to wait_limit_ns (1e3 .. 1e9; kq_gemm uses 2 s).  The waits
+ * run out, each CTA records the timeout in the workspace's device flag, waits (bounded) for its own
+ * copies and MMAs in flight, frees its tensor memory and returns: the call itself returns KQ_OK, y is
+ * left incomplete, and kq_read_device_flag then reports KQ_ERR_DEVICE_FLAG.  Nothing faults or hangs;
+ * the stream stays usable for the next call. */
+KQ_API kq_status kq_debug_tc_wait_timeout(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,
+                                          float *y, int64_t ldy, int64_t wait_limit_ns, void *workspace,
+                                          size_t ws_bytes, kq_stream_t stream);
 
 #ifdef __cplusplus
 }

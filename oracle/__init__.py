@@ -52,7 +52,9 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
+            # KQ_ORACLE_LIB: a differently built copy of this same oracle (the mutation test compiles
+            # deliberately broken copies and runs the pins against them)
+            path = os.environ.get("KQ_ORACLE_LIB") or build()
             L = ctypes.CDLL(path)
             P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
             L.orc_half_to_float.argtypes = [ctypes.c_uint16]
@@ -73,6 +75,8 @@ def lib():
             L.orc_gemm.argtypes = [I32, P, P, I64, I64, I64, P, I64, I32]
             L.orc_gemm_sampled.argtypes = [I32, P, P, I64, I64, P, P, P]
             L.orc_partials.argtypes = [I32, P, P, I64, I64, I64, P]
+            L.orc_gemm_sampled_terms.argtypes = [I32, P, P, I64, I64, P, P, P, P]
+            L.orc_block_sums.argtypes = [I32, P, P, I64, I64, I64, P, I32]
             L.orc_gemm_grouped.argtypes = [I32, P, I64, P, I64, P, I64, I64, I64, I64, P, I32]
             L.orc_gemm_grouped.restype = I64
             L.orc_moe_weighted_sum.argtypes = [P, P, I64, I64, I64, P]
@@ -136,7 +140,7 @@ def quantize_q8_1(x: np.ndarray) -> np.ndarray:
 
 
 def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
-    """y = (x * r) * gamma, r = 1 / sqrt(sum(x^2) / K + eps), fp32, sum in the fixed row-reduction order."""
+    """y = (x * r) * gamma, r = 1 / sqrt(sum(x^2) / K + eps), fp32, the sum of squares in ascending order."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     gamma = np.ascontiguousarray(gamma, dtype=np.float32)
     M, K = x.shape
@@ -184,6 +188,30 @@ def gemm_sampled(dtype: int, w: np.ndarray, xq: np.ndarray, K: int, m_idx, n_idx
     ni = np.ascontiguousarray(n_idx, dtype=np.int64)
     out = np.empty(mi.size, dtype=np.float32)
     lib().orc_gemm_sampled(dtype, _ptr(w), _ptr(xq), K, mi.size, _ptr(mi), _ptr(ni), _ptr(out))
+    return out
+
+
+def gemm_sampled_terms(dtype: int, w: np.ndarray, xq: np.ndarray, K: int, m_idx, n_idx):
+    """Sampled outputs and, per output, the f64 sum over blocks of |(d_a*d_w)*sumi| + |(d_a*dmin)*summ|
+    (the magnitude that any order of the fp32 block scaling rounds against)."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    mi = np.ascontiguousarray(m_idx, dtype=np.int64)
+    ni = np.ascontiguousarray(n_idx, dtype=np.int64)
+    out = np.empty(mi.size, dtype=np.float32)
+    terms = np.empty(mi.size, dtype=np.float64)
+    lib().orc_gemm_sampled_terms(dtype, _ptr(w), _ptr(xq), K, mi.size, _ptr(mi), _ptr(ni), _ptr(out), _ptr(terms))
+    return out, terms
+
+
+def block_sums(dtype: int, w: np.ndarray, xq: np.ndarray, M: int, N: int, K: int, threads: int = 0) -> np.ndarray:
+    """int64 [M, N, nblk, 2]: per scale block (256 elements; Q8_0: 32) the integer sums the keep-quant
+    formula scales -- (sum_j sc_j*P_j, sum_j m_j*(bs_2j + bs_2j+1)) for Q4_K/Q5_K, (sum_j sc_j*P_j, 0)
+    for Q6_K, (P_b, 0) for Q8_0."""
+    w, xq = _check_gemm_args(dtype, w, xq, N, K)
+    nblk = K // BLOCK_ELEMS[dtype]
+    out = np.empty((M, N, nblk, 2), dtype=np.int64)
+    lib().orc_block_sums(dtype, _ptr(w), _ptr(xq), M, N, K, _ptr(out), threads or max_threads())
     return out
 
 

@@ -344,29 +344,24 @@ ORC_API void orc_swiglu(const float *g, const float *u, int64_t M, int64_t K, in
 
 /* RMSNorm producer (vllm.cpp PR #2890, the fused norm-quant epilogue commit: the norm row kernel
  * emits the row's Q8_K blocks beside its normalized output, byte-identical to quantizing that output
- * with the standalone quantizer).  The pages give no formula; the reading is the usual one:
+ * with the standalone quantizer).  The pages give no formula; the reading is the usual definition:
  *   ss = sum_i x_i^2,  r = 1 / sqrt(ss / K + eps),  y_i = (x_i * r) * gamma_i        (all fp32)
- * with the sum in the fixed order of a 256-thread row reduction, because the quantised codes of y
- * depend on every rounding of r: thread t adds x[t]^2, x[t+256]^2, ... in ascending order; the 32
- * thread sums of each group of 32 combine in xor-butterfly order (butterfly_sum32); the 8 group sums
- * are added in ascending order.  Division and square root are the IEEE ones (sqrtf, /).
+ * with the sum of squares taken in plain ascending order (i = 0, 1, ..., K-1), each square and each
+ * add rounded on its own.  Division and square root are the IEEE ones (sqrtf, /).  A GPU row
+ * reduction sums in another order, so its ss differs from this one within the error bound of
+ * recursive summation; the tests bound y by that, and check the Q8_K bytes on the GPU's own y.
  * Parity pinned: f64 RMSNorm within the fp32 error bound, a constant row (exact), the zero row,
- * invariance under scaling x by a power of two, position independence of x_i*gamma_i. */
+ * invariance under scaling x by a power of two, position independence of x_i*gamma_i, and the
+ * ascending order itself by rows whose total is a closed form only in that order. */
 ORC_API void orc_rmsnorm(const float *x, const float *gamma, float eps, int64_t M, int64_t K, int64_t ldx, float *y,
                          int64_t ldy) {
     for (int64_t m = 0; m < M; ++m) {
         const float *xr = x + m * ldx;
-        float th[256];
-        for (int t = 0; t < 256; ++t) {
-            float s = 0.0f;
-            for (int64_t i = t; i < K; i += 256) {
-                float sq = xr[i] * xr[i];
-                s = s + sq;
-            }
-            th[t] = s;
-        }
         float total = 0.0f;
-        for (int w = 0; w < 8; ++w) total = total + butterfly_sum32(th + 32 * w);
+        for (int64_t i = 0; i < K; ++i) {
+            float sq = xr[i] * xr[i];
+            total = total + sq;
+        }
         float mean = total / (float)K;
         float r = 1.0f / sqrtf(mean + eps);
         for (int64_t i = 0; i < K; ++i) {
@@ -428,31 +423,58 @@ ORC_API void orc_partials_row(int dtype, const uint8_t *wrow, const uint8_t *xro
     }
 }
 
+/* The integer sums of one scale block, built from the partial dots and the block's integer scales:
+ *   Q4_K, Q5_K (per 256): sumi = sum_j sc_j*P_j,  summ = sum_j m_j*(bs_2j + bs_2j+1)  (j < 8)
+ *   Q6_K (per 256):       sumi = sum_j sc_j*P_j (j < 16),  summ = 0
+ *   Q8_0 (per 32):        sumi = P_b,  summ = 0
+ * wb / xb point at the weight and activation block.  These are the integers the keep-quant formula
+ * scales: y = sum over blocks of d_a*(d_w*sumi - dmin*summ) (vllm.cpp PR #2890, keep-quant
+ * provider commit: integer dots in the CPU accumulation order). */
+static void block_sums(int dtype, const uint8_t *wb, const uint8_t *xb, int64_t *sumi, int64_t *summ) {
+    *sumi = 0;
+    *summ = 0;
+    if (dtype == ORC_Q4_K || dtype == ORC_Q5_K) {
+        int32_t P[8];
+        orc_partials_row(dtype, wb, xb, 256, P);
+        for (int j = 0; j < 8; ++j) {
+            int sc, mn;
+            q4k_scale_min(wb + 4, j, &sc, &mn);
+            *sumi += (int64_t)sc * P[j];
+            *summ += (int64_t)mn * (rd_i16(xb + 260 + 4 * j) + rd_i16(xb + 262 + 4 * j));
+        }
+    } else if (dtype == ORC_Q6_K) {
+        int32_t P[16];
+        orc_partials_row(ORC_Q6_K, wb, xb, 256, P);
+        const int8_t *sc = (const int8_t *)(wb + 192);
+        for (int j = 0; j < 16; ++j) *sumi += (int64_t)sc[j] * P[j];
+    } else if (dtype == ORC_Q8_0) {
+        int32_t P;
+        orc_partials_row(ORC_Q8_0, wb, xb, 32, &P);
+        *sumi = P;
+    }
+}
+
 /* One output y = sum over blocks of the scaled integer dots, in ascending
  * block order, fp32, no fused multiply-add:
  *   Q4_K: acc += (d_a*d_w)*(float)sumi - (d_a*dmin)*(float)summ,
  *         sumi = sum_j sc_j*P_j, summ = sum_j m_j*(bs_2j + bs_2j+1)
  *   Q6_K: acc += (d_a*d_w)*(float)sumi,  sumi = sum_j sc_j*P_j
  *   Q8_0: acc += (d_w*d_a)*(float)P_b
+ * absterms (may be NULL) receives, in f64, the sum over blocks of |(d_a*d_w)*sumi| + |(d_a*dmin)*summ|:
+ * the scale of the rounding errors of any order of these fp32 operations.
  * Parity pinned: f64 dequant band, integer-matmul special cases, zero input,
  * independent brute force on tiny inputs. */
-ORC_API float orc_dot_row(int dtype, const uint8_t *wrow, const uint8_t *xrow, int64_t K) {
+static float dot_row(int dtype, const uint8_t *wrow, const uint8_t *xrow, int64_t K, double *absterms) {
     float acc = 0.0f;
+    double mag = 0.0;
     if (dtype == ORC_Q4_K || dtype == ORC_Q5_K) {
         /* Q5_K: the Q4_K formula over 5-bit codes (same header: d, dmin, packed scales and mins) */
         const int64_t bb = dtype == ORC_Q4_K ? 144 : 176;
         for (int64_t b = 0; b < K / 256; ++b) {
             const uint8_t *wb = wrow + bb * b;
             const uint8_t *xb = xrow + 292 * b;
-            int32_t P[8];
-            orc_partials_row(dtype, wb, xb, 256, P);
-            int64_t sumi = 0, summ = 0;
-            for (int j = 0; j < 8; ++j) {
-                int sc, mn;
-                q4k_scale_min(wb + 4, j, &sc, &mn);
-                sumi += (int64_t)sc * P[j];
-                summ += (int64_t)mn * (rd_i16(xb + 260 + 4 * j) + rd_i16(xb + 262 + 4 * j));
-            }
+            int64_t sumi, summ;
+            block_sums(dtype, wb, xb, &sumi, &summ);
             float da = rd_f32(xb);
             float dw = orc_half_to_float((uint16_t)(wb[0] | (wb[1] << 8)));
             float dmin = orc_half_to_float((uint16_t)(wb[2] | (wb[3] << 8)));
@@ -462,36 +484,41 @@ ORC_API float orc_dot_row(int dtype, const uint8_t *wrow, const uint8_t *xrow, i
             float t4 = t3 * (float)(int32_t)summ;
             float t5 = t2 - t4;
             acc = acc + t5;
+            mag += fabs((double)t2) + fabs((double)t4);
         }
     } else if (dtype == ORC_Q6_K) {
         for (int64_t b = 0; b < K / 256; ++b) {
             const uint8_t *wb = wrow + 210 * b;
             const uint8_t *xb = xrow + 292 * b;
-            int32_t P[16];
-            orc_partials_row(ORC_Q6_K, wb, xb, 256, P);
-            const int8_t *sc = (const int8_t *)(wb + 192);
-            int64_t sumi = 0;
-            for (int j = 0; j < 16; ++j) sumi += (int64_t)sc[j] * P[j];
+            int64_t sumi, summ;
+            block_sums(ORC_Q6_K, wb, xb, &sumi, &summ);
             float da = rd_f32(xb);
             float dw = orc_half_to_float((uint16_t)(wb[208] | (wb[209] << 8)));
             float t1 = da * dw;
             float t2 = t1 * (float)(int32_t)sumi;
             acc = acc + t2;
+            mag += fabs((double)t2);
         }
     } else if (dtype == ORC_Q8_0) {
         for (int64_t b = 0; b < K / 32; ++b) {
             const uint8_t *wb = wrow + 34 * b;
             const uint8_t *xb = xrow + 36 * b;
-            int32_t P;
-            orc_partials_row(ORC_Q8_0, wb, xb, 32, &P);
+            int64_t P, unused;
+            block_sums(ORC_Q8_0, wb, xb, &P, &unused);
             float dw = orc_half_to_float((uint16_t)(wb[0] | (wb[1] << 8)));
             float da = orc_half_to_float((uint16_t)(xb[0] | (xb[1] << 8)));
             float t1 = dw * da;
-            float t2 = t1 * (float)P;
+            float t2 = t1 * (float)(int32_t)P;
             acc = acc + t2;
+            mag += fabs((double)t2);
         }
     }
+    if (absterms) *absterms = mag;
     return acc;
+}
+
+ORC_API float orc_dot_row(int dtype, const uint8_t *wrow, const uint8_t *xrow, int64_t K) {
+    return dot_row(dtype, wrow, xrow, K, NULL);
 }
 
 static int64_t act_row_bytes(int wdtype, int64_t K) {
@@ -522,6 +549,36 @@ ORC_API void orc_gemm_sampled(int dtype, const uint8_t *w, const uint8_t *xq, in
                               const int64_t *m_idx, const int64_t *n_idx, float *out) {
     int64_t wrb = w_row_bytes(dtype, K), xrb = act_row_bytes(dtype, K);
     for (int64_t s = 0; s < S; ++s) out[s] = orc_dot_row(dtype, w + n_idx[s] * wrb, xq + m_idx[s] * xrb, K);
+}
+
+/* Sampled outputs together with their error scale (dot_row's absterms), for elementwise bounds. */
+ORC_API void orc_gemm_sampled_terms(int dtype, const uint8_t *w, const uint8_t *xq, int64_t K, int64_t S,
+                                    const int64_t *m_idx, const int64_t *n_idx, float *out, double *absterms) {
+    int64_t wrb = w_row_bytes(dtype, K), xrb = act_row_bytes(dtype, K);
+    for (int64_t s = 0; s < S; ++s)
+        out[s] = dot_row(dtype, w + n_idx[s] * wrb, xq + m_idx[s] * xrb, K, absterms + s);
+}
+
+/* The integer sums (block_sums) of every scale block of a whole GEMM: out[m][n][nblk][2] holds
+ * (sumi, summ) as int64, nblk = K/256 (Q4_K, Q5_K, Q6_K) or K/32 (Q8_0).  Rows are independent. */
+ORC_API void orc_block_sums(int dtype, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K,
+                            int64_t *out, int nthreads) {
+    int64_t wrb = w_row_bytes(dtype, K), xrb = act_row_bytes(dtype, K);
+    int64_t be = orc_block_elems(dtype), bb = orc_block_bytes(dtype);
+    int64_t ab = dtype == ORC_Q8_0 ? 36 : 292;
+    int64_t nblk = K / be;
+    int64_t total = M * N;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads > 0 ? nthreads : 1)
+#endif
+    for (int64_t t = 0; t < total; ++t) {
+        int64_t m = t / N, n = t % N;
+        for (int64_t b = 0; b < nblk; ++b) {
+            int64_t *o = out + (t * nblk + b) * 2;
+            block_sums(dtype, w + n * wrb + b * bb, xq + m * xrb + b * ab, o, o + 1);
+        }
+    }
+    (void)nthreads;
 }
 
 /* Partials for a whole GEMM: out[m][n][K/subblock]. */

@@ -91,3 +91,28 @@ def test_host_validation_errors_without_gpu(built):
     assert st == 4
     # int8 probe: iters must be positive
     assert L.kq_probe_int8_mma_sync(0, 16, None, None) == 1
+    # debug twins of the tensor-core path: same argument checks, and only tensor-core shapes
+    st = L.kq_debug_tc_sums(kq.Q4_K, 16, 16, 8, 256, 1024, 16, 256, 16, 256, 1 << 30, None)
+    assert st == 1 and b"tensor-core" in L.kq_last_error()          # M = 8 is the batched-decode path
+    st = L.kq_debug_tc_sums(kq.Q4_K, 16, 16, 256, 256, 1024, 16, 256, None, 256, 1 << 30, None)
+    assert st == 1 and b"sums" in L.kq_last_error()
+    st = L.kq_debug_tc_wait_timeout(kq.Q4_K, 16, 16, 256, 256, 1024, 16, 256, 10, 256, 1 << 30, None)
+    assert st == 1 and b"wait_limit_ns" in L.kq_last_error()
+    st = L.kq_debug_tc_sums_grouped(kq.Q4_K, 16, 4, 16, 1, 16, 8, 2, 256, 1024, 16, None, 256, 1 << 20, None)
+    assert st == 1
+
+
+def test_split_factor_host_logic(built):
+    """The split-K choice is host logic: 0 off the tensor-core path, 1 for Q8_0 (one ascending sum per
+    output), a power of two up to 8 that leaves at least two super-blocks per cluster rank, and a split
+    for the few-tile long-K shapes (two 128-row tiles over K = 4096: nothing else fills the SMs)."""
+    assert kq.kq_debug_tc_splits(kq.Q4_K, 8, 256, 4096) == 0       # batched decode
+    assert kq.kq_debug_tc_splits(kq.Q4_K, 256, 64, 4096) == 0      # N < 128
+    assert kq.kq_debug_tc_splits(kq.Q8_0, 128, 256, 4096) == 1
+    for dt in (kq.Q4_K, kq.Q5_K, kq.Q6_K):
+        for (M, N, K) in [(128, 256, 4096), (128, 4096, 4096), (512, 4096, 14336), (2048, 14336, 4096), (130, 200, 768)]:
+            S = kq.kq_debug_tc_splits(dt, M, N, K)
+            assert S in (1, 2, 4, 8)
+            assert S == 1 or -(-(K // 256) // S) >= 2      # at least two super-blocks per rank
+        assert kq.kq_debug_tc_splits(dt, 128, 256, 4096) > 1
+        assert kq.kq_debug_tc_splits(dt, 2048, 14336, 4096) == 1    # 1792 tiles fill the SMs many times

@@ -24,6 +24,19 @@ def _oracle_act(dtype, x):
     return oracle.quantize_q8_1(x) if dtype == kq.Q8_0 else oracle.quantize_q8_k(x)
 
 
+def tc_bound(terms: np.ndarray, K: int, splits: int) -> np.ndarray:
+    """Elementwise bound on |y_gpu - y_oracle| for the tensor-core Q4_K/Q5_K/Q6_K outputs.
+
+    The integer sums of every super-block are exact on both sides (below 2^24 in fp32); only the fp32
+    scaling differs.  The oracle rounds each product, the difference and the running sum (at most
+    3 roundings per block plus one per add of the running sum, which is bounded by the sum of the
+    magnitudes of the block terms); the kernel fuses the products into two FMAs and adds K/256 terms,
+    and a split-K cluster adds its partial sums once more per rank.  Each side is therefore within
+    (K/256 + 3 + splits) * 2^-24 * terms of the exact value, with terms = sum over super-blocks of
+    |(d_a*d_w)*sumi| + |(d_a*dmin)*summ| (oracle.gemm_sampled_terms); the difference within twice that."""
+    return (K // 256 + 4 + splits) * 2.0 ** -23 * terms
+
+
 # ----------------------------------------------------------------------------- GEMV
 
 
@@ -124,6 +137,14 @@ def test_gemm_small_and_partials(dtype, M, N, K):
     ref = oracle.gemm(dtype, w, xq_ref, M, N, K)
     assert np.isfinite(y).all()
     assert nmse(y, ref) <= 1e-6
+    S = kq.kq_debug_tc_splits(dtype, M, N, K)
+    if S and dtype != kq.Q8_0:
+        # tensor-core Q4_K/Q5_K/Q6_K: every output within the elementwise rounding bound
+        mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+        _, terms = oracle.gemm_sampled_terms(dtype, w, xq_ref, K, mi, ni)
+        assert np.all(np.abs(y.reshape(-1).astype(np.float64) - ref.reshape(-1)) <= tc_bound(terms, K, S))
+    elif S:
+        assert np.array_equal(y, ref)    # Q8_0 on the tensor cores adds its blocks in the CPU order
     sub = oracle.SUBBLOCK[dtype]
     P = torch.full((M, N, K // sub), -7, dtype=torch.int32, device=DEV)
     kq.kq_debug_partials(dtype, wn, xq, M, N, K, P)
@@ -246,14 +267,19 @@ def test_gemm_adversarial_max_magnitudes(M):
 
 @pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q5_K, kq.Q6_K])
 @pytest.mark.parametrize("shape", synth.PREFILL_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
-def test_gemm_prefill_full_size_sampled(dtype, shape):
+@pytest.mark.parametrize("M", synth.PREFILL_M)
+def test_gemm_prefill_full_size_sampled(dtype, shape, M):
+    """Every prefill workload shape at every token count, in the launch configuration the benchmark
+    times (the M = 128 shapes take split-K clusters): 3000 sampled outputs against the oracle, each
+    within the elementwise rounding bound, and NMSE <= 1e-6 overall."""
     N, K = shape
-    M = 2048
     g = synth.rng(0)
     w = synth.weights(dtype, N, K, g)
     x = synth.activations(M, K, g, outliers=True)
     wn = repack(dtype, w, N, K)
     xq = act_quant(dtype, dev(x), M, K)
+    S = kq.kq_debug_tc_splits(dtype, M, N, K)
+    assert S >= 1, "expected the tensor-core path"
     y = host(gemm(dtype, wn, xq, M, N, K))
     assert np.isfinite(y).all()
     xq_h = host(xq).reshape(M, -1)
@@ -261,8 +287,32 @@ def test_gemm_prefill_full_size_sampled(dtype, shape):
     ni = g.integers(0, N, 3000)
     mi[:4] = [0, M - 1, 0, M - 1]
     ni[:4] = [0, N - 1, N - 1, 0]
-    ref = oracle.gemm_sampled(dtype, w, xq_h, K, mi, ni)
+    ref, terms = oracle.gemm_sampled_terms(dtype, w, xq_h, K, mi, ni)
+    err = np.abs(y[mi, ni].astype(np.float64) - ref)
+    bound = tc_bound(terms, K, S)
+    assert np.all(err <= bound), (S, (err / bound).max())
     assert nmse(y[mi, ni], ref) <= 1e-6
+
+
+@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q5_K, kq.Q6_K])
+@pytest.mark.parametrize("M,N,K,S", [(250, 600, 4096, 8), (129, 1280, 3072, 4), (130, 2200, 2048, 2),
+                                     (300, 392, 1536, 1)])
+def test_gemm_split_k_every_output(dtype, M, N, K, S):
+    """Shapes whose few output tiles make the tensor-core path split K across a cluster of S CTAs
+    (reduced in rank order through distributed shared memory), ragged in M and N: the split taken is
+    asserted, and EVERY output is checked against the oracle with the elementwise rounding bound."""
+    assert kq.kq_debug_tc_splits(dtype, M, N, K) == S
+    g = synth.rng(900 + M + N + K + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    y = host(gemm(dtype, wn, xq, M, N, K))
+    mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+    ref, terms = oracle.gemm_sampled_terms(dtype, w, host(xq).reshape(M, -1), K, mi, ni)
+    err = np.abs(y.reshape(-1).astype(np.float64) - ref)
+    assert np.all(err <= tc_bound(terms, K, S)), (err / tc_bound(terms, K, S)).max()
+    assert nmse(y.reshape(-1), ref) <= 1e-6
 
 
 def test_q8_0_swiglu_full_size_sampled():

@@ -474,6 +474,45 @@ def _brute_force_f64(dtype, w, x_blocks, M, N, K):
 
 
 @pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0])
+def test_block_sums_against_brute_force(dtype):
+    """The integer sums per scale block (sum_j sc_j*P_j and the min term), scaled in f64 as
+    d_a*(d_w*sumi - dmin*summ) and added over blocks, equal the independent pure-Python f64 brute force
+    to 1e-12 relative; their error scale (sum of |scaled terms|) bounds |y| from above."""
+    g = np.random.default_rng(23 + dtype)
+    M, N, K = 2, 3, 512
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    xq = oracle.quantize_q8_1(x) if dtype == oracle.Q8_0 else oracle.quantize_q8_k(x)
+    S = oracle.block_sums(dtype, w, xq, M, N, K)
+    ref = _brute_force_f64(dtype, w, xq, M, N, K)
+    for m in range(M):
+        for n in range(N):
+            tot = 0.0
+            if dtype == oracle.Q8_0:
+                for b in range(K // 32):
+                    dw = float(w[n, 34 * b:34 * b + 2].view(np.float16)[0])
+                    da = float(xq[m, 36 * b:36 * b + 2].view(np.float16)[0])
+                    assert S[m, n, b, 1] == 0
+                    tot += dw * da * int(S[m, n, b, 0])
+            else:
+                bb = {oracle.Q4_K: 144, oracle.Q5_K: 176, oracle.Q6_K: 210}[dtype]
+                for b in range(K // 256):
+                    blk = w[n, bb * b:bb * b + bb]
+                    da = float(np.frombuffer(xq[m, 292 * b:292 * b + 4].tobytes(), np.float32)[0])
+                    if dtype == oracle.Q6_K:
+                        dw, dmin = float(blk[208:210].view(np.float16)[0]), 0.0
+                        assert S[m, n, b, 1] == 0
+                    else:
+                        dw, dmin = (float(v) for v in blk[0:4].view(np.float16))
+                    tot += da * (dw * int(S[m, n, b, 0]) - dmin * int(S[m, n, b, 1]))
+            assert abs(tot - ref[m, n]) <= 1e-12 * max(1.0, abs(ref[m, n])), (m, n, tot, ref[m, n])
+    mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+    y, terms = oracle.gemm_sampled_terms(dtype, w, xq, K, mi, ni)
+    assert np.array_equal(y, oracle.gemm(dtype, w, xq, M, N, K).reshape(-1))
+    assert np.all(terms >= np.abs(ref.reshape(-1)) * (1 - 1e-6))
+
+
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0])
 def test_brute_force_tiny(dtype):
     g = np.random.default_rng(20 + dtype)
     M, N, K = 3, 4, 512
@@ -613,15 +652,18 @@ def test_q8_k_half_way_ties_go_to_even():
 # ----------------------------------------------------------------------------- RMSNorm producer
 
 
-def test_rmsnorm_sum_of_squares_order():
-    """Pins the order of the sum of squares (thread t adds x[t]^2, x[t+256]^2, ... in sequence) with a
-    closed form: x[0] = 4096, x[256] = x[512] = 1, the rest 0, K = 768.  Thread 0 adds 2^24 + 1, which
-    rounds to 2^24 (a tie, to even), then + 1 again: the total is exactly 2^24; the other partial sums
-    are 0.  An order that adds the two 1s first keeps 2^24 + 2 and gives another r (checked, so the pin
-    can fail).  Expected y_0 = (4096 * r) * 1 with r = 1 / sqrt(2^24 / 768), each an IEEE fp32 step."""
+@pytest.mark.parametrize("pos", [(1, 2), (700, 767), (383, 384)])
+def test_rmsnorm_sum_of_squares_ascending(pos):
+    """Pins the plain ascending sum of squares with a closed form: x[0] = 4096 (square 2^24), two other
+    elements 1 at the given positions, the rest 0, K = 768.  Added left to right, 2^24 + 1 is a tie
+    that rounds to even (2^24), and so is the second + 1: the total is exactly 2^24.  Any order that
+    adds the two 1s together before meeting 2^24 (a tree, a reversed loop, strided partial sums) keeps
+    2^24 + 2, which gives another r (checked, so the pin can fail).  Expected y_0 = (4096 * r) * 1 with
+    r = 1 / sqrt(2^24 / 768), each an IEEE fp32 step."""
     K = 768
     x = np.zeros((1, K), np.float32)
-    x[0, 0], x[0, 256], x[0, 512] = 4096.0, 1.0, 1.0
+    x[0, 0] = 4096.0
+    x[0, list(pos)] = 1.0
     gamma = np.ones(K, np.float32)
     y = oracle.rmsnorm(x, gamma, 0.0)
 
@@ -629,8 +671,20 @@ def test_rmsnorm_sum_of_squares_order():
         return np.float32(np.float32(1.0) / np.sqrt(np.float32(np.float32(total) / np.float32(K))))
 
     r = r_of(2.0 ** 24)
-    assert y[0, 0] == np.float32(np.float32(4096.0) * r) and y[0, 256] == r and y[0, 512] == r
+    assert y[0, 0] == np.float32(np.float32(4096.0) * r) and y[0, pos[0]] == r and y[0, pos[1]] == r
     assert np.float32(np.float32(4096.0) * r) != np.float32(np.float32(4096.0) * r_of(2.0 ** 24 + 2))
+
+
+def test_rmsnorm_sum_of_squares_small_first():
+    """The other direction of the same pin: ones first, then the large square.  Left to right the ones
+    add exactly (1 + 1 = 2), and 2 + 2^24 is exact too, so the total is 2^24 + 2: an order that puts the
+    large element first would round the ones away."""
+    K = 512
+    x = np.zeros((1, K), np.float32)
+    x[0, 10], x[0, 20], x[0, 300] = 1.0, 1.0, 4096.0
+    y = oracle.rmsnorm(x, np.ones(K, np.float32), 0.0)
+    r = np.float32(np.float32(1.0) / np.sqrt(np.float32(np.float32(2.0 ** 24 + 2) / np.float32(K))))
+    assert y[0, 10] == r and y[0, 300] == np.float32(np.float32(4096.0) * r)
 
 
 def test_rmsnorm_against_f64():
