@@ -295,8 +295,8 @@ def test_gemm_prefill_full_size_sampled(dtype, shape, M):
 
 
 @pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q5_K, kq.Q6_K])
-@pytest.mark.parametrize("M,N,K,S", [(250, 600, 4096, 8), (129, 1280, 3072, 4), (130, 2200, 2048, 2),
-                                     (300, 392, 1536, 1)])
+@pytest.mark.parametrize("M,N,K,S", [(250, 600, 4096, 8), (129, 1280, 3072, 4), (130, 2200, 2048, 4),
+                                     (300, 392, 1536, 2)])
 def test_gemm_split_k_every_output(dtype, M, N, K, S):
     """Shapes whose few output tiles make the tensor-core path split K across a cluster of S CTAs
     (reduced in rank order through distributed shared memory), ragged in M and N: the split taken is
