@@ -194,6 +194,26 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// Eight kind::f16 MMAs into the accumulator at d_tmem, A from tensor memory, issued back to back from
+// operands the caller computed beforehand (no integer work between the MMAs); the first one
+// accumulates iff acc0 != 0, the other seven always accumulate.
+__device__ __forceinline__ void mma8_f16_ts(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                           uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %17, 0;\n setp.eq.u32 q, %17, %17;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %18, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %18, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %18, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %18, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %18, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %18, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %18, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %18, q;\n}" ::"r"(d_tmem),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]),
+        "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc0), "r"(idesc)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

@@ -253,20 +253,24 @@ __device__ __forceinline__ void convert_q5k_kblock(uint4 v0, uint4 v1, const uin
     }
 }
 
-// Q6_K sub-block of one row (16 elements: 4 nibble words already shifted into the low nibbles, 4
-// high-bit words whose 2-bit fields for this sub-block sit at bit `hs`) -> 8 lo columns
-// (sc & 15)*(c-32) and 8 hi columns 16*(sc >> 4)*(c-32).  (0x6400 | c) = 1024 + c, so c-32 is one
-// exact subtraction; every product is an integer of at most 11 significant bits.
-__device__ __forceinline__ void convert_q6k_sub(const uint32_t (&nib)[4], const uint32_t (&hb)[4], int hs, int sc,
+// Q6_K sub-block of one row (16 elements: 4 nibble words whose codes sit in the low nibbles (HI =
+// false) or the high nibbles (HI = true) of each byte, 4 high-bit words whose 2-bit fields for this
+// sub-block sit at bit HS) -> 8 lo columns (sc & 15)*(c-32) and 8 hi columns 16*(sc >> 4)*(c-32).
+// The byte permute with 0x64 bytes builds (0x6400 | c) = 1024 + c directly, so c-32 is one exact
+// subtraction; every product is an integer of at most 11 significant bits.
+template <bool HI, int HS>
+__device__ __forceinline__ void convert_q6k_sub(const uint32_t (&nib)[4], const uint32_t (&hb)[4], int sc,
                                                 uint32_t (&lo)[8], uint32_t (&hi)[8]) {
     const int l = sc & 15, h16 = 16 * (sc >> 4);
     const __half2 ml = __float2half2_rn((float)l), nl = __float2half2_rn(-1056.0f * l);
     const __half2 mh = __float2half2_rn((float)h16), c1056 = __float2half2_rn(1056.0f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t c = (nib[i] & 0x0f0f0f0fu) | (((hb[i] >> hs) & 0x03030303u) << 4);
-        const __half2 x01 = u2h(__byte_perm(c, 0u, 0x4140) | 0x64006400u);
-        const __half2 x23 = u2h(__byte_perm(c, 0u, 0x4342) | 0x64006400u);
+        // high bits of the sub-block to bits 4-5 of every byte, the code's low 4 bits to bits 0-3
+        const uint32_t h = (HS <= 4 ? (hb[i] << (4 - HS)) : (hb[i] >> (HS - 4))) & 0x30303030u;
+        const uint32_t c = (HI ? ((nib[i] >> 4) & 0x0f0f0f0fu) : (nib[i] & 0x0f0f0f0fu)) | h;
+        const __half2 x01 = u2h(__byte_perm(c, 0x64646464u, 0x4140));
+        const __half2 x23 = u2h(__byte_perm(c, 0x64646464u, 0x4342));
         lo[2 * i] = h2u(__hfma2(x01, ml, nl));
         lo[2 * i + 1] = h2u(__hfma2(x23, ml, nl));
         hi[2 * i] = h2u(__hmul2(__hsub2(x01, c1056), mh));
@@ -475,18 +479,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_fence_after();
                 for (int pr = 0; pr < 2 && ok; ++pr) {
                     const int pp = 2 * t + pr, s = pp % NPAIR;
-                    if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
-                    tc_fence_after();
+                    // operands of the pair's MMAs, computed while the pair is still being filled, so the MMAs
+                    // go out back to back with no integer work between them
+                    uint32_t aa[2][8];
+                    uint64_t bb[2][8];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
                         const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
 #pragma unroll
                         for (int k16 = 0; k16 < 4; ++k16) {
-                            mma_f16_ts(d1, a0 + k16 * 8, bd + (uint64_t)(k16 * 2), idesc, (pr | h | k16) != 0);
-                            if (!C::EXT) mma_f16_ts(d1, a0 + 32 + k16 * 8, bd + (uint64_t)(k16 * 2), idesc, 1);
+                            if (C::EXT) {  // one MMA per 16 K: A column k16*8 of kblock h
+                                aa[0][h * 4 + k16] = a0 + k16 * 8;
+                                bb[0][h * 4 + k16] = bd + (uint64_t)(k16 * 2);
+                            } else {       // Q6_K: the lo and the 16*hi product of the same 16 K
+                                aa[h][2 * k16] = a0 + k16 * 8;
+                                aa[h][2 * k16 + 1] = a0 + 32 + k16 * 8;
+                                bb[h][2 * k16] = bb[h][2 * k16 + 1] = bd + (uint64_t)(k16 * 2);
+                            }
                         }
                     }
+                    if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
+                    tc_fence_after();
+                    mma8_f16_ts(d1, aa[0], bb[0], idesc, pr);
+                    if (!C::EXT) mma8_f16_ts(d1, aa[1], bb[1], idesc, 1);
                     mma_commit(&k_empty[s]);
                 }
                 if (!ok) break;
@@ -494,7 +510,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int e = t % C::NE;
                     if (!(ok = mbar_wait_sleep(&e_full[e], (t / C::NE) & 1, abort_flag, P.wait_ns))) break;
                     if (t > 0 && !(ok = C::Q5 ? mbar_wait_sleep(s2_empty, (t - 1) & 1, abort_flag, P.wait_ns)
-                                              : mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, P.wait_ns)))
+                                              : mbar_wait_sleep(&acc_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag,
+                                                                P.wait_ns)))
                         break;
                     tc_fence_after();
                     mma_f16(tbase + C::TM_S2, dEA + (uint64_t)(e * (4096 >> 4)), dEB + (uint64_t)(e * (4096 >> 4)),
@@ -628,17 +645,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tmem_st32(ta, r);
                 } else {
                     const uint32_t hb[4] = {qh[j].x, qh[j].y, qh[j].z, qh[j].w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        // sub-block 4kb+k: low nibbles of bytes 0-15 / 16-31, then high nibbles
-                        const uint4 v = (k & 1) ? cv[j][1] : cv[j][0];
-                        const int ns = (k >> 1) * 4;
-                        const uint32_t nib[4] = {v.x >> ns, v.y >> ns, v.z >> ns, v.w >> ns};
-                        uint32_t lo[8], hi[8];
-                        convert_q6k_sub(nib, hb, 2 * k, ksc[j][k], lo, hi);
-                        tmem_st8(ta + 8 * k, lo);
-                        tmem_st8(ta + 32 + 8 * k, hi);
-                    }
+                    // sub-block 4kb+k: low nibbles of bytes 0-15 / 16-31, then high nibbles
+                    const uint32_t n0[4] = {cv[j][0].x, cv[j][0].y, cv[j][0].z, cv[j][0].w};
+                    const uint32_t n1[4] = {cv[j][1].x, cv[j][1].y, cv[j][1].z, cv[j][1].w};
+                    uint32_t lo[8], hi[8];
+                    convert_q6k_sub<false, 0>(n0, hb, ksc[j][0], lo, hi);
+                    tmem_st8(ta, lo);
+                    tmem_st8(ta + 32, hi);
+                    convert_q6k_sub<false, 2>(n1, hb, ksc[j][1], lo, hi);
+                    tmem_st8(ta + 8, lo);
+                    tmem_st8(ta + 40, hi);
+                    convert_q6k_sub<true, 4>(n0, hb, ksc[j][2], lo, hi);
+                    tmem_st8(ta + 16, lo);
+                    tmem_st8(ta + 48, hi);
+                    convert_q6k_sub<true, 6>(n1, hb, ksc[j][3], lo, hi);
+                    tmem_st8(ta + 24, lo);
+                    tmem_st8(ta + 56, hi);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -785,7 +807,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // it, so it is read first, folded in as acc += da*(-dmin*S2) and released on its own
                 // barrier before the main accumulator (acc += da*(d*S1)).  With Q5_K's heavier
                 // conversion this takes the epilogue's second half off the chain that paces the steps
-                // (measured faster for Q5_K only; Q4_K reads both tiles together below).
+                // (measured faster for Q5_K only; Q4_K reads both tiles together below: with Q4_K the
+                // early release, also with the next step's main MMAs held behind this extension MMA,
+                // measured 1-9% slower).
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float s2[8];
@@ -808,8 +832,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int c = 0; c < 4; ++c) {
                 const uint32_t col = tq * 32 + c * 8;
                 float s1[8], s2[8];
+                constexpr bool S2LATE = C::EXT && !C::Q5;
                 tmem_ld8(lane_base + buf * TC_TOK + col, s1);
-                if (C::EXT && !C::Q5) tmem_ld8(lane_base + C::TM_S2 + col, s2);
+                if (S2LATE) tmem_ld8(lane_base + C::TM_S2 + col, s2);
                 tmem_wait_ld();
                 if (DBG) {
                     const TcTile T = tile_of(tile_i);
@@ -817,7 +842,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (!C::EXT) {
                         const float zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                         dbg_put(T, (int)col, gsb, 1, zero);
-                    } else if (!C::Q5) {
+                    } else if (S2LATE) {
                         dbg_put(T, (int)col, gsb, 1, s2);
                     }
                 }
@@ -827,13 +852,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int i = 0; i < 8; i += 2) {
                     float2 &a = *reinterpret_cast<float2 *>(&acc[c * 8 + i]);
                     const float2 dap2 = make_float2(da[i], da[i + 1]);
-                    if (C::Q5) {
-                        a = ffma2(fmul2(make_float2(s1[i], s1[i + 1]), dw2), dap2, a);  // acc += da*(d*S1)
-                    } else if (C::EXT) {
+                    if (S2LATE) {
                         // acc += da * (d*S1 - dmin*S2)
                         const float2 u = fmul2(make_float2(s2[i], s2[i + 1]), nm2);
                         const float2 v = ffma2(make_float2(s1[i], s1[i + 1]), dw2, u);
                         a = ffma2(v, dap2, a);
+                    } else if (C::EXT) {
+                        a = ffma2(fmul2(make_float2(s1[i], s1[i + 1]), dw2), dap2, a);  // acc += da*(d*S1)
                     } else {
                         // acc += (da*d) * S
                         a = ffma2(fmul2(dap2, dw2), make_float2(s1[i], s1[i + 1]), a);

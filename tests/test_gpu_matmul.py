@@ -28,13 +28,15 @@ def tc_bound(terms: np.ndarray, K: int, splits: int) -> np.ndarray:
     """Elementwise bound on |y_gpu - y_oracle| for the tensor-core Q4_K/Q5_K/Q6_K outputs.
 
     The integer sums of every super-block are exact on both sides (below 2^24 in fp32); only the fp32
-    scaling differs.  The oracle rounds each product, the difference and the running sum (at most
-    3 roundings per block plus one per add of the running sum, which is bounded by the sum of the
-    magnitudes of the block terms); the kernel fuses the products into two FMAs and adds K/256 terms,
-    and a split-K cluster adds its partial sums once more per rank.  Each side is therefore within
-    (K/256 + 3 + splits) * 2^-24 * terms of the exact value, with terms = sum over super-blocks of
-    |(d_a*d_w)*sumi| + |(d_a*dmin)*summ| (oracle.gemm_sampled_terms); the difference within twice that."""
-    return (K // 256 + 4 + splits) * 2.0 ** -23 * terms
+    scaling differs.  With nsb = K/256 super-blocks, u = 2^-24 and T = the sum over super-blocks of
+    |(d_a*d_w)*sumi| + |(d_a*dmin)*summ| (oracle.gemm_sampled_terms):
+      * the oracle rounds two products per term (error <= 2u|term|), their difference (u) and each of
+        the nsb adds of the running sum, whose magnitude never exceeds T: within (nsb + 3)*u*T;
+      * the kernel folds each super-block in with fused multiply-adds -- one add per super-block for
+        Q4_K and Q6_K, two for Q5_K (its min term first, then the main term) -- and a split-K cluster
+        adds its partial sums once more per rank: within (2*nsb + 1 + splits)*u*T at most.
+    So the difference is within (3*nsb + 4 + splits)*u*T; the bound takes two units more."""
+    return (3 * (K // 256) + 6 + splits) * 2.0 ** -24 * terms
 
 
 # ----------------------------------------------------------------------------- GEMV
