@@ -494,12 +494,18 @@ def _aux_q8_0(device):
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
     t_pro = _time_graph(lambda: kq.kq_swiglu_quantize_q8_1(gu, gu[:, K:], M, K, 2 * K, xq), 5)
     t_gemm = _time_graph(lambda: kq.kq_gemm(synth.Q8_0, wn, xq, M, N, K, y, N, ws, wsb), 5)
+    # the same GEMM with the block scales folded into the f16 operands (kq_gemm_ex, KQ_GEMM_FOLD_SCALES):
+    # one accumulator per tile instead of one read-out per 32-block; not bit-exact (rounding-bounded)
+    t_fold = _time_graph(lambda: kq.kq_gemm_ex(synth.Q8_0, wn, xq, M, N, K, y, N, kq.GEMM_FOLD_SCALES, ws, wsb), 5)
     pro_bytes = 2 * M * K * 4 + kq.q8_1_bytes(M, K)
+    ops = 2.0 * M * N * K
     out["q8_0_swiglu_gemm"] = {
         "workload": c["name"], "prologue_us": round(t_pro * 1e3, 1),
         "prologue_gbs": round(pro_bytes / (t_pro * 1e-3) / 1e9, 1), "gemm_us": round(t_gemm * 1e3, 1),
-        "gemm_tops": round(2.0 * M * N * K / (t_gemm * 1e-3) / 1e12, 2),
-        "total_us": round((t_pro + t_gemm) * 1e3, 1)}
+        "gemm_tops": round(ops / (t_gemm * 1e-3) / 1e12, 2),
+        "total_us": round((t_pro + t_gemm) * 1e3, 1),
+        "gemm_folded_us": round(t_fold * 1e3, 1), "gemm_folded_tops": round(ops / (t_fold * 1e-3) / 1e12, 2),
+        "total_folded_us": round((t_pro + t_fold) * 1e3, 1)}
     del gu, xq, y, ws, wn
     return out
 

@@ -424,6 +424,22 @@ kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t
     return launch_mmq_exact(wt, 0, false, a, (unsigned)gy, st);
 }
 
+kq_status kq_gemm_ex(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
+                     int64_t ldy, unsigned flags, void *workspace, size_t ws_bytes, kq_stream_t stream) {
+    if (flags & ~(unsigned)KQ_GEMM_FOLD_SCALES)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_ex: unknown flags 0x%x", flags & ~(unsigned)KQ_GEMM_FOLD_SCALES);
+    if (!(flags & KQ_GEMM_FOLD_SCALES)) return kq_gemm(wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes, stream);
+    kq_status s = check_gemm_call("kq_gemm_ex", wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes);
+    if (s != KQ_OK) return s;
+    if (wt != KQ_Q8_0)
+        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_ex: KQ_GEMM_FOLD_SCALES takes Q8_0 weights, not %s",
+                    dtype_name(wt));
+    // shapes off the tensor-core path have no folded form: the exact kernels serve them
+    if (!tc_eligible(wt, M, N, K)) return kq_gemm(wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes, stream);
+    return tc_gemm_folded(static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
+                          static_cast<uint8_t *>(workspace), (cudaStream_t)stream);
+}
+
 size_t kq_gemm_f32_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || K % 256) return 0;
     // kq_gemm's workspace first (at least the 256-byte header holding the device flag, so

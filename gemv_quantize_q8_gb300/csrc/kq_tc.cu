@@ -62,6 +62,7 @@ struct TcCfg<KQ_Q4_K> {
     static constexpr bool EXT = true;     // min term through the extension MMA
     static constexpr bool Q8 = false;     // per-32-block scales (Q8_0 x Q8_1)
     static constexpr bool Q5 = false;     // fifth code bit from the row's high-bit bytes (Q5_K)
+    static constexpr bool FOLD = false;   // scales folded into the f16 operands (one accumulator per tile)
     static constexpr int A_COLS = 32;     // TMEM columns of one converted kblock (64 f16)
     static constexpr int NACC = 2;        // accumulator buffers
     static constexpr int BPS = 1;         // accumulator read-outs per step (scale blocks per 256 K)
@@ -73,14 +74,14 @@ struct TcCfg<KQ_Q4_K> {
 template <>
 struct TcCfg<KQ_Q5_K> {  // Q4_K's header and min term; 5-bit codes, sc*c <= 63*31 exact in f16
     static constexpr int CB = kQ5KChunk;
-    static constexpr bool EXT = true, Q8 = false, Q5 = true;
+    static constexpr bool EXT = true, Q8 = false, Q5 = true, FOLD = false;
     static constexpr int A_COLS = 32, NACC = 2, BPS = 1, H_ROW = 8, NP = 2, NE = 2;
     static constexpr uint32_t TM_S2 = 256, TM_A = 384;
 };
 template <>
 struct TcCfg<KQ_Q6_K> {
     static constexpr int CB = kQ6KChunk;
-    static constexpr bool EXT = false, Q8 = false, Q5 = false;
+    static constexpr bool EXT = false, Q8 = false, Q5 = false, FOLD = false;
     static constexpr int A_COLS = 64;     // lo tile (32 columns) then 16*hi tile (32 columns)
     static constexpr int NACC = 2, BPS = 1, H_ROW = 8;  // f32 (d, 0)
     static constexpr int NP = 2, NE = 2;
@@ -89,13 +90,26 @@ struct TcCfg<KQ_Q6_K> {
 template <>
 struct TcCfg<KQ_Q8_0> {
     static constexpr int CB = kQ80Chunk;
-    static constexpr bool EXT = false, Q8 = true, Q5 = false;
+    static constexpr bool EXT = false, Q8 = true, Q5 = false, FOLD = false;
     static constexpr int A_COLS = 32;
     // every 32-element block has its own weight and activation scale, so every block's integer
     // dot P_b is read out of its own accumulator: three buffers rotate along the blocks
     static constexpr int NACC = 3, BPS = 8, H_ROW = 16;  // the row's 8 f16 block scales
     static constexpr int NP = 2, NE = 2;
     static constexpr uint32_t TM_S2 = 0, TM_A = 384;
+};
+// Q8_0 x Q8_1 with the block scales folded into the f16 operands: the converters write f16(d_w*w), the
+// activation panel holds f16(d_a*q), so every product is the scaled one (each operand rounded once to
+// f16) and a tile accumulates over the whole of K in one TMEM buffer, read out once per tile.
+constexpr int KQ_Q8_0F = 103;  // internal: not a kq_dtype of the ABI
+template <>
+struct TcCfg<KQ_Q8_0F> {
+    static constexpr int CB = kQ80Chunk;
+    static constexpr bool EXT = false, Q8 = false, Q5 = false, FOLD = true;
+    static constexpr int A_COLS = 32;
+    static constexpr int NACC = 2, BPS = 1, H_ROW = 16;  // accumulators alternate per tile
+    static constexpr int NP = 2, NE = 2;
+    static constexpr uint32_t TM_S2 = 0, TM_A = 256;
 };
 // TMEM map: accumulator buffers at columns 0, 128 (and 256 for Q8_0); Q4_K min-term tile at 256;
 // converted kblock stages from TM_A on (4 stages = one super-block).
@@ -123,6 +137,8 @@ static_assert(TcLayout<KQ_Q4_K>::ALLOC <= 227 * 1024, "Q4_K tensor-core smem bud
 static_assert(TcLayout<KQ_Q6_K>::ALLOC <= 227 * 1024, "Q6_K tensor-core smem budget");
 static_assert(TcLayout<KQ_Q5_K>::ALLOC <= 227 * 1024, "Q5_K tensor-core smem budget");
 static_assert(TcLayout<KQ_Q8_0>::ALLOC <= 227 * 1024, "Q8_0 tensor-core smem budget");
+static_assert(TcLayout<KQ_Q8_0F>::ALLOC <= 227 * 1024, "folded Q8_0 tensor-core smem budget");
+static_assert(TcCfg<KQ_Q8_0F>::TM_A + 4 * TcCfg<KQ_Q8_0F>::A_COLS <= TMEM_COLS, "folded Q8_0 TMEM map");
 // the split-K reduction parks a 128 x (128 + 4) fp32 tile in the activation ring
 static_assert(TC_TOK * (TC_ROWS + 4) * 4 <= NACT * ACT_TILE, "split-K staging fits the activation ring");
 
@@ -378,7 +394,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tma_load_2d(sEB + e * 4096, &tmE, &e_full[e], gsb * 16, T.m0);
                     last_e[e] = eph;
                 }
-                {
+                if (!C::FOLD) {  // the folded path has no per-step scales
                     const int h = st & 3, hph = (st >> 2) & 1;
                     if (!(ok = mbar_wait_sleep(&h_empty[h], hph ^ 1, abort_flag, P.wait_ns))) break;
                     // the scale panel has one row of M_pad floats per scale block (256 or 32 K)
@@ -474,7 +490,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
             }
-            for (int t = w; t < nsteps && ok && !C::Q8; t += 2) {  // t: step
+            if (C::FOLD) {
+                // folded Q8_0: one issuer (the MMAs into a tile's accumulator then go in one fixed order,
+                // so the result is deterministic); a tile's steps all accumulate into buffer (tile & 1),
+                // committed once at the tile's last step
+                for (int t = 0, ti = 0, tt = 0; t < nsteps && ok && w == 0; ++t) {
+                    const int ab = ti & 1;
+                    const bool first = tt == 0, last = tt == nsb - 1;
+                    if (first) {
+                        if (!(ok = mbar_wait_sleep(&acc_empty[ab], ((ti >> 1) & 1) ^ 1, abort_flag, P.wait_ns))) break;
+                        tc_fence_after();
+                    }
+                    for (int pr = 0; pr < 2 && ok; ++pr) {
+                        const int pp = 2 * t + pr, s = pp % NPAIR;
+                        uint32_t aa[8];
+                        uint64_t bb[8];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
+                            const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
+#pragma unroll
+                            for (int k16 = 0; k16 < 4; ++k16) {
+                                aa[h * 4 + k16] = a0 + k16 * 8;
+                                bb[h * 4 + k16] = bd + (uint64_t)(k16 * 2);
+                            }
+                        }
+                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
+                        tc_fence_after();
+                        mma8_f16_ts(tbase + ab * TC_TOK, aa, bb, idesc, (first && pr == 0) ? 0u : 1u);
+                        mma_commit(&k_empty[s]);
+                    }
+                    if (!ok) break;
+                    if (last) mma_commit(&acc_full[ab]);
+                    if (++tt == nsb) { tt = 0; ++ti; }
+                }
+            }
+            for (int t = w; t < nsteps && ok && !C::Q8 && !C::FOLD; t += 2) {  // t: step
                 if (!(ok = mbar_wait_sleep(&acc_empty[w], ((t >> 1) & 1) ^ 1, abort_flag, P.wait_ns))) break;
                 tc_fence_after();
                 for (int pr = 0; pr < 2 && ok; ++pr) {
@@ -543,9 +594,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // rows past N were not loaded: their scales are forced to 0, so they convert to zeros
             const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
             const int r16 = row & 15;
-            if (C::Q8) {
+            if (C::Q8 || C::FOLD) {
                 // Q8_0: the row's 64 codes of kblock kb sit at kb*1024 + r16*64; its 8 f16 block
-                // scales at 4096 + r16*16.  Codes go to f16 exactly: (0x6400 | (c ^ 0x80)) = 1152 + c.
+                // scales at 4096 + r16*16.  Codes go to f16 exactly: (0x6400 | (c ^ 0x80)) = 1152 + c;
+                // the folded path then multiplies each code by its block's f16 scale (one rounding).
                 uint4 cv[2][4];
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
@@ -563,14 +615,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     tc_fence_after();
                     uint32_t r[32];
+                    // folded: kblock kb = grp + 2j holds blocks 2kb (codes 0-31) and 2kb+1 (32-63), whose
+                    // scales are the two halves of word kb of the row's scale vector
+                    const uint32_t dword = (grp + 2 * j == 0) ? dv.x : (grp + 2 * j == 1) ? dv.y
+                                         : (grp + 2 * j == 2) ? dv.z : dv.w;
+                    const __half2 dlo = u2h((dword & 0xffffu) * 0x10001u), dhi = u2h((dword >> 16) * 0x10001u);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const uint32_t wv[4] = {cv[j][i].x ^ 0x80808080u, cv[j][i].y ^ 0x80808080u,
                                                 cv[j][i].z ^ 0x80808080u, cv[j][i].w ^ 0x80808080u};
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            r[8 * i + 2 * k] = h2u(__hsub2(u2h(__byte_perm(wv[k], 0x64646464u, 0x4140)), c1152));
-                            r[8 * i + 2 * k + 1] = h2u(__hsub2(u2h(__byte_perm(wv[k], 0x64646464u, 0x4342)), c1152));
+                            __half2 a = __hsub2(u2h(__byte_perm(wv[k], 0x64646464u, 0x4140)), c1152);
+                            __half2 b = __hsub2(u2h(__byte_perm(wv[k], 0x64646464u, 0x4342)), c1152);
+                            if (C::FOLD) {
+                                a = __hmul2(a, i < 2 ? dlo : dhi);
+                                b = __hmul2(b, i < 2 ? dlo : dhi);
+                            }
+                            r[8 * i + 2 * k] = h2u(a);
+                            r[8 * i + 2 * k + 1] = h2u(b);
                         }
                     }
                     tmem_st32(lane_base + C::TM_A + (grp + 2 * j) * C::A_COLS, r);
@@ -579,7 +642,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     mbar_arrive(&k_full[(2 * t + j) % NPAIR]);
                 }
                 if (!ok) break;
-                if (grp == 0) {
+                if (grp == 0 && !C::FOLD) {
                     const int h = t & 3;
                     if (!(ok = mbar_wait_sleep(&h_empty[h], ((t >> 2) & 1) ^ 1, abort_flag, P.wait_ns))) break;
                     reinterpret_cast<uint4 *>(sH + h * TC_ROWS * C::H_ROW)[row] = dv;
@@ -746,7 +809,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
             }
-            if (C::Q8) {
+            if (C::FOLD) {
+                // folded Q8_0: the tile's accumulator holds the finished sums; read it once, at the
+                // tile's last step, and release the buffer for the tile after next
+                if (!last) continue;
+                const int ab = tile_i & 1;
+                if (!(ok = mbar_wait_sleep(&acc_full[ab], (tile_i >> 1) & 1, abort_flag, P.wait_ns))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[8];
+                    tmem_ld8(lane_base + ab * TC_TOK + tq * 32 + c * 8, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[c * 8 + i] = v[i];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            } else if (C::Q8) {
                 // Q8_0: per 32-element block b, acc += (d_w*d_a)*P_b with each product rounded on its
                 // own and the blocks added in ascending K order -- the CPU oracle's arithmetic, so the
                 // result is bit-identical to it
@@ -1080,6 +1161,35 @@ __global__ void act_panel_q81_kernel(const uint8_t *__restrict__ xq, int M, int 
     if ((lane & 3) == 0) D[(int64_t)blk * M_pad + m] = d;
 }
 
+// Activation prologue of the folded Q8_0 path: Q8_1 rows -> f16 panel [M_pad][K] of d*q (the f16 block
+// scale times the code, exact in fp32 and rounded once to f16); rows past M are zero.  One warp per
+// (row, 256 elements): lane l takes elements 8l .. 8l+7 of block l/4.  Also clears the device flag.
+__global__ void act_panel_q81_fold_kernel(const uint8_t *__restrict__ xq, int M, int M_pad, int nsb,
+                                          __half *__restrict__ A, unsigned long long *__restrict__ err) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (int64_t)M_pad * nsb) return;
+    const int m = (int)(wid / nsb), sb = (int)(wid % nsb);
+    const int64_t K = (int64_t)nsb * 256;
+    const int blk = sb * 8 + (lane >> 2);
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (m < M) {
+        const uint8_t *b = xq + ((int64_t)m * nsb * 8 + blk) * kQ81Bytes;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(b + 4 + (lane & 3) * 8);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(b + 8 + (lane & 3) * 8);
+        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(b));
+        __half hv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            hv[i] = __float2half_rn(d * (float)(int8_t)((w0 >> (8 * i)) & 0xff));
+            hv[4 + i] = __float2half_rn(d * (float)(int8_t)((w1 >> (8 * i)) & 0xff));
+        }
+        out = *reinterpret_cast<uint4 *>(hv);
+    }
+    *reinterpret_cast<uint4 *>(A + (int64_t)m * K + sb * 256 + lane * 8) = out;
+}
+
 // Routed-expert prologue: list entry s (pair lists[s], routed order) goes to panel row prow[s] of the
 // f16 code panel, the f16 bsum panel and the f32 scale panel; its activation is Q8_K row pair / top_k
 // (one row per token) or row pair (one row per pair).  One warp per (list entry, super-block); only
@@ -1401,7 +1511,8 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     return KQ_OK;
 }
 
-static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st) {
+static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st, bool fold = false) {
+    if (fold) return launch_tc<KQ_Q8_0F>(a, st);
     switch (wt) {
     case KQ_Q4_K: return launch_tc<KQ_Q4_K>(a, st);
     case KQ_Q5_K: return launch_tc<KQ_Q5_K>(a, st);
@@ -1414,7 +1525,7 @@ static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st) {
 // stride ldx quantised to Q8_K inside the prologue.
 static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, const float *xf, int64_t ldx, int64_t M,
                               int64_t N, int64_t K, float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st,
-                              const TcDebug *dbg) {
+                              const TcDebug *dbg, bool fold = false) {
     const TcWs L = tc_ws(wt, M, K);
     if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || L.M_pad / TC_TOK > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm: shape too large for the tensor-core grid");
@@ -1427,6 +1538,11 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
         kern<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
             xf, ldx, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
             reinterpret_cast<__half *>(workspace + L.off_e), reinterpret_cast<float *>(workspace + L.off_d),
+            reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
+    } else if (fold) {
+        if (wt != KQ_Q8_0) return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_ex: folded scales need Q8_0 weights");
+        act_panel_q81_fold_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+            xq, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
             reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
     } else if (wt == KQ_Q8_0)
         act_panel_q81_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
@@ -1446,7 +1562,8 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
     a.nsplit = tc_splits(wt, M, N, K);
     a.err = reinterpret_cast<unsigned long long *>(workspace + L.off_flag);
     a.dbg = dbg;
-    s = launch_tc_dt(wt, a, st);
+    if (fold && dbg && dbg->sums) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_ex: no integer sums with folded scales");
+    s = launch_tc_dt(wt, a, st, fold);
     if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
     return s;
 }
@@ -1454,6 +1571,11 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, uint8_t *workspace, cudaStream_t st, const TcDebug *dbg) {
     return tc_gemm_impl(wt, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st, dbg);
+}
+
+kq_status tc_gemm_folded(const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                         uint8_t *workspace, cudaStream_t st, const TcDebug *dbg) {
+    return tc_gemm_impl(KQ_Q8_0, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st, dbg, true);
 }
 
 kq_status tc_gemm_f32(kq_dtype wt, const uint8_t *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,

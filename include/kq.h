@@ -191,6 +191,20 @@ KQ_API size_t kq_gemm_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t
 KQ_API kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream);
 
+/* kq_gemm with options.  flags = 0 is kq_gemm itself.
+ * KQ_GEMM_FOLD_SCALES (Q8_0 weights x Q8_1 activations, the tensor-core shapes M >= 9, N >= 128):
+ * every 32-block's scales are folded into the tensor-core operands -- the weights enter the MMA as
+ * f16(d_w*w), the activations as f16(d_a*q), each rounded once to f16 -- so a 128 x 128 output tile
+ * accumulates over the whole of K in one fp32 tensor-memory buffer, read out once per tile, instead of
+ * once per 32-block as the exact kernel must ([llama-18] keeps the Q8_0 x Q8_1 dot per 32-block; this
+ * is the throughput form of the same product).  Not bit-exact: each product carries two f16 roundings
+ * (relative error below 2^-10), so |y - y_exact| <= (2^-10 + K*2^-24) * sum_i |w_i*x_i| (dequantized
+ * values); NMSE against the exact result is ~1e-7 on N(0,1) data.  Other shapes take kq_gemm's exact
+ * kernels.  Other weight types: KQ_ERR_UNSUPPORTED_DTYPE.  Workspace: kq_gemm_workspace_bytes. */
+#define KQ_GEMM_FOLD_SCALES 1u
+KQ_API kq_status kq_gemm_ex(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
+                            int64_t ldy, unsigned flags, void *workspace, size_t ws_bytes, kq_stream_t stream);
+
 /* kq_gemm from fp32 activations, with the activation quantizer moved into the GEMM that consumes it
  * ([vllm-2890]: a standalone quantizer launch costs a noticeable share of a step, so it belongs in its
  * consumer): x is fp32 [M][ldx] (ldx >= K, 4-byte aligned).  On the tensor-core

@@ -77,6 +77,7 @@ def lib():
             L.orc_partials.argtypes = [I32, P, P, I64, I64, I64, P]
             L.orc_gemm_sampled_terms.argtypes = [I32, P, P, I64, I64, P, P, P, P]
             L.orc_block_sums.argtypes = [I32, P, P, I64, I64, I64, P, I32]
+            L.orc_absdot_sampled.argtypes = [I32, P, P, I64, I64, P, P, P]
             L.orc_gemm_grouped.argtypes = [I32, P, I64, P, I64, P, I64, I64, I64, I64, P, I32]
             L.orc_gemm_grouped.restype = I64
             L.orc_moe_weighted_sum.argtypes = [P, P, I64, I64, I64, P]
@@ -202,6 +203,18 @@ def gemm_sampled_terms(dtype: int, w: np.ndarray, xq: np.ndarray, K: int, m_idx,
     terms = np.empty(mi.size, dtype=np.float64)
     lib().orc_gemm_sampled_terms(dtype, _ptr(w), _ptr(xq), K, mi.size, _ptr(mi), _ptr(ni), _ptr(out), _ptr(terms))
     return out, terms
+
+
+def absdot_sampled(dtype: int, w: np.ndarray, xq: np.ndarray, K: int, m_idx, n_idx) -> np.ndarray:
+    """f64 [S, 3]: for each sampled (m, n), sum |a_i*b_i|, sum |a_i| and sum |b_i| over the dequantised
+    weight row a and activation row b."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    mi = np.ascontiguousarray(m_idx, dtype=np.int64)
+    ni = np.ascontiguousarray(n_idx, dtype=np.int64)
+    out = np.empty((mi.size, 3), dtype=np.float64)
+    lib().orc_absdot_sampled(dtype, _ptr(w), _ptr(xq), K, mi.size, _ptr(mi), _ptr(ni), _ptr(out))
+    return out
 
 
 def block_sums(dtype: int, w: np.ndarray, xq: np.ndarray, M: int, N: int, K: int, threads: int = 0) -> np.ndarray:

@@ -581,6 +581,46 @@ ORC_API void orc_block_sums(int dtype, const uint8_t *w, const uint8_t *xq, int6
     (void)nthreads;
 }
 
+/* Magnitudes of a sampled dot product, from the dequantised values a_i (weight row n) and b_i
+ * (activation row m), in f64: out[3s] = sum |a_i*b_i|, out[3s+1] = sum |a_i|, out[3s+2] = sum |b_i|.
+ * The scale of the rounding error of any computation that rounds the operands themselves. */
+ORC_API void orc_absdot_sampled(int dtype, const uint8_t *w, const uint8_t *xq, int64_t K, int64_t S,
+                                const int64_t *m_idx, const int64_t *n_idx, double *out) {
+    int64_t wrb = w_row_bytes(dtype, K), xrb = act_row_bytes(dtype, K);
+    int64_t we = orc_block_elems(dtype), wb = orc_block_bytes(dtype);
+    int adt = dtype == ORC_Q8_0 ? ORC_Q8_1 : ORC_Q8_K;
+    int64_t ae = orc_block_elems(adt), ab = orc_block_bytes(adt);
+    double wv[256], av[256];
+    for (int64_t s = 0; s < S; ++s) {
+        const uint8_t *wr = w + n_idx[s] * wrb, *xr = xq + m_idx[s] * xrb;
+        double sab = 0.0, sa = 0.0, sb = 0.0;
+        for (int64_t k0 = 0; k0 < K; k0 += 256) {
+            for (int64_t k = k0; k < k0 + 256; k += we) {
+                const uint8_t *blk = wr + (k / we) * wb;
+                switch (dtype) {
+                case ORC_Q4_K: orc_dequant_q4_k(blk, wv + (k - k0)); break;
+                case ORC_Q5_K: orc_dequant_q5_k(blk, wv + (k - k0)); break;
+                case ORC_Q6_K: orc_dequant_q6_k(blk, wv + (k - k0)); break;
+                default: orc_dequant_q8_0(blk, wv + (k - k0)); break;
+                }
+            }
+            for (int64_t k = k0; k < k0 + 256; k += ae) {
+                const uint8_t *blk = xr + (k / ae) * ab;
+                if (adt == ORC_Q8_1) orc_dequant_q8_1(blk, av + (k - k0));
+                else orc_dequant_q8_k(blk, av + (k - k0));
+            }
+            for (int i = 0; i < 256; ++i) {
+                sab += fabs(wv[i] * av[i]);
+                sa += fabs(wv[i]);
+                sb += fabs(av[i]);
+            }
+        }
+        out[3 * s] = sab;
+        out[3 * s + 1] = sa;
+        out[3 * s + 2] = sb;
+    }
+}
+
 /* Partials for a whole GEMM: out[m][n][K/subblock]. */
 ORC_API void orc_partials(int dtype, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K,
                           int32_t *out) {

@@ -170,6 +170,72 @@ def test_gemm_q8_0_tensor_core_bit_exact(M, N, K):
     assert np.array_equal(y, ref), (nmse(y, ref), np.abs(y - ref).max())
 
 
+def folded_bound(absd: np.ndarray, K: int) -> np.ndarray:
+    """Elementwise bound on |y_folded - y_oracle| for Q8_0 with the block scales folded into the f16
+    operands.  With a_i = d_w*w_i and b_i = d_a*q_i (exact reals): the kernel multiplies f16(a_i) by
+    f16(b_i) -- each rounded once to f16, relative error <= 2^-11 for normal values and absolute error
+    <= 2^-25 in the subnormal range -- exactly, and adds the K products in fp32 (<= K*2^-24 of sum
+    |a_i*b_i| in any order); the oracle rounds (d_w*d_a), its product with the exact block dot and each
+    of the K/32 adds (<= (K/32 + 3)*2^-24 of the same sum).  absd = oracle.absdot_sampled rows
+    (sum |a_i*b_i|, sum |a_i|, sum |b_i|)."""
+    rel = 2.0 ** -10 + 2.0 ** -22 + (K + K // 32 + 4) * 2.0 ** -24
+    return rel * absd[:, 0] + 2.0 ** -24 * (absd[:, 1] + absd[:, 2])
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 200, 768), (300, 392, 1536), (384, 1040, 2560), (9, 128, 256)])
+def test_gemm_q8_0_folded_scales(M, N, K):
+    """kq_gemm_ex with KQ_GEMM_FOLD_SCALES: every output within the folded-operand rounding bound of
+    the oracle (which keeps the exact per-block integer dots) and NMSE <= 1e-6; deterministic from call
+    to call; on shapes off the tensor-core path it is the exact kernel, bit for bit."""
+    g = synth.rng(380 + M + N + K)
+    w = synth.weights(kq.Q8_0, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(kq.Q8_0, w, N, K)
+    xq = q8_1(dev(x), M, K)
+    wsb = kq.gemm_workspace_bytes(kq.Q8_0, M, N, K)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=DEV)
+    ys = []
+    for _ in range(2):
+        y = torch.full((M, N), float("nan"), device=DEV)
+        kq.kq_gemm_ex(kq.Q8_0, wn, xq, M, N, K, y, N, kq.GEMM_FOLD_SCALES, ws, wsb)
+        ys.append(host(y))
+    assert kq.kq_read_device_flag(ws) == 0
+    assert np.array_equal(ys[0], ys[1])
+    got = ys[0].reshape(-1)
+    xq_h = host(xq).reshape(M, -1)
+    ref = oracle.gemm(kq.Q8_0, w, xq_h, M, N, K).reshape(-1)
+    mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+    absd = oracle.absdot_sampled(kq.Q8_0, w, xq_h, K, mi, ni)
+    assert np.all(np.abs(got.astype(np.float64) - ref) <= folded_bound(absd, K))
+    assert nmse(got, ref) <= 1e-6
+
+
+def test_gemm_q8_0_folded_full_size_sampled():
+    """The Q8_0 + SwiGLU workload ([2560 x 9728] Q8_0 weights, 2048 SwiGLU rows quantised to Q8_1) through
+    the folded path, 2000 sampled outputs against the oracle on the GPU's own activation codes."""
+    c = synth.SWIGLU_Q8_0
+    M, N, K = c["M"], c["N"], c["K"]
+    g = synth.rng(0)
+    w = synth.weights(kq.Q8_0, N, K, g)
+    gu = synth.activations(M, 2 * K, g)
+    wn = repack(kq.Q8_0, w, N, K)
+    d = dev(gu)
+    xq = torch.empty(kq.q8_1_bytes(M, K), dtype=torch.uint8, device=DEV)
+    kq.kq_swiglu_quantize_q8_1(d, d[:, K:], M, K, 2 * K, xq)
+    wsb = kq.gemm_workspace_bytes(kq.Q8_0, M, N, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    y = torch.full((M, N), float("nan"), device=DEV)
+    kq.kq_gemm_ex(kq.Q8_0, wn, xq, M, N, K, y, N, kq.GEMM_FOLD_SCALES, ws, wsb)
+    yh = host(y)
+    assert np.isfinite(yh).all()
+    mi, ni = g.integers(0, M, 2000), g.integers(0, N, 2000)
+    xq_h = host(xq).reshape(M, -1)
+    ref = oracle.gemm_sampled(kq.Q8_0, w, xq_h, K, mi, ni)
+    absd = oracle.absdot_sampled(kq.Q8_0, w, xq_h, K, mi, ni)
+    assert np.all(np.abs(yh[mi, ni].astype(np.float64) - ref) <= folded_bound(absd, K))
+    assert nmse(yh[mi, ni], ref) <= 1e-6
+
+
 def test_gemm_q8_0_tensor_core_integer_special_case():
     """All weight and activation scales 1.0: the tensor-core Q8_0 GEMM must then return the exact
     integer product W.X (K = 768 keeps every sum below 2^24), which pins the integer block dots

@@ -512,6 +512,23 @@ def test_block_sums_against_brute_force(dtype):
     assert np.all(terms >= np.abs(ref.reshape(-1)) * (1 - 1e-6))
 
 
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+def test_absdot_magnitudes(dtype):
+    """The error-scale helper: sum |a_i*b_i|, sum |a_i| and sum |b_i| over the dequantised weight row a and
+    activation row b, against numpy on the dequantised blocks (whose values the fixtures pin)."""
+    g = np.random.default_rng(31 + dtype)
+    N, K, M = 3, 512, 2
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    xq = oracle.quantize_q8_1(x) if dtype == oracle.Q8_0 else oracle.quantize_q8_k(x)
+    a = oracle.dequant(dtype, w).reshape(N, K)
+    b = oracle.dequant(oracle.ACT_DTYPE[dtype], xq).reshape(M, K)
+    r = oracle.absdot_sampled(dtype, w, xq, K, [0, 1, 1], [2, 0, 1])
+    for s, (m, n) in enumerate([(0, 2), (1, 0), (1, 1)]):
+        want = [np.abs(a[n] * b[m]).sum(), np.abs(a[n]).sum(), np.abs(b[m]).sum()]
+        assert np.allclose(r[s], want, rtol=1e-12, atol=0)
+
+
 @pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0])
 def test_brute_force_tiny(dtype):
     g = np.random.default_rng(20 + dtype)
