@@ -2,10 +2,11 @@
 // GEMM (routing compaction + per-expert tiles), device flag, weighted expert sum.
 //
 // Routed experts follow strix-llama.cpp PR #18 ("Optimize ROCM Prefill and Decode"): the
-// (token, slot) pairs are compacted per expert and each expert gets tiles sized by ITS row count,
-// not by the total number of pairs (the routed-compact commit's lesson: a tile chosen from the total
-// left 50-87% of every tile as padding).  The compaction is a stable per-expert scan, so the row
-// order -- and the result -- is deterministic.
+// (token, slot) pairs are compacted per expert and each expert gets as many tiles as ITS row count
+// needs, not a tiling chosen from the total number of pairs (the routed-compact commit's lesson: a
+// tile chosen from the total left 50-87% of every tile as padding).  The tile width is the
+// tensor-core tile's for every expert.  The compaction is a stable per-expert scan, so the row order
+// -- and the result -- is deterministic.
 #include <mutex>
 
 #include <cuda.h>

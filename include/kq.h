@@ -219,7 +219,11 @@ KQ_API size_t kq_gemm_f32_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int
 KQ_API kq_status kq_gemm_f32(kq_dtype wt, const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
                              float *y, int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream);
 
-/* Routed-expert GEMM (MUL_MAT_ID; [llama-18] routed-compact MMQ and per-expert tile width).
+/* Routed-expert GEMM (MUL_MAT_ID; [llama-18] routed-compact MMQ: each expert's tiles cover only the
+ * rows routed to it, never a width chosen from the total number of pairs).  The tile width itself is
+ * the tensor-core tile's 128 rows for every expert; the pages' narrower per-expert widths (J by rows
+ * per expert) are not applied, since here a tile's cost is set by its weight conversion, which a
+ * narrower tile does not reduce.
  * w: n_experts native weights, repacked together as one [n_experts*N][K] matrix (N % 16 == 0).
  * ids: int32 [M][top_k] expert of each (token, slot).  xq: activation rows; xq_rows_per_token = 1
  * ("broadcast": slot (t,k) reads row t) or top_k ("per-row": slot (t,k) reads row t*top_k+k).
