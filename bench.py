@@ -318,6 +318,20 @@ def run_prefill(args, device, rank, world):
         per_case[f"{'q4_k' if dt == 1 else 'q6_k'}_{N}x{K}_m{M}"] = round(2.0 * M * N * K / (t * 1e-3) / 1e12, 2)
         del gc
 
+    # the opt-in folded-scale mode (KQ_GEMM_FOLD_SCALES: dequantised f16 weights times f16(d_a*q), 256- or
+    # 128-token tiles; not bit-exact, rounding-bounded): the same step from the fp32 rows through
+    # kq_gemm_f32_ex (the Q8_K quantiser in the folded prologue), and each folded GEMM alone
+    def step_folded():
+        for (M, dt, N, K) in cases:
+            kq.kq_gemm_f32_ex(dt, weights[(dt, N, K)], x_dev, Kmax, M, N, K, y, N, kq.GEMM_FOLD_SCALES, wsf, wsf_need)
+    fold_ms = _time_graph(step_folded, 5)
+    fold_case = {}
+    for (M, dt, N, K) in cases:
+        kq.kq_quantize_q8k(x_dev, M, K, Kmax, xq)
+        t = _time_graph(lambda: kq.kq_gemm_ex(dt, weights[(dt, N, K)], xq, M, N, K, y, N, kq.GEMM_FOLD_SCALES, ws,
+                                              ws_need), 5)
+        fold_case[f"{'q4_k' if dt == 1 else 'q6_k'}_{N}x{K}_m{M}"] = round(2.0 * M * N * K / (t * 1e-3) / 1e12, 2)
+
     # the step's 18 activation quantisations alone (excluded from the GEMM TOPS, reported beside them)
     def quant_all():
         for (M, dt, N, K) in cases:
@@ -353,7 +367,7 @@ def run_prefill(args, device, rank, world):
     h2d = sum(M * K * 4 for (M, _, _, K) in cases)
     d2h = sum(M * N * 4 for (M, _, N, _) in cases)
     return dict(ops=ops, ms=ms, gemm_ms=gemm_ms, per_case=per_case, clocks=clk, launches=launches,
-                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, cases=cases, quant_ms=quant_ms)
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, cases=cases, quant_ms=quant_ms, fold_ms=fold_ms, fold_case=fold_case)
 
 
 def int8_mma_sync_peak(device):
@@ -911,6 +925,14 @@ def main():
                          "achieved_per_gemm_replays": round(gemm_tops, 2),
                          "peak_source": f"{src} bf16_tflops burst (f16 tensor rate = bf16 rate)"},
             "per_gemm_tops": res["per_case"],
+            "prefill_folded": {
+                "mode": "opt-in KQ_GEMM_FOLD_SCALES through kq_gemm_f32_ex: block scales folded into the f16 "
+                        "operands, 256-token tiles (128 with split-K for few tiles); not bit-exact "
+                        "(rounding-bounded, NMSE ~1e-7)",
+                "ms_per_step": round(res["fold_ms"], 4),
+                "tops": round(res["ops"] / (res["fold_ms"] * 1e-3) / 1e12, 2),
+                "frac_of_peak": round(res["ops"] / (res["fold_ms"] * 1e-3) / 1e12 / tensor_peak, 4),
+                "per_gemm_tops": res["fold_case"]},
             "quantize_us_per_step": round(res["quant_ms"] * 1e3, 1),
             "clocks": res["clocks"],
         }

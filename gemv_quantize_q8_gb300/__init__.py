@@ -70,6 +70,7 @@ _SIGS = {
     "kq_gemm_grouped_swiglu_q8k": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _SZ, _P], _I32),
     "kq_debug_tc_splits": ([_I32, _I64, _I64, _I64], _I32),
     "kq_gemm_ex": ([_I32, _P, _P, _I64, _I64, _I64, _P, _I64, ctypes.c_uint, _P, _SZ, _P], _I32),
+    "kq_gemm_f32_ex": ([_I32, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, ctypes.c_uint, _P, _SZ, _P], _I32),
     "kq_debug_tc_sums": ([_I32, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _SZ, _P], _I32),
     "kq_debug_tc_sums_grouped": ([_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _SZ, _P], _I32),
     "kq_debug_tc_wait_timeout": ([_I32, _P, _P, _I64, _I64, _I64, _P, _I64, _I64, _P, _SZ, _P], _I32),
@@ -192,6 +193,12 @@ def kq_gemm_ex(wt, w, xq, M, N, K, y, ldy, flags, workspace=None, ws_bytes=0, st
     """kq_gemm with options (flags: GEMM_FOLD_SCALES folds the Q8_0 block scales into the f16 operands)."""
     _check(lib().kq_gemm_ex(wt, _ptr(w), _ptr(xq), M, N, K, _ptr(y), ldy, flags, _ptr(workspace), ws_bytes,
                             _stream(stream)))
+
+
+def kq_gemm_f32_ex(wt, w, x, ldx, M, N, K, y, ldy, flags, workspace, ws_bytes, stream=None):
+    """kq_gemm_f32 with kq_gemm_ex's flags (GEMM_FOLD_SCALES: the folded mode, quantised in its prologue)."""
+    _check(lib().kq_gemm_f32_ex(wt, _ptr(w), _ptr(x), ldx, M, N, K, _ptr(y), ldy, flags, _ptr(workspace), ws_bytes,
+                                _stream(stream)))
 
 
 def kq_gemm_f32_workspace_bytes(wt, M, N, K) -> int:

@@ -432,12 +432,12 @@ kq_status kq_gemm_ex(kq_dtype wt, const void *w, const void *xq, int64_t M, int6
     if (!(flags & KQ_GEMM_FOLD_SCALES)) return kq_gemm(wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes, stream);
     kq_status s = check_gemm_call("kq_gemm_ex", wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes);
     if (s != KQ_OK) return s;
-    if (wt != KQ_Q8_0)
-        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_ex: KQ_GEMM_FOLD_SCALES takes Q8_0 weights, not %s",
-                    dtype_name(wt));
+    if (wt != KQ_Q4_K && wt != KQ_Q5_K && wt != KQ_Q6_K && wt != KQ_Q8_0)
+        return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_ex: KQ_GEMM_FOLD_SCALES takes Q4_K, Q5_K, Q6_K or Q8_0 "
+                    "weights, not %s", dtype_name(wt));
     // shapes off the tensor-core path have no folded form: the exact kernels serve them
     if (!tc_eligible(wt, M, N, K)) return kq_gemm(wt, w, xq, M, N, K, y, ldy, workspace, ws_bytes, stream);
-    return tc_gemm_folded(static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
+    return tc_gemm_folded(wt, static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(xq), M, N, K, y, ldy,
                           static_cast<uint8_t *>(workspace), (cudaStream_t)stream);
 }
 
@@ -453,6 +453,14 @@ size_t kq_gemm_f32_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K)
 
 kq_status kq_gemm_f32(kq_dtype wt, const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
                       float *y, int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream) {
+    return kq_gemm_f32_ex(wt, w, x, ldx, M, N, K, y, ldy, 0u, workspace, ws_bytes, stream);
+}
+
+kq_status kq_gemm_f32_ex(kq_dtype wt, const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                         float *y, int64_t ldy, unsigned flags, void *workspace, size_t ws_bytes, kq_stream_t stream) {
+    if (flags & ~(unsigned)KQ_GEMM_FOLD_SCALES)
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm_f32_ex: unknown flags 0x%x", flags & ~(unsigned)KQ_GEMM_FOLD_SCALES);
+    const bool fold = (flags & KQ_GEMM_FOLD_SCALES) != 0;
     kq_status s = check_matmul_args("kq_gemm_f32", wt, w, x, M, N, K);
     if (s != KQ_OK) return s;
     if (!y) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_f32: null y");
@@ -468,14 +476,14 @@ kq_status kq_gemm_f32(kq_dtype wt, const void *w, const float *x, int64_t ldx, i
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (wt != KQ_Q8_0 && tc_eligible(wt, M, N, K))
-        return tc_gemm_f32(wt, static_cast<const uint8_t *>(w), x, ldx, M, N, K, y, ldy, ws, st);
-    // other paths: quantise into the workspace's tail, then the plain GEMM
+        return tc_gemm_f32(wt, static_cast<const uint8_t *>(w), x, ldx, M, N, K, y, ldy, ws, st, fold);
+    // other paths: quantise into the workspace's tail, then the GEMM
     const size_t gneed = kq_gemm_workspace_bytes(wt, M, N, K, 0, 0);
     const size_t g = std::max<size_t>(256, (gneed + 255) & ~(size_t)255);
     uint8_t *xq = ws + g;
     s = wt == KQ_Q8_0 ? kq_quantize_q8_1(x, M, K, ldx, xq, stream) : kq_quantize_q8k(x, M, K, ldx, xq, stream);
     if (s != KQ_OK) return s;
-    return kq_gemm(wt, w, xq, M, N, K, y, ldy, gneed ? workspace : nullptr, gneed, stream);
+    return kq_gemm_ex(wt, w, xq, M, N, K, y, ldy, flags, gneed ? workspace : nullptr, gneed, stream);
 }
 
 kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K,

@@ -63,6 +63,9 @@ struct TcCfg<KQ_Q4_K> {
     static constexpr bool Q8 = false;     // per-32-block scales (Q8_0 x Q8_1)
     static constexpr bool Q5 = false;     // fifth code bit from the row's high-bit bytes (Q5_K)
     static constexpr bool FOLD = false;   // scales folded into the f16 operands (one accumulator per tile)
+    static constexpr int TOK = TC_TOK;    // tokens per tile (MMA N)
+    static constexpr int BASE = KQ_Q4_K;  // the weight format
+    static constexpr int NACT = 8;        // activation-ring tiles (64 K each)
     static constexpr int A_COLS = 32;     // TMEM columns of one converted kblock (64 f16)
     static constexpr int NACC = 2;        // accumulator buffers
     static constexpr int BPS = 1;         // accumulator read-outs per step (scale blocks per 256 K)
@@ -75,6 +78,7 @@ template <>
 struct TcCfg<KQ_Q5_K> {  // Q4_K's header and min term; 5-bit codes, sc*c <= 63*31 exact in f16
     static constexpr int CB = kQ5KChunk;
     static constexpr bool EXT = true, Q8 = false, Q5 = true, FOLD = false;
+    static constexpr int TOK = TC_TOK, NACT = 8, BASE = KQ_Q5_K;
     static constexpr int A_COLS = 32, NACC = 2, BPS = 1, H_ROW = 8, NP = 2, NE = 2;
     static constexpr uint32_t TM_S2 = 256, TM_A = 384;
 };
@@ -82,6 +86,7 @@ template <>
 struct TcCfg<KQ_Q6_K> {
     static constexpr int CB = kQ6KChunk;
     static constexpr bool EXT = false, Q8 = false, Q5 = false, FOLD = false;
+    static constexpr int TOK = TC_TOK, NACT = 8, BASE = KQ_Q6_K;
     static constexpr int A_COLS = 64;     // lo tile (32 columns) then 16*hi tile (32 columns)
     static constexpr int NACC = 2, BPS = 1, H_ROW = 8;  // f32 (d, 0)
     static constexpr int NP = 2, NE = 2;
@@ -91,6 +96,7 @@ template <>
 struct TcCfg<KQ_Q8_0> {
     static constexpr int CB = kQ80Chunk;
     static constexpr bool EXT = false, Q8 = true, Q5 = false, FOLD = false;
+    static constexpr int TOK = TC_TOK, NACT = 8, BASE = KQ_Q8_0;
     static constexpr int A_COLS = 32;
     // every 32-element block has its own weight and activation scale, so every block's integer
     // dot P_b is read out of its own accumulator: three buffers rotate along the blocks
@@ -98,19 +104,37 @@ struct TcCfg<KQ_Q8_0> {
     static constexpr int NP = 2, NE = 2;
     static constexpr uint32_t TM_S2 = 0, TM_A = 384;
 };
-// Q8_0 x Q8_1 with the block scales folded into the f16 operands: the converters write f16(d_w*w), the
-// activation panel holds f16(d_a*q), so every product is the scaled one (each operand rounded once to
-// f16) and a tile accumulates over the whole of K in one TMEM buffer, read out once per tile.
-constexpr int KQ_Q8_0F = 103;  // internal: not a kq_dtype of the ABI
-template <>
-struct TcCfg<KQ_Q8_0F> {
-    static constexpr int CB = kQ80Chunk;
-    static constexpr bool EXT = false, Q8 = false, Q5 = false, FOLD = true;
+// Folded scales (an opt-in throughput mode): the block scales are multiplied into the f16 operands --
+// the converters write the dequantised weight f16(d*sc*c - dmin*m) (Q4_K, Q5_K), f16(d*sc*(c-32))
+// (Q6_K) or f16(d_w*w) (Q8_0), the activation panel holds f16(d_a*q) -- so every product is the
+// scaled one and a tile accumulates over the whole of K in one fp32 TMEM buffer, read out once per
+// tile.  Without a per-step read-out the accumulator need not be double-buffered, which leaves room
+// for 256-token tiles (one 128 x 256 accumulator + four kblock stages): every converted weight then
+// serves twice the tokens.  Not bit-exact: each operand is rounded to f16.
+// Few output tiles (small M) take 128-token tiles instead, two accumulators alternating per tile, and
+// split K across a cluster as the exact kernels do.
+constexpr int KQ_Q4_KF = 101, KQ_Q6_KF = 102, KQ_Q8_0F = 103, KQ_Q5_KF = 106;  // internal, not kq_dtype values
+constexpr int KQ_FOLD128 = 100;  // added to a folded code: the 128-token form
+template <int BASEDT, int CHUNK, int T>
+struct TcFoldCfg {
+    static constexpr int CB = CHUNK;
+    static constexpr int BASE = BASEDT;  // the weight format
+    static constexpr bool EXT = false, Q8 = false, Q5 = BASEDT == KQ_Q5_K, FOLD = true;
+    static constexpr int TOK = T;                 // 256: two pairs of 32 KB activation tiles; 128: four of 16 KB
+    static constexpr int NACT = T == 256 ? 4 : 8;
     static constexpr int A_COLS = 32;
-    static constexpr int NACC = 2, BPS = 1, H_ROW = 16;  // accumulators alternate per tile
+    static constexpr int NACC = T == 256 ? 1 : 2, BPS = 1, H_ROW = 16;  // accumulators (of TOK columns)
     static constexpr int NP = 2, NE = 2;
     static constexpr uint32_t TM_S2 = 0, TM_A = 256;
 };
+template <> struct TcCfg<KQ_Q4_KF> : TcFoldCfg<KQ_Q4_K, kQ4KChunk, 256> {};
+template <> struct TcCfg<KQ_Q5_KF> : TcFoldCfg<KQ_Q5_K, kQ5KChunk, 256> {};
+template <> struct TcCfg<KQ_Q6_KF> : TcFoldCfg<KQ_Q6_K, kQ6KChunk, 256> {};
+template <> struct TcCfg<KQ_Q8_0F> : TcFoldCfg<KQ_Q8_0, kQ80Chunk, 256> {};
+template <> struct TcCfg<KQ_Q4_KF + KQ_FOLD128> : TcFoldCfg<KQ_Q4_K, kQ4KChunk, 128> {};
+template <> struct TcCfg<KQ_Q5_KF + KQ_FOLD128> : TcFoldCfg<KQ_Q5_K, kQ5KChunk, 128> {};
+template <> struct TcCfg<KQ_Q6_KF + KQ_FOLD128> : TcFoldCfg<KQ_Q6_K, kQ6KChunk, 128> {};
+template <> struct TcCfg<KQ_Q8_0F + KQ_FOLD128> : TcFoldCfg<KQ_Q8_0, kQ80Chunk, 128> {};
 // TMEM map: accumulator buffers at columns 0, 128 (and 256 for Q8_0); Q4_K min-term tile at 256;
 // converted kblock stages from TM_A on (4 stages = one super-block).
 static_assert(TcCfg<KQ_Q4_K>::TM_A + 4 * TcCfg<KQ_Q4_K>::A_COLS <= TMEM_COLS, "Q4_K TMEM map");
@@ -121,13 +145,15 @@ static_assert(TcCfg<KQ_Q8_0>::NACC * 128 <= (int)TcCfg<KQ_Q8_0>::TM_A &&
 template <int DT>
 struct TcLayout {
     using C = TcCfg<DT>;
+    static constexpr int ACTT = C::TOK * TC_KB * 2;  // one activation tile: TOK tokens x 64 f16
+    static constexpr int NPAIR = C::NACT / 2;        // the ring is handed over in pairs of kblocks
     static constexpr int ACT_OFF = 0;
-    static constexpr int P_OFF = ACT_OFF + NACT * ACT_TILE;
+    static constexpr int P_OFF = ACT_OFF + C::NACT * ACTT;
     static constexpr int EA_OFF = (P_OFF + C::NP * 8 * C::CB + 1023) & ~1023;
     static constexpr int EB_OFF = EA_OFF + (C::EXT ? C::NE * 4096 : 0);
     static constexpr int H_OFF = EB_OFF + (C::EXT ? C::NE * 4096 : 0);
     static constexpr int DA_OFF = H_OFF + 4 * TC_ROWS * C::H_ROW;
-    static constexpr int BAR_OFF = DA_OFF + 4 * TC_TOK * 4 * C::BPS;
+    static constexpr int BAR_OFF = DA_OFF + 4 * C::TOK * 4 * C::BPS;
     static constexpr int NBAR = 2 * NPAIR + 2 * 3 + 2 * 3 + 3 * 4 + 2 * 3 + 2 + 4 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = MISC_OFF + 16;
@@ -138,7 +164,10 @@ static_assert(TcLayout<KQ_Q6_K>::ALLOC <= 227 * 1024, "Q6_K tensor-core smem bud
 static_assert(TcLayout<KQ_Q5_K>::ALLOC <= 227 * 1024, "Q5_K tensor-core smem budget");
 static_assert(TcLayout<KQ_Q8_0>::ALLOC <= 227 * 1024, "Q8_0 tensor-core smem budget");
 static_assert(TcLayout<KQ_Q8_0F>::ALLOC <= 227 * 1024, "folded Q8_0 tensor-core smem budget");
-static_assert(TcCfg<KQ_Q8_0F>::TM_A + 4 * TcCfg<KQ_Q8_0F>::A_COLS <= TMEM_COLS, "folded Q8_0 TMEM map");
+static_assert(TcLayout<KQ_Q6_KF>::ALLOC <= 227 * 1024, "folded Q6_K tensor-core smem budget");
+static_assert(TcLayout<KQ_Q5_KF>::ALLOC <= 227 * 1024, "folded Q5_K tensor-core smem budget");
+static_assert(TcCfg<KQ_Q8_0F>::TOK <= (int)TcCfg<KQ_Q8_0F>::TM_A &&
+                  TcCfg<KQ_Q8_0F>::TM_A + 4 * TcCfg<KQ_Q8_0F>::A_COLS <= TMEM_COLS, "folded TMEM map");
 // the split-K reduction parks a 128 x (128 + 4) fp32 tile in the activation ring
 static_assert(TC_TOK * (TC_ROWS + 4) * 4 <= NACT * ACT_TILE, "split-K staging fits the activation ring");
 
@@ -188,7 +217,7 @@ struct TcTile {
 
 // Geometry of tile `tile`: weight rows n0.., first panel row m0, stored token rows, first weight row
 // group, row groups present, and (grouped) the first pair-list entry.
-template <bool SWQ>
+template <bool SWQ, int TOK>
 __device__ __forceinline__ TcTile tc_tile(const TcParams &P, int tile, int m_tiles) {
     TcTile T;
     const int nt = tile % P.n_tiles, mt = tile / P.n_tiles;
@@ -198,12 +227,12 @@ __device__ __forceinline__ TcTile tc_tile(const TcParams &P, int tile, int m_til
     T.valid_groups = min(8, (P.N + 15) / 16 - T.n0 / 16);
     if (P.grouped) {
         const int e = P.tiles[2 * mt], j = P.tiles[2 * mt + 1];
-        T.m0 = P.poff[e] + j * TC_TOK;
-        T.tok_valid = min(TC_TOK, P.count[e] - j * TC_TOK);
+        T.m0 = P.poff[e] + j * TOK;
+        T.tok_valid = min(TOK, P.count[e] - j * TOK);
         T.g0 = e * (P.N / 16) + T.n0 / 16;
-        T.list_base = P.offset[e] + j * TC_TOK;
+        T.list_base = P.offset[e] + j * TOK;
     } else {
-        T.m0 = mt * TC_TOK;
+        T.m0 = mt * TOK;
         T.tok_valid = P.M - T.m0;
         T.g0 = T.n0 / 16;
         T.list_base = 0;
@@ -294,6 +323,52 @@ __device__ __forceinline__ void convert_q6k_sub(const uint32_t (&nib)[4], const 
     }
 }
 
+// Folded-scale conversions (opt-in mode): each code becomes its dequantised f16 weight.
+// Q4_K/Q5_K kblock: x = c*S + M with S = f16(d*sc), M = f16(-dmin*m) of the element's sub-block (low
+// nibbles: sub-block 2kb, high nibbles: 2kb+1), the code recovered exactly from the magic-biased f16
+// first (1024 + c - 1024, 64 + c - 64), then one fused multiply-add (one rounding).  With Q5 the fifth
+// code bit comes from the row's high-bit words as in convert_q5k_kblock.
+template <bool Q5>
+__device__ __forceinline__ void convert_q4k_kblock_fold(uint4 v0, uint4 v1, const uint32_t (&hq)[8], int kb,
+                                                        __half2 s_lo, __half2 m_lo, __half2 s_hi, __half2 m_hi,
+                                                        uint32_t (&r)[32]) {
+    const __half2 c1024 = __float2half2_rn(1024.0f), c64 = __float2half2_rn(64.0f);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t d01 = __byte_perm(w[i], 0u, 0x4140), d23 = __byte_perm(w[i], 0u, 0x4342);
+        uint32_t l01 = 0, l23 = 0, u01 = 0, u23 = 0;
+        if (Q5) {
+            const uint32_t h01 = __byte_perm(hq[i], 0u, 0x4140), h23 = __byte_perm(hq[i], 0u, 0x4342);
+            l01 = ((h01 >> (2 * kb)) & 0x00010001u) << 4;
+            l23 = ((h23 >> (2 * kb)) & 0x00010001u) << 4;
+            u01 = ((h01 >> (2 * kb + 1)) & 0x00010001u) << 8;
+            u23 = ((h23 >> (2 * kb + 1)) & 0x00010001u) << 8;
+        }
+        r[2 * i] = h2u(__hfma2(__hsub2(u2h((d01 & 0x000F000Fu) | l01 | 0x64006400u), c1024), s_lo, m_lo));
+        r[2 * i + 1] = h2u(__hfma2(__hsub2(u2h((d23 & 0x000F000Fu) | l23 | 0x64006400u), c1024), s_lo, m_lo));
+        r[16 + 2 * i] = h2u(__hfma2(__hsub2(u2h((d01 & 0x00F000F0u) | u01 | 0x54005400u), c64), s_hi, m_hi));
+        r[16 + 2 * i + 1] = h2u(__hfma2(__hsub2(u2h((d23 & 0x00F000F0u) | u23 | 0x54005400u), c64), s_hi, m_hi));
+    }
+}
+
+// Q6_K sub-block (as convert_q6k_sub): x = (c - 32)*S with S = f16(d*sc): one exact subtraction, one
+// rounding multiply.
+template <bool HI, int HS>
+__device__ __forceinline__ void convert_q6k_sub_fold(const uint32_t (&nib)[4], const uint32_t (&hb)[4], __half2 sd,
+                                                     uint32_t (&o)[8]) {
+    const __half2 c1056 = __float2half2_rn(1056.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t h = (HS <= 4 ? (hb[i] << (4 - HS)) : (hb[i] >> (HS - 4))) & 0x30303030u;
+        const uint32_t c = (HI ? ((nib[i] >> 4) & 0x0f0f0f0fu) : (nib[i] & 0x0f0f0f0fu)) | h;
+        o[2 * i] = h2u(__hmul2(__hsub2(u2h(__byte_perm(c, 0x64646464u, 0x4140)), c1056), sd));
+        o[2 * i + 1] = h2u(__hmul2(__hsub2(u2h(__byte_perm(c, 0x64646464u, 0x4342)), c1056), sd));
+    }
+}
+
+__device__ __forceinline__ __half2 h2dup(float v) { return __float2half2_rn(v); }
+
 // SWQ: fused SwiGLU -> Q8_K epilogue (routed gate/up); DBG: the debug read-out of the integer sums
 // (P.dbg).  Each is a separate instantiation, so the plain GEMM's register allocation is untouched.
 template <int DT, bool SWQ, bool DBG>
@@ -313,8 +388,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // k_full/k_empty: one slot per pair of kblocks -- its two activation tiles (TMA) and its two
     // converted kblocks (TMEM, from both converter groups) complete the same phase, and a single MMA
     // commit frees both, so the MMA thread waits once per 128 K-elements.
-    uint64_t *k_full = bars, *k_empty = k_full + NPAIR;
-    uint64_t *p_full = k_empty + NPAIR, *p_empty = p_full + 3;   // up to 3 packed-weight slots
+    uint64_t *k_full = bars, *k_empty = k_full + L::NPAIR;
+    uint64_t *p_full = k_empty + L::NPAIR, *p_empty = p_full + 3;   // up to 3 packed-weight slots
     uint64_t *e_full = p_empty + 3, *e_empty = e_full + 3;       // Q4_K: bsums (TMA) + mins (converters)
     uint64_t *h_full = e_empty + 3, *da_full = h_full + 4, *h_empty = da_full + 4;
     uint64_t *acc_full = h_empty + 4, *acc_empty = acc_full + 3;
@@ -340,11 +415,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int nsteps = (nunits - unit0 + ustride - 1) / ustride * (SWQ ? 4 : 1) * nsb;
     // roles keep (tile i, super-block t) counters along the steps instead of dividing by nsb
     auto tile_of = [&](int i) {
-        return tc_tile<SWQ>(P, SWQ ? (unit0 + (i >> 2) * ustride) * 4 + (i & 3) : unit0 + i * ustride, m_tiles);
+        return tc_tile<SWQ, C::TOK>(P, SWQ ? (unit0 + (i >> 2) * ustride) * 4 + (i & 3) : unit0 + i * ustride, m_tiles);
     };
 
     if (tid == 0) {
-        for (int i = 0; i < NPAIR; ++i) { mbar_init(&k_full[i], 32 * TC_CONV_WARPS + 1); mbar_init(&k_empty[i], 1); }
+        for (int i = 0; i < L::NPAIR; ++i) { mbar_init(&k_full[i], 32 * TC_CONV_WARPS + 1); mbar_init(&k_empty[i], 1); }
         for (int i = 0; i < C::NP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 32 * TC_CONV_WARPS); }
         for (int i = 0; i < C::NE; ++i) { mbar_init(&e_full[i], 32 * TC_CONV_WARPS / 2 + 1); mbar_init(&e_empty[i], 1); }
         for (int i = 0; i < C::NACC; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS); }
@@ -398,10 +473,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int h = st & 3, hph = (st >> 2) & 1;
                     if (!(ok = mbar_wait_sleep(&h_empty[h], hph ^ 1, abort_flag, P.wait_ns))) break;
                     // the scale panel has one row of M_pad floats per scale block (256 or 32 K)
-                    mbar_arrive_expect_tx(&da_full[h], C::BPS * TC_TOK * 4);
+                    mbar_arrive_expect_tx(&da_full[h], C::BPS * C::TOK * 4);
                     for (int b = 0; b < C::BPS; ++b)
-                        bulk_load(sDA + (h * C::BPS + b) * TC_TOK * 4,
-                                  P.da + (int64_t)(gsb * C::BPS + b) * P.M_pad + T.m0, TC_TOK * 4, &da_full[h]);
+                        bulk_load(sDA + (h * C::BPS + b) * C::TOK * 4,
+                                  P.da + (int64_t)(gsb * C::BPS + b) * P.M_pad + T.m0, C::TOK * 4, &da_full[h]);
                     last_d[h] = hph;
                 }
             }
@@ -421,25 +496,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == TC_WARP_ACT) {
         // ------------------------------------------------------------ activation-tile producer
         if (lane == 0) {
-            int last_k[NPAIR];
-            for (int i = 0; i < NPAIR; ++i) last_k[i] = -1;
+            int last_k[L::NPAIR];
+            for (int i = 0; i < L::NPAIR; ++i) last_k[i] = -1;
             bool ok = true;
             int m0 = 0, ti = 0, tt = 0;
             for (int pp = 0; pp < nsteps * 2 && ok && !P.withhold; ++pp) {
                 if ((pp & 1) == 0 && tt == 0) m0 = tile_of(ti).m0;
-                const int s = pp % NPAIR, ph = (pp / NPAIR) & 1;
+                const int s = pp % L::NPAIR, ph = (pp / L::NPAIR) & 1;
                 if (!(ok = mbar_wait_sleep(&k_empty[s], ph ^ 1, abort_flag, P.wait_ns))) break;
-                mbar_arrive_expect_tx(&k_full[s], 2 * ACT_TILE);
+                mbar_arrive_expect_tx(&k_full[s], 2 * L::ACTT);
                 const int x = (sb0 + tt) * 256 + (pp & 1) * 2 * TC_KB;
                 if ((pp & 1) && ++tt == nsb) { tt = 0; ++ti; }
-                tma_load_2d(sAct + (2 * s) * ACT_TILE, &tmA, &k_full[s], x, m0);
-                tma_load_2d(sAct + (2 * s + 1) * ACT_TILE, &tmA, &k_full[s], x + TC_KB, m0);
+                tma_load_2d(sAct + (2 * s) * L::ACTT, &tmA, &k_full[s], x, m0);
+                tma_load_2d(sAct + (2 * s + 1) * L::ACTT, &tmA, &k_full[s], x + TC_KB, m0);
                 last_k[s] = ph;
             }
             if (!ok) {
                 // bounded drain (see the weight-side producer)
                 volatile int no_abort = 0;
-                for (int i = 0; i < NPAIR; ++i)
+                for (int i = 0; i < L::NPAIR; ++i)
                     if (last_k[i] >= 0) { no_abort = 0; mbar_wait(&k_full[i], last_k[i], &no_abort, 100000000ull); }
             }
         }
@@ -456,10 +531,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // read t-1's min term).
         if (lane == 0) {
             const int w = warp == TC_WARP_MMA ? 0 : 1;
-            constexpr uint32_t idesc = idesc_f16_f32(TC_ROWS, TC_TOK);
+            constexpr uint32_t idesc = idesc_f16_f32(TC_ROWS, C::TOK);
             const uint64_t dAct = smem_desc(smem_u32(sAct), 1024, 2);
             const uint64_t dEA = smem_desc(smem_u32(sEA), 256, 6), dEB = smem_desc(smem_u32(sEB), 256, 6);
-            const uint32_t d1 = tbase + w * TC_TOK;
+            const uint32_t d1 = tbase + w * C::TOK;
             bool ok = true;
             if (C::Q8) {
                 // Q8_0: each 32-element block (two K16 MMAs) fills its own accumulator buffer, the
@@ -470,15 +545,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int t = 0; t < nsteps && ok && w == 0; ++t) {
                     int g = 8 * t, buf = g % C::NACC, use = g / C::NACC;
                     for (int pr = 0; pr < 2 && ok; ++pr) {
-                        const int pp = 2 * t + pr, s = pp % NPAIR;
-                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
+                        const int pp = 2 * t + pr, s = pp % L::NPAIR;
+                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / L::NPAIR) & 1, abort_flag, P.wait_ns))) break;
                         for (int h = 0; h < 2 && ok; ++h) {
-                            const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
+                            const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (L::ACTT >> 4));
                             const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
                             for (int blk = 0; blk < 2; ++blk) {
                                 if (!(ok = mbar_wait_sleep(&acc_empty[buf], (use & 1) ^ 1, abort_flag, P.wait_ns))) break;
                                 tc_fence_after();
-                                const uint32_t dq = tbase + buf * TC_TOK;
+                                const uint32_t dq = tbase + buf * C::TOK;
                                 mma_f16_ts(dq, a0 + blk * 16, bd + (uint64_t)(blk * 4), idesc, 0);
                                 mma_f16_ts(dq, a0 + blk * 16 + 8, bd + (uint64_t)(blk * 4 + 2), idesc, 1);
                                 mma_commit(&acc_full[buf]);
@@ -491,23 +566,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
             if (C::FOLD) {
-                // folded Q8_0: one issuer (the MMAs into a tile's accumulator then go in one fixed order,
-                // so the result is deterministic); a tile's steps all accumulate into buffer (tile & 1),
-                // committed once at the tile's last step
+                // folded scales: one issuer (the MMAs into a tile's accumulator then go in one fixed
+                // order, so the result is deterministic); a tile's steps all accumulate into the one
+                // 128 x TOK accumulator, committed once at the tile's last step
                 for (int t = 0, ti = 0, tt = 0; t < nsteps && ok && w == 0; ++t) {
-                    const int ab = ti & 1;
                     const bool first = tt == 0, last = tt == nsb - 1;
-                    if (first) {
-                        if (!(ok = mbar_wait_sleep(&acc_empty[ab], ((ti >> 1) & 1) ^ 1, abort_flag, P.wait_ns))) break;
+                    // tile ti's accumulator: buffer ti % NACC, its use count ti / NACC
+                    const int ab = C::NACC == 1 ? 0 : (ti & 1), use = C::NACC == 1 ? ti : (ti >> 1);
+                    if (first) {  // the epilogue has read this buffer's previous tile out
+                        if (!(ok = mbar_wait_sleep(&acc_empty[ab], (use & 1) ^ 1, abort_flag, P.wait_ns))) break;
                         tc_fence_after();
                     }
                     for (int pr = 0; pr < 2 && ok; ++pr) {
-                        const int pp = 2 * t + pr, s = pp % NPAIR;
+                        const int pp = 2 * t + pr, s = pp % L::NPAIR;
                         uint32_t aa[8];
                         uint64_t bb[8];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
+                            const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (L::ACTT >> 4));
                             const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
 #pragma unroll
                             for (int k16 = 0; k16 < 4; ++k16) {
@@ -515,9 +591,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 bb[h * 4 + k16] = bd + (uint64_t)(k16 * 2);
                             }
                         }
-                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
+                        if (!(ok = mbar_wait_sleep(&k_full[s], (pp / L::NPAIR) & 1, abort_flag, P.wait_ns))) break;
                         tc_fence_after();
-                        mma8_f16_ts(tbase + ab * TC_TOK, aa, bb, idesc, (first && pr == 0) ? 0u : 1u);
+                        mma8_f16_ts(tbase + ab * C::TOK, aa, bb, idesc, (first && pr == 0) ? 0u : 1u);
                         mma_commit(&k_empty[s]);
                     }
                     if (!ok) break;
@@ -529,14 +605,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!(ok = mbar_wait_sleep(&acc_empty[w], ((t >> 1) & 1) ^ 1, abort_flag, P.wait_ns))) break;
                 tc_fence_after();
                 for (int pr = 0; pr < 2 && ok; ++pr) {
-                    const int pp = 2 * t + pr, s = pp % NPAIR;
+                    const int pp = 2 * t + pr, s = pp % L::NPAIR;
                     // operands of the pair's MMAs, computed while the pair is still being filled, so the MMAs
                     // go out back to back with no integer work between them
                     uint32_t aa[2][8];
                     uint64_t bb[2][8];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (ACT_TILE >> 4));
+                        const uint64_t bd = dAct + (uint64_t)((2 * s + h) * (L::ACTT >> 4));
                         const uint32_t a0 = tbase + C::TM_A + (2 * pr + h) * C::A_COLS;
 #pragma unroll
                         for (int k16 = 0; k16 < 4; ++k16) {
@@ -550,7 +626,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             }
                         }
                     }
-                    if (!(ok = mbar_wait_sleep(&k_full[s], (pp / NPAIR) & 1, abort_flag, P.wait_ns))) break;
+                    if (!(ok = mbar_wait_sleep(&k_full[s], (pp / L::NPAIR) & 1, abort_flag, P.wait_ns))) break;
                     tc_fence_after();
                     mma8_f16_ts(d1, aa[0], bb[0], idesc, pr);
                     if (!C::EXT) mma8_f16_ts(d1, aa[1], bb[1], idesc, 1);
@@ -586,6 +662,82 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int row = 32 * q + lane;
         const uint32_t lane_base = tbase + ((uint32_t)(32 * q) << 16);
         bool ok = true, rvalid = false;
+        // folded scales, K-quant weights: step t's kblocks {grp, grp+2} of this row as dequantised f16
+        auto fold_convert_kquant = [&](int t, int grp, int row, bool rvalid, const uint8_t *chunk, int r16,
+                                       uint32_t lane_base) -> bool {
+            constexpr bool K4 = C::BASE == KQ_Q4_K || C::BASE == KQ_Q5_K;
+            uint4 cv[2][2], qh[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint8_t *codes = chunk + (grp + 2 * j) * 512 + r16 * 32;
+                cv[j][0] = *reinterpret_cast<const uint4 *>(codes);
+                cv[j][1] = *reinterpret_cast<const uint4 *>(codes + 16);
+                qh[j] = K4 ? make_uint4(0, 0, 0, 0)
+                           : *reinterpret_cast<const uint4 *>(chunk + 2048 + (grp + 2 * j) * 256 + r16 * 16);
+            }
+            const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + (K4 ? 2048 : 3072) + r16 * 16);
+            float d = K4 ? half_bits_to_float((uint16_t)(hv.x & 0xffff))
+                         : half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + r16 * 2));
+            float dmin = K4 ? half_bits_to_float((uint16_t)(hv.x >> 16)) : 0.0f;
+            if (!rvalid) d = dmin = 0.0f;  // rows past N were not loaded
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int kb = grp + 2 * j;
+                if (t > 0) {
+                    const int pq = 2 * (t - 1) + j;
+                    if (!mbar_wait_sleep(&k_empty[pq % L::NPAIR], (pq / L::NPAIR) & 1, abort_flag, P.wait_ns))
+                        return false;
+                }
+                tc_fence_after();
+                const uint32_t ta = lane_base + C::TM_A + kb * C::A_COLS;
+                if (K4) {
+                    // the scales and mins of sub-blocks 2kb and 2kb+1 from the 12 packed bytes
+                    const uint32_t lo = grp ? (hv.y >> 16) : hv.y;   // scale bytes 2g, 2g+1
+                    const uint32_t mz = grp ? (hv.z >> 16) : hv.z;   // min bytes 2g, 2g+1 (bytes 4+2g, 5+2g)
+                    const uint32_t hi8 = grp ? (hv.w >> 16) : hv.w;  // bytes 8+2g, 9+2g
+                    int sc0, sc1, m0, m1;
+                    if (j == 0) {
+                        sc0 = lo & 63; sc1 = (lo >> 8) & 63;
+                        m0 = mz & 63; m1 = (mz >> 8) & 63;
+                    } else {
+                        sc0 = (hi8 & 0x0f) | (((lo >> 6) & 3) << 4);
+                        sc1 = ((hi8 >> 8) & 0x0f) | (((lo >> 14) & 3) << 4);
+                        m0 = ((hi8 >> 4) & 0x0f) | (((mz >> 6) & 3) << 4);
+                        m1 = ((hi8 >> 12) & 0x0f) | (((mz >> 14) & 3) << 4);
+                    }
+                    uint32_t q5w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    if (C::Q5) {
+                        const uint4 a = *reinterpret_cast<const uint4 *>(chunk + 2304 + r16 * 32);
+                        const uint4 b = *reinterpret_cast<const uint4 *>(chunk + 2304 + r16 * 32 + 16);
+                        q5w[0] = a.x; q5w[1] = a.y; q5w[2] = a.z; q5w[3] = a.w;
+                        q5w[4] = b.x; q5w[5] = b.y; q5w[6] = b.z; q5w[7] = b.w;
+                    }
+                    uint32_t r[32];
+                    convert_q4k_kblock_fold<C::Q5>(cv[j][0], cv[j][1], q5w, kb, h2dup(d * (float)sc0),
+                                                   h2dup(-dmin * (float)m0), h2dup(d * (float)sc1),
+                                                   h2dup(-dmin * (float)m1), r);
+                    tmem_st32(ta, r);
+                } else {
+                    const uint32_t ws = j ? (grp ? hv.w : hv.z) : (grp ? hv.y : hv.x);  // scales 4kb..4kb+3
+                    const uint32_t hb[4] = {qh[j].x, qh[j].y, qh[j].z, qh[j].w};
+                    const uint32_t n0[4] = {cv[j][0].x, cv[j][0].y, cv[j][0].z, cv[j][0].w};
+                    const uint32_t n1[4] = {cv[j][1].x, cv[j][1].y, cv[j][1].z, cv[j][1].w};
+                    uint32_t o[8];
+                    convert_q6k_sub_fold<false, 0>(n0, hb, h2dup(d * (float)(int8_t)(ws & 0xff)), o);
+                    tmem_st8(ta, o);
+                    convert_q6k_sub_fold<false, 2>(n1, hb, h2dup(d * (float)(int8_t)((ws >> 8) & 0xff)), o);
+                    tmem_st8(ta + 8, o);
+                    convert_q6k_sub_fold<true, 4>(n0, hb, h2dup(d * (float)(int8_t)((ws >> 16) & 0xff)), o);
+                    tmem_st8(ta + 16, o);
+                    convert_q6k_sub_fold<true, 6>(n1, hb, h2dup(d * (float)(int8_t)(ws >> 24)), o);
+                    tmem_st8(ta + 24, o);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&k_full[(2 * t + j) % L::NPAIR]);
+            }
+            return true;
+        };
         for (int t = 0, ti = 0, tt = 0; t < nsteps && ok; ++t) {  // t: step
             if (tt == 0) rvalid = row < tile_of(ti).valid_groups * 16;
             if (++tt == nsb) { tt = 0; ++ti; }
@@ -594,6 +746,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // rows past N were not loaded: their scales are forced to 0, so they convert to zeros
             const uint8_t *chunk = sP + p * 8 * C::CB + (row >> 4) * C::CB;
             const int r16 = row & 15;
+            if (C::FOLD && C::BASE != KQ_Q8_0) {
+                if (!(ok = fold_convert_kquant(t, grp, row, rvalid, chunk, r16, lane_base))) break;
+                mbar_arrive(&p_empty[p]);
+                continue;
+            }
             if (C::Q8 || C::FOLD) {
                 // Q8_0: the row's 64 codes of kblock kb sit at kb*1024 + r16*64; its 8 f16 block
                 // scales at 4096 + r16*16.  Codes go to f16 exactly: (0x6400 | (c ^ 0x80)) = 1152 + c;
@@ -611,7 +768,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int j = 0; j < 2; ++j) {
                     if (t > 0) {
                         const int pq = 2 * (t - 1) + j;
-                        if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag, P.wait_ns))) break;
+                        if (!(ok = mbar_wait_sleep(&k_empty[pq % L::NPAIR], (pq / L::NPAIR) & 1, abort_flag, P.wait_ns))) break;
                     }
                     tc_fence_after();
                     uint32_t r[32];
@@ -639,7 +796,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tmem_st32(lane_base + C::TM_A + (grp + 2 * j) * C::A_COLS, r);
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(&k_full[(2 * t + j) % NPAIR]);
+                    mbar_arrive(&k_full[(2 * t + j) % L::NPAIR]);
                 }
                 if (!ok) break;
                 if (grp == 0 && !C::FOLD) {
@@ -690,7 +847,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int kb = grp + 2 * j;
                 if (t > 0) {
                     const int pq = 2 * (t - 1) + j;
-                    if (!(ok = mbar_wait_sleep(&k_empty[pq % NPAIR], (pq / NPAIR) & 1, abort_flag, P.wait_ns))) break;
+                    if (!(ok = mbar_wait_sleep(&k_empty[pq % L::NPAIR], (pq / L::NPAIR) & 1, abort_flag, P.wait_ns))) break;
                 }
                 tc_fence_after();
                 const uint32_t ta = lane_base + C::TM_A + kb * C::A_COLS;
@@ -727,7 +884,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&k_full[(2 * t + j) % NPAIR]);
+                mbar_arrive(&k_full[(2 * t + j) % L::NPAIR]);
             }
             if (!ok) break;
             if (grp == 0) {
@@ -780,7 +937,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int plist = 0, pb = 0;        // its pair-list offset (token quarter included), its column block
         bool pwait = true;            // its barrier phase has been waited for
         auto swq_token = [&](int j) {  // quantize token j of the pending unit into its hq block
-            const float *hs = P.scr + ((int64_t)blockIdx.x * 2 + ((sw_u - 1) & 1)) * (TC_TOK * 256) + (tq * 32 + j) * 256;
+            const float *hs = P.scr + ((int64_t)blockIdx.x * 2 + ((sw_u - 1) & 1)) * (C::TOK * 256) + (tq * 32 + j) * 256;
             const float4 *hv = reinterpret_cast<const float4 *>(hs) + 2 * lane;
             const float4 h0 = hv[0], h1 = hv[1];
             const float v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
@@ -810,23 +967,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
             }
             if (C::FOLD) {
-                // folded Q8_0: the tile's accumulator holds the finished sums; read it once, at the
-                // tile's last step, and release the buffer for the tile after next
+                // folded scales: the tile's accumulator holds the finished sums; read once, at the tile's
+                // last step: warp (lane quarter q, token quarter tq) takes rows 32q.. and tokens 64tq..,
+                // in two halves of 32 tokens, then releases the accumulator for the next tile
                 if (!last) continue;
-                const int ab = tile_i & 1;
-                if (!(ok = mbar_wait_sleep(&acc_full[ab], (tile_i >> 1) & 1, abort_flag, P.wait_ns))) break;
+                constexpr int TPW = C::TOK / 4;  // tokens of one warp's token quarter
+                const int ab = C::NACC == 1 ? 0 : (tile_i & 1), use = C::NACC == 1 ? tile_i : (tile_i >> 1);
+                if (!(ok = mbar_wait_sleep(&acc_full[ab], use & 1, abort_flag, P.wait_ns))) break;
                 tc_fence_after();
+                const TcTile T = tile_of(tile_i);
+                for (int hh = 0; hh < TPW / 32; ++hh) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[8];
-                    tmem_ld8(lane_base + ab * TC_TOK + tq * 32 + c * 8, v);
-                    tmem_wait_ld();
+                    for (int c = 0; c < 4; ++c) {
+                        float v[8];
+                        tmem_ld8(lane_base + ab * C::TOK + tq * TPW + hh * 32 + c * 8, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[c * 8 + i] = v[i];
+                        for (int i = 0; i < 8; ++i) acc[c * 8 + i] = v[i];
+                    }
+                    // a split-K tile keeps its sums in acc for the cluster reduction after the loop
+                    if (P.nsplit == 1 && T.n0 + row < P.N) {
+                        const int mrem = T.tok_valid - tq * TPW - hh * 32;
+                        float *yc = P.y + (int64_t)(T.m0 + tq * TPW + hh * 32) * P.ldy + T.n0 + row;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < mrem) yc[(int64_t)i * P.ldy] = acc[i];
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                continue;
             } else if (C::Q8) {
                 // Q8_0: per 32-element block b, acc += (d_w*d_a)*P_b with each product rounded on its
                 // own and the blocks added in ascending K order -- the CPU oracle's arithmetic, so the
@@ -842,11 +1013,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t dword = (b & 4) ? ((b & 2) ? dwv.w : dwv.z) : ((b & 2) ? dwv.y : dwv.x);
                     const float dw = half_bits_to_float((uint16_t)((b & 1) ? (dword >> 16) : (dword & 0xffff)));
                     const float2 dw2 = make_float2(dw, dw);
-                    const float4 *dap = reinterpret_cast<const float4 *>(sDA + (h * 8 + b) * TC_TOK * 4) + tq * 8;
+                    const float4 *dap = reinterpret_cast<const float4 *>(sDA + (h * 8 + b) * C::TOK * 4) + tq * 8;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float pv[8];
-                        tmem_ld8(lane_base + qb * TC_TOK + tq * 32 + c * 8, pv);
+                        tmem_ld8(lane_base + qb * C::TOK + tq * 32 + c * 8, pv);
                         tmem_wait_ld();
                         if (DBG) {
                             const TcTile T = tile_of(tile_i);
@@ -881,7 +1052,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag, P.wait_ns))) break;
             tc_fence_after();
             const float2 rs = reinterpret_cast<const float2 *>(sH + h * TC_ROWS * 8)[row];  // (d, -dmin)
-            const float4 *dap = reinterpret_cast<const float4 *>(sDA + h * TC_TOK * 4) + tq * 8;
+            const float4 *dap = reinterpret_cast<const float4 *>(sDA + h * C::TOK * 4) + tq * 8;
             const float2 dw2 = make_float2(rs.x, rs.x), nm2 = make_float2(rs.y, rs.y);
             if (C::Q5) {
                 // Q5_K: the min-term tile is single and the next super-block's extension MMA waits for
@@ -914,7 +1085,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t col = tq * 32 + c * 8;
                 float s1[8], s2[8];
                 constexpr bool S2LATE = C::EXT && !C::Q5;
-                tmem_ld8(lane_base + buf * TC_TOK + col, s1);
+                tmem_ld8(lane_base + buf * C::TOK + col, s1);
                 if (S2LATE) tmem_ld8(lane_base + C::TM_S2 + col, s2);
                 tmem_wait_ld();
                 if (DBG) {
@@ -968,7 +1139,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // for this thread's 32 tokens: gate (s < 2) is parked, up (s >= 2) turns it into h.
                 const int s = tile_i & 3;
                 const int mrem = T.tok_valid - tq * 32;
-                float *sc = P.scr + ((int64_t)blockIdx.x * 2 + (sw_u & 1)) * (TC_TOK * 256) + tq * 32 * 256 +
+                float *sc = P.scr + ((int64_t)blockIdx.x * 2 + (sw_u & 1)) * (C::TOK * 256) + tq * 32 * 256 +
                             TC_ROWS * (s & 1) + row;
                 if (s < 2) {
 #pragma unroll
@@ -1041,8 +1212,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
         cluster.sync();
         const int S = P.nsplit, rank = blockIdx.z;
-        const int rows_per = (TC_TOK + S - 1) / S;
-        const int r0 = rank * rows_per, r1 = min(TC_TOK, r0 + rows_per);
+        const int rows_per = (C::TOK + S - 1) / S;
+        const int r0 = rank * rows_per, r1 = min(C::TOK, r0 + rows_per);
         for (int idx = tid; idx < (r1 - r0) * TC_ROWS; idx += TC_THREADS) {
             const int ml = r0 + idx / TC_ROWS, nl = idx % TC_ROWS;
             float v = 0.0f;
@@ -1130,6 +1301,40 @@ __global__ void act_panel_f32_kernel(const float *__restrict__ x, int64_t ldx, i
     if (lane == 0) D[(int64_t)sb * M_pad + m] = d;
 }
 
+// Activation prologue of the folded K-quant path from fp32 rows: each warp quantises one 256-element
+// block of row m with the Q8_K block arithmetic (q8k_block_codes, the standalone quantizer's) and writes
+// f16(d*q) for its 8 elements -- the panel act_panel_fold_kernel builds from the Q8_K block, without the
+// Q8_K round trip through memory.  One warp per (row, super-block); rows past M are zero.  Also clears
+// the workspace's device flag.
+template <bool VEC>
+__global__ void act_panel_f32_fold_kernel(const float *__restrict__ x, int64_t ldx, int M, int M_pad, int nsb,
+                                          __half *__restrict__ A, unsigned long long *__restrict__ err) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (int64_t)M_pad * nsb) return;
+    const int m = (int)(wid / nsb), sb = (int)(wid % nsb);
+    const int64_t K = (int64_t)nsb * 256;
+    int q[8] = {0, 0, 0, 0, 0, 0, 0, 0}, pair = 0;
+    float d = 0.0f;
+    if (m < M) {
+        const float *p = x + (int64_t)m * ldx + sb * 256 + lane * 8;
+        float v[8];
+        if (VEC) {
+            const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = p[i];
+        }
+        q8k_block_codes(v, q, pair, d);
+    }
+    __half hv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hv[i] = __float2half_rn(d * (float)q[i]);
+    *reinterpret_cast<uint4 *>(A + (int64_t)m * K + sb * 256 + lane * 8) = *reinterpret_cast<uint4 *>(hv);
+}
+
 // Activation prologue for Q8_0 weights: Q8_1 rows -> f16 code panel [M_pad][K] and f32 scale panel
 // [K/32][M_pad] (the f16 block scale widened); rows past M are zero.  One warp per (row, 256
 // elements): lane l takes elements 8l .. 8l+7 of block l/4.  Also clears the workspace's device flag.
@@ -1179,6 +1384,34 @@ __global__ void act_panel_q81_fold_kernel(const uint8_t *__restrict__ xq, int M,
         const uint32_t w0 = *reinterpret_cast<const uint32_t *>(b + 4 + (lane & 3) * 8);
         const uint32_t w1 = *reinterpret_cast<const uint32_t *>(b + 8 + (lane & 3) * 8);
         const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(b));
+        __half hv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            hv[i] = __float2half_rn(d * (float)(int8_t)((w0 >> (8 * i)) & 0xff));
+            hv[4 + i] = __float2half_rn(d * (float)(int8_t)((w1 >> (8 * i)) & 0xff));
+        }
+        out = *reinterpret_cast<uint4 *>(hv);
+    }
+    *reinterpret_cast<uint4 *>(A + (int64_t)m * K + sb * 256 + lane * 8) = out;
+}
+
+// Activation prologue of the folded K-quant path: Q8_K rows -> f16 panel [M_pad][K] of d*q (the fp32
+// block scale times the code, rounded once to f16); rows past M are zero.  One warp per (row,
+// super-block).  Also clears the device flag.
+__global__ void act_panel_fold_kernel(const uint8_t *__restrict__ xq, int M, int M_pad, int nsb,
+                                      __half *__restrict__ A, unsigned long long *__restrict__ err) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (int64_t)M_pad * nsb) return;
+    const int m = (int)(wid / nsb), sb = (int)(wid % nsb);
+    const int64_t K = (int64_t)nsb * 256;
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (m < M) {
+        const uint8_t *blk = xq + ((int64_t)m * nsb + sb) * kQ8KBytes;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(blk + 4 + lane * 8);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(blk + 8 + lane * 8);
+        const float d = *reinterpret_cast<const float *>(blk);
         __half hv[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -1267,9 +1500,9 @@ static size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // Workspace of the dense tensor-core GEMM: device flag, f16 code panel, (Q4_K/Q6_K) f16 bsum panel,
 // f32 scale panel with one row per scale block (256 elements for Q8_K, 32 for Q8_1).
-static TcWs tc_ws(kq_dtype wt, int64_t M, int64_t K) {
+static TcWs tc_ws(kq_dtype wt, int64_t M, int64_t K, int tok = TC_TOK) {
     TcWs w{};
-    w.M_pad = (int)((M + TC_TOK - 1) / TC_TOK * TC_TOK);
+    w.M_pad = (int)((M + tok - 1) / tok * tok);
     const int64_t nsb = K / 256;
     const bool q8 = wt == KQ_Q8_0;
     size_t o = 0;
@@ -1392,7 +1625,8 @@ int tc_split_factor(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
 
 size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     if (!tc_eligible(wt, M, N, K)) return 0;
-    return tc_ws(wt, M, K).total;
+    // room for either form: the exact kernels' 128-token tiles and the folded mode's 256-token tiles
+    return std::max(tc_ws(wt, M, K).total, tc_ws(wt, M, K, TcCfg<KQ_Q8_0F>::TOK).total);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -1438,7 +1672,7 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.rows};
         cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-        cuuint32_t box[2] = {TC_KB, TC_TOK};
+        cuuint32_t box[2] = {TC_KB, (cuuint32_t)TcCfg<DT>::TOK};
         cuuint32_t es[2] = {1, 1};
         CUresult r = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.A, dims, strides, box, es,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1511,8 +1745,23 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     return KQ_OK;
 }
 
-static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st, bool fold = false) {
-    if (fold) return launch_tc<KQ_Q8_0F>(a, st);
+static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st, bool fold = false, int tok = TC_TOK) {
+    if (fold && tok == TC_TOK) {
+        switch (wt) {
+        case KQ_Q4_K: return launch_tc<KQ_Q4_KF + KQ_FOLD128>(a, st);
+        case KQ_Q5_K: return launch_tc<KQ_Q5_KF + KQ_FOLD128>(a, st);
+        case KQ_Q6_K: return launch_tc<KQ_Q6_KF + KQ_FOLD128>(a, st);
+        default: return launch_tc<KQ_Q8_0F + KQ_FOLD128>(a, st);
+        }
+    }
+    if (fold) {
+        switch (wt) {
+        case KQ_Q4_K: return launch_tc<KQ_Q4_KF>(a, st);
+        case KQ_Q5_K: return launch_tc<KQ_Q5_KF>(a, st);
+        case KQ_Q6_K: return launch_tc<KQ_Q6_KF>(a, st);
+        default: return launch_tc<KQ_Q8_0F>(a, st);
+        }
+    }
     switch (wt) {
     case KQ_Q4_K: return launch_tc<KQ_Q4_K>(a, st);
     case KQ_Q5_K: return launch_tc<KQ_Q5_K>(a, st);
@@ -1521,17 +1770,32 @@ static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st, b
     }
 }
 
+// Token-tile width of the folded mode: 256 tokens once they give at least as many tiles as there are
+// SMs, else 128 (which may also split K).
+static int fold_tok(int64_t M, int64_t N) {
+    const int64_t tiles256 = ((M + 255) / 256) * ((N + TC_ROWS - 1) / TC_ROWS);
+    return tiles256 >= sm_count() ? 256 : TC_TOK;
+}
+
 // The tensor-core GEMM from quantised rows xq, or (xf != NULL, Q4_K/Q5_K/Q6_K) from fp32 rows xf of
 // stride ldx quantised to Q8_K inside the prologue.
 static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, const float *xf, int64_t ldx, int64_t M,
                               int64_t N, int64_t K, float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st,
                               const TcDebug *dbg, bool fold = false) {
-    const TcWs L = tc_ws(wt, M, K);
-    if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || L.M_pad / TC_TOK > 65535)
+    const int tok = fold ? fold_tok(M, N) : TC_TOK;
+    const TcWs L = tc_ws(wt, M, K, tok);
+    if ((N + TC_ROWS - 1) / TC_ROWS > 65535 || L.M_pad / tok > 65535)
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm: shape too large for the tensor-core grid");
     const int64_t nsb = K / 256;
     const int64_t warps = (int64_t)L.M_pad * nsb;
-    if (xf) {
+    if (xf && fold) {
+        if (wt == KQ_Q8_0) return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_f32: Q8_0 weights take Q8_1 activations");
+        const bool vec = (reinterpret_cast<uintptr_t>(xf) & 15) == 0 && ldx % 4 == 0;
+        auto kern = vec ? act_panel_f32_fold_kernel<true> : act_panel_f32_fold_kernel<false>;
+        kern<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(xf, ldx, (int)M, L.M_pad, (int)nsb,
+                                                          reinterpret_cast<__half *>(workspace + L.off_a),
+                                                          reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
+    } else if (xf) {
         if (wt == KQ_Q8_0) return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_f32: Q8_0 weights take Q8_1 activations");
         const bool vec = (reinterpret_cast<uintptr_t>(xf) & 15) == 0 && ldx % 4 == 0;
         auto kern = vec ? act_panel_f32_kernel<true> : act_panel_f32_kernel<false>;
@@ -1539,9 +1803,12 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
             xf, ldx, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
             reinterpret_cast<__half *>(workspace + L.off_e), reinterpret_cast<float *>(workspace + L.off_d),
             reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
-    } else if (fold) {
-        if (wt != KQ_Q8_0) return fail(KQ_ERR_UNSUPPORTED_DTYPE, "kq_gemm_ex: folded scales need Q8_0 weights");
+    } else if (fold && wt == KQ_Q8_0) {
         act_panel_q81_fold_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+            xq, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
+            reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
+    } else if (fold) {
+        act_panel_fold_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
             xq, (int)M, L.M_pad, (int)nsb, reinterpret_cast<__half *>(workspace + L.off_a),
             reinterpret_cast<unsigned long long *>(workspace + L.off_flag));
     } else if (wt == KQ_Q8_0)
@@ -1558,12 +1825,14 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
     TcLaunch a{};
     a.w = w; a.y = y; a.ldy = ldy; a.M = M; a.N = N; a.K = K;
     a.A = workspace + L.off_a; a.E = workspace + L.off_e; a.D = reinterpret_cast<float *>(workspace + L.off_d);
-    a.rows = L.M_pad; a.dstride = L.M_pad; a.m_tiles = (int)(L.M_pad / TC_TOK);
-    a.nsplit = tc_splits(wt, M, N, K);
+    a.rows = L.M_pad; a.dstride = L.M_pad; a.m_tiles = (int)(L.M_pad / tok);
+    // the 256-token folded tiles are never split (their epilogue writes y); the 128-token ones split as
+    // the exact kernels do, with the Q4_K cost model (their steps cost alike)
+    a.nsplit = !fold ? tc_splits(wt, M, N, K) : tok == TC_TOK ? tc_splits(KQ_Q4_K, M, N, K) : 1;
     a.err = reinterpret_cast<unsigned long long *>(workspace + L.off_flag);
     a.dbg = dbg;
     if (fold && dbg && dbg->sums) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_ex: no integer sums with folded scales");
-    s = launch_tc_dt(wt, a, st, fold);
+    s = launch_tc_dt(wt, a, st, fold, tok);
     if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
     return s;
 }
@@ -1573,14 +1842,14 @@ kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, i
     return tc_gemm_impl(wt, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st, dbg);
 }
 
-kq_status tc_gemm_folded(const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
-                         uint8_t *workspace, cudaStream_t st, const TcDebug *dbg) {
-    return tc_gemm_impl(KQ_Q8_0, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st, dbg, true);
+kq_status tc_gemm_folded(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
+                         int64_t ldy, uint8_t *workspace, cudaStream_t st, const TcDebug *dbg) {
+    return tc_gemm_impl(wt, w, xq, nullptr, 0, M, N, K, y, ldy, workspace, st, dbg, true);
 }
 
 kq_status tc_gemm_f32(kq_dtype wt, const uint8_t *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
-                      float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st) {
-    return tc_gemm_impl(wt, w, nullptr, x, ldx, M, N, K, y, ldy, workspace, st, nullptr);
+                      float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st, bool fold) {
+    return tc_gemm_impl(wt, w, nullptr, x, ldx, M, N, K, y, ldy, workspace, st, nullptr, fold);
 }
 
 // ---- routed experts on the tensor cores

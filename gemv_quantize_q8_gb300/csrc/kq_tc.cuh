@@ -21,17 +21,18 @@ bool tc_eligible(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 kq_status tc_gemm(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
                   int64_t ldy, uint8_t *workspace, cudaStream_t st, const TcDebug *dbg = nullptr);
-// Q8_0 x Q8_1 with the block scales folded into the f16 operands (f16(d_w*w) times f16(d_a*q), one fp32
-// accumulator per tile over the whole of K): not bit-exact; shape and workspace as tc_gemm.
-kq_status tc_gemm_folded(const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
-                         uint8_t *workspace, cudaStream_t st, const TcDebug *dbg = nullptr);
+// The GEMM with the block scales folded into the f16 operands (dequantised weights times f16(d_a*q), one
+// fp32 accumulator per 128 x 256 tile over the whole of K): not bit-exact; Q4_K, Q5_K, Q6_K (Q8_K rows)
+// and Q8_0 (Q8_1 rows); shape and workspace as tc_gemm.
+kq_status tc_gemm_folded(kq_dtype wt, const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K, float *y,
+                         int64_t ldy, uint8_t *workspace, cudaStream_t st, const TcDebug *dbg = nullptr);
 // Split-K factor (CTAs per output tile) the tensor-core path takes for this shape on the current
 // device; 0 when the shape does not take the tensor-core path.
 int tc_split_factor(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 // The same GEMM from fp32 activation rows (stride ldx), quantised to Q8_K inside the prologue with the
 // standalone quantizer's arithmetic (Q4_K, Q5_K, Q6_K weights).
 kq_status tc_gemm_f32(kq_dtype wt, const uint8_t *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
-                      float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st);
+                      float *y, int64_t ldy, uint8_t *workspace, cudaStream_t st, bool fold = false);
 
 // Routed experts on the tensor cores: 128-row tiles of each expert's routed rows (a tile table built
 // by the routing pass), activation panels gathered in routed order, outputs scattered back to their

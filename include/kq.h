@@ -192,15 +192,19 @@ KQ_API kq_status kq_gemm(kq_dtype wt, const void *w, const void *xq, int64_t M, 
                   int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream);
 
 /* kq_gemm with options.  flags = 0 is kq_gemm itself.
- * KQ_GEMM_FOLD_SCALES (Q8_0 weights x Q8_1 activations, the tensor-core shapes M >= 9, N >= 128):
- * every 32-block's scales are folded into the tensor-core operands -- the weights enter the MMA as
- * f16(d_w*w), the activations as f16(d_a*q), each rounded once to f16 -- so a 128 x 128 output tile
- * accumulates over the whole of K in one fp32 tensor-memory buffer, read out once per tile, instead of
- * once per 32-block as the exact kernel must ([llama-18] keeps the Q8_0 x Q8_1 dot per 32-block; this
- * is the throughput form of the same product).  Not bit-exact: each product carries two f16 roundings
- * (relative error below 2^-10), so |y - y_exact| <= (2^-10 + K*2^-24) * sum_i |w_i*x_i| (dequantized
- * values); NMSE against the exact result is ~1e-7 on N(0,1) data.  Other shapes take kq_gemm's exact
- * kernels.  Other weight types: KQ_ERR_UNSUPPORTED_DTYPE.  Workspace: kq_gemm_workspace_bytes. */
+ * KQ_GEMM_FOLD_SCALES -- an opt-in throughput mode for the tensor-core shapes (M >= 9, N >= 128) of
+ * Q4_K, Q5_K, Q6_K (Q8_K rows) and Q8_0 (Q8_1 rows) weights: the block scales are folded into the
+ * tensor-core operands instead of being applied to integer block sums.  The weights enter the MMA as
+ * their dequantised f16 values -- f16(c*f16(d*sc) + f16(-dmin*m)) (Q4_K, Q5_K), f16((c-32)*f16(d*sc))
+ * (Q6_K), f16(d_w*w) (Q8_0) -- and the activations as f16(d_a*q), so a 128 x 256 output tile
+ * accumulates over the whole of K in one fp32 tensor-memory buffer read out once per tile: no per-block
+ * read-out, no min-term tile, one MMA per 16 K for Q6_K, and every converted weight serves 256 tokens.
+ * The weights stay packed in device memory ([vllm-2890] keep-quant: staged once, never expanded);
+ * only the integer dots give way to f16 products.  Not bit-exact: each operand is rounded to f16, so
+ * |y - y_exact| <= (3*2^-11 + (K + K/32 + 4)*2^-24) * sum_i (|d*sc*c_i| + |dmin*m_i|)*|x_i| (plus f16
+ * subnormal terms); NMSE against the exact result is ~1e-7 on N(0,1) data.  Deterministic.  Other
+ * shapes take kq_gemm's exact kernels; other weight types: KQ_ERR_UNSUPPORTED_DTYPE.  Workspace:
+ * kq_gemm_workspace_bytes (sized for both tile widths). */
 #define KQ_GEMM_FOLD_SCALES 1u
 KQ_API kq_status kq_gemm_ex(kq_dtype wt, const void *w, const void *xq, int64_t M, int64_t N, int64_t K, float *y,
                             int64_t ldy, unsigned flags, void *workspace, size_t ws_bytes, kq_stream_t stream);
@@ -218,6 +222,13 @@ KQ_API kq_status kq_gemm_ex(kq_dtype wt, const void *w, const void *xq, int64_t 
 KQ_API size_t kq_gemm_f32_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 KQ_API kq_status kq_gemm_f32(kq_dtype wt, const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
                              float *y, int64_t ldy, void *workspace, size_t ws_bytes, kq_stream_t stream);
+
+/* kq_gemm_f32 with kq_gemm_ex's flags: with KQ_GEMM_FOLD_SCALES on the tensor-core path the prologue
+ * quantises each 256-element block with the Q8_K quantizer's arithmetic and writes f16(d*q) straight
+ * into the folded mode's activation panel (same result as kq_quantize_q8k followed by kq_gemm_ex). */
+KQ_API kq_status kq_gemm_f32_ex(kq_dtype wt, const void *w, const float *x, int64_t ldx, int64_t M, int64_t N,
+                                int64_t K, float *y, int64_t ldy, unsigned flags, void *workspace, size_t ws_bytes,
+                                kq_stream_t stream);
 
 /* Routed-expert GEMM (MUL_MAT_ID; [llama-18] routed-compact MMQ: each expert's tiles cover only the
  * rows routed to it, never a width chosen from the total number of pairs).  The tile width itself is

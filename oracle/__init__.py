@@ -206,13 +206,14 @@ def gemm_sampled_terms(dtype: int, w: np.ndarray, xq: np.ndarray, K: int, m_idx,
 
 
 def absdot_sampled(dtype: int, w: np.ndarray, xq: np.ndarray, K: int, m_idx, n_idx) -> np.ndarray:
-    """f64 [S, 3]: for each sampled (m, n), sum |a_i*b_i|, sum |a_i| and sum |b_i| over the dequantised
-    weight row a and activation row b."""
+    """f64 [S, 4]: for each sampled (m, n) over the dequantised weight row a and activation row b:
+    sum |a_i*b_i|, sum |a_i|, sum |b_i|, and sum (|d*sc*c_i| + |dmin*m_i|)*|b_i| (the weight's two parts
+    apart; the first sum again for Q6_K and Q8_0)."""
     w = np.ascontiguousarray(w, dtype=np.uint8)
     xq = np.ascontiguousarray(xq, dtype=np.uint8)
     mi = np.ascontiguousarray(m_idx, dtype=np.int64)
     ni = np.ascontiguousarray(n_idx, dtype=np.int64)
-    out = np.empty((mi.size, 3), dtype=np.float64)
+    out = np.empty((mi.size, 4), dtype=np.float64)
     lib().orc_absdot_sampled(dtype, _ptr(w), _ptr(xq), K, mi.size, _ptr(mi), _ptr(ni), _ptr(out))
     return out
 

@@ -581,19 +581,45 @@ ORC_API void orc_block_sums(int dtype, const uint8_t *w, const uint8_t *xq, int6
     (void)nthreads;
 }
 
+/* Magnitudes of the two parts of a dequantised weight: |d*sc*c| and |dmin*m| (Q4_K, Q5_K), |x| and 0
+ * (Q6_K, Q8_0), for the 256 (Q8_0: 32) elements of one block. */
+static void weight_parts(int dtype, const uint8_t *blk, double *t1, double *t2) {
+    if (dtype == ORC_Q4_K || dtype == ORC_Q5_K) {
+        double d = orc_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+        double dmin = orc_half_to_float((uint16_t)(blk[2] | (blk[3] << 8)));
+        for (int i = 0; i < 256; ++i) {
+            int sc, mn;
+            q4k_scale_min(blk + 4, i / 32, &sc, &mn);
+            int c = dtype == ORC_Q4_K ? q4k_code(blk + 16, i) : q5k_code(blk, i);
+            t1[i] = fabs(d * sc * c);
+            t2[i] = fabs(dmin * mn);
+        }
+    } else {
+        int n = dtype == ORC_Q8_0 ? 32 : 256;
+        if (dtype == ORC_Q6_K) orc_dequant_q6_k(blk, t1);
+        else orc_dequant_q8_0(blk, t1);
+        for (int i = 0; i < n; ++i) {
+            t1[i] = fabs(t1[i]);
+            t2[i] = 0.0;
+        }
+    }
+}
+
 /* Magnitudes of a sampled dot product, from the dequantised values a_i (weight row n) and b_i
- * (activation row m), in f64: out[3s] = sum |a_i*b_i|, out[3s+1] = sum |a_i|, out[3s+2] = sum |b_i|.
- * The scale of the rounding error of any computation that rounds the operands themselves. */
+ * (activation row m), in f64: out[4s] = sum |a_i*b_i|, out[4s+1] = sum |a_i|, out[4s+2] = sum |b_i|,
+ * out[4s+3] = sum (|d*sc*c_i| + |dmin*m_i|)*|b_i| (the weight's two parts apart; equal to the first
+ * sum for Q6_K and Q8_0).  The scale of the rounding error of any computation that rounds the
+ * operands, or the parts of a weight, themselves. */
 ORC_API void orc_absdot_sampled(int dtype, const uint8_t *w, const uint8_t *xq, int64_t K, int64_t S,
                                 const int64_t *m_idx, const int64_t *n_idx, double *out) {
     int64_t wrb = w_row_bytes(dtype, K), xrb = act_row_bytes(dtype, K);
     int64_t we = orc_block_elems(dtype), wb = orc_block_bytes(dtype);
     int adt = dtype == ORC_Q8_0 ? ORC_Q8_1 : ORC_Q8_K;
     int64_t ae = orc_block_elems(adt), ab = orc_block_bytes(adt);
-    double wv[256], av[256];
+    double wv[256], av[256], p1[256], p2[256];
     for (int64_t s = 0; s < S; ++s) {
         const uint8_t *wr = w + n_idx[s] * wrb, *xr = xq + m_idx[s] * xrb;
-        double sab = 0.0, sa = 0.0, sb = 0.0;
+        double sab = 0.0, sa = 0.0, sb = 0.0, sm = 0.0;
         for (int64_t k0 = 0; k0 < K; k0 += 256) {
             for (int64_t k = k0; k < k0 + 256; k += we) {
                 const uint8_t *blk = wr + (k / we) * wb;
@@ -603,6 +629,7 @@ ORC_API void orc_absdot_sampled(int dtype, const uint8_t *w, const uint8_t *xq, 
                 case ORC_Q6_K: orc_dequant_q6_k(blk, wv + (k - k0)); break;
                 default: orc_dequant_q8_0(blk, wv + (k - k0)); break;
                 }
+                weight_parts(dtype, blk, p1 + (k - k0), p2 + (k - k0));
             }
             for (int64_t k = k0; k < k0 + 256; k += ae) {
                 const uint8_t *blk = xr + (k / ae) * ab;
@@ -613,11 +640,13 @@ ORC_API void orc_absdot_sampled(int dtype, const uint8_t *w, const uint8_t *xq, 
                 sab += fabs(wv[i] * av[i]);
                 sa += fabs(wv[i]);
                 sb += fabs(av[i]);
+                sm += (p1[i] + p2[i]) * fabs(av[i]);
             }
         }
-        out[3 * s] = sab;
-        out[3 * s + 1] = sa;
-        out[3 * s + 2] = sb;
+        out[4 * s] = sab;
+        out[4 * s + 1] = sa;
+        out[4 * s + 2] = sb;
+        out[4 * s + 3] = sm;
     }
 }
 

@@ -82,3 +82,34 @@ def test_gemm_f32_prefill_full_size_equals_two_step():
     a = _fused(dtype, wn, xd, M, N, K, K)
     b = _two_step(dtype, wn, xd, M, N, K, K)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dtype", DTS)
+@pytest.mark.parametrize("M,N,K,pad", [(160, 256, 512, 0), (300, 392, 1536, 4), (8, 256, 1024, 0), (1100, 4300, 256, 0)])
+def test_gemm_f32_folded_equals_quantize_then_folded_gemm(dtype, M, N, K, pad):
+    """kq_gemm_f32_ex with KQ_GEMM_FOLD_SCALES: the prologue's f16(d*q) panel from the fp32 rows is the one
+    the folded GEMM builds from the quantiser's Q8_K rows, so the result equals kq_quantize_q8k (Q8_0:
+    kq_quantize_q8_1) followed by kq_gemm_ex with the same flag, bit for bit -- with 128-token tiles
+    (split or not), 256-token tiles (M = 1100) and the exact fallback (M = 8)."""
+    g = synth.rng(970 + dtype + M + K)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    ldx = K + pad
+    xp = np.zeros((M, ldx), np.float32)
+    xp[:, :K] = x
+    wn = repack(dtype, w, N, K)
+    xd = dev(xp)
+    ya = torch.full((M, N), float("nan"), device=DEV)
+    wsa = kq.kq_gemm_f32_workspace_bytes(dtype, M, N, K)
+    wsa_t = torch.zeros(wsa, dtype=torch.uint8, device=DEV)
+    kq.kq_gemm_f32_ex(dtype, wn, xd.reshape(-1), ldx, M, N, K, ya, N, kq.GEMM_FOLD_SCALES, wsa_t, wsa)
+    assert kq.kq_read_device_flag(wsa_t) == 0
+    xq = act_quant(dtype, xd[:, :K].contiguous(), M, K)
+    yb = torch.full((M, N), float("nan"), device=DEV)
+    wsb = kq.gemm_workspace_bytes(dtype, M, N, K)
+    wsb_t = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=DEV)
+    kq.kq_gemm_ex(dtype, wn, xq, M, N, K, yb, N, kq.GEMM_FOLD_SCALES, wsb_t if wsb else None, wsb)
+    assert torch.equal(ya, yb), "kq_gemm_f32_ex (folded) differs from quantize + kq_gemm_ex"
+    xa = oracle.quantize_q8_1(x) if dtype == kq.Q8_0 else oracle.quantize_q8_k(x)
+    mi, ni = g.integers(0, M, 1500), g.integers(0, N, 1500)
+    assert nmse(host(ya)[mi, ni], oracle.gemm_sampled(dtype, w, xa, K, mi, ni)) <= 1e-6

@@ -171,43 +171,79 @@ def test_gemm_q8_0_tensor_core_bit_exact(M, N, K):
 
 
 def folded_bound(absd: np.ndarray, K: int) -> np.ndarray:
-    """Elementwise bound on |y_folded - y_oracle| for Q8_0 with the block scales folded into the f16
-    operands.  With a_i = d_w*w_i and b_i = d_a*q_i (exact reals): the kernel multiplies f16(a_i) by
-    f16(b_i) -- each rounded once to f16, relative error <= 2^-11 for normal values and absolute error
-    <= 2^-25 in the subnormal range -- exactly, and adds the K products in fp32 (<= K*2^-24 of sum
-    |a_i*b_i| in any order); the oracle rounds (d_w*d_a), its product with the exact block dot and each
-    of the K/32 adds (<= (K/32 + 3)*2^-24 of the same sum).  absd = oracle.absdot_sampled rows
-    (sum |a_i*b_i|, sum |a_i|, sum |b_i|)."""
-    rel = 2.0 ** -10 + 2.0 ** -22 + (K + K // 32 + 4) * 2.0 ** -24
-    return rel * absd[:, 0] + 2.0 ** -24 * (absd[:, 1] + absd[:, 2])
+    """Elementwise bound on |y_folded - y_oracle| with the block scales folded into the f16 operands
+    (kq_gemm_ex, KQ_GEMM_FOLD_SCALES).  Per element, with u = 2^-11 (f16) and the weight written as its two
+    parts t1 = d*sc*c and t2 = dmin*m (Q6_K, Q8_0: t2 = 0):
+      * the weight operand is f16(c*f16(d*sc) + f16(-dmin*m)) (Q6_K: f16((c-32)*f16(d*sc)), Q8_0:
+        f16(d_w*w)): within 2u*(|t1| + |t2|);
+      * the activation operand f16(d_a*q) (d_a*q rounded to fp32 first): within (u + 2^-24)*|b|;
+      * the product of two f16 values is exact in fp32, and the K products are added in fp32: within
+        K*2^-24 of their magnitudes; f16 subnormals add at most 2^-25 per rounding in absolute terms;
+      * the oracle's own fp32 scaling is within (K/32 + 3)*2^-24 of the same magnitudes.
+    With M4 = sum (|t1| + |t2|)*|b| (absd[:, 3], from oracle.absdot_sampled) the difference is within
+    (3u + (K + K/32 + 4)*2^-24)*M4 plus the subnormal terms; the bound takes 2^-9 for 3u and
+    2^-22*(sum |a| + sum |b|) for the subnormal terms."""
+    rel = 2.0 ** -9 + (K + K // 32 + 8) * 2.0 ** -24
+    return rel * absd[:, 3] + 2.0 ** -22 * (absd[:, 1] + absd[:, 2])
 
 
-@pytest.mark.parametrize("M,N,K", [(130, 200, 768), (300, 392, 1536), (384, 1040, 2560), (9, 128, 256)])
-def test_gemm_q8_0_folded_scales(M, N, K):
-    """kq_gemm_ex with KQ_GEMM_FOLD_SCALES: every output within the folded-operand rounding bound of
-    the oracle (which keeps the exact per-block integer dots) and NMSE <= 1e-6; deterministic from call
-    to call; on shapes off the tensor-core path it is the exact kernel, bit for bit."""
-    g = synth.rng(380 + M + N + K)
-    w = synth.weights(kq.Q8_0, N, K, g)
+@pytest.mark.parametrize("dtype", DTS)
+@pytest.mark.parametrize("M,N,K", [(130, 200, 768), (300, 392, 1536), (384, 1040, 2560), (9, 128, 256),
+                                   (520, 256, 4096), (250, 600, 4096), (129, 1280, 3072)])
+def test_gemm_folded_scales(dtype, M, N, K):
+    """kq_gemm_ex with KQ_GEMM_FOLD_SCALES (256-token tiles, scales folded into the f16 operands): every
+    output within the folded-operand rounding bound of the oracle (which keeps the exact per-block
+    integer dots) and NMSE <= 1e-6; deterministic from call to call; several 128 x 256 tiles, ragged in
+    M and N, and a tile whose 256 tokens hold a single valid row (M = 9)."""
+    g = synth.rng(380 + M + N + K + dtype)
+    w = synth.weights(dtype, N, K, g)
     x = synth.activations(M, K, g, outliers=True)
-    wn = repack(kq.Q8_0, w, N, K)
-    xq = q8_1(dev(x), M, K)
-    wsb = kq.gemm_workspace_bytes(kq.Q8_0, M, N, K)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    wsb = kq.gemm_workspace_bytes(dtype, M, N, K)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=DEV)
     ys = []
     for _ in range(2):
         y = torch.full((M, N), float("nan"), device=DEV)
-        kq.kq_gemm_ex(kq.Q8_0, wn, xq, M, N, K, y, N, kq.GEMM_FOLD_SCALES, ws, wsb)
+        kq.kq_gemm_ex(dtype, wn, xq, M, N, K, y, N, kq.GEMM_FOLD_SCALES, ws, wsb)
         ys.append(host(y))
     assert kq.kq_read_device_flag(ws) == 0
     assert np.array_equal(ys[0], ys[1])
     got = ys[0].reshape(-1)
     xq_h = host(xq).reshape(M, -1)
-    ref = oracle.gemm(kq.Q8_0, w, xq_h, M, N, K).reshape(-1)
+    ref = oracle.gemm(dtype, w, xq_h, M, N, K).reshape(-1)
     mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
-    absd = oracle.absdot_sampled(kq.Q8_0, w, xq_h, K, mi, ni)
-    assert np.all(np.abs(got.astype(np.float64) - ref) <= folded_bound(absd, K))
+    absd = oracle.absdot_sampled(dtype, w, xq_h, K, mi, ni)
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(err <= folded_bound(absd, K)), (err / folded_bound(absd, K)).max()
     assert nmse(got, ref) <= 1e-6
+
+
+@pytest.mark.parametrize("dtype,shape,M", [(kq.Q4_K, (4096, 14336), 2048), (kq.Q6_K, (14336, 4096), 512),
+                                           (kq.Q5_K, (4096, 4096), 128), (kq.Q8_0, (4300, 1024), 1100),
+                                           (kq.Q6_K, (4300, 512), 1100)])
+def test_gemm_folded_prefill_sampled(dtype, shape, M):
+    """Prefill workload shapes through the folded path (256-token tiles at M = 2048, 512 and 1100 -- the last
+    ragged in M and N --, 128-token split-K tiles at M = 128): 3000 sampled outputs against the oracle."""
+    N, K = shape
+    g = synth.rng(0)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    wsb = kq.gemm_workspace_bytes(dtype, M, N, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    y = torch.full((M, N), float("nan"), device=DEV)
+    kq.kq_gemm_ex(dtype, wn, xq, M, N, K, y, N, kq.GEMM_FOLD_SCALES, ws, wsb)
+    yh = host(y)
+    assert np.isfinite(yh).all()
+    mi, ni = g.integers(0, M, 3000), g.integers(0, N, 3000)
+    mi[:2], ni[:2] = [0, M - 1], [N - 1, 0]
+    xq_h = host(xq).reshape(M, -1)
+    ref = oracle.gemm_sampled(dtype, w, xq_h, K, mi, ni)
+    absd = oracle.absdot_sampled(dtype, w, xq_h, K, mi, ni)
+    assert np.all(np.abs(yh[mi, ni].astype(np.float64) - ref) <= folded_bound(absd, K))
+    assert nmse(yh[mi, ni], ref) <= 1e-6
 
 
 def test_gemm_q8_0_folded_full_size_sampled():

@@ -512,10 +512,13 @@ def test_block_sums_against_brute_force(dtype):
     assert np.all(terms >= np.abs(ref.reshape(-1)) * (1 - 1e-6))
 
 
-@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+@pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0])
 def test_absdot_magnitudes(dtype):
-    """The error-scale helper: sum |a_i*b_i|, sum |a_i| and sum |b_i| over the dequantised weight row a and
-    activation row b, against numpy on the dequantised blocks (whose values the fixtures pin)."""
+    """The error-scale helper: sum |a_i*b_i|, sum |a_i|, sum |b_i| over the dequantised weight row a and
+    activation row b, against numpy on the dequantised blocks (whose values the fixtures pin); and the
+    two-part magnitude sum (|d*sc*c_i| + |dmin*m_i|)*|b_i|: equal to the first sum for Q6_K and Q8_0;
+    for Q4_K/Q5_K at least the first sum and at most it plus 2*sum |dmin*m_i|*|b_i|, where dmin*m_i is
+    read off a copy of the weights with every code 0 (its dequantised values are exactly -dmin*m_i)."""
     g = np.random.default_rng(31 + dtype)
     N, K, M = 3, 512, 2
     w = synth.weights(dtype, N, K, g)
@@ -523,10 +526,24 @@ def test_absdot_magnitudes(dtype):
     xq = oracle.quantize_q8_1(x) if dtype == oracle.Q8_0 else oracle.quantize_q8_k(x)
     a = oracle.dequant(dtype, w).reshape(N, K)
     b = oracle.dequant(oracle.ACT_DTYPE[dtype], xq).reshape(M, K)
-    r = oracle.absdot_sampled(dtype, w, xq, K, [0, 1, 1], [2, 0, 1])
-    for s, (m, n) in enumerate([(0, 2), (1, 0), (1, 1)]):
+    pairs = [(0, 2), (1, 0), (1, 1)]
+    r = oracle.absdot_sampled(dtype, w, xq, K, [p[0] for p in pairs], [p[1] for p in pairs])
+    for s, (m, n) in enumerate(pairs):
         want = [np.abs(a[n] * b[m]).sum(), np.abs(a[n]).sum(), np.abs(b[m]).sum()]
-        assert np.allclose(r[s], want, rtol=1e-12, atol=0)
+        assert np.allclose(r[s, :3], want, rtol=1e-12, atol=0)
+    if dtype in (oracle.Q6_K, oracle.Q8_0):
+        assert np.allclose(r[:, 3], r[:, 0], rtol=1e-12, atol=0)
+    else:
+        bb = {oracle.Q4_K: 144, oracle.Q5_K: 176}[dtype]
+        w0 = w.reshape(N, K // 256, bb).copy()
+        w0[:, :, bb - 128:] = 0                  # every 4-bit code 0
+        if dtype == oracle.Q5_K:
+            w0[:, :, 16:48] = 0                  # and every fifth bit
+        mins = -oracle.dequant(dtype, w0.reshape(N, -1)).reshape(N, K)   # dmin*m_i
+        assert (mins >= 0).all()
+        for s, (m, n) in enumerate(pairs):
+            assert r[s, 3] >= r[s, 0] * (1 - 1e-12)
+            assert r[s, 3] <= (r[s, 0] + 2 * (mins[n] * np.abs(b[m])).sum()) * (1 + 1e-12)
 
 
 @pytest.mark.parametrize("dtype", [oracle.Q4_K, oracle.Q5_K, oracle.Q6_K, oracle.Q8_0])
