@@ -40,11 +40,11 @@ sys.path.insert(0, ROOT)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) per tcgen05 GEMM launch, averaged over the 36 launches of two timed step
-# replays, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum; Q6_K 75.0 MB, Q4_K
-# 51.8 MB per launch).  Valid only for the kernel sources it was taken on: null once their hash differs.
-TC_TRAFFIC = {"bytes_per_launch": 63.42e6,
+# replays, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum; Q6_K 73.6 MB, Q4_K
+# 51.9 MB per launch).  Valid only for the kernel sources it was taken on: null once their hash differs.
+TC_TRAFFIC = {"bytes_per_launch": 62.78e6,
               "sources": ("gemv_quantize_q8_gb300/csrc/kq_tc.cu", "gemv_quantize_q8_gb300/csrc/kq_sm100.cuh"),
-              "sha256": "95b69b379b8ff0872aeae64060ac4adf2e2fc1bc3a5bd4f69b081e8f8bebe4e2"}
+              "sha256": "ea9425bb4ef9bd31fb425953080bb05012e0bd50030a7b165a8233ef399b56c1"}
 
 
 def max_over_ranks(vals, world, device=None):
@@ -66,7 +66,7 @@ def whole_job_tops(ops_per_rank, world, ms):
 
 TC_KERNEL_END = b"// Activation prologue: Q8_K rows"
 # The tcgen05 kernel's share of the prefill step in the committed ncu launch list (same source hash).
-TC_SHARE = {"share": 0.905}
+TC_SHARE = {"share": 0.907}
 
 
 def tc_share():
