@@ -1596,24 +1596,26 @@ static int resident_ctas_dt(kq_dtype wt, int S) {
 }
 
 // Split-K factor: the number of CTAs per output tile (a cluster along z).  Chosen with a small
-// cost model measured on GB300 -- every CTA pays a pipeline fill and drain (~2.5 us) and each
-// super-block costs ~1.3 us (Q4_K) or ~1.75 us (Q6_K); a split adds a cluster reduction (~1 us),
-// and only as many clusters run at once as the device holds (resident_ctas) -- over power-of-two
-// splits that leave at least two super-blocks per CTA.
+// cost model measured on GB300: a persistent CTA (S = 1) pays its pipeline fill and drain (~2.5 us)
+// once and walks its whole tiles at ~1.3 us (Q4_K), ~1.5 us (Q5_K) or ~1.75 us (Q6_K) per
+// super-block; split-K clusters pay the fill in every wave, run their super-blocks ~15% slower
+// (measured on the M = 2048, K = 14336 shapes) and add a cluster reduction (~1 us), and only as many
+// clusters run at once as the device holds (resident_ctas) -- over power-of-two splits that leave at
+// least two super-blocks per CTA.
 static int tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     if (wt == KQ_Q8_0) return 1;  // keeps every output's blocks in one ascending sum (bit-exact)
     const int64_t tiles = ((M + TC_TOK - 1) / TC_TOK) * ((N + TC_ROWS - 1) / TC_ROWS);
     const int nsb = (int)(K / 256);
     const double t_sb = wt == KQ_Q4_K ? 1.3 : wt == KQ_Q5_K ? 1.5 : 1.75, t_fill = 2.5, t_red = 1.0;
     int best = 1;
-    double best_t = 1e30;
-    for (int S = 1; S <= 8; S *= 2) {
+    double best_t = t_fill + (double)((tiles + resident_ctas_dt(wt, 1) - 1) / resident_ctas_dt(wt, 1)) * nsb * t_sb;
+    for (int S = 2; S <= 8; S *= 2) {
         const int per = (nsb + S - 1) / S;
-        if (S > 1 && per < 2) break;
+        if (per < 2) break;
         if ((nsb + per - 1) / per != S) continue;  // S must be exactly realisable
         const int64_t usable = resident_ctas_dt(wt, S);
         const int64_t waves = (tiles * S + usable - 1) / usable;
-        const double t = (double)waves * (t_fill + per * t_sb + (S > 1 ? t_red : 0.0));
+        const double t = (double)waves * (t_fill + per * 1.15 * t_sb + t_red);
         if (t < best_t - 1e-9) { best_t = t; best = S; }
     }
     return best;
