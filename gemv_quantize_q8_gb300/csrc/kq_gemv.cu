@@ -33,7 +33,14 @@ namespace kq {
 
 using namespace sm100;
 
-constexpr int kGemvRows = 32;      // rows per thread block (two native row groups), one per lane
+#ifndef GEMV16_OK
+#define GEMV16_OK 1
+#endif
+
+constexpr int kGemvRows = 32;
+// gemv16_kernel: at most 20 warps (40 chunks, K <= 10240), registers for two blocks per SM -- this
+// call's and the next one's
+constexpr int kGemv16MaxWarps = 20;      // rows per thread block (two native row groups), one per lane
 constexpr int kGemvMaxWarps = 32;
 
 template <int DT>
@@ -342,6 +349,95 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     }
 }
 
+// Long-K GEMV without a cluster: one block per 16-row group over the whole of K.  grid: ceil(N/16);
+// block: 32 * ceil(nchunk/2) threads (at most kGemv16MaxWarps warps).  Warp w stages chunks 2w and 2w+1 of the group (one bulk copy
+// each) and their activation blocks; half-warp h (lane >> 4) then forms the terms of chunk 2w+h, a
+// lane per row (lane & 15), exactly as gemv_kernel does, and one thread per row adds the row's terms
+// in ascending K order.  Every block covers its rows over the whole K, so no partial sums cross
+// blocks and the launch needs no cluster: the next call's blocks start beside it under programmatic
+// dependent launch, and with 16 rows per block the blocks of a 2560-row GEMV cover every SM.
+template <int DT, bool FUSED>
+__global__ void __launch_bounds__(32 * kGemv16MaxWarps, 2) gemv16_kernel(const uint8_t *__restrict__ w,
+                                                                           const float *__restrict__ x,
+                                                                           const uint8_t *__restrict__ xq,
+                                                                           int64_t N, int nchunk,
+                                                                           float *__restrict__ y) {
+    using Tr = GemvTraits<DT>;
+    using WS = GemvWarpSmem<DT, 2>;  // two chunks' codes (one row group each) and two activation blocks
+    constexpr int CB = chunk_bytes(DT);
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t bars[kGemvMaxWarps];
+    __shared__ int abort_flag;
+    const int64_t g = blockIdx.x;  // row group: rows 16g .. 16g+15
+    const int nw = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tstride = nchunk * Tr::terms;
+    float *terms = reinterpret_cast<float *>(smem + (size_t)nw * WS::BYTES);  // [16][nchunk][terms]
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nw; ++i) mbar_init(&bars[i], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    grid_launch_dependents();
+
+    const int c0 = 2 * warp, nc = min(2, nchunk - c0);
+    uint8_t *ws = smem + (size_t)warp * WS::BYTES;
+    // the weights are never written by the kernel before this one: their copies start before the wait
+    if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[warp], nc * CB);
+        for (int h = 0; h < nc; ++h) bulk_load(ws + h * CB, w + (g * nchunk + c0 + h) * (int64_t)CB, CB, &bars[warp]);
+    }
+    grid_dependency_wait();
+    for (int h = 0; h < nc; ++h) {
+        int8_t *q_s = reinterpret_cast<int8_t *>(ws + WS::Q_OFF + h * WS::XB);
+        float *da_s = reinterpret_cast<float *>(ws + WS::D_OFF + h * WS::XB);
+        int16_t *bs_s = reinterpret_cast<int16_t *>(ws + WS::B_OFF + h * WS::XB);
+        const int c = c0 + h;
+        if (FUSED) {
+            if (!Tr::q81) {
+                warp_quantize_q8k_smem(x + (int64_t)c * 256, q_s, da_s, bs_s);
+            } else {
+                warp_quantize_q8_1x4_smem(x + (int64_t)c * 256, q_s, da_s);
+                warp_quantize_q8_1x4_smem(x + (int64_t)c * 256 + 128, q_s + 128, da_s + 4);
+            }
+        } else if (!Tr::q81) {
+            const uint8_t *blk = xq + (int64_t)c * kQ8KBytes;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4);
+            reinterpret_cast<uint2 *>(q_s)[lane] = make_uint2(src[2 * lane], src[2 * lane + 1]);
+            if (lane < 16) bs_s[lane] = reinterpret_cast<const int16_t *>(blk + 260)[lane];
+            if (lane == 0) da_s[0] = *reinterpret_cast<const float *>(blk);
+        } else {
+            const int b = lane >> 2, part = lane & 3;  // 8 blocks x 4 lanes
+            const uint8_t *blk = xq + ((int64_t)c * 8 + b) * kQ81Bytes;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4 + 8 * part);
+            reinterpret_cast<uint2 *>(q_s + 32 * b)[part] = make_uint2(src[0], src[1]);
+            if (part == 0) da_s[b] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+        }
+    }
+    __syncwarp();
+    if (mbar_wait_sleep(&bars[warp], 0, &abort_flag)) {
+        const int h = lane >> 4;
+        if (h < nc)
+            gemv_row_chunk<DT>(ws + h * CB, lane & 15, reinterpret_cast<const int8_t *>(ws + WS::Q_OFF + h * WS::XB),
+                               reinterpret_cast<const float *>(ws + WS::D_OFF + h * WS::XB),
+                               reinterpret_cast<const int16_t *>(ws + WS::B_OFF + h * WS::XB),
+                               terms + (lane & 15) * tstride + (c0 + h) * Tr::terms);
+    } else if (lane == 0) {
+        int no_abort = 0;  // drain this warp's copies (bounded) before the block may exit
+        mbar_wait(&bars[warp], 0, &no_abort, 100000000ull);
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) {  // ordered reduction: one thread per row, ascending K
+        const int64_t n = g * 16 + threadIdx.x;
+        const float *tr = terms + threadIdx.x * tstride;
+        float acc = 0.0f;
+        for (int i = 0; i < tstride; ++i) acc = __fadd_rn(acc, tr[i]);
+        if (n < N) y[n] = abort_flag ? __int_as_float(0x7fc00000) : acc;
+    }
+}
+
 // Number of SMs of the current device (looked up once per device).
 static int gemv_sm_count() {
     static int cache[64] = {0};
@@ -384,6 +480,35 @@ static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq
     if (smem > 220 * 1024) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: K=%lld too large", (long long)K);
     if (ldy == 0) ldy = N;
     if (rblocks > 65535) return fail(KQ_ERR_INVALID_ARG, "kq_gemv: N=%lld too large", (long long)N);
+    if (MC == 1 && S > 1 && GEMV16_OK) {
+        // one column whose K the cluster split would share out: 16-row blocks over the whole K
+        // instead, when they fit (at most 40 chunks, the row group's whole K in shared memory)
+        using WS2 = GemvWarpSmem<DT, 2>;
+        const int nw = (nchunk + 1) / 2;
+        const size_t smem16 = (size_t)nw * WS2::BYTES + (size_t)16 * nchunk * Tr::terms * 4;
+        const int64_t groups = (N + 15) / 16;
+        // only where two calls' blocks fit on an SM together: otherwise the next call cannot start
+        // beside this one and the cluster split, with less post-wait work per warp, is as fast
+        if (nw <= kGemv16MaxWarps && 2 * smem16 <= 220 * 1024 && groups <= 0x7fffffff) {
+            auto k16 = gemv16_kernel<DT, FUSED>;
+            cudaError_t e = cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem16);
+            if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: %s", cudaGetErrorString(e));
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)groups, 1, 1);
+            cfg.blockDim = dim3(32 * nw, 1, 1);
+            cfg.dynamicSmemBytes = smem16;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, k16, w, x, xq, N, nchunk, y);
+            if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: launch failed: %s", cudaGetErrorString(e));
+            count_launch(R_GEMV);
+            return KQ_OK;
+        }
+    }
     auto kern = gemv_kernel<DT, FUSED, MC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: %s", cudaGetErrorString(e));

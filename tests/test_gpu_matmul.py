@@ -43,7 +43,8 @@ def tc_bound(terms: np.ndarray, K: int, splits: int) -> np.ndarray:
 
 
 @pytest.mark.parametrize("dtype", DTS)
-@pytest.mark.parametrize("N,K", [(40, 512), (256, 1024), (100, 4096), (16, 256), (48, 16384)])
+@pytest.mark.parametrize("N,K", [(40, 512), (256, 1024), (100, 4096), (16, 256), (48, 16384), (1000, 9472),
+                                 (72, 9728)])
 @pytest.mark.parametrize("fused", [True, False])
 def test_gemv_small(dtype, N, K, fused):
     g = synth.rng(200 + N + K + dtype)
