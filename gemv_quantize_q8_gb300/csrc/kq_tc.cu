@@ -300,15 +300,17 @@ __device__ __forceinline__ void convert_q5k_kblock(uint4 v0, uint4 v1, const uin
 
 // Q6_K sub-block of one row (16 elements: 4 nibble words whose codes sit in the low nibbles (HI =
 // false) or the high nibbles (HI = true) of each byte, 4 high-bit words whose 2-bit fields for this
-// sub-block sit at bit HS) -> 8 lo columns (sc & 15)*(c-32) and 8 hi columns 16*(sc >> 4)*(c-32).
-// The byte permute with 0x64 bytes builds (0x6400 | c) = 1024 + c directly, so c-32 is one exact
-// subtraction; every product is an integer of at most 11 significant bits.
+// sub-block sit at bit HS) -> 8 lo columns ((sc & 15)/16)*(c-32) and 8 hi columns (sc >> 4)*(c-32), so
+// the two MMAs of a 16-K slice accumulate (sc/16)*sum((c-32)*q): the super-block's integer sum over 16,
+// which the epilogue scales back with 16*d (exact: a power of two).  The byte permute with 0x64 bytes
+// builds (0x6400 | c) = 1024 + c directly and one fused multiply-add per pair gives each product
+// exactly (at most 9 significant bits, the lo ones with 4 fractional bits).
 template <bool HI, int HS>
 __device__ __forceinline__ void convert_q6k_sub(const uint32_t (&nib)[4], const uint32_t (&hb)[4], int sc,
                                                 uint32_t (&lo)[8], uint32_t (&hi)[8]) {
-    const int l = sc & 15, h16 = 16 * (sc >> 4);
-    const __half2 ml = __float2half2_rn((float)l), nl = __float2half2_rn(-1056.0f * l);
-    const __half2 mh = __float2half2_rn((float)h16), c1056 = __float2half2_rn(1056.0f);
+    const int l = sc & 15, hs = sc >> 4;
+    const __half2 ml = __float2half2_rn(0.0625f * l), nl = __float2half2_rn(-66.0f * l);
+    const __half2 mh = __float2half2_rn((float)hs), nh = __float2half2_rn(-1056.0f * hs);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         // high bits of the sub-block to bits 4-5 of every byte, the code's low 4 bits to bits 0-3
@@ -318,8 +320,8 @@ __device__ __forceinline__ void convert_q6k_sub(const uint32_t (&nib)[4], const 
         const __half2 x23 = u2h(__byte_perm(c, 0x64646464u, 0x4342));
         lo[2 * i] = h2u(__hfma2(x01, ml, nl));
         lo[2 * i + 1] = h2u(__hfma2(x23, ml, nl));
-        hi[2 * i] = h2u(__hmul2(__hsub2(x01, c1056), mh));
-        hi[2 * i + 1] = h2u(__hmul2(__hsub2(x23, c1056), mh));
+        hi[2 * i] = h2u(__hfma2(x01, mh, nh));
+        hi[2 * i + 1] = h2u(__hfma2(x23, mh, nh));
     }
 }
 
@@ -895,9 +897,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (C::EXT)
                     dpair = make_float2(half_bits_to_float((uint16_t)(hv.x & 0xffff)),
                                         -half_bits_to_float((uint16_t)(hv.x >> 16)));
-                else if (rvalid)
+                else if (rvalid)  // Q6_K: 16*d, as the accumulator holds the integer sum over 16
                     dpair = make_float2(
-                        half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + r16 * 2)), 0.0f);
+                        16.0f * half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + r16 * 2)), 0.0f);
                 reinterpret_cast<float2 *>(sH + h * TC_ROWS * 8)[row] = dpair;
                 mbar_arrive(&h_full[h]);
             } else if (C::EXT) {
@@ -1090,7 +1092,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tmem_wait_ld();
                 if (DBG) {
                     const TcTile T = tile_of(tile_i);
-                    dbg_put(T, (int)col, gsb, 0, s1);
+                    if (!C::EXT) {  // Q6_K: the accumulator holds the integer sum over 16 (exact)
+                        float s16[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) s16[i] = 16.0f * s1[i];
+                        dbg_put(T, (int)col, gsb, 0, s16);
+                    } else {
+                        dbg_put(T, (int)col, gsb, 0, s1);
+                    }
                     if (!C::EXT) {
                         const float zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                         dbg_put(T, (int)col, gsb, 1, zero);
