@@ -40,11 +40,11 @@ sys.path.insert(0, ROOT)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) per tcgen05 GEMM launch, averaged over the 36 launches of two timed step
-# replays, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum; Q6_K 73.6 MB, Q4_K
+# replays, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum; Q6_K 78.5 MB, Q4_K
 # 51.9 MB per launch).  Valid only for the kernel sources it was taken on: null once their hash differs.
-TC_TRAFFIC = {"bytes_per_launch": 62.78e6,
+TC_TRAFFIC = {"bytes_per_launch": 65.17e6,
               "sources": ("gemv_quantize_q8_gb300/csrc/kq_tc.cu", "gemv_quantize_q8_gb300/csrc/kq_sm100.cuh"),
-              "sha256": "ea9425bb4ef9bd31fb425953080bb05012e0bd50030a7b165a8233ef399b56c1"}
+              "sha256": "30b34075a76a5e7c1c40ac6cff9975c6a4da83eafc78d7f8757e3086d23ef2e7"}
 
 
 def max_over_ranks(vals, world, device=None):
@@ -66,7 +66,7 @@ def whole_job_tops(ops_per_rank, world, ms):
 
 TC_KERNEL_END = b"// Activation prologue: Q8_K rows"
 # The tcgen05 kernel's share of the prefill step in the committed ncu launch list (same source hash).
-TC_SHARE = {"share": 0.907}
+TC_SHARE = {"share": 0.904}
 
 
 def tc_share():
