@@ -162,7 +162,7 @@ KQ_API kq_status kq_swiglu_quantize_q8k(const float *g, const float *u, int64_t 
  * kernel issued just before it on `stream` is still running; it waits for that kernel before it
  * reads x/xq or writes y.  So w must already be in place when that earlier kernel runs: stage the
  * weights once (kq_repack_weights, then any synchronisation) as the keep-quant provider does.
- * w: native [N][K] of dtype wt (Q4_K or Q6_K: activation Q8_K; Q8_0: activation Q8_1).
+ * w: native [N][K] of dtype wt (Q4_K, Q5_K or Q6_K: activation Q8_K; Q8_0: activation Q8_1).
  * Exactly one of x (fp32 [K]: quantised inside the kernel, no separate launch) and xq (pre-quantised
  * activation row, K/256 Q8_K or K/32 Q8_1 blocks) must be non-NULL.  y: fp32 [N].
  * y[n] = sum over blocks of the scaled integer block dots (the kq_gemm formula); the reduction
