@@ -56,6 +56,13 @@ struct GemvTraits<KQ_Q8_0> { static constexpr int terms = 8; static constexpr bo
 
 __device__ __forceinline__ int sext8(uint32_t w, int i) { return (int)(int8_t)((w >> (8 * i)) & 0xff); }
 
+// Dot product of four unsigned bytes of a with four signed bytes of b, plus c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Per-warp shared region: the chunk's codes for the block's two row groups, then the chunk's
 // activation for each of the MC activation columns (320 bytes each: q[256], d, bsums).
 template <int DT, int MC>
@@ -104,26 +111,35 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int seg = i >> 2;  // elements 64kb+16seg+.. (low nibbles) / 64kb+32+16seg+.. (high)
-                uint32_t lo = w[i] & 0x0f0f0f0fu, hi = (w[i] >> 4) & 0x0f0f0f0fu;
-                if (DT == KQ_Q5_K) {  // fifth bit: bit 2kb of byte l (low nibbles), bit 2kb+1 (high)
-                    lo |= ((q5h[i] >> (2 * kb)) & 0x01010101u) << 4;
-                    hi |= ((q5h[i] >> (2 * kb + 1)) & 0x01010101u) << 4;
+                const uint32_t lo4 = w[i] & 0x0f0f0f0fu;
+                if (DT == KQ_Q4_K) {
+                    // high nibbles left in place: the bytes are 16*c, so the dot is 16 times the
+                    // sub-block's (divided out, exactly, below) and no shift is needed per word
+                    plo[seg] = dp4a((int)lo4, ql[i], plo[seg]);
+                    phi[seg] = dp4a_us(w[i] & 0xf0f0f0f0u, qh[i], phi[seg]);
+                } else if (DT == KQ_Q5_K) {  // fifth bit: bit 2kb of byte l (low nibbles), bit 2kb+1 (high)
+                    const uint32_t lo = lo4 | (((q5h[i] >> (2 * kb)) & 0x01010101u) << 4);
+                    const uint32_t hi = ((w[i] >> 4) & 0x0f0f0f0fu) | (((q5h[i] >> (2 * kb + 1)) & 0x01010101u) << 4);
+                    plo[seg] = dp4a((int)lo, ql[i], plo[seg]);
+                    phi[seg] = dp4a((int)hi, qh[i], phi[seg]);
+                } else {
+                    // Q6_K: the unsigned 6-bit codes c; the -32 offset comes off once per sub-block
+                    // below (sum (c-32)*q = sum c*q - 32*bsum, the activation's bsum of those 16)
+                    const uint32_t lo = lo4 | (((hb[i & 3] >> (2 * seg)) & 0x03030303u) << 4);
+                    const uint32_t hi = ((w[i] >> 4) & 0x0f0f0f0fu) | (((hb[i & 3] >> (4 + 2 * seg)) & 0x03030303u) << 4);
+                    plo[seg] = dp4a((int)lo, ql[i], plo[seg]);
+                    phi[seg] = dp4a((int)hi, qh[i], phi[seg]);
                 }
-                if (DT == KQ_Q6_K) {
-                    lo = __vsub4(lo | (((hb[i & 3] >> (2 * seg)) & 0x03030303u) << 4), 0x20202020u);
-                    hi = __vsub4(hi | (((hb[i & 3] >> (4 + 2 * seg)) & 0x03030303u) << 4), 0x20202020u);
-                }
-                plo[seg] = dp4a((int)lo, ql[i], plo[seg]);
-                phi[seg] = dp4a((int)hi, qh[i], phi[seg]);
             }
             if (K4) {
-                P[2 * kb] = plo[0] + plo[1];      // sub-block 2kb   (elements 64kb .. 64kb+31)
-                P[2 * kb + 1] = phi[0] + phi[1];  // sub-block 2kb+1 (elements 64kb+32 .. 64kb+63)
+                P[2 * kb] = plo[0] + plo[1];  // sub-block 2kb   (elements 64kb .. 64kb+31)
+                // sub-block 2kb+1 (elements 64kb+32 .. 64kb+63); Q4_K's sums are of 16*c, a multiple of 16
+                P[2 * kb + 1] = DT == KQ_Q4_K ? (phi[0] + phi[1]) >> 4 : phi[0] + phi[1];
             } else {
-                P[4 * kb] = plo[0];      // sub-block 4kb   (elements 64kb .. +15)
-                P[4 * kb + 1] = plo[1];  // sub-block 4kb+1 (64kb+16 .. +31)
-                P[4 * kb + 2] = phi[0];  // sub-block 4kb+2 (64kb+32 .. +47)
-                P[4 * kb + 3] = phi[1];  // sub-block 4kb+3 (64kb+48 .. +63)
+                P[4 * kb] = plo[0] - 32 * (int)bs[4 * kb];          // sub-block 4kb   (elements 64kb .. +15)
+                P[4 * kb + 1] = plo[1] - 32 * (int)bs[4 * kb + 1];  // sub-block 4kb+1 (64kb+16 .. +31)
+                P[4 * kb + 2] = phi[0] - 32 * (int)bs[4 * kb + 2];  // sub-block 4kb+2 (64kb+32 .. +47)
+                P[4 * kb + 3] = phi[1] - 32 * (int)bs[4 * kb + 3];  // sub-block 4kb+3 (64kb+48 .. +63)
             }
         }
         if (K4) {
