@@ -56,6 +56,24 @@ struct GemvTraits<KQ_Q8_0> { static constexpr int terms = 8; static constexpr bo
 
 __device__ __forceinline__ int sext8(uint32_t w, int i) { return (int)(int8_t)((w >> (8 * i)) & 0xff); }
 
+// Two-way dot products of the two signed 16-bit halves of a with two bytes of b (bytes 0-1: lo, 2-3: hi;
+// signed or unsigned bytes), plus c.
+__device__ __forceinline__ int dp2a_lo_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_lo_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Dot product of four unsigned bytes of a with four signed bytes of b, plus c.
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     int d;
@@ -136,29 +154,28 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
                 // sub-block 2kb+1 (elements 64kb+32 .. 64kb+63); Q4_K's sums are of 16*c, a multiple of 16
                 P[2 * kb + 1] = DT == KQ_Q4_K ? (phi[0] + phi[1]) >> 4 : phi[0] + phi[1];
             } else {
-                P[4 * kb] = plo[0] - 32 * (int)bs[4 * kb];          // sub-block 4kb   (elements 64kb .. +15)
-                P[4 * kb + 1] = plo[1] - 32 * (int)bs[4 * kb + 1];  // sub-block 4kb+1 (64kb+16 .. +31)
-                P[4 * kb + 2] = phi[0] - 32 * (int)bs[4 * kb + 2];  // sub-block 4kb+2 (64kb+32 .. +47)
-                P[4 * kb + 3] = phi[1] - 32 * (int)bs[4 * kb + 3];  // sub-block 4kb+3 (64kb+48 .. +63)
+                P[4 * kb] = plo[0];      // sub-block 4kb   (elements 64kb .. +15), sum c*q
+                P[4 * kb + 1] = plo[1];  // sub-block 4kb+1 (64kb+16 .. +31)
+                P[4 * kb + 2] = phi[0];  // sub-block 4kb+2 (64kb+32 .. +47)
+                P[4 * kb + 3] = phi[1];  // sub-block 4kb+3 (64kb+48 .. +63)
             }
         }
         if (K4) {
             const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + 2048 + r * 16);
-            uint8_t s12[12];
-            const uint32_t hw[3] = {hv.y, hv.z, hv.w};
-#pragma unroll
-            for (int i = 0; i < 12; ++i) s12[i] = (hw[i / 4] >> (8 * (i % 4))) & 0xff;
+            // the eight 6-bit scales and mins, four per word, from the 12 packed bytes (GGUF's packing:
+            // sub-blocks 0-3 in the low 6 bits of bytes 0-3 / 4-7; 4-7 from the nibbles of bytes 8-11
+            // and the top two bits of bytes 0-3 / 4-7)
+            const uint32_t scw[2] = {hv.y & 0x3f3f3f3fu, (hv.w & 0x0f0f0f0fu) | ((hv.y >> 2) & 0x30303030u)};
+            const uint32_t mw[2] = {hv.z & 0x3f3f3f3fu, ((hv.w >> 4) & 0x0f0f0f0fu) | ((hv.z >> 2) & 0x30303030u)};
             const uint4 b0 = *reinterpret_cast<const uint4 *>(bs);
             const uint4 b1 = *reinterpret_cast<const uint4 *>(bs + 8);
             const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
             int sumi = 0, summ = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                int sc, mn;
-                q4k_scale_min(s12, j, sc, mn);
-                sumi += sc * P[j];
-                // bsums 2j and 2j+1 are the two int16 halves of word j
-                summ += mn * ((int)(int16_t)(bw[j] & 0xffff) + (int)(int16_t)(bw[j] >> 16));
+                sumi += (int)((scw[j >> 2] >> (8 * (j & 3))) & 0xff) * P[j];
+                // m_j*(bs_2j + bs_2j+1): the two int16 halves of bsum word j against m_j in both bytes
+                summ = dp2a_lo_su(bw[j], __byte_perm(mw[j >> 2], 0u, 0x4400u | ((j & 3) * 0x11u)), summ);
             }
             const float dw = half_bits_to_float((uint16_t)(hv.x & 0xffff));
             const float dmin = half_bits_to_float((uint16_t)(hv.x >> 16));
@@ -171,9 +188,20 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
         } else {
             const uint4 sv = *reinterpret_cast<const uint4 *>(chunk + 3072 + r * 16);
             const uint32_t sw4[4] = {sv.x, sv.y, sv.z, sv.w};
-            int sumi = 0;
+            const uint4 b0 = *reinterpret_cast<const uint4 *>(bs);
+            const uint4 b1 = *reinterpret_cast<const uint4 *>(bs + 8);
+            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            // sum_j sc_j*(P_j - 32*bs_j): the codes' dots, then the offset through the bsums (sc_j with
+            // bsum j: two per word of each, two-way dot products)
+            int sumi = 0, sumb = 0;
 #pragma unroll
             for (int j = 0; j < 16; ++j) sumi += sext8(sw4[j / 4], j % 4) * P[j];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                sumb = dp2a_lo_ss(bw[2 * k], sw4[k], sumb);
+                sumb = dp2a_hi_ss(bw[2 * k + 1], sw4[k], sumb);
+            }
+            sumi -= 32 * sumb;
             const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + r * 2));
             const float t1 = __fmul_rn(da[0], dw);
             term[0] = __fmul_rn(t1, (float)sumi);
