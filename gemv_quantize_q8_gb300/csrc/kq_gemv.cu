@@ -228,6 +228,125 @@ __device__ __forceinline__ void gemv_row_chunk(const uint8_t *__restrict__ chunk
     }
 }
 
+// One lane = one row, M <= MC activation columns (Q4_K, Q5_K, Q6_K): the terms of gemv_row_chunk for
+// every column, each weight word unpacked once and dotted against all columns.  A column's integer sum
+// sum_j sc_j*P_j is gathered sub-block by sub-block (exact integers in any order), so every term is
+// formed exactly as gemv_row_chunk forms it.  Column m's activation block sits at q + m*xb (int8
+// q[256], then f32 d at +256, int16 bsums at +288); term m goes to term[m * tstep].
+template <int DT, int MC>
+__device__ __forceinline__ void gemv_row_chunk_mc(const uint8_t *__restrict__ chunk, int r, const uint8_t *__restrict__ q,
+                                                  int xb, int M, float *__restrict__ term, int tstep) {
+    constexpr bool K4 = DT == KQ_Q4_K || DT == KQ_Q5_K;
+    const uint4 hv = *reinterpret_cast<const uint4 *>(chunk + (K4 ? 2048 : 3072) + r * 16);
+    // per-sub-block scales: Q4_K/Q5_K four 6-bit scales per word, Q6_K four int8 scales per word
+    uint32_t scw[4], mw[2];
+    if (K4) {
+        scw[0] = hv.y & 0x3f3f3f3fu;
+        scw[1] = (hv.w & 0x0f0f0f0fu) | ((hv.y >> 2) & 0x30303030u);
+        mw[0] = hv.z & 0x3f3f3f3fu;
+        mw[1] = ((hv.w >> 4) & 0x0f0f0f0fu) | ((hv.z >> 2) & 0x30303030u);
+        scw[2] = scw[3] = 0u;
+    } else {
+        scw[0] = hv.x; scw[1] = hv.y; scw[2] = hv.z; scw[3] = hv.w;
+        mw[0] = mw[1] = 0u;
+    }
+    uint32_t q5h[8];
+    if (DT == KQ_Q5_K) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(chunk + 2304 + r * 32);
+        const uint4 b = *reinterpret_cast<const uint4 *>(chunk + 2304 + r * 32 + 16);
+        q5h[0] = a.x; q5h[1] = a.y; q5h[2] = a.z; q5h[3] = a.w; q5h[4] = b.x; q5h[5] = b.y; q5h[6] = b.z; q5h[7] = b.w;
+    }
+    int sumi[MC];
+#pragma unroll
+    for (int m = 0; m < MC; ++m) sumi[m] = 0;
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(chunk + kb * 512 + r * 32);
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(chunk + kb * 512 + r * 32 + 16);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t hb[4] = {0u, 0u, 0u, 0u};
+        if (DT == KQ_Q6_K) {
+            const uint4 h = *reinterpret_cast<const uint4 *>(chunk + 2048 + kb * 256 + r * 16);
+            hb[0] = h.x; hb[1] = h.y; hb[2] = h.z; hb[3] = h.w;
+        }
+        // the kblock's words unpacked once: lo = codes of the first 32 elements, hi = of the last 32
+        // (Q4_K: 16*c left in place)
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int seg = i >> 2;
+            lo[i] = w[i] & 0x0f0f0f0fu;
+            if (DT == KQ_Q4_K) {
+                hi[i] = w[i] & 0xf0f0f0f0u;
+            } else if (DT == KQ_Q5_K) {
+                lo[i] |= ((q5h[i] >> (2 * kb)) & 0x01010101u) << 4;
+                hi[i] = ((w[i] >> 4) & 0x0f0f0f0fu) | (((q5h[i] >> (2 * kb + 1)) & 0x01010101u) << 4);
+            } else {
+                lo[i] |= ((hb[i & 3] >> (2 * seg)) & 0x03030303u) << 4;
+                hi[i] = ((w[i] >> 4) & 0x0f0f0f0fu) | (((hb[i & 3] >> (4 + 2 * seg)) & 0x03030303u) << 4);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MC; ++m) {
+            if (m >= M) break;
+            const int8_t *qm = reinterpret_cast<const int8_t *>(q + m * xb) + 64 * kb;
+            const int4 qa0 = *reinterpret_cast<const int4 *>(qm);
+            const int4 qa1 = *reinterpret_cast<const int4 *>(qm + 16);
+            const int4 qb0 = *reinterpret_cast<const int4 *>(qm + 32);
+            const int4 qb1 = *reinterpret_cast<const int4 *>(qm + 48);
+            const int ql[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+            const int qh[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+            int plo[2] = {0, 0}, phi[2] = {0, 0};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                plo[i >> 2] = dp4a((int)lo[i], ql[i], plo[i >> 2]);
+                phi[i >> 2] = DT == KQ_Q4_K ? dp4a_us(hi[i], qh[i], phi[i >> 2]) : dp4a((int)hi[i], qh[i], phi[i >> 2]);
+            }
+            if (K4) {  // sub-blocks 2kb (lo) and 2kb+1 (hi)
+                const int s_lo = (int)((scw[kb >> 1] >> (16 * (kb & 1))) & 0xff);
+                const int s_hi = (int)((scw[kb >> 1] >> (16 * (kb & 1) + 8)) & 0xff);
+                const int ph = DT == KQ_Q4_K ? (phi[0] + phi[1]) >> 4 : phi[0] + phi[1];
+                sumi[m] += s_lo * (plo[0] + plo[1]) + s_hi * ph;
+            } else {  // sub-blocks 4kb .. 4kb+3, sum c*q (the -32 offset below)
+                sumi[m] += sext8(scw[kb], 0) * plo[0] + sext8(scw[kb], 1) * plo[1] + sext8(scw[kb], 2) * phi[0] +
+                           sext8(scw[kb], 3) * phi[1];
+            }
+        }
+    }
+    const float dw = K4 ? half_bits_to_float((uint16_t)(hv.x & 0xffff))
+                        : half_bits_to_float(*reinterpret_cast<const uint16_t *>(chunk + 3328 + r * 2));
+    const float dmin = K4 ? half_bits_to_float((uint16_t)(hv.x >> 16)) : 0.0f;
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+        if (m >= M) break;
+        const uint8_t *xm = q + m * xb;
+        const uint4 b0 = *reinterpret_cast<const uint4 *>(xm + 288);
+        const uint4 b1 = *reinterpret_cast<const uint4 *>(xm + 304);
+        const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const float a = *reinterpret_cast<const float *>(xm + 256);
+        if (K4) {
+            int summ = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                summ = dp2a_lo_su(bw[j], __byte_perm(mw[j >> 2], 0u, 0x4400u | ((j & 3) * 0x11u)), summ);
+            const float t1 = __fmul_rn(a, dw);
+            const float t2 = __fmul_rn(t1, (float)sumi[m]);
+            const float t3 = __fmul_rn(a, dmin);
+            const float t4 = __fmul_rn(t3, (float)summ);
+            term[m * tstep] = __fsub_rn(t2, t4);
+        } else {
+            int sumb = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                sumb = dp2a_lo_ss(bw[2 * k], scw[k], sumb);
+                sumb = dp2a_hi_ss(bw[2 * k + 1], scw[k], sumb);
+            }
+            const float t1 = __fmul_rn(a, dw);
+            term[m * tstep] = __fmul_rn(t1, (float)(sumi[m] - 32 * sumb));
+        }
+    }
+}
+
 // grid: (S, ceil(N/32)); cluster (S, 1, 1) when S > 1; block: 32 * cpr threads.  Warp w of cluster
 // rank k owns chunk k*cpr + w for all 32 rows of the block (lane = row): it bulk-copies that chunk's
 // codes for the block's two row groups into its own shared region, quantises (or copies) the
@@ -334,12 +453,17 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
         __syncwarp();
         if (mbar_wait_sleep(&bars[warp], 0, &abort_flag)) {
             const int gi = lane >> 4;
-            if (gi < ngroups)
-                for (int m = 0; m < (MC > 1 ? M : 1); ++m)
-                    gemv_row_chunk<DT>(ws + gi * CB, lane & 15, q_s + m * WS::XB,
-                                       reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(da_s) + m * WS::XB),
-                                       reinterpret_cast<const int16_t *>(reinterpret_cast<const uint8_t *>(bs_s) + m * WS::XB),
-                                       terms + lane * tstride + (m * cpr + warp) * Tr::terms);
+            if (gi < ngroups) {
+                if (MC > 1 && DT != KQ_Q8_0)  // several columns: each weight word unpacked once for all
+                    gemv_row_chunk_mc<DT, MC>(ws + gi * CB, lane & 15, reinterpret_cast<const uint8_t *>(q_s), WS::XB, M,
+                                              terms + lane * tstride + warp * Tr::terms, cpr * Tr::terms);
+                else
+                    for (int m = 0; m < (MC > 1 ? M : 1); ++m)
+                        gemv_row_chunk<DT>(ws + gi * CB, lane & 15, q_s + m * WS::XB,
+                                           reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(da_s) + m * WS::XB),
+                                           reinterpret_cast<const int16_t *>(reinterpret_cast<const uint8_t *>(bs_s) + m * WS::XB),
+                                           terms + lane * tstride + (m * cpr + warp) * Tr::terms);
+            }
         } else if (lane == 0) {
             int no_abort = 0;  // drain this warp's copies (bounded) before the block may exit
             mbar_wait(&bars[warp], 0, &no_abort, 100000000ull);
