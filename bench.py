@@ -241,27 +241,36 @@ def run_prefill(args, device, rank, world):
     nc = len(cases)
     ev_in, ev_q, ev_c, ev_out = ([torch.cuda.Event() for _ in range(nc)] for _ in range(4))
 
+    # The GEMMs of the step are independent, so the end-to-end step may take them in any order: copies
+    # in and out share the host link, and Johnson's rule for a two-stage flow shop (in-copy, out-copy)
+    # orders them so the link stays busy both ways: GEMMs whose input is smaller than their output
+    # first, by growing input, then the rest by shrinking output.
+    first = sorted((i for i, (M, _, N, K) in enumerate(cases) if K < N), key=lambda i: cases[i][0] * cases[i][3])
+    rest = sorted((i for i, (M, _, N, K) in enumerate(cases) if K >= N), key=lambda i: -cases[i][0] * cases[i][2])
+    e2e_order = first + rest
+
     def step_e2e():
         cs = torch.cuda.current_stream()
         s_in.wait_stream(cs)
         s_out.wait_stream(cs)
-        for i, (M, dt, N, K) in enumerate(cases):
-            b = i % NB
+        for j, i in enumerate(e2e_order):
+            M, dt, N, K = cases[i]
+            b = j % NB
             with torch.cuda.stream(s_in):
-                if i >= NB:
-                    s_in.wait_event(ev_q[i - NB])                 # buffer b no longer read
+                if j >= NB:
+                    s_in.wait_event(ev_q[j - NB])                 # buffer b no longer read
                 xbuf[b][:M * K].copy_(xh[i], non_blocking=True)   # host -> device, pinned
-                ev_in[i].record(s_in)
-            cs.wait_event(ev_in[i])
-            if i >= NB:
-                cs.wait_event(ev_out[i - NB])                     # output buffer b copied out
+                ev_in[j].record(s_in)
+            cs.wait_event(ev_in[j])
+            if j >= NB:
+                cs.wait_event(ev_out[j - NB])                     # output buffer b copied out
             kq.kq_gemm_f32(dt, weights[(dt, N, K)], xbuf[b], K, M, N, K, ybuf[b], N, wsf, wsf_need)
-            ev_q[i].record(cs)
-            ev_c[i].record(cs)
+            ev_q[j].record(cs)
+            ev_c[j].record(cs)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_c[i])
+                s_out.wait_event(ev_c[j])
                 yh[i].copy_(ybuf[b][:M * N], non_blocking=True)   # device -> host, pinned
-                ev_out[i].record(s_out)
+                ev_out[j].record(s_out)
         cs.wait_stream(s_in)
         cs.wait_stream(s_out)
 
