@@ -189,6 +189,10 @@ struct TcParams {
     // tiles.  persistent: CTA b runs tiles b, b + gridDim.x, ...; otherwise CTA (x, y) runs tile
     // y*n_tiles + x alone (the split-K launch).
     int persistent, n_tiles, m_tiles;
+    // Tile range of this launch (plain tiles): units [unit_base, unit_limit).  A dense GEMM whose last
+    // wave would leave most SMs idle runs its whole waves in a persistent launch and the leftover tiles
+    // in a second, split-K launch.
+    int unit_base, unit_limit;
     // Fused SwiGLU -> Q8_K (swq != 0; routed gate/up weights: N = 2F rows per expert, gate rows [0, F),
     // up rows [F, 2F)).  The scheduled unit is four tiles of one token tile: gate rows 256b..256b+255
     // as two 128-row tiles, then the up rows of the same columns.  The epilogue parks the gate tiles
@@ -408,9 +412,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int m_tiles = P.grouped ? *P.tile_count : P.m_tiles;
     const int ntiles = P.n_tiles * m_tiles;
     // scheduled units: single tiles, or (fused SwiGLU) runs of four consecutive tiles
-    const int nunits = SWQ ? ntiles >> 2 : ntiles;
-    const int unit0 = P.persistent ? (int)blockIdx.x : (int)(blockIdx.y * P.n_tiles + blockIdx.x);
-    const int ustride = P.persistent ? (int)gridDim.x : nunits;
+    const int nunits = min(SWQ ? ntiles >> 2 : ntiles, P.unit_limit);
+    const int unit0 = P.unit_base + (P.persistent ? (int)blockIdx.x : (int)(blockIdx.y * P.n_tiles + blockIdx.x));
+    const int ustride = P.persistent ? (int)gridDim.x : nunits - P.unit_base;
     if (unit0 >= nunits) return;  // no tile for this CTA: it leaves before any setup
     // One step = one (tile, super-block); every role walks steps 0 .. nsteps-1 in the same order, so
     // the rings and accumulators run on across tile boundaries without draining.
@@ -1630,8 +1634,38 @@ static int tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
     return best;
 }
 
+// The split tail: a persistent launch whose last wave would hold R < one wave of tiles runs its whole
+// waves persistent and the R leftover tiles as a second launch of split-K clusters (S' CTAs per tile,
+// all in one wave of clusters), when the cost model (the same figures, plus ~2 us for the second
+// launch) says it saves at least 3%.  tail_split = 1: no tail.
+struct TcTail {
+    int64_t tiles;
+    int split;
+};
+
+static TcTail tc_tail(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
+    TcTail tl{0, 1};
+    if (wt == KQ_Q8_0 || tc_splits(wt, M, N, K) != 1) return tl;
+    const int64_t tiles = ((M + TC_TOK - 1) / TC_TOK) * ((N + TC_ROWS - 1) / TC_ROWS);
+    const int nsb = (int)(K / 256);
+    const double t_sb = wt == KQ_Q4_K ? 1.3 : wt == KQ_Q5_K ? 1.5 : 1.75, t_fill = 2.5, t_red = 1.0, t_launch = 2.0;
+    const int64_t G = resident_ctas_dt(wt, 1), W = tiles / G, R = tiles - W * G;
+    if (W == 0 || R == 0) return tl;
+    double best = t_fill + (double)(W + 1) * nsb * t_sb;
+    const double keep = 0.97 * best;
+    for (int S = 2; S <= 4; S *= 2) {
+        const int per = (nsb + S - 1) / S;
+        if (per < 2) break;
+        if ((nsb + per - 1) / per != S || R * S > resident_ctas_dt(wt, S)) continue;
+        const double t = t_fill + (double)W * nsb * t_sb + (t_fill + per * 1.15 * t_sb + t_red) + t_launch;
+        if (t < keep && t < best - 1e-9) { best = t; tl = TcTail{R, S}; }
+    }
+    return tl;
+}
+
 int tc_split_factor(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
-    return tc_eligible(wt, M, N, K) ? tc_splits(wt, M, N, K) : 0;
+    if (!tc_eligible(wt, M, N, K)) return 0;
+    return std::max(tc_splits(wt, M, N, K), tc_tail(wt, M, N, K).split);
 }
 
 size_t tc_workspace_bytes(kq_dtype wt, int64_t M, int64_t N, int64_t K) {
@@ -1671,6 +1705,8 @@ struct TcLaunch {
     uint8_t *hq;          // non-NULL: fused SwiGLU -> Q8_K output (grouped gate/up only), y unused
     float *scr;           // its scratch: tc_swq_scratch_bytes()
     const TcDebug *dbg;   // NULL, or the debug read-out / wait-limit hooks
+    int64_t tail_tiles;   // > 0 (dense, nsplit = 1): the last tail_tiles tiles run as a split-K launch
+    int tail_split;       // of tail_split CTAs per tile
 };
 
 template <int DT>
@@ -1736,24 +1772,42 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
                       : dbg_sums ? tc_gemm_kernel<DT, false, true> : tc_gemm_kernel<DT, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm: %s", cudaGetErrorString(e));
-    cudaLaunchConfig_t cfg = {};
-    if (S > 1)
-        cfg.gridDim = dim3((unsigned)p.n_tiles, (unsigned)a.m_tiles, (unsigned)S);
-    else
-        cfg.gridDim = dim3((unsigned)std::min<int64_t>(units, sm_count()), 1, 1);  // one CTA per SM, units strided
-    cfg.blockDim = dim3(TC_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Lay::ALLOC;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = (unsigned)S;
-    cfg.attrs = attr;
-    cfg.numAttrs = S > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmE, p);
-    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemm (tensor core): launch failed: %s", cudaGetErrorString(e));
-    return KQ_OK;
+    const int64_t R = a.tail_tiles;  // > 0: the last R tiles go to a second, split-K launch
+    if (R && (S != 1 || a.grouped || p.swq || R >= tiles || a.tail_split < 2))
+        return fail(KQ_ERR_INVALID_ARG, "kq_gemm (tensor core): invalid split tail");
+    auto launch = [&](TcParams q, int split, dim3 grid) -> kq_status {
+        q.nsplit = split;
+        q.sb_per_split = (int)((nsb + split - 1) / split);
+        q.persistent = split > 1 ? 0 : 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(TC_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Lay::ALLOC;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)split;
+        cfg.attrs = attr;
+        cfg.numAttrs = split > 1 ? 1 : 0;
+        cudaError_t le = cudaLaunchKernelEx(&cfg, kern, tmA, tmE, q);
+        if (le != cudaSuccess)
+            return fail(KQ_ERR_CUDA, "kq_gemm (tensor core): launch failed: %s", cudaGetErrorString(le));
+        return KQ_OK;
+    };
+    p.unit_base = 0;
+    p.unit_limit = 0x7fffffff;
+    if (S > 1) return launch(p, S, dim3((unsigned)p.n_tiles, (unsigned)a.m_tiles, (unsigned)S));
+    if (!R) return launch(p, 1, dim3((unsigned)std::min<int64_t>(units, sm_count()), 1, 1));  // one CTA per SM
+    // whole waves persistent, then the R leftover tiles as split-K clusters (one tile per cluster)
+    TcParams q = p;
+    q.unit_limit = (int)(tiles - R);
+    kq_status ks = launch(q, 1, dim3((unsigned)std::min<int64_t>(tiles - R, sm_count()), 1, 1));
+    if (ks != KQ_OK) return ks;
+    q.unit_base = (int)(tiles - R);
+    q.unit_limit = (int)tiles;
+    return launch(q, a.tail_split, dim3((unsigned)R, 1, (unsigned)a.tail_split));
 }
 
 static kq_status launch_tc_dt(kq_dtype wt, const TcLaunch &a, cudaStream_t st, bool fold = false, int tok = TC_TOK) {
@@ -1840,6 +1894,11 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
     // the 256-token folded tiles are never split (their epilogue writes y); the 128-token ones split as
     // the exact kernels do, with the Q4_K cost model (their steps cost alike)
     a.nsplit = !fold ? tc_splits(wt, M, N, K) : tok == TC_TOK ? tc_splits(KQ_Q4_K, M, N, K) : 1;
+    if (!fold) {
+        const TcTail tl = tc_tail(wt, M, N, K);
+        a.tail_tiles = tl.tiles;
+        a.tail_split = tl.split;
+    }
     a.err = reinterpret_cast<unsigned long long *>(workspace + L.off_flag);
     a.dbg = dbg;
     if (fold && dbg && dbg->sums) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_ex: no integer sums with folded scales");

@@ -322,8 +322,10 @@ KQ_API kq_status kq_debug_partials(kq_dtype wt, const void *w, const void *xq, i
                             int32_t *partials, kq_stream_t stream);
 
 /* Debug: the split-K factor (CTAs of a thread-block cluster per 128 x 128 output tile, 1 = no split)
- * that kq_gemm's tensor-core path takes for this shape on the current device, or 0 when the shape does
- * not take the tensor-core path.  Host only; launches nothing. */
+ * that kq_gemm's tensor-core path takes for this shape on the current device -- the most CTAs any output
+ * tile's K is shared between: the cluster split, or the split of the tail launch (a persistent launch
+ * whose last wave would leave most SMs idle runs its whole waves and then the leftover tiles as split-K
+ * clusters) -- or 0 when the shape does not take the tensor-core path.  Host only; launches nothing. */
 KQ_API int kq_debug_tc_splits(kq_dtype wt, int64_t M, int64_t N, int64_t K);
 
 /* Debug twin of kq_gemm's tensor-core path ([vllm-2890] keep-quant provider commit: integer dots

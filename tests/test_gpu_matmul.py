@@ -420,6 +420,32 @@ def test_gemm_split_k_every_output(dtype, M, N, K, S):
     assert nmse(y.reshape(-1), ref) <= 1e-6
 
 
+@pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q5_K, kq.Q6_K])
+def test_gemm_split_tail(dtype):
+    """More tiles than the SMs hold, with a short last wave: the whole waves run persistent and the
+    leftover tiles (the last token tiles) as a second launch of split-K clusters.  Every output of two
+    full weight-row tile columns (whole-wave and tail tiles) and 20000 sampled outputs against the
+    oracle with the elementwise bound, and two calls give identical bits."""
+    M, N, K = 2048, 2560, 2048
+    S = kq.kq_debug_tc_splits(dtype, M, N, K)
+    assert S > 1    # 320 tiles: two whole waves, the 16 leftover tiles split
+    g = synth.rng(1300 + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    y = host(gemm(dtype, wn, xq, M, N, K))
+    assert np.array_equal(y, host(gemm(dtype, wn, xq, M, N, K)))
+    cols = np.r_[0:128, N - 128:N]
+    mi = np.concatenate([np.repeat(np.arange(M), cols.size), g.integers(0, M, 20000)])
+    ni = np.concatenate([np.tile(cols, M), g.integers(0, N, 20000)])
+    ref, terms = oracle.gemm_sampled_terms(dtype, w, host(xq).reshape(M, -1), K, mi, ni)
+    err = np.abs(y[mi, ni].astype(np.float64) - ref)
+    bound = tc_bound(terms, K, S)
+    assert np.all(err <= bound), (err / bound).max()
+    assert nmse(y[mi, ni], ref) <= 1e-6
+
+
 def test_q8_0_swiglu_full_size_sampled():
     c = synth.SWIGLU_Q8_0
     M, N, K = c["M"], c["N"], c["K"]

@@ -62,10 +62,12 @@ def test_tc_integer_sums_bit_exact(dtype, M, N, K):
 
 
 @pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q6_K])
-def test_tc_integer_sums_full_size_split_k(dtype):
+@pytest.mark.parametrize("M,N,K", [(128, 4096, 4096), (2048, 2560, 2048)])
+def test_tc_integer_sums_full_size_split_k(dtype, M, N, K):
     """The benchmark's M = 128 [4096 x 4096] GEMM, which the tensor-core path splits across clusters of
-    CTAs: the integer sums of the first 16 token rows and every weight row against the oracle."""
-    M, N, K = 128, 4096, 4096
+    CTAs, and a [2560 x 2048] M = 2048 GEMM whose leftover tiles after two whole waves run as a split-K
+    launch: the integer sums of 16 token rows (for the second, also 16 rows of the last token tile, in
+    the split tail) and every weight row against the oracle."""
     assert kq.kq_debug_tc_splits(dtype, M, N, K) > 1
     g = synth.rng(0)
     w = synth.weights(dtype, N, K, g)
@@ -74,8 +76,9 @@ def test_tc_integer_sums_full_size_split_k(dtype):
     xq = act_quant(dtype, dev(x), M, K)
     _, sums = _tc_sums(dtype, wn, xq, M, N, K)
     xq_h = host(xq).reshape(M, -1)
-    ref = oracle.block_sums(dtype, w, xq_h[:16], 16, N, K)
-    assert np.array_equal(sums[:16].astype(np.int64), ref)
+    for r in ([np.arange(16)] + ([np.arange(M - 100, M - 84)] if M > 128 else [])):
+        ref = oracle.block_sums(dtype, w, np.ascontiguousarray(xq_h[r]), 16, N, K)
+        assert np.array_equal(sums[r].astype(np.int64), ref)
 
 
 @pytest.mark.parametrize("dtype", [kq.Q4_K, kq.Q5_K, kq.Q6_K, kq.Q8_0])
