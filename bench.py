@@ -39,12 +39,13 @@ sys.path.insert(0, ROOT)
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per tcgen05 GEMM launch, averaged over the 36 launches of two timed step
-# replays, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum; Q6_K 78.5 MB, Q4_K
-# 51.9 MB per launch).  Valid only for the kernel sources it was taken on: null once their hash differs.
-TC_TRAFFIC = {"bytes_per_launch": 65.17e6,
+# DRAM bytes (read + write) of the tcgen05 kernel per GEMM of the prefill step (its persistent launch and,
+# where it has one, its split-tail launch), averaged over the 18 GEMMs of two timed step replays, from
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum).  Valid only for the kernel sources it
+# was taken on: null once their hash differs.
+TC_TRAFFIC = {"bytes_per_gemm": 70.36e6,
               "sources": ("gemv_quantize_q8_gb300/csrc/kq_tc.cu", "gemv_quantize_q8_gb300/csrc/kq_sm100.cuh"),
-              "sha256": "30b34075a76a5e7c1c40ac6cff9975c6a4da83eafc78d7f8757e3086d23ef2e7"}
+              "sha256": "2dad95e1ef8e57899204aa2097fb979b6c303cbbae4ba9b25010a8b51f11809a"}
 
 
 def max_over_ranks(vals, world, device=None):
@@ -66,7 +67,7 @@ def whole_job_tops(ops_per_rank, world, ms):
 
 TC_KERNEL_END = b"// Activation prologue: Q8_K rows"
 # The tcgen05 kernel's share of the prefill step in the committed ncu launch list (same source hash).
-TC_SHARE = {"share": 0.904}
+TC_SHARE = {"share": 0.902}
 
 
 def tc_share():
@@ -79,7 +80,7 @@ def tc_traffic():
     """The recorded traffic while the GEMM kernel's sources are the ones it was measured on: the headers,
     and kq_tc.cu up to the first prologue kernel (host code and the prologues after it do not enter
     the tcgen05 kernel)."""
-    return TC_TRAFFIC["bytes_per_launch"] if _tc_sources_hash() == TC_TRAFFIC["sha256"] else None
+    return TC_TRAFFIC["bytes_per_gemm"] if _tc_sources_hash() == TC_TRAFFIC["sha256"] else None
 
 
 def _tc_sources_hash():

@@ -1903,7 +1903,7 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
     a.dbg = dbg;
     if (fold && dbg && dbg->sums) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_ex: no integer sums with folded scales");
     s = launch_tc_dt(wt, a, st, fold, tok);
-    if (s == KQ_OK) count_launch(R_MMQ_TC, 2);
+    if (s == KQ_OK) count_launch(R_MMQ_TC, a.tail_tiles ? 3 : 2);  // prologue, GEMM (and its split tail)
     return s;
 }
 
