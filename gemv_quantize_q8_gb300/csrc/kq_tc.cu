@@ -6,16 +6,21 @@
 //     TMA loads with 128-byte swizzle into a shared-memory ring.  One activation tile serves every
 //     weight row of the CTA (the cooperative activation share of vllm.cpp PR #3035).
 //   * weights stay packed in HBM; converter warps unpack each 64-element kblock of their row into
-//     the integer products sc_j*c (Q4_K, <= 945) or, for Q6_K, into (sc & 15)*(c-32) and
-//     16*(sc >> 4)*(c-32) (|.| <= 4096, multiples of 16 above 2048), all exact in f16, and store
-//     them straight into TENSOR MEMORY, where the MMA reads them as its A operand.  Converted
+//     the integer products sc_j*c (Q4_K, <= 945) or, for Q6_K, into ((sc & 15)/16)*(c-32) and
+//     (sc >> 4)*(c-32) (at most 9 significant bits), all exact in f16, and store them straight into
+//     TENSOR MEMORY, where the MMA reads them as its A operand.  Converted
 //     weights never touch shared memory, so shared-memory bandwidth goes to the activation tiles.
 //   * each super-block (256 elements) accumulates into its own TMEM tile (weight rows = lanes,
 //     tokens = columns): the sums are integers below 2^24 for any realistic input, so the fp32
 //     accumulator holds them exactly.  Q4_K's min term sum_j m_j*bsum_j is a 16-wide extension MMA
-//     (mins and bsums are exact in f16) into a second tile; Q6_K's two halves share one tile.
+//     (mins and bsums are exact in f16) into a second tile; Q6_K's two halves share one tile, which
+//     holds the super-block's integer sum over 16.
 //   * epilogue warps promote each super-block to fp32 while the MMA fills the other TMEM buffer:
-//     acc += d_a*(d_w*S1 - dmin*S2) (Q4_K) or acc += (d_a*d_w)*S (Q6_K).
+//     acc += d_a*(d_w*S1 - dmin*S2) (Q4_K) or acc += (d_a*16*d_w)*S (Q6_K).
+// Q5_K follows Q4_K (a fifth code bit), Q8_0 x Q8_1 reads every 32-block's dot out of its own
+// accumulator; an opt-in folded-scale mode instead dequantises to f16 in the converters and
+// accumulates a whole tile in one accumulator (not bit-exact).  Schedule: persistent CTAs over whole
+// tiles, split-K clusters for few tiles, or both (a split tail) when the last wave would be short.
 // The integer parts are therefore the oracle's integers; only the fp32 scaling uses fused
 // multiply-adds, which keeps the result within a few ulps of the sequential CPU order.
 //
