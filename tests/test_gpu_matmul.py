@@ -446,6 +446,31 @@ def test_gemm_split_tail(dtype):
     assert nmse(y[mi, ni], ref) <= 1e-6
 
 
+@pytest.mark.parametrize("dtype", DTS)
+def test_gemm_long_k(dtype):
+    """A long reduction on the tensor-core path (K = 65536: 256 super-blocks, 2048 Q8_0 blocks), ragged in
+    M and N (split-K clusters of 8 for the K-quants, one ascending sum for Q8_0): every output against the
+    oracle, within the elementwise bound (K-quants) or bit for bit (Q8_0)."""
+    M, N, K = 130, 136, 65536
+    S = kq.kq_debug_tc_splits(dtype, M, N, K)
+    assert S >= 1
+    g = synth.rng(1400 + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(M, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xq = act_quant(dtype, dev(x), M, K)
+    y = host(gemm(dtype, wn, xq, M, N, K))
+    xq_h = host(xq).reshape(M, -1)
+    if dtype == kq.Q8_0:
+        assert np.array_equal(y, oracle.gemm(dtype, w, xq_h, M, N, K))
+        return
+    mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+    ref, terms = oracle.gemm_sampled_terms(dtype, w, xq_h, K, mi, ni)
+    err = np.abs(y.reshape(-1).astype(np.float64) - ref)
+    assert np.all(err <= tc_bound(terms, K, S)), (err / tc_bound(terms, K, S)).max()
+    assert nmse(y.reshape(-1), ref) <= 1e-6
+
+
 def test_q8_0_swiglu_full_size_sampled():
     c = synth.SWIGLU_Q8_0
     M, N, K = c["M"], c["N"], c["K"]
