@@ -20,7 +20,8 @@
 // Q5_K follows Q4_K (a fifth code bit), Q8_0 x Q8_1 reads every 32-block's dot out of its own
 // accumulator; an opt-in folded-scale mode instead dequantises to f16 in the converters and
 // accumulates a whole tile in one accumulator (not bit-exact).  Schedule: persistent CTAs over whole
-// tiles, split-K clusters for few tiles, or both (a split tail) when the last wave would be short.
+// tiles, split-K clusters for few tiles, or both (a split tail) when the last wave would be short; a
+// dense GEMM starts under programmatic dependent launch beside the end of its activation prologue.
 // The integer parts are therefore the oracle's integers; only the fp32 scaling uses fused
 // multiply-adds, which keeps the result within a few ulps of the sequential CPU order.
 //
@@ -473,6 +474,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     bulk_load(sP + (p * 8 + gi) * C::CB, P.w + ((int64_t)(T.g0 + gi) * nchunk + gsb) * C::CB, C::CB,
                               &p_full[p]);
                 last_p[p] = pph;
+                // The packed weights are never written by the prologue kernel just before this one; the
+                // bsum and scale panels are: under programmatic dependent launch, wait for it here, after
+                // the first weight copy is on its way (a no-op in a launch without the attribute).
+                if (st == 0) grid_dependency_wait();
                 if (C::EXT) {
                     const int e = st % C::NE, eph = (st / C::NE) & 1;
                     if (!(ok = mbar_wait_sleep(&e_empty[e], eph ^ 1, abort_flag, P.wait_ns))) break;
@@ -511,6 +516,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int i = 0; i < L::NPAIR; ++i) last_k[i] = -1;
             bool ok = true;
             int m0 = 0, ti = 0, tt = 0;
+            grid_dependency_wait();  // the activation panel is the prologue kernel's output
             for (int pp = 0; pp < nsteps * 2 && ok && !P.withhold; ++pp) {
                 if ((pp & 1) == 0 && tt == 0) m0 = tile_of(ti).m0;
                 const int s = pp % L::NPAIR, ph = (pp / L::NPAIR) & 1;
@@ -1058,9 +1064,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&h_empty[h]);
             } else {
-            if (!(ok = mbar_wait_sleep(&acc_full[buf], (t >> 1) & 1, abort_flag, P.wait_ns))) break;
+            // the step's scales are published long before its sums are complete: their barriers are
+            // passed first, so nothing but the accumulator's own wait sits between the MMA and the reads
             if (!(ok = mbar_wait_sleep(&h_full[h], (t >> 2) & 1, abort_flag, P.wait_ns))) break;
             if (!(ok = mbar_wait_sleep(&da_full[h], (t >> 2) & 1, abort_flag, P.wait_ns))) break;
+            if (!(ok = mbar_wait_sleep(&acc_full[buf], (t >> 1) & 1, abort_flag, P.wait_ns))) break;
             tc_fence_after();
             const float2 rs = reinterpret_cast<const float2 *>(sH + h * TC_ROWS * 8)[row];  // (d, -dmin)
             const float4 *dap = reinterpret_cast<const float4 *>(sDA + h * C::TOK * 4) + tq * 8;
@@ -1242,7 +1250,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         cluster.sync();
     }
-    if (tid == 0 && *abort_flag) atomicAdd(P.err, 1ull);
+    if (tid == 0 && *abort_flag) {
+        grid_dependency_wait();  // the prologue clears the flag: count only after it has finished
+        atomicAdd(P.err, 1ull);
+    }
     if (warp == TC_WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tbase, TMEM_COLS);
@@ -1255,6 +1266,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 __global__ void act_panel_kernel(const uint8_t *__restrict__ xq, int M, int M_pad, int nsb, __half *__restrict__ A,
                                  __half *__restrict__ E, float *__restrict__ D, unsigned long long *__restrict__ err) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;  // the GEMM that follows counts timeouts here
+    grid_launch_dependents();  // the GEMM may start its setup and weight loads beside this grid
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)M_pad * nsb) return;
@@ -1292,6 +1304,7 @@ __global__ void act_panel_f32_kernel(const float *__restrict__ x, int64_t ldx, i
                                      __half *__restrict__ A, __half *__restrict__ E, float *__restrict__ D,
                                      unsigned long long *__restrict__ err) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    grid_launch_dependents();  // the GEMM may start its setup and weight loads beside this grid
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)M_pad * nsb) return;
@@ -1328,6 +1341,7 @@ template <bool VEC>
 __global__ void act_panel_f32_fold_kernel(const float *__restrict__ x, int64_t ldx, int M, int M_pad, int nsb,
                                           __half *__restrict__ A, unsigned long long *__restrict__ err) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    grid_launch_dependents();  // the GEMM may start its setup and weight loads beside this grid
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)M_pad * nsb) return;
@@ -1359,6 +1373,7 @@ __global__ void act_panel_f32_fold_kernel(const float *__restrict__ x, int64_t l
 __global__ void act_panel_q81_kernel(const uint8_t *__restrict__ xq, int M, int M_pad, int nsb, __half *__restrict__ A,
                                      float *__restrict__ D, unsigned long long *__restrict__ err) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    grid_launch_dependents();  // the GEMM may start its setup and weight loads beside this grid
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)M_pad * nsb) return;
@@ -1390,6 +1405,7 @@ __global__ void act_panel_q81_kernel(const uint8_t *__restrict__ xq, int M, int 
 __global__ void act_panel_q81_fold_kernel(const uint8_t *__restrict__ xq, int M, int M_pad, int nsb,
                                           __half *__restrict__ A, unsigned long long *__restrict__ err) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    grid_launch_dependents();  // the GEMM may start its setup and weight loads beside this grid
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)M_pad * nsb) return;
@@ -1419,6 +1435,7 @@ __global__ void act_panel_q81_fold_kernel(const uint8_t *__restrict__ xq, int M,
 __global__ void act_panel_fold_kernel(const uint8_t *__restrict__ xq, int M, int M_pad, int nsb,
                                       __half *__restrict__ A, unsigned long long *__restrict__ err) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0ull;
+    grid_launch_dependents();  // the GEMM may start its setup and weight loads beside this grid
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)M_pad * nsb) return;
@@ -1712,6 +1729,7 @@ struct TcLaunch {
     const TcDebug *dbg;   // NULL, or the debug read-out / wait-limit hooks
     int64_t tail_tiles;   // > 0 (dense, nsplit = 1): the last tail_tiles tiles run as a split-K launch
     int tail_split;       // of tail_split CTAs per tile
+    bool pdl;             // the first launch may start while the prologue kernel before it finishes
 };
 
 template <int DT>
@@ -1780,6 +1798,11 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
     const int64_t R = a.tail_tiles;  // > 0: the last R tiles go to a second, split-K launch
     if (R && (S != 1 || a.grouped || p.swq || R >= tiles || a.tail_split < 2))
         return fail(KQ_ERR_INVALID_ARG, "kq_gemm (tensor core): invalid split tail");
+    // Dense launches follow their activation prologue in the stream and may start beside its last
+    // blocks: the CTAs set up, load and convert their first weights, and wait on the prologue only
+    // before the first activation, bsum or scale access.  Routed launches read tile tables that
+    // earlier kernels wrote from their first instruction, so they take no such head start.
+    bool pdl = a.pdl && !a.grouped;
     auto launch = [&](TcParams q, int split, dim3 grid) -> kq_status {
         q.nsplit = split;
         q.sb_per_split = (int)((nsb + split - 1) / split);
@@ -1789,13 +1812,23 @@ static kq_status launch_tc(const TcLaunch &a, cudaStream_t st) {
         cfg.blockDim = dim3(TC_THREADS, 1, 1);
         cfg.dynamicSmemBytes = Lay::ALLOC;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = (unsigned)split;
+        cudaLaunchAttribute attr[2];
+        unsigned na = 0;
+        if (split > 1) {
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = 1;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = (unsigned)split;
+            ++na;
+        }
+        if (pdl) {
+            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
         cfg.attrs = attr;
-        cfg.numAttrs = split > 1 ? 1 : 0;
+        cfg.numAttrs = na;
+        pdl = false;  // a second (split-tail) launch waits for the first in full
         cudaError_t le = cudaLaunchKernelEx(&cfg, kern, tmA, tmE, q);
         if (le != cudaSuccess)
             return fail(KQ_ERR_CUDA, "kq_gemm (tensor core): launch failed: %s", cudaGetErrorString(le));
@@ -1906,6 +1939,7 @@ static kq_status tc_gemm_impl(kq_dtype wt, const uint8_t *w, const uint8_t *xq, 
     }
     a.err = reinterpret_cast<unsigned long long *>(workspace + L.off_flag);
     a.dbg = dbg;
+    a.pdl = true;
     if (fold && dbg && dbg->sums) return fail(KQ_ERR_INVALID_ARG, "kq_gemm_ex: no integer sums with folded scales");
     s = launch_tc_dt(wt, a, st, fold, tok);
     if (s == KQ_OK) count_launch(R_MMQ_TC, a.tail_tiles ? 3 : 2);  // prologue, GEMM (and its split tail)
