@@ -43,9 +43,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # where it has one, its split-tail launch), averaged over the 18 GEMMs of two timed step replays, from
 # one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum).  Valid only for the kernel sources it
 # was taken on: null once their hash differs.
-TC_TRAFFIC = {"bytes_per_gemm": 70.36e6,
+TC_TRAFFIC = {"bytes_per_gemm": 70.80e6,
               "sources": ("gemv_quantize_q8_gb300/csrc/kq_tc.cu", "gemv_quantize_q8_gb300/csrc/kq_sm100.cuh"),
-              "sha256": "771930c20e93594476d2697c42ed7155b63df0a12ee5ec10cf4965cf947575a3"}
+              "sha256": "b69b0cbab78f690a89eac645a397ad1d41f2618652ac84ea95660b6479bd0359"}
 
 
 def max_over_ranks(vals, world, device=None):
@@ -67,7 +67,7 @@ def whole_job_tops(ops_per_rank, world, ms):
 
 TC_KERNEL_END = b"// Activation prologue: Q8_K rows"
 # The tcgen05 kernel's share of the prefill step in the committed ncu launch list (same source hash).
-TC_SHARE = {"share": 0.902}
+TC_SHARE = {"share": 0.901}
 
 
 def tc_share():
