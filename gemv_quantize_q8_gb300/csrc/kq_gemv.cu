@@ -383,6 +383,10 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     float *terms = reinterpret_cast<float *>(smem + (size_t)cpr * WS::BYTES);
     float *gather = terms + kGemvRows * tstride;
 
+    // Let the next kernel in the stream get scheduled; it waits on this grid before touching memory.
+    // Fed a quantised row, the trigger goes first (measured: the pre-quantised Q4_K [9728 x 2560] call
+    // 10% faster); with the fused quantizer it goes after the set-up (there, first was 2% slower).
+    if (!FUSED) grid_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < cpr; ++i) mbar_init(&bars[i], 1);
         if (S > 1) mbar_init(&gather_bar, S - 1);
@@ -391,8 +395,7 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     }
     __syncthreads();
     if (S > 1) cluster_arrive_relaxed();  // "my barriers are initialised"; waited for before any remote access
-    // Let the next kernel in the stream get scheduled; it waits on this grid before touching memory.
-    grid_launch_dependents();
+    if (FUSED) grid_launch_dependents();
 
     const bool active = warp < nloc;
     const int c = c_begin + warp;
