@@ -113,3 +113,32 @@ def test_gemm_f32_folded_equals_quantize_then_folded_gemm(dtype, M, N, K, pad):
     xa = oracle.quantize_q8_1(x) if dtype == kq.Q8_0 else oracle.quantize_q8_k(x)
     mi, ni = g.integers(0, M, 1500), g.integers(0, N, 1500)
     assert nmse(host(ya)[mi, ni], oracle.gemm_sampled(dtype, w, xa, K, mi, ni)) <= 1e-6
+
+
+def test_gemm_f32_chain_sharing_one_workspace():
+    """GEMMs of different shapes and schedules (split-K clusters, persistent CTAs, a split tail) issued
+    back to back on one stream with one shared workspace, no synchronisation between them: each GEMM's
+    tensor-core launch may start beside its own activation prologue, but the next prologue rewrites the
+    shared panels only once the GEMM before it has finished, so every output equals the same GEMM run
+    alone, bit for bit."""
+    cases = [(kq.Q4_K, 128, 1024, 4096), (kq.Q6_K, 512, 1024, 2048), (kq.Q4_K, 2048, 2560, 2048),
+             (kq.Q6_K, 130, 768, 4096), (kq.Q4_K, 300, 392, 1536)]
+    g = synth.rng(980)
+    prepared = []
+    wsb = 0
+    for dtype, M, N, K in cases:
+        w = synth.weights(dtype, N, K, g)
+        x = synth.activations(M, K, g, outliers=True)
+        prepared.append((dtype, M, N, K, repack(dtype, w, N, K), dev(x)))
+        wsb = max(wsb, kq.kq_gemm_f32_workspace_bytes(dtype, M, N, K))
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    chain = []
+    for dtype, M, N, K, wn, xd in prepared:
+        y = torch.full((M, N), float("nan"), device=DEV)
+        kq.kq_gemm_f32(dtype, wn, xd, K, M, N, K, y, N, ws, wsb)
+        chain.append(y)
+    torch.cuda.synchronize()
+    assert kq.kq_read_device_flag(ws) == 0
+    for (dtype, M, N, K, wn, xd), y in zip(prepared, chain):
+        alone = _fused(dtype, wn, xd, M, N, K, K)
+        assert torch.equal(y, alone), (dtype, M, N, K)
