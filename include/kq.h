@@ -166,7 +166,10 @@ KQ_API kq_status kq_swiglu_quantize_q8k(const float *g, const float *u, int64_t 
  * Exactly one of x (fp32 [K]: quantised inside the kernel, no separate launch) and xq (pre-quantised
  * activation row, K/256 Q8_K or K/32 Q8_1 blocks) must be non-NULL.  y: fp32 [N].
  * y[n] = sum over blocks of the scaled integer block dots (the kq_gemm formula); the reduction
- * order is fixed, so results are deterministic.  Pointers: w 16-byte aligned, x/xq/y 4-byte. */
+ * order is fixed, so results are deterministic.  Pointers: w 16-byte aligned, x/xq/y 4-byte.
+ * K is at most 65536 (Q4_K, Q5_K), 55296 (Q6_K) or 26624 (Q8_0): a thread block stages its share of
+ * every row's weights in shared memory; a larger K returns KQ_ERR_INVALID_ARG ("too large") without
+ * launching (kq_gemm with M = 1 takes a larger K through its other kernels). */
 KQ_API kq_status kq_gemv(kq_dtype wt, const void *w, const float *x, const void *xq, int64_t N, int64_t K, float *y,
                   kq_stream_t stream);
 

@@ -44,7 +44,7 @@ def tc_bound(terms: np.ndarray, K: int, splits: int) -> np.ndarray:
 
 @pytest.mark.parametrize("dtype", DTS)
 @pytest.mark.parametrize("N,K", [(40, 512), (256, 1024), (100, 4096), (16, 256), (48, 16384), (1000, 9472),
-                                 (72, 9728)])
+                                 (72, 9728), (32, 10240), (32, 10496)])
 @pytest.mark.parametrize("fused", [True, False])
 def test_gemv_small(dtype, N, K, fused):
     g = synth.rng(200 + N + K + dtype)
@@ -60,6 +60,36 @@ def test_gemv_small(dtype, N, K, fused):
     ref = oracle.gemm(dtype, w, _oracle_act(dtype, x), 1, N, K)[0]
     got = host(y)
     assert np.array_equal(got, ref), (nmse(got, ref), np.abs(got - ref).max())
+
+
+# the largest K each weight type's GEMV stages (its shared memory per block): one 256-block more is
+# rejected on the host before any launch
+GEMV_MAX_K = {kq.Q4_K: 65536, kq.Q5_K: 65536, kq.Q6_K: 55296, kq.Q8_0: 26624}
+
+
+@pytest.mark.parametrize("dtype", DTS)
+def test_gemv_max_k(dtype):
+    K, N = GEMV_MAX_K[dtype], 40
+    g = synth.rng(230 + dtype)
+    w = synth.weights(dtype, N, K, g)
+    x = synth.activations(1, K, g, outliers=True)
+    wn = repack(dtype, w, N, K)
+    xd = dev(x)
+    ref = oracle.gemm(dtype, w, _oracle_act(dtype, x), 1, N, K)[0]
+    for fused in (True, False):
+        y = torch.full((N,), float("nan"), device=DEV)
+        if fused:
+            kq.kq_gemv(dtype, wn, xd, None, N, K, y)
+        else:
+            kq.kq_gemv(dtype, wn, None, act_quant(dtype, xd, 1, K), N, K, y)
+        assert np.array_equal(host(y), ref), (fused, nmse(host(y), ref))
+    K2 = K + 256
+    w2 = torch.zeros(kq.native_bytes(dtype, N, K2), dtype=torch.uint8, device=DEV)
+    x2 = torch.zeros(K2, device=DEV)
+    y2 = torch.zeros(N, device=DEV)
+    with pytest.raises(kq.KqError) as e:
+        kq.kq_gemv(dtype, w2, x2, None, N, K2, y2)
+    assert e.value.status == 1 and "too large" in str(e.value)  # KQ_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("dtype", DTS)
