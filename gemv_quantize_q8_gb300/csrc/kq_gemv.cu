@@ -21,6 +21,11 @@
 // With x != NULL the activation is quantised inside the kernel (fused-quant MMVQ of
 // strix-llama.cpp PR #18): each warp quantises the 256 activation values of its own chunk into
 // shared memory while its weight copies are in flight.
+//
+// Long K without a cluster: gemv16_kernel (one column) and gemv16_mc_kernel (up to 8 pre-quantised
+// columns) give each 16-row group one block over the whole K, so successive calls are not clustered
+// launches; several columns stage their activation blocks with every load issued before the first
+// store.
 #include <cooperative_groups.h>
 
 #include "kq_act_smem.cuh"
@@ -347,6 +352,39 @@ __device__ __forceinline__ void gemv_row_chunk_mc(const uint8_t *__restrict__ ch
     }
 }
 
+// Stage the Q8_K blocks of M <= MC activation columns (column m's block at src + m*src_stride) into
+// shared memory at dst + m*xb in the layout the dot reads (int8 q[256], f32 d at +256, int16 bsums at
+// +288).  Every column's loads are issued before the first store, so the warp waits for one memory
+// round trip instead of one per column.
+template <int MC>
+__device__ __forceinline__ void stage_q8k_cols(const uint8_t *__restrict__ src, int64_t src_stride, int M,
+                                               uint8_t *__restrict__ dst, int xb) {
+    const int lane = threadIdx.x & 31;
+    uint32_t a[MC], b[MC];
+    int16_t bsv[MC];
+    float dv[MC];
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+        if (m < M) {
+            const uint8_t *blk = src + m * src_stride;
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(blk + 4);
+            a[m] = q32[2 * lane];
+            b[m] = q32[2 * lane + 1];
+            bsv[m] = reinterpret_cast<const int16_t *>(blk + 260)[lane & 15];
+            dv[m] = *reinterpret_cast<const float *>(blk);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+        if (m < M) {
+            uint8_t *d = dst + m * xb;
+            reinterpret_cast<uint2 *>(d)[lane] = make_uint2(a[m], b[m]);
+            if (lane < 16) reinterpret_cast<int16_t *>(d + 288)[lane] = bsv[m];
+            if (lane == 0) *reinterpret_cast<float *>(d + 256) = dv[m];
+        }
+    }
+}
+
 // grid: (S, ceil(N/32)); cluster (S, 1, 1) when S > 1; block: 32 * cpr threads.  Warp w of cluster
 // rank k owns chunk k*cpr + w for all 32 rows of the block (lane = row): it bulk-copies that chunk's
 // codes for the block's two row groups into its own shared region, quantises (or copies) the
@@ -415,17 +453,13 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
         int16_t *bs_s = reinterpret_cast<int16_t *>(ws + WS::B_OFF);
         if (MC > 1) {
             // batched decode: column m's chunk c is block (m, c) of the quantised activation rows
-            for (int m = 0; m < M; ++m) {
-                int8_t *qm = q_s + m * WS::XB;
-                float *dm = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(da_s) + m * WS::XB);
-                int16_t *bm = reinterpret_cast<int16_t *>(reinterpret_cast<uint8_t *>(bs_s) + m * WS::XB);
-                if (!Tr::q81) {
-                    const uint8_t *blk = xq + ((int64_t)m * nchunk + c) * kQ8KBytes;
-                    const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4);
-                    reinterpret_cast<uint2 *>(qm)[lane] = make_uint2(src[2 * lane], src[2 * lane + 1]);
-                    if (lane < 16) bm[lane] = reinterpret_cast<const int16_t *>(blk + 260)[lane];
-                    if (lane == 0) dm[0] = *reinterpret_cast<const float *>(blk);
-                } else {
+            if (!Tr::q81) {
+                stage_q8k_cols<MC>(xq + (int64_t)c * kQ8KBytes, (int64_t)nchunk * kQ8KBytes, M,
+                                   reinterpret_cast<uint8_t *>(q_s), WS::XB);
+            } else {
+                for (int m = 0; m < M; ++m) {
+                    int8_t *qm = q_s + m * WS::XB;
+                    float *dm = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(da_s) + m * WS::XB);
                     const int b = lane >> 2, part = lane & 3;  // 8 blocks x 4 lanes
                     const uint8_t *blk = xq + (((int64_t)m * nchunk + c) * 8 + b) * kQ81Bytes;
                     const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4 + 8 * part);
@@ -609,6 +643,72 @@ __global__ void __launch_bounds__(32 * kGemv16MaxWarps, 2) gemv16_kernel(const u
     }
 }
 
+// Batched long-K decode (M <= MC pre-quantised activation rows, K-quant weights) without a cluster:
+// one block per 16-row group over the whole K, as gemv16_kernel, with every staged weight chunk dotted
+// against all M columns (gemv_row_chunk_mc: each weight word unpacked once).  Warp w stages chunks 2w
+// and 2w+1 of the group (one bulk copy each) and their M activation blocks; half-warp h forms the
+// terms of chunk 2w+h for its 16 rows, and one thread per (row, column) adds that column's terms in
+// ascending K order -- every output formed exactly as for one column.  A block takes most of an SM's
+// shared memory, so the grid runs as 16-row blocks one per SM; y[m*ldy + n].
+template <int DT, int MC>
+__global__ void __launch_bounds__(32 * kGemv16MaxWarps, 1) gemv16_mc_kernel(const uint8_t *__restrict__ w,
+                                                                              const uint8_t *__restrict__ xq,
+                                                                              int64_t N, int nchunk,
+                                                                              float *__restrict__ y, int M,
+                                                                              int64_t ldy) {
+    constexpr int CB = chunk_bytes(DT);
+    constexpr int XB = GemvWarpSmem<DT, 1>::XB;    // one column's activation block: q[256], d, bsums
+    constexpr int WB = 2 * CB + 2 * MC * XB;       // per warp: two chunks' codes, then their activations
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t bars[kGemvMaxWarps];
+    __shared__ int abort_flag;
+    const int64_t g = blockIdx.x;  // row group: rows 16g .. 16g+15
+    const int nw = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rstride = MC * nchunk;                                          // a row's terms: [column][chunk]
+    float *terms = reinterpret_cast<float *>(smem + (size_t)nw * WB);         // [16][MC][nchunk]
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nw; ++i) mbar_init(&bars[i], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    grid_launch_dependents();
+
+    const int c0 = 2 * warp, nc = min(2, nchunk - c0);
+    uint8_t *ws = smem + (size_t)warp * WB;
+    // the weights are never written by the kernel before this one: their copies start before the wait
+    if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[warp], nc * CB);
+        for (int h = 0; h < nc; ++h) bulk_load(ws + h * CB, w + (g * nchunk + c0 + h) * (int64_t)CB, CB, &bars[warp]);
+    }
+    grid_dependency_wait();
+    // column m's chunk c is Q8_K block (m, c) of the activation rows
+    for (int h = 0; h < nc; ++h)
+        stage_q8k_cols<MC>(xq + (int64_t)(c0 + h) * kQ8KBytes, (int64_t)nchunk * kQ8KBytes, M, ws + 2 * CB + h * MC * XB,
+                           XB);
+    __syncwarp();
+    if (mbar_wait_sleep(&bars[warp], 0, &abort_flag)) {
+        const int h = lane >> 4;
+        if (h < nc)
+            gemv_row_chunk_mc<DT, MC>(ws + h * CB, lane & 15, ws + 2 * CB + h * MC * XB, XB, M,
+                                      terms + (lane & 15) * rstride + c0 + h, nchunk);
+    } else if (lane == 0) {
+        int no_abort = 0;  // drain this warp's copies (bounded) before the block may exit
+        mbar_wait(&bars[warp], 0, &no_abort, 100000000ull);
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < 16 * M; t += blockDim.x) {  // ordered reduction: one thread per (row, column)
+        const int r = t & 15, m = t >> 4;
+        const int64_t n = g * 16 + r;
+        const float *tr = terms + r * rstride + m * nchunk;
+        float acc = 0.0f;
+        for (int i = 0; i < nchunk; ++i) acc = __fadd_rn(acc, tr[i]);
+        if (n < N) y[m * ldy + n] = abort_flag ? __int_as_float(0x7fc00000) : acc;
+    }
+}
+
 // Number of SMs of the current device (looked up once per device).
 static int gemv_sm_count() {
     static int cache[64] = {0};
@@ -675,6 +775,33 @@ static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             e = cudaLaunchKernelEx(&cfg, k16, w, x, xq, N, nchunk, y);
+            if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: launch failed: %s", cudaGetErrorString(e));
+            count_launch(R_GEMV);
+            return KQ_OK;
+        }
+    }
+    if constexpr (MC > 1 && DT != KQ_Q8_0) if (S > 1 && GEMV16_OK) {
+        // several columns whose K the cluster split would share out: 16-row blocks over the whole K
+        // instead (no cluster), one per SM, where the group's whole K and its activations fit
+        constexpr int WB = 2 * chunk_bytes(DT) + 2 * MC * GemvWarpSmem<DT, 1>::XB;
+        const int nw = (nchunk + 1) / 2;
+        const size_t smem16 = (size_t)nw * WB + (size_t)16 * MC * nchunk * 4;
+        const int64_t groups = (N + 15) / 16;
+        if (nw <= kGemv16MaxWarps && smem16 <= 226 * 1024 && groups <= 0x7fffffff) {
+            auto k16 = gemv16_mc_kernel<DT, MC>;
+            cudaError_t e = cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem16);
+            if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: %s", cudaGetErrorString(e));
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)groups, 1, 1);
+            cfg.blockDim = dim3(32 * nw, 1, 1);
+            cfg.dynamicSmemBytes = smem16;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, k16, w, xq, N, nchunk, y, M, ldy);
             if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "kq_gemv: launch failed: %s", cudaGetErrorString(e));
             count_launch(R_GEMV);
             return KQ_OK;

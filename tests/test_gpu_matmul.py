@@ -324,7 +324,8 @@ def test_gemm_q8_0_tensor_core_integer_special_case():
 
 
 @pytest.mark.parametrize("dtype", DTS)
-@pytest.mark.parametrize("M,N,K", [(2, 100, 1024), (3, 256, 2560), (5, 48, 9728), (8, 130, 4096), (8, 64, 16384)])
+@pytest.mark.parametrize("M,N,K", [(2, 100, 1024), (3, 256, 2560), (5, 48, 9728), (8, 130, 4096), (8, 64, 16384),
+                                   (2, 2560, 9728), (8, 2560, 9728)])
 def test_gemm_batched_decode_bit_exact(dtype, M, N, K):
     """Batched decode (M <= 8) runs the weight-streaming GEMV kernel with every staged chunk serving all
     M activation rows; each output is the oracle's sequential sum, so the result is bit-identical --
