@@ -79,6 +79,34 @@ def test_q8_1_special_values():
     assert np.array_equal(got, ref)
 
 
+def test_q8_1_half_integer_quotients():
+    """Values whose quotient v/d lies on or within a few ulps of a half-integer (where the rounding
+    is decided by the last bits of the IEEE quotient): blocks with d exactly 1 (amax 127), with
+    d = amax/127 of arbitrary amax, and with amax near and below 2^-100; bytes equal the oracle's."""
+    rng = np.random.default_rng(7)
+    rows = []
+    for _ in range(4):
+        blocks = []
+        for amax in (127.0, 3.7, 0.0123, 1.0e-30, 1.0e-29, 5.0e3, 5.0e-32, 0.5):
+            d = np.float32(np.float32(amax) / np.float32(127.0))
+            blk = np.zeros(32, np.float32)
+            blk[0] = amax
+            k = rng.integers(-126, 126, 31).astype(np.float64) + 0.5
+            vals = (k * np.float64(d)).astype(np.float32)
+            # the half-integer multiple itself and its float neighbours (up to 3 ulps either way)
+            for i, st in enumerate(rng.integers(-3, 4, 31)):
+                for _ in range(abs(int(st))):
+                    vals[i] = np.nextafter(vals[i], np.float32(np.inf if st > 0 else -np.inf), dtype=np.float32)
+            blk[1:] = np.clip(vals, -amax, amax)
+            blocks.append(blk)
+        rows.append(np.concatenate(blocks))
+    x = np.stack(rows).astype(np.float32)
+    M, K = x.shape
+    got = host(q8_1(dev(x), M, K)).reshape(M, -1)
+    ref = oracle.quantize_q8_1(x)
+    assert np.array_equal(got, ref)
+
+
 def _swiglu_gpu(fn, g, u, M, K, ld, nbytes):
     xq = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device=DEV)
     h = torch.full((M, K), float("nan"), dtype=torch.float32, device=DEV)
