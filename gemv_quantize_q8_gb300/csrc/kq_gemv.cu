@@ -648,10 +648,12 @@ __global__ void __launch_bounds__(32 * kGemv16MaxWarps, 2) gemv16_kernel(const u
 // against all M columns (gemv_row_chunk_mc: each weight word unpacked once).  Warp w stages chunks 2w
 // and 2w+1 of the group (one bulk copy each) and their M activation blocks; half-warp h forms the
 // terms of chunk 2w+h for its 16 rows, and one thread per (row, column) adds that column's terms in
-// ascending K order -- every output formed exactly as for one column.  A block takes most of an SM's
-// shared memory, so the grid runs as 16-row blocks one per SM; y[m*ldy + n].
+// ascending K order -- every output formed exactly as for one column.  A lane's M terms for its chunk
+// go into the 32 bytes of that row's first kblock codes, which only that lane reads and has read by
+// then, so the terms need no shared memory of their own; y[m*ldy + n].  Q4_K with two columns keeps
+// to two blocks per SM (registers and shared memory), so the next call's blocks can start beside it.
 template <int DT, int MC>
-__global__ void __launch_bounds__(32 * kGemv16MaxWarps, 1) gemv16_mc_kernel(const uint8_t *__restrict__ w,
+__global__ void __launch_bounds__(32 * kGemv16MaxWarps, (MC == 2 && DT == KQ_Q4_K) ? 2 : 1) gemv16_mc_kernel(const uint8_t *__restrict__ w,
                                                                               const uint8_t *__restrict__ xq,
                                                                               int64_t N, int nchunk,
                                                                               float *__restrict__ y, int M,
@@ -659,14 +661,13 @@ __global__ void __launch_bounds__(32 * kGemv16MaxWarps, 1) gemv16_mc_kernel(cons
     constexpr int CB = chunk_bytes(DT);
     constexpr int XB = GemvWarpSmem<DT, 1>::XB;    // one column's activation block: q[256], d, bsums
     constexpr int WB = 2 * CB + 2 * MC * XB;       // per warp: two chunks' codes, then their activations
+    static_assert(MC * 4 <= 32, "a row's terms fit its first kblock's 32 code bytes");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t bars[kGemvMaxWarps];
     __shared__ int abort_flag;
     const int64_t g = blockIdx.x;  // row group: rows 16g .. 16g+15
     const int nw = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rstride = MC * nchunk;                                          // a row's terms: [column][chunk]
-    float *terms = reinterpret_cast<float *>(smem + (size_t)nw * WB);         // [16][MC][nchunk]
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nw; ++i) mbar_init(&bars[i], 1);
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(32 * kGemv16MaxWarps, 1) gemv16_mc_kernel(cons
         const int h = lane >> 4;
         if (h < nc)
             gemv_row_chunk_mc<DT, MC>(ws + h * CB, lane & 15, ws + 2 * CB + h * MC * XB, XB, M,
-                                      terms + (lane & 15) * rstride + c0 + h, nchunk);
+                                      reinterpret_cast<float *>(ws + h * CB + (lane & 15) * 32), 1);
     } else if (lane == 0) {
         int no_abort = 0;  // drain this warp's copies (bounded) before the block may exit
         mbar_wait(&bars[warp], 0, &no_abort, 100000000ull);
@@ -702,9 +703,9 @@ __global__ void __launch_bounds__(32 * kGemv16MaxWarps, 1) gemv16_mc_kernel(cons
     for (int t = threadIdx.x; t < 16 * M; t += blockDim.x) {  // ordered reduction: one thread per (row, column)
         const int r = t & 15, m = t >> 4;
         const int64_t n = g * 16 + r;
-        const float *tr = terms + r * rstride + m * nchunk;
         float acc = 0.0f;
-        for (int i = 0; i < nchunk; ++i) acc = __fadd_rn(acc, tr[i]);
+        for (int i = 0; i < nchunk; ++i)  // chunk i's terms: warp i/2's buffer, chunk slot i%2, row r
+            acc = __fadd_rn(acc, reinterpret_cast<const float *>(smem + (size_t)(i >> 1) * WB + (i & 1) * CB + r * 32)[m]);
         if (n < N) y[m * ldy + n] = abort_flag ? __int_as_float(0x7fc00000) : acc;
     }
 }
@@ -785,7 +786,7 @@ static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq
         // instead (no cluster), one per SM, where the group's whole K and its activations fit
         constexpr int WB = 2 * chunk_bytes(DT) + 2 * MC * GemvWarpSmem<DT, 1>::XB;
         const int nw = (nchunk + 1) / 2;
-        const size_t smem16 = (size_t)nw * WB + (size_t)16 * MC * nchunk * 4;
+        const size_t smem16 = (size_t)nw * WB;
         const int64_t groups = (N + 15) / 16;
         if (nw <= kGemv16MaxWarps && smem16 <= 226 * 1024 && groups <= 0x7fffffff) {
             auto k16 = gemv16_mc_kernel<DT, MC>;
