@@ -417,6 +417,10 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     const int nloc = max(0, min(nchunk, c_begin + cpr) - c_begin);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tstride = MC * cpr * Tr::terms;  // a row's terms: [column][local chunk][term]
+    // Eight K-quant columns and no cluster: a lane's terms go into the 32 bytes of its row's first-
+    // kblock codes (read by that lane alone, and read by then) instead of the terms buffer, which
+    // lets a third block share the SM
+    const bool inplace = MC == 8 && !Tr::q81 && S == 1;
     // shared layout: per-warp buffers [cpr][WS] | terms [32][tstride] | (S > 1) gather [S-1][32][tstride]
     float *terms = reinterpret_cast<float *>(smem + (size_t)cpr * WS::BYTES);
     float *gather = terms + kGemvRows * tstride;
@@ -493,7 +497,9 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
             if (gi < ngroups) {
                 if (MC > 1 && DT != KQ_Q8_0)  // several columns: each weight word unpacked once for all
                     gemv_row_chunk_mc<DT, MC>(ws + gi * CB, lane & 15, reinterpret_cast<const uint8_t *>(q_s), WS::XB, M,
-                                              terms + lane * tstride + warp * Tr::terms, cpr * Tr::terms);
+                                              inplace ? reinterpret_cast<float *>(ws + gi * CB + (lane & 15) * 32)
+                                                      : terms + lane * tstride + warp * Tr::terms,
+                                              inplace ? 1 : cpr * Tr::terms);
                 else
                     for (int m = 0; m < (MC > 1 ? M : 1); ++m)
                         gemv_row_chunk<DT>(ws + gi * CB, lane & 15, q_s + m * WS::XB,
@@ -512,11 +518,19 @@ __global__ void __launch_bounds__(kGemvRows * kGemvMaxWarps) gemv_kernel(const u
     if (S == 1) {
         __syncthreads();
         for (int t = threadIdx.x; t < kGemvRows * ncol; t += blockDim.x) {
-            const int r = t & (kGemvRows - 1), m = t / kGemvRows;
+            // in place, column fastest: a warp's reads of one chunk then cover whole 32-byte rows
+            const int r = inplace ? t / ncol : t & (kGemvRows - 1), m = inplace ? t % ncol : t / kGemvRows;
             const int64_t n = rb * kGemvRows + r;
-            const float *tr = terms + r * tstride + m * cpr * Tr::terms;
             float acc = 0.0f;
-            for (int i = 0; i < nloc * Tr::terms; ++i) acc = __fadd_rn(acc, tr[i]);
+            if (inplace) {
+                // chunk i's terms for row r: warp i's buffer, row group r/16, row r%16's first code bytes
+                for (int i = 0; i < nloc; ++i)
+                    acc = __fadd_rn(acc, reinterpret_cast<const float *>(smem + (size_t)i * WS::BYTES + (r >> 4) * CB +
+                                                                       (r & 15) * 32)[m]);
+            } else {
+                const float *tr = terms + r * tstride + m * cpr * Tr::terms;
+                for (int i = 0; i < nloc * Tr::terms; ++i) acc = __fadd_rn(acc, tr[i]);
+            }
             if (n < N) y[m * ldy + n] = abort_flag ? __int_as_float(0x7fc00000) : acc;
         }
     } else {
@@ -742,7 +756,9 @@ static kq_status launch_gemv(const uint8_t *w, const float *x, const uint8_t *xq
     // them), keeping >= 5 chunks per block.
     auto smem_for = [&](int s) {
         const int c = (nchunk + s - 1) / s;
-        return (size_t)c * WS::BYTES + (size_t)s * kGemvRows * c * Tr::terms * MC * 4;
+        // no terms buffer where the kernel keeps eight K-quant columns' terms in place (no cluster)
+        const bool inplace = MC == 8 && !Tr::q81 && s == 1;
+        return (size_t)c * WS::BYTES + (inplace ? 0 : (size_t)s * kGemvRows * c * Tr::terms * MC * 4);
     };
     while (S < 8 && (rblocks * S < gemv_sm_count() || smem_for(S) > 112 * 1024) && (nchunk + 2 * S - 1) / (2 * S) >= 5)
         S *= 2;
