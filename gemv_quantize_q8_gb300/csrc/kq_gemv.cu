@@ -609,7 +609,10 @@ __global__ void __launch_bounds__(32 * kGemv16MaxWarps, 2) gemv16_kernel(const u
         for (int h = 0; h < nc; ++h) bulk_load(ws + h * CB, w + (g * nchunk + c0 + h) * (int64_t)CB, CB, &bars[warp]);
     }
     grid_dependency_wait();
-    for (int h = 0; h < nc; ++h) {
+    // a pre-quantised row: both chunks' Q8_K blocks staged with every load issued before the first store
+    if (!FUSED && !Tr::q81)
+        stage_q8k_cols<2>(xq + (int64_t)c0 * kQ8KBytes, kQ8KBytes, nc, ws + WS::Q_OFF, WS::XB);
+    for (int h = 0; h < nc && (FUSED || Tr::q81); ++h) {
         int8_t *q_s = reinterpret_cast<int8_t *>(ws + WS::Q_OFF + h * WS::XB);
         float *da_s = reinterpret_cast<float *>(ws + WS::D_OFF + h * WS::XB);
         int16_t *bs_s = reinterpret_cast<int16_t *>(ws + WS::B_OFF + h * WS::XB);
@@ -621,12 +624,6 @@ __global__ void __launch_bounds__(32 * kGemv16MaxWarps, 2) gemv16_kernel(const u
                 warp_quantize_q8_1x4_smem(x + (int64_t)c * 256, q_s, da_s);
                 warp_quantize_q8_1x4_smem(x + (int64_t)c * 256 + 128, q_s + 128, da_s + 4);
             }
-        } else if (!Tr::q81) {
-            const uint8_t *blk = xq + (int64_t)c * kQ8KBytes;
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(blk + 4);
-            reinterpret_cast<uint2 *>(q_s)[lane] = make_uint2(src[2 * lane], src[2 * lane + 1]);
-            if (lane < 16) bs_s[lane] = reinterpret_cast<const int16_t *>(blk + 260)[lane];
-            if (lane == 0) da_s[0] = *reinterpret_cast<const float *>(blk);
         } else {
             const int b = lane >> 2, part = lane & 3;  // 8 blocks x 4 lanes
             const uint8_t *blk = xq + ((int64_t)c * 8 + b) * kQ81Bytes;
